@@ -1,0 +1,501 @@
+"""Plain CPU oracle of the EAGLE hot path.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py`` for who may import it
+and for the source keys [E3], [E1], [M7.5], [E3-blog], [Philox]).
+
+Every floating-point result is computed in fp64 from the exact values the GPU
+sees (bf16/fp32 inputs widen exactly).  The one exception is the EAGLE-2 path
+value used to rank tree candidates: that ranking decides integers (which node
+is expanded / kept), the pages fix no precision for it, and so both the oracle
+and the kernel take it in fp32 -- one correctly rounded fp32 addition per tree
+level, which has a single possible result.
+"""
+
+import math
+
+import numpy as np
+
+from .philox import accept_uniforms, race_uniforms
+
+# ---------------------------------------------------------------------------
+# a1: EAGLE-3 multi-layer feature fusion
+# ---------------------------------------------------------------------------
+
+
+def fuse_proj(h_low, h_mid, h_high, w_proj, bias=None):
+    """Fused feature g = W_proj [h_low; h_mid; h_high] (+ bias), fp64.
+
+    [E3] section 3.4, "Change 2: The fusion FC layer": the three k-dimensional
+    features l, m, h are concatenated into a 3k vector and a fully connected
+    layer maps it back to k dimensions; the bias is optional.  [M7.5] 0x08B
+    writes the same map as r_t = W_R [f_low; f_mid; f_high], W_R in R^{d x 3d};
+    [E3-blog] "What EAGLE-3 changes" as g_t = W_proj @ concat(h_low, h_mid, h_high).
+
+    Shapes: h_* [M, d]; w_proj [d, 3d] (out x in, row-major); bias [d] or None.
+    """
+    x = np.concatenate([np.asarray(h_low, np.float64), np.asarray(h_mid, np.float64),
+                        np.asarray(h_high, np.float64)], axis=1)
+    w = np.asarray(w_proj, np.float64)
+    if x.shape[1] != w.shape[1]:
+        raise ValueError("w_proj must be [d, 3d] with d the width of each feature")
+    g = x @ w.T
+    if bias is not None:
+        g = g + np.asarray(bias, np.float64)[None, :]
+    return g
+
+
+# ---------------------------------------------------------------------------
+# a5 helper: tree ancestry mask (flatten step)
+# ---------------------------------------------------------------------------
+
+
+def ancestor_mask(parent_row, n_rows=None):
+    """Visibility bitmask of each flattened tree row.
+
+    Bit j of mask[r] is set iff row j is row r itself or one of its ancestors
+    (the root, row 0, is an ancestor of every row).  This is the draft part of
+    the visibility rule A(u, v) = 1 iff v in TargetPrefix(u) u DraftAncestors(u)
+    u {u} of [M7.5] 0x08C; [E3] "The Attention Mechanism Modifications" states
+    the same: a drafted token sees its ancestors but NOT tokens in other
+    branches.  Rows at or beyond ``n_rows`` see only themselves.
+
+    parent_row: int array [R] (row 0 = -1, parent_row[i] < i).  Returns uint64 [R].
+    """
+    parent_row = np.asarray(parent_row)
+    R = parent_row.shape[0]
+    if R > 64:
+        raise ValueError("at most 64 tree rows fit a 64-bit mask")
+    n = R if n_rows is None else int(n_rows)
+    mask = np.zeros(R, dtype=np.uint64)
+    for r in range(R):
+        bits = 1 << r
+        if r < n:
+            j = r
+            while True:
+                pj = int(parent_row[j])
+                if j == 0:
+                    break
+                if not 0 <= pj < j:
+                    raise ValueError("parent_row must be topological: 0 <= parent_row[i] < i")
+                bits |= 1 << pj
+                j = pj
+        mask[r] = np.uint64(bits)
+    return mask
+
+
+# ---------------------------------------------------------------------------
+# a2: tree-masked attention against a paged KV cache plus the tree's own rows
+# ---------------------------------------------------------------------------
+
+
+def tree_attn(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, tree_mask,
+              page_size=16, scale=None, sample=None):
+    """Tree attention, fp64, max-subtracted softmax.
+
+    For tree row r of request b and query head h (kv head h // G, G = Hq/Hkv):
+        keys = the ctx_lens[b] committed prefix tokens (read through the page
+               table) followed by the tree rows j with bit j of tree_mask[b, r];
+        o    = sum_j softmax_j(scale * q . k_j) v_j,  lse = log sum_j exp(scale q.k_j).
+    [M7.5] 0x08C visibility rule (TargetPrefix u DraftAncestors u self);
+    [E1] "Tree-Structured Draft Generation": each node attends only to its
+    ancestors; [M7.5] 0x05D: tree K/V are temporary branch rows, separate from
+    the committed cache.  Readings: scale = 1/sqrt(D); kv head = h // G; Q and
+    K arrive with positions already applied.
+
+    Shapes: q [B,R,Hq,D]; k_tree, v_tree [B,R,Hkv,D]; k_cache, v_cache
+    [P, page_size, Hkv, D]; block_table [B, max_pages]; ctx_lens [B];
+    tree_mask uint64 [B,R].  ``sample``: optional list of (b, r, h) to compute
+    only those outputs (returns dict keyed by the tuple).
+    Returns (out [B,R,Hq,D], lse [B,R,Hq]) in fp64, or the sampled dict.
+    """
+    q = np.asarray(q, np.float64)
+    B, R, Hq, D = q.shape
+    Hkv = k_tree.shape[2]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    k_tree = np.asarray(k_tree, np.float64)
+    v_tree = np.asarray(v_tree, np.float64)
+    block_table = np.asarray(block_table)
+    ctx_lens = np.asarray(ctx_lens)
+    tree_mask = np.asarray(tree_mask, dtype=np.uint64)
+
+    def prefix(b):
+        n = int(ctx_lens[b])
+        npg = (n + page_size - 1) // page_size
+        pages = block_table[b, :npg].astype(np.int64)
+        kc = np.asarray(k_cache[pages], np.float64).reshape(npg * page_size, Hkv, D)[:n]
+        vc = np.asarray(v_cache[pages], np.float64).reshape(npg * page_size, Hkv, D)[:n]
+        return kc, vc
+
+    def one_row(b, r, kc, vc, heads):
+        m = int(tree_mask[b, r])
+        vis = [j for j in range(R) if (m >> j) & 1]
+        keys = np.concatenate([kc, k_tree[b, vis]], axis=0)  # [n+t, Hkv, D]
+        vals = np.concatenate([vc, v_tree[b, vis]], axis=0)
+        res = {}
+        for h in heads:
+            kv = h // G
+            s = scale * (keys[:, kv, :] @ q[b, r, h])
+            mx = s.max()
+            w = np.exp(s - mx)
+            z = w.sum()
+            res[h] = ((w @ vals[:, kv, :]) / z, mx + math.log(z))
+        return res
+
+    if sample is not None:
+        out = {}
+        by_b = {}
+        for (b, r, h) in sample:
+            by_b.setdefault(b, []).append((r, h))
+        for b, items in by_b.items():
+            kc, vc = prefix(b)
+            for r in sorted({r for r, _ in items}):
+                heads = [h for rr, h in items if rr == r]
+                for h, val in one_row(b, r, kc, vc, heads).items():
+                    out[(b, r, h)] = val
+        return out
+
+    out = np.zeros((B, R, Hq, D))
+    lse = np.zeros((B, R, Hq))
+    for b in range(B):
+        kc, vc = prefix(b)
+        for r in range(R):
+            for h, (o, l) in one_row(b, r, kc, vc, range(Hq)).items():
+                out[b, r, h] = o
+                lse[b, r, h] = l
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# a3: LM head with per-row top-k and log-softmax
+# ---------------------------------------------------------------------------
+
+
+def lmhead_topk(x, w_lm, k, temperature=1.0, bias=None, rows=None):
+    """Vocabulary logits z = W_U a (+ b), per-row top-k ids and log-probs.
+
+    [E3] "Output path to LM head": logits_i = W_LM a_i + b_LM (bias if
+    present), tokens drawn from softmax(logits / T).  [E1] "Tree-Structured
+    Draft Generation": in greedy mode the top-k tokens become child nodes.
+    [M7.5] 0x06B: a child's confidence is its conditional probability under
+    the parent's prefix, normalised over the whole vocabulary ("omitted
+    vocabulary mass is allowed").  Readings: top-k order is z descending with
+    ties to the lower id; log-prob = z/T - logsumexp(z/T) over all V.
+
+    x [M, d]; w_lm [V, d]; bias [V] or None; rows: optional row subset.
+    Returns dict(ids [M,k] int64, logprobs [M,k], row_max [M] = max z/T,
+    row_sumexp [M] = sum exp(z/T - row_max), z [M, V] fp64).
+    """
+    if not (1 <= k):
+        raise ValueError("k must be >= 1")
+    if not temperature > 0:
+        raise ValueError("temperature must be > 0")
+    x = np.asarray(x, np.float64)
+    if rows is not None:
+        x = x[np.asarray(rows)]
+    w = np.asarray(w_lm, np.float64)
+    V = w.shape[0]
+    if k > V:
+        raise ValueError("k must not exceed V")
+    z = x @ w.T
+    if bias is not None:
+        z = z + np.asarray(bias, np.float64)[None, :]
+    y = z / temperature
+    m = y.max(axis=1)
+    s = np.exp(y - m[:, None]).sum(axis=1)
+    lse = m + np.log(s)
+    vid = np.arange(V)
+    ids = np.empty((z.shape[0], k), dtype=np.int64)
+    for i in range(z.shape[0]):
+        ids[i] = np.lexsort((vid, -z[i]))[:k]
+    logprobs = np.take_along_axis(y, ids, axis=1) - lse[:, None]
+    return dict(ids=ids, logprobs=logprobs, row_max=m, row_sumexp=s, z=z)
+
+
+# ---------------------------------------------------------------------------
+# a4/a5: EAGLE-2 dynamic tree expansion, rerank and flatten
+# ---------------------------------------------------------------------------
+
+EPSILON = 1e-12
+LOG_EPS32 = np.float32(math.log(EPSILON))  # ranking floor log(1e-12) in fp32
+MASS_TOL = 1e-4  # sibling-mass slack for fp32 log-probabilities (reading)
+
+
+def _key(st, n):
+    """Ranking key (-log V, depth, node_id) of [M7.5] 0x06B (fp32 log V)."""
+    return (-float(st["logv"][n]), st["depth"][n], n)
+
+
+def tree_expand_init(root_token):
+    """Tree store holding only the seed: depth 0, log path value 0, node_id 0.
+
+    [M7.5] 0x06B: the seed is the context anchor at depth zero with log path
+    value zero and is not counted in the verification budget.
+    """
+    return dict(parent=[-1], token=[int(root_token)], logv=[np.float32(0.0)],
+                depth=[0], frontier=[0])
+
+
+def tree_expand_step(st, cand_ids, cand_logprobs, width):
+    """One expansion step of EAGLE-2 ([M7.5] 0x06A, 0x06B).
+
+    ``st["frontier"]`` is the list of expandable parents (node ids, in key
+    order) that the drafter was run on; row j of ``cand_ids`` /
+    ``cand_logprobs`` [n_par, k] holds the top-k children of frontier[j] with
+    their log conditional probabilities.  Every child becomes a stored node:
+        log V(child) = log V(parent) + log max(c, 1e-12)      (fp32)
+    with log c clamped to <= 0, depth = parent depth + 1 and node ids in
+    creation order (parent slot, then child rank); an id < 0 marks a missing
+    alternative and creates no node.  The next expandable set is
+    the top-``width`` of the new nodes by (-log V, depth, node_id).
+
+    Validation follows the pages' eagle2_tree checks: finite probabilities
+    (log-prob NaN or +inf rejected), no duplicate token under one parent,
+    sibling mass <= 1 (with MASS_TOL slack for fp32 inputs).
+    Returns the new expandable list (also stored in st["frontier"]).
+    """
+    if type(width) is not int or width < 1:
+        raise ValueError("expansion width must be a positive integer")
+    cand_ids = np.asarray(cand_ids)
+    cand_lp = np.asarray(cand_logprobs, dtype=np.float32)
+    parents = list(st["frontier"])
+    if cand_ids.shape[0] < len(parents) or cand_lp.shape != cand_ids.shape:
+        raise ValueError("need one candidate row per expandable parent")
+    new = []
+    for j, p in enumerate(parents):
+        seen = set()
+        mass = 0.0
+        for i in range(cand_ids.shape[1]):
+            tok = int(cand_ids[j, i])
+            if tok < 0:  # fewer than k alternatives for this parent
+                continue
+            lp = cand_lp[j, i]
+            if np.isnan(lp) or lp == np.inf:
+                raise ValueError("confidence must be a finite probability")
+            if tok in seen:
+                raise ValueError("duplicate token alternative under one parent")
+            seen.add(tok)
+            lp = min(lp, np.float32(0.0))
+            mass += math.exp(float(lp))
+            if mass > 1.0 + MASS_TOL:
+                raise ValueError("sibling probability mass exceeds one")
+            term = max(lp, LOG_EPS32)
+            logv = np.float32(st["logv"][p] + term)  # one fp32 addition
+            n = len(st["parent"])
+            st["parent"].append(p)
+            st["token"].append(tok)
+            st["logv"].append(logv)
+            st["depth"].append(st["depth"][p] + 1)
+            new.append(n)
+    st["frontier"] = sorted(new, key=lambda n: _key(st, n))[:width]
+    return list(st["frontier"])
+
+
+def tree_expand_finalize(st, budget, ctx_len=0, R_out=None):
+    """Global rerank + flatten ([M7.5] 0x06A, 0x06B, 0x05C).
+
+    selected = the first ``budget`` non-root nodes in (-log V, depth, node_id)
+    order; because a child's value never exceeds its parent's and ties go to
+    the shallower node, every prefix of that order is ancestor-closed, so no
+    ancestors are added afterwards.  Flattened rows: row 0 = seed, row i =
+    selected[i-1]; parent_row = row of the parent (seed -> 0); depth; position
+    = ctx_len + depth ([M7.5] 0x05C ancestry-aware positions); mask = ancestry
+    bits (see ``ancestor_mask``); node_id = retrieve map from row to node.
+    Rows past n_rows (when R_out is larger) are padding: token -1,
+    parent_row -1, depth 0, position ctx_len, node_id -1, mask = own bit.
+    """
+    for value in (budget,):
+        if type(value) is not int or value < 0:
+            raise ValueError("verification budget must be a nonnegative integer")
+    nodes = list(range(1, len(st["parent"])))
+    selected = sorted(nodes, key=lambda n: _key(st, n))[:budget]
+    n_rows = 1 + len(selected)
+    R = n_rows if R_out is None else int(R_out)
+    if R < n_rows:
+        raise ValueError("R_out smaller than 1 + budget")
+    row_of = {0: 0}
+    for i, n in enumerate(selected):
+        row_of[n] = i + 1
+    token = np.full(R, -1, np.int64)
+    parent_row = np.full(R, -1, np.int64)
+    depth = np.zeros(R, np.int64)
+    node_id = np.full(R, -1, np.int64)
+    token[0] = st["token"][0]
+    node_id[0] = 0
+    for i, n in enumerate(selected):
+        p = st["parent"][n]
+        if p not in row_of or row_of[p] >= i + 1:
+            raise AssertionError("selection is not ancestor-closed")
+        token[i + 1] = st["token"][n]
+        parent_row[i + 1] = row_of[p]
+        depth[i + 1] = st["depth"][n]
+        node_id[i + 1] = n
+    mask = ancestor_mask(parent_row, n_rows) if R <= 64 else None
+    position = ctx_len + depth
+    return dict(token=token, parent_row=parent_row, depth=depth, mask=mask,
+                node_id=node_id, position=position, n_rows=n_rows)
+
+
+def eagle2_tree(draft, root_token, expand_width, verify_budget, max_depth, ctx_len=0):
+    """The pages' eagle2_tree composition ([M7.5] 0x06B) over a ``draft``
+    callback: draft(step, parents) -> (cand_ids [len(parents), k],
+    cand_logprobs [len(parents), k]).  Returns (flat tree dict, tree store)."""
+    if type(expand_width) is not int or expand_width < 1:
+        raise ValueError("expansion width must be a positive integer")
+    for value in (verify_budget, max_depth):
+        if type(value) is not int or value < 0:
+            raise ValueError("verification budget and depth must be nonnegative integers")
+    st = tree_expand_init(root_token)
+    if verify_budget == 0:
+        return tree_expand_finalize(st, 0, ctx_len), st
+    for step in range(max_depth):
+        if not st["frontier"]:
+            break
+        ids, lps = draft(step, list(st["frontier"]))
+        tree_expand_step(st, ids, lps, expand_width)
+    return tree_expand_finalize(st, verify_budget, ctx_len), st
+
+
+# ---------------------------------------------------------------------------
+# a6/a7: lossless tree verification
+# ---------------------------------------------------------------------------
+
+
+def _softmax64(row, temperature):
+    y = np.asarray(row, np.float64) / temperature
+    y = y - y.max()
+    w = np.exp(y)
+    return w / w.sum()
+
+
+def _argmax_low(row):
+    row = np.asarray(row)
+    return int(np.flatnonzero(row == row.max())[0])
+
+
+def tree_verify(parent_row, token, temperature, max_depth, n_rows=None,
+                target_logits=None, target_argmax=None, draft_logits=None,
+                mode="deterministic", seed=0, offset=0, accept_u=None, race_u=None):
+    """Tree verification: greedy longest accepted path, or multi-round
+    speculative sampling with residual correction.
+
+    [E1] "Verification Phase: Multi-Round Speculative Sampling on Trees"
+    (the paper's Algorithm 1): the candidates under one node are tried in
+    order; candidate t_i is accepted when r < p(t_i) / p_hat_i(t_i) with
+    r ~ U(0,1); after a rejection p <- norm(max(0, p - p_hat_i)) (read as the
+    vector update: the page prints it garbled as a scalar); if every candidate
+    is rejected a token is drawn from the final p.  [E3] "Stage 2:
+    Verification" gives the same min(1, p/p_hat) rule.  At T = 0 p is the
+    one-hot argmax of the target logits (lowest id on ties), which reduces the
+    walk to "accept the child whose token is the parent row's argmax".
+
+    Target logits row r give the distribution of the children of row r.
+    ``mode``:
+      * "deterministic" (default; EAGLE-2 trees are deterministic top-k, not
+        draws): proposal of each candidate is the point mass on its token, so
+        accept iff u < p(t) and on rejection p loses t and is renormalised;
+      * "sampled": the siblings were i.i.d. draws from q = softmax(draft
+        logits of the parent row / T): Algorithm 1 verbatim with p_hat = q.
+    Readings: the children of a row are tried in row order; a residual whose
+    mass is zero leaves p unchanged; the final draw is an exponential race
+    argmax_y (log w_y - log(-log u_y)) over allowed ids (ties to lower id).
+
+    Uniforms come from ``oracle.philox`` (accept test per row, race per id) or
+    from ``accept_u`` [B,R] / ``race_u`` callable(b) -> [V] overrides.
+    Returns dict(accept_len [B], path_rows [B, max_depth+1] (row 0 first,
+    -1 padded), out_tokens [B, max_depth+1] (accepted tokens then the bonus
+    token, -1 padded), margins: list of (kind, b, |decision margin|)).
+    """
+    parent_row = np.asarray(parent_row)
+    token = np.asarray(token)
+    B, R = parent_row.shape
+    greedy = temperature == 0
+    if temperature < 0 or not math.isfinite(temperature):
+        raise ValueError("temperature must be finite and >= 0")
+    if mode not in ("deterministic", "sampled"):
+        raise ValueError("unknown proposal mode")
+    if mode == "sampled" and (greedy or draft_logits is None):
+        raise ValueError("sampled proposals need T > 0 and draft logits")
+    if greedy and target_logits is None and target_argmax is None:
+        raise ValueError("greedy verification needs target logits or argmax")
+    if not greedy and target_logits is None:
+        raise ValueError("stochastic verification needs target logits")
+    if accept_u is None and not greedy:
+        accept_u = accept_uniforms(seed, offset, B, R)
+    V = None if target_logits is None else np.asarray(target_logits).shape[2]
+
+    accept_len = np.zeros(B, np.int64)
+    path_rows = np.full((B, max_depth + 1), -1, np.int64)
+    out_tokens = np.full((B, max_depth + 1), -1, np.int64)
+    margins = []
+    for b in range(B):
+        n = R if n_rows is None else int(n_rows[b])
+        if not 1 <= n <= R or parent_row[b, 0] != -1:
+            raise ValueError("row 0 must be the root and 1 <= n_rows <= R")
+        for i in range(1, n):
+            if not 0 <= parent_row[b, i] < i:
+                raise ValueError("parent_row must be topological")
+        cur = 0
+        path = [0]
+        toks = []
+        while True:
+            children = [c for c in range(cur + 1, n) if parent_row[b, c] == cur]
+            accepted = None
+            if greedy:
+                a = (int(target_argmax[b, cur]) if target_argmax is not None
+                     else _argmax_low(target_logits[b, cur]))
+                for c in children:
+                    if int(token[b, c]) == a:
+                        accepted = c
+                        break
+                bonus_dist = None
+            else:
+                p = _softmax64(target_logits[b, cur], temperature)
+                q = (_softmax64(draft_logits[b, cur], temperature)
+                     if mode == "sampled" else None)
+                for c in children:
+                    t = int(token[b, c])
+                    u = float(accept_u[b, c])
+                    if mode == "deterministic":
+                        ratio = p[t]
+                    else:
+                        ratio = p[t] / q[t] if q[t] > 0 else (math.inf if p[t] > 0 else 0.0)
+                    margins.append(("accept", b, abs(u - ratio) if math.isfinite(ratio) else math.inf))
+                    if u < ratio:
+                        accepted = c
+                        break
+                    if mode == "deterministic":
+                        res = p.copy()
+                        res[t] = 0.0
+                    else:
+                        res = np.maximum(0.0, p - q)
+                    mass = res.sum()
+                    if mass > 0:
+                        p = res / mass
+                bonus_dist = p
+            if accepted is None:
+                if greedy:
+                    bonus = a
+                else:
+                    ur = race_u(b) if race_u is not None else race_uniforms(seed, offset, b, V)
+                    with np.errstate(divide="ignore"):
+                        keyv = np.where(bonus_dist > 0,
+                                        np.log(bonus_dist) - np.log(-np.log(ur)), -np.inf)
+                    bonus = _argmax_low(keyv)
+                    top2 = np.sort(keyv)[-2:]
+                    margins.append(("race", b, float(top2[1] - top2[0])))
+                toks.append(bonus)
+                break
+            if len(path) > max_depth:
+                raise ValueError("tree deeper than max_depth")
+            path.append(accepted)
+            toks.append(int(token[b, accepted]))
+            cur = accepted
+        accept_len[b] = len(path) - 1
+        path_rows[b, :len(path)] = path
+        out_tokens[b, :len(toks)] = toks
+    return dict(accept_len=accept_len, path_rows=path_rows, out_tokens=out_tokens,
+                margins=margins)
