@@ -1,0 +1,280 @@
+/*
+ * eagle.h -- C-ABI of the GB300 (sm_103a) EAGLE speculative-decoding hot path.
+ *
+ * One tree-verify round of EAGLE-family speculative decoding is served by
+ * six calls:
+ *   eagle_fuse_proj             EAGLE-3 fused feature g = W_proj [h_low; h_mid; h_high]
+ *   eagle_tree_attn             tree-masked attention vs a paged KV cache + the tree rows
+ *   eagle_lmhead_topk           LM-head GEMM with fused per-row top-k and log-softmax
+ *   eagle_tree_expand           one EAGLE-2 dynamic-tree expansion step
+ *   eagle_tree_expand_finalize  EAGLE-2 global rerank + flatten (rows, mask, positions)
+ *   eagle_tree_verify           lossless verification (greedy / rejection sampling)
+ *
+ * Sources (web pages cited by title and section):
+ *   [E3]   "EAGLE-3: Scaling up Inference Acceleration of Large Language Models
+ *          via Training-Time Test" (paper summary)
+ *   [E1]   "EAGLE: Speculative Sampling Requires Rethinking Feature Uncertainty"
+ *          (paper summary)
+ *   [M7.5] "M7.5 - EAGLE Feature Drafting: Uncertainty, Dynamic Trees, HASS,
+ *          and EAGLE-3"
+ *   [BLOG] "EAGLE-3: Why the Best Draft Models Stopped Predicting Features"
+ *
+ * Conventions shared by every call
+ *   - All array arguments are DEVICE pointers to contiguous row-major arrays
+ *     owned by the caller.  The library never allocates or frees memory;
+ *     scratch space comes from a caller buffer `ws` of at least the size
+ *     returned by the matching *_workspace_size() query.
+ *   - Matrix operands read by TMA (weights, activations) must be 16-byte
+ *     aligned; leading dimensions are given by the shapes.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous, never synchronise, keep no state between calls, and may be
+ *     issued from several host threads on different streams and buffers.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned as eagle_status.  Errors that only the device can see (a
+ *     malformed tree, a non-finite value, a timed-out wait) are written to the
+ *     optional `dev_status` word (first error wins; 0 = OK); pass NULL to skip.
+ *     A timed-out wait never hangs the device: the kernel records
+ *     EAGLE_ERR_TIMEOUT, drains its in-flight copies, frees its tensor memory
+ *     and returns.
+ */
+#ifndef EAGLE_GB300_EAGLE_H
+#define EAGLE_GB300_EAGLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum ...     */
+  EAGLE_ERR_UNSUPPORTED = 2, /* shape or dtype outside the kernels' limits     */
+  EAGLE_ERR_WORKSPACE = 3,   /* ws too small or misaligned                      */
+  EAGLE_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed     */
+  EAGLE_ERR_BAD_TREE = 5,    /* device: non-topological parents, duplicate
+                                sibling token, sibling mass > 1, too deep      */
+  EAGLE_ERR_BAD_KV = 6,      /* device: page id out of range                    */
+  EAGLE_ERR_NONFINITE = 7,   /* device: NaN / +inf where a probability is read */
+  EAGLE_ERR_TIMEOUT = 8      /* device: a bounded wait ran out                  */
+} eagle_status;
+
+typedef enum { EAGLE_FP32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
+
+typedef enum {
+  EAGLE_PROPOSAL_DETERMINISTIC = 0, /* children are deterministic top-k       */
+  EAGLE_PROPOSAL_SAMPLED = 1        /* children are i.i.d. draws from q       */
+} eagle_proposal;
+
+/* Human-readable name of a status code (static string). */
+const char* eagle_status_string(int status);
+
+/* Synchronises `stream`, copies *dev_status to *host_status and returns it
+ * as an eagle_status (test helper; the only call that synchronises). */
+int eagle_read_status(const int32_t* dev_status, void* stream, int32_t* host_status);
+
+/* Number of kernels this library has launched in this process (counter for
+ * benchmarks; incremented on every launch, never reset). */
+uint64_t eagle_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * eagle_fuse_proj -- EAGLE-3 multi-layer feature fusion.
+ *   g[i, o] = sum_c W[o, c] h_low[i, c] + W[o, d+c] h_mid[i, c]
+ *             + W[o, 2d+c] h_high[i, c]  (+ bias[o])
+ * [E3] section 3.4 "Change 2: The fusion FC layer" (concatenate l, m, h into
+ * 3k and project back to k; bias optional); [M7.5] section 0x08B
+ * "Multi-Layer Feature Fusion" (r_t = W_R [f_low; f_mid; f_high],
+ * W_R in R^{d x 3d}); [BLOG] "What EAGLE-3 changes" (g_t = W_proj @ concat).
+ *
+ *   h_low, h_mid, h_high : [M, d]   activations of dtype `dtype`
+ *   w_proj               : [d, 3d]  row o = output feature o (out x in)
+ *   bias                 : [d] fp32, or NULL
+ *   g                    : [M, d]   output, dtype `dtype`
+ * The concatenation is never materialised: the K loop walks the three inputs.
+ * fp32 runs on the TF32 tensor-core kind; bf16 accumulates in fp32.
+ * Limits: 1 <= M <= 4096, d % 128 == 0, d <= 16384.
+ * ---------------------------------------------------------------------- */
+size_t eagle_fuse_proj_workspace_size(int M, int d, int dtype);
+int eagle_fuse_proj(const void* h_low, const void* h_mid, const void* h_high,
+                    const void* w_proj, const float* bias, void* g, int M, int d,
+                    int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
+                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_attn -- attention of the tree rows against the committed prefix
+ * (read through a page table) plus the visible tree rows.
+ *   For tree row r of request b and query head h (kv head h / (Hq/Hkv)):
+ *     keys = prefix tokens 0..ctx_lens[b]-1 followed by tree rows j whose bit
+ *            j is set in tree_mask[b, r];
+ *     out[b, r, h] = softmax(scale * q k^T) v over those keys;
+ *     lse[b, r, h] = natural-log sum of exp(scale * q k^T) over those keys.
+ * [M7.5] section 0x08C "Training-Time Test": A(u, v) = 1 iff v is in
+ * TargetPrefix(u), DraftAncestors(u) or {u}; [E1] "Tree-Structured Draft
+ * Generation": each node attends only to its ancestors; [E3] "The Attention
+ * Mechanism Modifications": never to tokens in other branches.
+ *
+ *   q            : [B, R, Hq, D]       (positions already applied)
+ *   k_tree, v_tree : [B, R, Hkv, D]    the tree's own K/V rows
+ *   k_cache, v_cache : [P, page_size, Hkv, D]  paged committed prefix
+ *   num_pages    : P (pool size), for page-id range checks (EAGLE_ERR_BAD_KV)
+ *   block_table  : [B, max_pages] int32 page ids (entries past the prefix unused)
+ *   ctx_lens     : [B] int32, 0 <= ctx_lens[b] <= max_pages * page_size
+ *   tree_mask    : [B, R] uint64, bit j = row j visible (self bit required)
+ *   out          : [B, R, Hq, D] dtype `dtype`;  lse: [B, R, Hq] fp32 or NULL
+ *   scale        : score scale (pass 1/sqrt(D) for the standard one)
+ *   num_splits   : split-KV factor (0 = choose from the SM count)
+ * Limits: R <= 64, D in {64, 128}, page_size == 16, Hq % Hkv == 0,
+ * Hq / Hkv <= 16.
+ * ---------------------------------------------------------------------- */
+size_t eagle_tree_attn_workspace_size(int B, int R, int Hq, int Hkv, int D,
+                                      int max_pages, int page_size, int num_splits,
+                                      int dtype);
+int eagle_tree_attn(const void* q, const void* k_tree, const void* v_tree,
+                    const void* k_cache, const void* v_cache, int num_pages,
+                    const int32_t* block_table, int max_pages, const int32_t* ctx_lens,
+                    const uint64_t* tree_mask, void* out, float* lse, int B, int R,
+                    int Hq, int Hkv, int D, int page_size, float scale, int num_splits,
+                    int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
+                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_lmhead_topk -- vocabulary logits and per-row top-k, fused.
+ *   z[i, v] = sum_c W_U[v, c] x[i, c] (+ bias[v])
+ *   topk_ids[i, :]      = the k ids of largest z (z descending, ties to the
+ *                         lower id)
+ *   topk_logprobs[i, j] = z[i, id_j]/T - logsumexp_v(z[i, v]/T)
+ *   row_max[i]          = max_v z[i, v]/T;  row_sumexp[i] = sum_v exp(z/T - row_max)
+ * Full-vocabulary logits are never written to memory.
+ * [E3] "Output path to LM head" (logits = W_LM a + b_LM, bias if present);
+ * [E1] "Tree-Structured Draft Generation" (greedy: top-k tokens become the
+ * children); [M7.5] section 0x06B (confidence = conditional token probability
+ * under the parent's prefix; omitted vocabulary mass allowed).
+ *
+ *   x            : [M, d] dtype `dtype`;  w_lm: [V, d] dtype `dtype`
+ *   bias         : [V] fp32 or NULL
+ *   topk_ids     : [M, k] int32;  topk_logprobs: [M, k] fp32
+ *   row_max, row_sumexp : [M] fp32 or NULL
+ * Limits: 1 <= M <= 2048, 1 <= k <= 32, k <= V, d % 64 == 0,
+ * V % 128 == 0, temperature > 0.
+ * ---------------------------------------------------------------------- */
+size_t eagle_lmhead_topk_workspace_size(int M, int d, int V, int k, int dtype);
+int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M, int d,
+                      int V, int k, float temperature, int32_t* topk_ids,
+                      float* topk_logprobs, float* row_max, float* row_sumexp, int dtype,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_expand -- one EAGLE-2 expansion step for B requests.
+ * [M7.5] section 0x06A "Path Value Derivation" and 0x06B "Expansion And
+ * Reranking": every child of an expanded parent is stored with
+ *   log V(child) = log V(parent) + log max(c, 1e-12)     (fp32)
+ * (c = exp(logprob), logprob clamped to <= 0), depth = parent depth + 1 and a
+ * creation-ordered node id; only the new nodes form the next frontier, and
+ * the next nodes to expand are its top `width` by the key
+ * (-log V, depth, node_id).
+ *
+ *   step          : 0 initialises the store with the seed (node 0: parent -1,
+ *                   token root_token[b], log V 0, depth 0) and expands it.
+ *   cand_ids      : [B, P, k] int32 top-k ids per expanded parent, P = 1 at
+ *                   step 0, else `width`; row j belongs to frontier[b, j]
+ *                   (rows j >= n_frontier[b] are ignored); an id < 0 marks a
+ *                   missing alternative (no node is created).
+ *   cand_logprobs : [B, P, k] fp32 log conditional probabilities.
+ *   root_token    : [B] int32 (read at step 0 only)
+ *   node_parent, node_token, node_depth : [B, max_nodes] int32 tree store
+ *   node_logv     : [B, max_nodes] fp32
+ *   node_count    : [B] int32 nodes stored (seed included)
+ *   frontier      : [B, width] int32 in/out: parents expanded by this step on
+ *                   entry, the next parents to expand (key order) on exit
+ *   n_frontier    : [B] int32 in/out: valid entries of frontier
+ * Device-detected: duplicate id under one parent, sibling probability mass
+ * above 1 (+1e-4 slack for fp32) -> EAGLE_ERR_BAD_TREE; NaN or +inf
+ * log-prob -> EAGLE_ERR_NONFINITE (the request's step is then skipped).
+ * Limits: width <= 64, k <= 32, width*k <= 1024, max_nodes <= 4096, and
+ * max_nodes >= 1 + k + step*width*k (checked on the host).
+ * ---------------------------------------------------------------------- */
+int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
+                      const int32_t* cand_ids, const float* cand_logprobs,
+                      const int32_t* root_token, int32_t* node_parent,
+                      int32_t* node_token, float* node_logv, int32_t* node_depth,
+                      int32_t* node_count, int32_t* frontier, int32_t* n_frontier,
+                      int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_expand_finalize -- EAGLE-2 rerank, then flatten for verification.
+ * [M7.5] section 0x06B: selected = the first `budget` non-seed nodes in
+ * (-log V, depth, node_id) order; since a child never outranks its parent
+ * the selection is ancestor-closed with no repair.  [M7.5] section 0x05C
+ * "Target Verification": the selection is flattened with ancestry-aware
+ * positions and a tree mask; section 0x09: a retrieve map ties rows to nodes.
+ *
+ *   Output rows per request: R (>= 1 + budget, <= 64).  Row 0 = seed,
+ *   row i = i-th selected node.  Rows >= n_rows[b] are padding (token -1,
+ *   parent_row -1, depth 0, mask = own bit, node_id -1, position ctx).
+ *   token, parent_row, depth, node_id, position : [B, R] int32
+ *   mask        : [B, R] uint64 (bit j = row j is the row itself or an ancestor)
+ *   n_rows      : [B] int32 = 1 + min(budget, node_count[b] - 1)
+ *   ctx_lens    : [B] int32 (positions = ctx_lens[b] + depth), or NULL (0)
+ * Device-detected: a selected node whose parent is not selected before it
+ * -> EAGLE_ERR_BAD_TREE.  Limits: max_nodes <= 4096.
+ * ---------------------------------------------------------------------- */
+int eagle_tree_expand_finalize(int B, int max_nodes, int budget, int R,
+                               const int32_t* node_parent, const int32_t* node_token,
+                               const float* node_logv, const int32_t* node_depth,
+                               const int32_t* node_count, const int32_t* ctx_lens,
+                               int32_t* token, int32_t* parent_row, int32_t* depth,
+                               uint64_t* mask, int32_t* node_id, int32_t* position,
+                               int32_t* n_rows, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_verify -- lossless acceptance of a flattened draft tree.
+ * [E1] "Verification Phase: Multi-Round Speculative Sampling on Trees"
+ * (Algorithm 1): candidates under a node are tried in order, t_i accepted
+ * when r < p(t_i)/p_hat_i(t_i); after a rejection p <- norm(max(0, p -
+ * p_hat_i)); if all are rejected a token is drawn from the final p.  [E3]
+ * "Stage 2: Verification".  The target logits of row r give the distribution
+ * p of the children of row r (softmax of z/T).
+ *   temperature == 0 : greedy; p = one-hot(argmax z) (ties to the lower id),
+ *                      i.e. accept the child whose token is the argmax.
+ *   DETERMINISTIC    : the children are deterministic top-k (EAGLE-2); the
+ *                      proposal of a child is the point mass on its token, so
+ *                      accept iff u < p(t), and a rejected token is removed
+ *                      from p, which is renormalised.
+ *   SAMPLED          : Algorithm 1 with p_hat = softmax(draft logits / T)
+ *                      (children i.i.d. from it).  Not yet available on the
+ *                      GPU: returns EAGLE_ERR_UNSUPPORTED.
+ * The final draw is an exponential race argmax_y (z_y/T - log(-log u_y)) over
+ * the ids not rejected at the stop row.
+ * Uniforms: Philox4x32-10 (Salmon et al., SC'11), key = seed; accept test of
+ * row i of request b = word 0 at counter (i, b, 2*offset_hi, offset_lo); race
+ * uniform of id y = word (y & 3) at counter (y >> 2, b, 2*offset_hi + 1,
+ * offset_lo); u = (2*(x >> 9) + 1) * 2^-24.  `uniforms_override` [B, R]
+ * replaces the accept-test uniforms when non-NULL.
+ *
+ *   parent_row, token : [B, R] int32 (row 0 = seed with parent -1;
+ *                       0 <= parent_row[i] < i), n_rows: [B] int32 or NULL (= R)
+ *   target_logits     : [B, R, V] fp32 (may be NULL when temperature == 0 and
+ *                       target_argmax is given)
+ *   target_argmax     : [B, R] int32 or NULL
+ *   accept_len        : [B] int32 accepted drafted nodes
+ *   path_rows         : [B, max_depth+1] int32, row 0 then the accepted rows
+ *   out_tokens        : [B, max_depth+1] int32, accepted tokens then the
+ *                       bonus token; unused entries -1
+ * Device-detected: non-topological parents, path deeper than max_depth ->
+ * EAGLE_ERR_BAD_TREE; NaN in a read logit row -> EAGLE_ERR_NONFINITE.
+ * Limits: R <= 1024, V >= 2, max_depth <= 64, offset < 2^63.
+ * ---------------------------------------------------------------------- */
+size_t eagle_tree_verify_workspace_size(int B, int R, int V);
+int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row, const int32_t* token,
+                      const int32_t* n_rows, const float* target_logits,
+                      const int32_t* target_argmax, const float* draft_logits,
+                      float temperature, int proposal_mode, uint64_t seed, uint64_t offset,
+                      const float* uniforms_override, int max_depth, int32_t* accept_len,
+                      int32_t* path_rows, int32_t* out_tokens, void* ws, size_t ws_bytes,
+                      int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_GB300_EAGLE_H */
