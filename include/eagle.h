@@ -191,7 +191,7 @@ int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M,
  * Device-detected: duplicate id under one parent, sibling probability mass
  * above 1 (+1e-4 slack for fp32) -> EAGLE_ERR_BAD_TREE; NaN or +inf
  * log-prob -> EAGLE_ERR_NONFINITE (the request's step is then skipped).
- * Limits: width <= 64, k <= 32, width*k <= 1024, max_nodes <= 4096, and
+ * Limits: width <= 64, k <= 32, width*k <= 1024, max_nodes <= 2048, and
  * max_nodes >= 1 + k + step*width*k (checked on the host).
  * ---------------------------------------------------------------------- */
 int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
@@ -217,7 +217,7 @@ int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
  *   n_rows      : [B] int32 = 1 + min(budget, node_count[b] - 1)
  *   ctx_lens    : [B] int32 (positions = ctx_lens[b] + depth), or NULL (0)
  * Device-detected: a selected node whose parent is not selected before it
- * -> EAGLE_ERR_BAD_TREE.  Limits: max_nodes <= 4096.
+ * -> EAGLE_ERR_BAD_TREE.  Limits: max_nodes <= 2048.
  * ---------------------------------------------------------------------- */
 int eagle_tree_expand_finalize(int B, int max_nodes, int budget, int R,
                                const int32_t* node_parent, const int32_t* node_token,
