@@ -1,0 +1,210 @@
+"""Thin ctypes binding of libeagle_gb300.so (include/eagle.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the current CUDA device, passes their data pointers, shapes and the
+current stream to the C entry point of the same name, and raises if the call
+returns an error.  No computation happens here and there is no fallback: if
+the library is missing, the first call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libeagle_gb300.so")
+
+EAGLE_FP32, EAGLE_BF16 = 0, 1
+EAGLE_PROPOSAL_DETERMINISTIC, EAGLE_PROPOSAL_SAMPLED = 0, 1
+STATUS = {0: "EAGLE_OK", 1: "EAGLE_ERR_INVALID_ARG", 2: "EAGLE_ERR_UNSUPPORTED",
+          3: "EAGLE_ERR_WORKSPACE", 4: "EAGLE_ERR_CUDA", 5: "EAGLE_ERR_BAD_TREE",
+          6: "EAGLE_ERR_BAD_KV", 7: "EAGLE_ERR_NONFINITE", 8: "EAGLE_ERR_TIMEOUT"}
+
+_P, _I, _F, _Z, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+
+_SIGS = {
+    "eagle_status_string": (ctypes.c_char_p, [_I]),
+    "eagle_read_status": (_I, [_P, _P, _P]),
+    "eagle_launch_count": (_U64, []),
+    "eagle_fuse_proj_workspace_size": (_Z, [_I, _I, _I]),
+    "eagle_fuse_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
+    "eagle_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "eagle_tree_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                             _I, _F, _I, _I, _P, _Z, _P, _P]),
+    "eagle_lmhead_topk_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "eagle_lmhead_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
+    "eagle_tree_expand": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "eagle_tree_expand_finalize": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P, _P, _P, _P]),
+    "eagle_tree_verify_workspace_size": (_Z, [_I, _I, _I]),
+    "eagle_tree_verify": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _F, _I, _U64, _U64, _P, _I, _P,
+                               _P, _P, _P, _Z, _P, _P]),
+}
+
+_lib = None
+
+
+class EagleError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+def lib():
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t):
+    if t.dtype == torch.bfloat16:
+        return EAGLE_BF16
+    if t.dtype == torch.float32:
+        return EAGLE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(fn, code):
+    if code != 0:
+        raise EagleError(fn, code)
+
+
+def workspace(nbytes, device=None):
+    """A caller-owned device buffer of at least ``nbytes`` (torch allocation)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def launch_count():
+    return int(lib().eagle_launch_count())
+
+
+def read_status(status, stream=None):
+    host = ctypes.c_int32(0)
+    lib().eagle_read_status(_ptr(status), _stream(stream), ctypes.byref(host))
+    return int(host.value)
+
+
+# ------------------------------------------------------------------ a1
+def eagle_fuse_proj_workspace_size(M, d, dtype):
+    return int(lib().eagle_fuse_proj_workspace_size(M, d, dtype))
+
+
+def eagle_fuse_proj(h_low, h_mid, h_high, w_proj, g, bias=None, ws=None, status=None, stream=None):
+    M, d = h_low.shape
+    dt = _dtype(h_low)
+    if ws is None:
+        ws = workspace(eagle_fuse_proj_workspace_size(M, d, dt), h_low.device)
+    _check("eagle_fuse_proj", lib().eagle_fuse_proj(
+        _ptr(h_low), _ptr(h_mid), _ptr(h_high), _ptr(w_proj), _ptr(bias), _ptr(g), M, d, dt,
+        _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return g
+
+
+# ------------------------------------------------------------------ a2
+def eagle_tree_attn_workspace_size(B, R, Hq, Hkv, D, max_pages, page_size=16, num_splits=0,
+                                   dtype=EAGLE_BF16):
+    return int(lib().eagle_tree_attn_workspace_size(B, R, Hq, Hkv, D, max_pages, page_size,
+                                                    num_splits, dtype))
+
+
+def eagle_tree_attn(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, tree_mask, out,
+                    lse=None, scale=None, num_splits=0, ws=None, status=None, stream=None):
+    B, R, Hq, D = q.shape
+    Hkv = k_tree.shape[2]
+    P, page = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    dt = _dtype(q)
+    if scale is None:
+        scale = D ** -0.5
+    if ws is None:
+        ws = workspace(eagle_tree_attn_workspace_size(B, R, Hq, Hkv, D, max_pages, page, num_splits,
+                                                      dt), q.device)
+    _check("eagle_tree_attn", lib().eagle_tree_attn(
+        _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache), _ptr(v_cache), P, _ptr(block_table),
+        max_pages, _ptr(ctx_lens), _ptr(tree_mask), _ptr(out), _ptr(lse), B, R, Hq, Hkv, D, page,
+        float(scale), num_splits, dt, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ a3
+def eagle_lmhead_topk_workspace_size(M, d, V, k, dtype):
+    return int(lib().eagle_lmhead_topk_workspace_size(M, d, V, k, dtype))
+
+
+def eagle_lmhead_topk(x, w_lm, k, topk_ids, topk_logprobs, temperature=1.0, bias=None,
+                      row_max=None, row_sumexp=None, ws=None, status=None, stream=None):
+    M, d = x.shape
+    V = w_lm.shape[0]
+    dt = _dtype(x)
+    if ws is None:
+        ws = workspace(eagle_lmhead_topk_workspace_size(M, d, V, k, dt), x.device)
+    _check("eagle_lmhead_topk", lib().eagle_lmhead_topk(
+        _ptr(x), _ptr(w_lm), _ptr(bias), M, d, V, k, float(temperature), _ptr(topk_ids),
+        _ptr(topk_logprobs), _ptr(row_max), _ptr(row_sumexp), dt, _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+    return topk_ids, topk_logprobs
+
+
+# ------------------------------------------------------------------ a4 / a5
+def eagle_tree_expand(step, width, cand_ids, cand_logprobs, root_token, node_parent, node_token,
+                      node_logv, node_depth, node_count, frontier, n_frontier, status=None,
+                      stream=None):
+    B, max_nodes = node_parent.shape
+    k = cand_ids.shape[-1]
+    _check("eagle_tree_expand", lib().eagle_tree_expand(
+        B, step, width, k, max_nodes, _ptr(cand_ids), _ptr(cand_logprobs), _ptr(root_token),
+        _ptr(node_parent), _ptr(node_token), _ptr(node_logv), _ptr(node_depth), _ptr(node_count),
+        _ptr(frontier), _ptr(n_frontier), _ptr(status), _stream(stream)))
+
+
+def eagle_tree_expand_finalize(budget, node_parent, node_token, node_logv, node_depth, node_count,
+                               ctx_lens, token, parent_row, depth, mask, node_id, position, n_rows,
+                               status=None, stream=None):
+    B, max_nodes = node_parent.shape
+    R = token.shape[1]
+    _check("eagle_tree_expand_finalize", lib().eagle_tree_expand_finalize(
+        B, max_nodes, budget, R, _ptr(node_parent), _ptr(node_token), _ptr(node_logv),
+        _ptr(node_depth), _ptr(node_count), _ptr(ctx_lens), _ptr(token), _ptr(parent_row),
+        _ptr(depth), _ptr(mask), _ptr(node_id), _ptr(position), _ptr(n_rows), _ptr(status),
+        _stream(stream)))
+
+
+# ------------------------------------------------------------------ a6 / a7
+def eagle_tree_verify_workspace_size(B, R, V):
+    return int(lib().eagle_tree_verify_workspace_size(B, R, V))
+
+
+def eagle_tree_verify(parent_row, token, temperature, max_depth, accept_len, path_rows, out_tokens,
+                      n_rows=None, target_logits=None, target_argmax=None, draft_logits=None,
+                      proposal_mode=EAGLE_PROPOSAL_DETERMINISTIC, seed=0, offset=0,
+                      uniforms_override=None, V=None, ws=None, status=None, stream=None):
+    B, R = parent_row.shape
+    if V is None:
+        V = target_logits.shape[2]
+    if ws is None:
+        ws = workspace(eagle_tree_verify_workspace_size(B, R, V), parent_row.device)
+    _check("eagle_tree_verify", lib().eagle_tree_verify(
+        B, R, V, _ptr(parent_row), _ptr(token), _ptr(n_rows), _ptr(target_logits),
+        _ptr(target_argmax), _ptr(draft_logits), float(temperature), proposal_mode, int(seed),
+        int(offset), _ptr(uniforms_override), max_depth, _ptr(accept_len), _ptr(path_rows),
+        _ptr(out_tokens), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))

@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kStatThreads) verify_rowstats_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ n_rows, int R, int V,
     float inv_t, int want_argmax, RowStat* __restrict__ stats, int32_t* __restrict__ amax,
     int32_t* dev_status) {
-  const int r = blockIdx.x, b = blockIdx.y;
+  const int r = blockIdx.x % R, b = blockIdx.x / R;
   const int n = n_rows ? n_rows[b] : R;
   if (r >= n || r >= R) return;
   const float* z = logits + ((size_t)b * R + r) * V;
@@ -306,7 +306,7 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
   const bool need_stats = !greedy || !target_argmax;
   if (need_stats && (!ws || ws_bytes < eagle_tree_verify_workspace_size(B, R, V)))
     return EAGLE_ERR_WORKSPACE;
-  if (B > 65535) return EAGLE_ERR_UNSUPPORTED;
+  if ((long long)B * R > 2147483647LL) return EAGLE_ERR_UNSUPPORTED;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* cur = static_cast<char*>(ws);
@@ -318,7 +318,7 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
   }
   const float inv_t = greedy ? 0.f : 1.f / temperature;
   if (need_stats) {
-    verify_rowstats_kernel<<<dim3(R, B), kStatThreads, 0, s>>>(
+    verify_rowstats_kernel<<<(unsigned)(B * R), kStatThreads, 0, s>>>(
         target_logits, n_rows, R, V, inv_t, greedy ? 1 : 0, stats, amax, dev_status);
     note_launch();
   }

@@ -1,0 +1,116 @@
+"""GPU parity of eagle_lmhead_topk and eagle_fuse_proj against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from eagle_speculative_decoding_gb300 import synth
+from gpu_helpers import REL_TOL, need_gpu, rel_err, check_topk
+
+pytestmark = pytest.mark.gpu
+
+
+def _lm_gpu(b, x, w, k, T, bias=None):
+    d = "cuda"
+    M = x.shape[0]
+    ids = torch.empty((M, k), dtype=torch.int32, device=d)
+    lp = torch.empty((M, k), dtype=torch.float32, device=d)
+    rm = torch.empty(M, dtype=torch.float32, device=d)
+    rs = torch.empty(M, dtype=torch.float32, device=d)
+    st = torch.zeros(1, dtype=torch.int32, device=d)
+    b.eagle_lmhead_topk(x.to(d), w.to(d), k, ids, lp, temperature=T,
+                        bias=None if bias is None else bias.to(d), row_max=rm, row_sumexp=rs, status=st)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), lp.cpu().numpy(), rm.cpu().numpy(), rs.cpu().numpy(), int(st.item())
+
+
+def _lm_check(b, M, d, V, k, T, dtype, seed, rows=None, bias=False):
+    gen = synth.generator(seed)
+    dt = synth.torch_dtype(dtype)
+    x = synth.normal((M, d), 1.0, dt, gen)
+    w = synth.normal((V, d), synth.WEIGHT_STD, dt, gen)
+    bb = synth.normal((V,), 0.5, torch.float32, gen) if bias else None
+    ids, lp, rm, rs, st = _lm_gpu(b, x, w, k, T, bb)
+    assert st == 0
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    ref = oracle.lmhead_topk(x.float().numpy(), w.float().numpy(), k, temperature=T,
+                             bias=None if bb is None else bb.numpy(), rows=rows)
+    z = ref["z"]
+    lse = ref["row_max"] + np.log(ref["row_sumexp"])
+    tol = 1e-2 if dtype == "fp32" else 1e-3
+    near = check_topk(ids[rows], lp[rows], z, lambda i, v: z[i, v] / T - lse[i], k, tol)
+    assert np.abs(rm[rows] - ref["row_max"]).max() < 1e-3
+    assert np.abs(np.log(rs[rows]) + rm[rows] - lse).max() < 1e-3
+    return near
+
+
+@pytest.mark.parametrize("M,d,V,k,T,dtype", [
+    (1, 64, 128, 1, 1.0, "bf16"),
+    (10, 256, 1024, 4, 1.0, "fp32"),     # toy, tf32 tensor cores
+    (17, 256, 1024, 4, 1.0, "fp32"),
+    (13, 512, 4096, 10, 0.7, "bf16"),    # ragged M, several vocab tiles
+    (61, 1024, 8192, 1, 1.0, "bf16"),
+    (100, 512, 4096, 32, 1.0, "bf16"),   # k = 32
+    (300, 256, 2048, 2, 1.0, "bf16"),    # two activation groups
+])
+def test_lmhead_small(M, d, V, k, T, dtype):
+    b = need_gpu()
+    near = _lm_check(b, M, d, V, k, T, dtype, seed=M * 7 + k)
+    assert near <= max(2, M * k // 20)
+
+
+def test_lmhead_bias():
+    b = need_gpu()
+    _lm_check(b, 9, 256, 2048, 5, 1.0, "bf16", seed=3, bias=True)
+
+
+@pytest.mark.parametrize("M,d,k,T,rows", [
+    (10, 4096, 10, 1.0, None),                  # llama8b draft rows, width 10
+    (61, 4096, 1, 1.0, [0, 17, 33, 60]),        # llama8b verify rows
+    (576, 4096, 1, 1.0, [0, 191, 192, 383, 384, 575]),  # serve64 verify rows, 3 groups
+    (128, 4096, 2, 1.0, [0, 64, 127]),          # serve64 draft rows
+    (32, 4096, 8, 0.6, [0, 31]),                # long4 draft rows
+    (10, 8192, 10, 1.0, [0, 9]),                # llama70b draft rows
+])
+def test_lmhead_full_vocab(M, d, k, T, rows):
+    b = need_gpu()
+    _lm_check(b, M, d, 128256, k, T, "bf16", seed=M + d, rows=rows)
+
+
+def _fp_check(b, M, d, dtype, seed, rows=None, bias=False):
+    gen = synth.generator(seed)
+    dt = synth.torch_dtype(dtype)
+    hl, hm, hh = (synth.normal((M, d), 1.0, dt, gen) for _ in range(3))
+    w = synth.normal((d, 3 * d), synth.WEIGHT_STD, dt, gen)
+    bb = synth.normal((d,), 0.1, torch.float32, gen) if bias else None
+    dv = "cuda"
+    g = torch.empty((M, d), dtype=dt, device=dv)
+    st = torch.zeros(1, dtype=torch.int32, device=dv)
+    b.eagle_fuse_proj(hl.to(dv), hm.to(dv), hh.to(dv), w.to(dv), g,
+                      bias=None if bb is None else bb.to(dv), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    f = lambda t: t.float().numpy()[rows]
+    ref = oracle.fuse_proj(f(hl), f(hm), f(hh), w.float().numpy(), None if bb is None else bb.numpy())
+    err = rel_err(g.float().cpu().numpy()[rows], ref)
+    assert err < (1e-3 if dtype == "fp32" else REL_TOL), err
+
+
+@pytest.mark.parametrize("M,d,dtype", [(17, 256, "fp32"), (1, 128, "bf16"), (61, 512, "bf16"),
+                                       (300, 256, "bf16"), (5, 1024, "fp32")])
+def test_fuse_proj_small(M, d, dtype):
+    b = need_gpu()
+    _fp_check(b, M, d, dtype, seed=M + d)
+
+
+def test_fuse_proj_bias():
+    b = need_gpu()
+    _fp_check(b, 7, 384, "bf16", seed=11, bias=True)
+
+
+@pytest.mark.parametrize("M,d,rows", [(61, 4096, None), (61, 8192, [0, 30, 60]),
+                                      (576, 4096, [0, 200, 575]), (244, 4096, [0, 243])])
+def test_fuse_proj_full_size(M, d, rows):
+    b = need_gpu()
+    _fp_check(b, M, d, "bf16", seed=M * d % 1000, rows=rows)
