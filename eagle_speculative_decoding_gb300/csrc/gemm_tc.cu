@@ -23,6 +23,8 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (lane = weight row)
 // Every wait is bounded (2 s); on expiry the CTA records EAGLE_ERR_TIMEOUT,
 // drains its copies and MMAs, frees tensor memory and exits.
+// fp32 operands run on the CUDA cores in exact fp32 (the tensor cores would
+// truncate them to TF32): small SIMT kernels that share the top-k epilogue.
 #include <math.h>
 
 #include "common.cuh"
@@ -294,6 +296,149 @@ __device__ __forceinline__ void warp_topk_merge(float (&z)[NPL], int (&id)[NPL],
   }
 }
 
+// Per-column running state of the LM-head epilogue (one column = one
+// activation row): online max / sum-exp of z/T and a sorted top-K list.
+struct LmEpi {
+  float* T;      // [16][128] transpose buffer: 16 columns x 128 vocab rows
+  float* col_m;  // [bn]
+  float* col_s;  // [bn]
+  int* col_c;    // [bn] entries in the list
+  float* top_v;  // [bn][K]
+  int* top_i;    // [bn][K]
+  int K;
+  float inv_t;
+};
+
+__device__ __forceinline__ LmEpi lm_epi_carve(unsigned char* p, int bn, int K, float inv_t) {
+  LmEpi E;
+  E.T = reinterpret_cast<float*>(p);
+  E.col_m = E.T + 16 * 128;
+  E.col_s = E.col_m + bn;
+  E.col_c = reinterpret_cast<int*>(E.col_s + bn);
+  E.top_v = reinterpret_cast<float*>(E.col_c + bn);
+  E.top_i = reinterpret_cast<int*>(E.top_v + bn * K);
+  E.K = K;
+  E.inv_t = inv_t;
+  return E;
+}
+
+// Fold 16 columns of one 128-row vocabulary tile into the running state.
+// Called by the 128 epilogue threads together: thread e holds v[j] = z of
+// vocabulary row v0+e for column c16*16+j.  Warp ew then owns columns
+// ew*4..ew*4+3 of the chunk.
+__device__ __forceinline__ void lm_chunk(const LmEpi& E, const float (&v)[16], int e, int ew,
+                                         int lane, int v0, int c16, int ncol) {
+  const int K = E.K;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) E.T[j * 128 + e] = v[j];
+  named_bar(1, kEpiThreads);
+#pragma unroll 1
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = ew * 4 + jj, col = c16 * 16 + j;
+    if (col >= ncol) continue;
+    float z[4];
+    int id[4];
+    bool cand[4];
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      z[i] = E.T[j * 128 + lane + 32 * i];
+      id[i] = v0 + lane + 32 * i;
+      tmax = fmaxf(tmax, z[i] * E.inv_t);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    float ts = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ts += exp2f((z[i] * E.inv_t - tmax) * kLog2e);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
+    int cnt = E.col_c[col];
+    float lv = lane < cnt ? E.top_v[col * K + lane] : -INFINITY;
+    int li = lane < cnt ? E.top_i[col * K + lane] : 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cand[i] = !isnan(z[i]);
+    warp_topk_merge<4>(z, id, cand, lv, li, cnt, K);
+    if (lane < cnt) {
+      E.top_v[col * K + lane] = lv;
+      E.top_i[col * K + lane] = li;
+    }
+    if (lane == 0) {
+      const float om = E.col_m[col];
+      const float nm = fmaxf(om, tmax);
+      E.col_s[col] = (om == -INFINITY ? 0.f : E.col_s[col] * exp2f((om - nm) * kLog2e)) +
+                     ts * exp2f((tmax - nm) * kLog2e);
+      E.col_m[col] = nm;
+      E.col_c[col] = cnt;
+    }
+    __syncwarp();
+  }
+  named_bar(1, kEpiThreads);
+}
+
+// Publish this CTA's per-column partial state; the last CTA of the group
+// (atomic ticket, no waiting) merges all partials of the group and writes the
+// final top-k ids, log-probs and row statistics.
+__device__ __forceinline__ void lm_publish_merge(const LmParams& p, const LmEpi& E, int* flag, int g,
+                                                 int m0, int ncol, int et, int ew, int lane) {
+  const int cta = blockIdx.x, bn = p.bn, K = p.K;
+  for (int c = et; c < ncol; c += kEpiThreads) {
+    p.part_ms[(size_t)cta * bn + c] = make_float2(E.col_m[c], E.col_s[c]);
+    p.part_cnt[(size_t)cta * bn + c] = E.col_c[c];
+  }
+  for (int x = et; x < ncol * K; x += kEpiThreads) {
+    p.part_v[(size_t)cta * bn * K + x] = E.top_v[x];
+    p.part_i[(size_t)cta * bn * K + x] = E.top_i[x];
+  }
+  __threadfence();
+  named_bar(1, kEpiThreads);
+  if (et == 0) *flag = (atomicAdd(&p.counters[g], 1) == p.ctas_per_group - 1) ? 1 : 0;
+  named_bar(1, kEpiThreads);
+  if (!*reinterpret_cast<volatile int*>(flag)) return;
+  __threadfence();
+  const int c0 = g * p.ctas_per_group, nc = p.ctas_per_group;
+  for (int col = ew; col < ncol; col += 4) {
+    float M = -INFINITY;
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, p.part_ms[(size_t)(c0 + c) * bn + col].x);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float S = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+      const float2 ms = p.part_ms[(size_t)(c0 + c) * bn + col];
+      if (ms.x != -INFINITY) S += ms.y * exp2f((ms.x - M) * kLog2e);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    float lv = -INFINITY;
+    int li = 0x7fffffff, cnt = 0;
+    for (int f0 = 0; f0 < nc * K; f0 += 32) {
+      const int f = f0 + lane;
+      float z[1] = {-INFINITY};
+      int id[1] = {0x7fffffff};
+      bool cand[1] = {false};
+      if (f < nc * K) {
+        const int c = f / K, j = f % K;
+        if (j < p.part_cnt[(size_t)(c0 + c) * bn + col]) {
+          z[0] = p.part_v[((size_t)(c0 + c) * bn + col) * K + j];
+          id[0] = p.part_i[((size_t)(c0 + c) * bn + col) * K + j];
+          cand[0] = true;
+        }
+      }
+      warp_topk_merge<1>(z, id, cand, lv, li, cnt, K);
+    }
+    const int row = m0 + col;
+    const float lse = M + logf(S);
+    if (lane < K) {
+      p.topk_ids[(size_t)row * K + lane] = lane < cnt ? li : -1;
+      p.topk_lp[(size_t)row * K + lane] = lane < cnt ? lv * p.inv_t - lse : -INFINITY;
+    }
+    if (lane == 0) {
+      if (p.row_max) p.row_max[row] = M;
+      if (p.row_sumexp) p.row_sumexp[row] = S;
+    }
+  }
+}
+
 template <bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
@@ -301,17 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ CtaShared sh;
   extern __shared__ unsigned char dsmem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bn = p.bn, K = p.K, stages = p.stages;
+  const int bn = p.bn, stages = p.stages;
   const uint32_t tmem_cols = tmem_cols_for(bn);
   const uint32_t base = align1024(smem_u32(dsmem));
   const uint32_t sA = base, sB = sA + stages * kTileA;
   unsigned char* gbase = dsmem + (base - smem_u32(dsmem));
-  float* T = reinterpret_cast<float*>(gbase + stages * (kTileA + bn * 128));  // [16][128]
-  float* col_m = T + 16 * 128;
-  float* col_s = col_m + bn;
-  int* col_c = reinterpret_cast<int*>(col_s + bn);
-  float* top_v = reinterpret_cast<float*>(col_c + bn);  // [bn][K]
-  int* top_i = reinterpret_cast<int*>(top_v + bn * K);
+  const LmEpi E = lm_epi_carve(gbase + stages * (kTileA + bn * 128), bn, p.K, p.inv_t);
 
   const int g = blockIdx.x / p.ctas_per_group, ci = blockIdx.x % p.ctas_per_group;
   LmSched<TF32> sc;
@@ -329,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_x);
   }
   for (int c = threadIdx.x; c < bn; c += kThreads) {
-    col_m[c] = -INFINITY;
-    col_s[c] = 0.f;
-    col_c[c] = 0;
+    E.col_m[c] = -INFINITY;
+    E.col_s[c] = 0.f;
+    E.col_c[c] = 0;
   }
   cta_setup(sh, stages, tmem_cols);
 
@@ -358,120 +498,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[16];
         tmem_ld16(taddr + c16 * 16, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) T[j * 128 + e] = v[j] + bias_e;
-        named_bar(1, kEpiThreads);
-#pragma unroll 1
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = ew * 4 + jj, col = c16 * 16 + j;
-          if (col >= ncol) continue;
-          float z[4];
-          int id[4];
-          bool cand[4];
-          float tmax = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            z[i] = T[j * 128 + lane + 32 * i];
-            id[i] = v0 + lane + 32 * i;
-            tmax = fmaxf(tmax, z[i] * p.inv_t);
-          }
-#pragma unroll
-          for (int o = 16; o; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-          float ts = 0.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) ts += exp2f((z[i] * p.inv_t - tmax) * kLog2e);
-#pragma unroll
-          for (int o = 16; o; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
-          int cnt = col_c[col];
-          float lv = lane < cnt ? top_v[col * K + lane] : -INFINITY;
-          int li = lane < cnt ? top_i[col * K + lane] : 0x7fffffff;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) cand[i] = !isnan(z[i]);
-          warp_topk_merge<4>(z, id, cand, lv, li, cnt, K);
-          if (lane < cnt) {
-            top_v[col * K + lane] = lv;
-            top_i[col * K + lane] = li;
-          }
-          if (lane == 0) {
-            const float om = col_m[col];
-            const float nm = fmaxf(om, tmax);
-            col_s[col] = (om == -INFINITY ? 0.f : col_s[col] * exp2f((om - nm) * kLog2e)) +
-                         ts * exp2f((tmax - nm) * kLog2e);
-            col_m[col] = nm;
-            col_c[col] = cnt;
-          }
-          __syncwarp();
-        }
-        named_bar(1, kEpiThreads);
+        for (int j = 0; j < 16; ++j) v[j] += bias_e;
+        lm_chunk(E, v, e, ew, lane, v0, c16, ncol);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
     }
-
-    // ---- publish this CTA's partial state, last CTA of the group merges
     named_bar(1, kEpiThreads);
-    if (!*reinterpret_cast<volatile int*>(&sh.epi_abort)) {
-      const int cta = blockIdx.x;
-      const int et = threadIdx.x - 64;
-      for (int c = et; c < ncol; c += kEpiThreads) {
-        p.part_ms[(size_t)cta * bn + c] = make_float2(col_m[c], col_s[c]);
-        p.part_cnt[(size_t)cta * bn + c] = col_c[c];
-      }
-      for (int x = et; x < ncol * K; x += kEpiThreads) {
-        p.part_v[(size_t)cta * bn * K + x] = top_v[x];
-        p.part_i[(size_t)cta * bn * K + x] = top_i[x];
-      }
-      __threadfence();
-      named_bar(1, kEpiThreads);
-      if (et == 0) sh.flag = (atomicAdd(&p.counters[g], 1) == p.ctas_per_group - 1) ? 1 : 0;
-      named_bar(1, kEpiThreads);
-      if (sh.flag) {
-        __threadfence();
-        const int c0 = g * p.ctas_per_group, nc = p.ctas_per_group;
-        for (int col = ew; col < ncol; col += 4) {
-          float M = -INFINITY;
-          for (int c = lane; c < nc; c += 32) M = fmaxf(M, p.part_ms[(size_t)(c0 + c) * bn + col].x);
-#pragma unroll
-          for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          float S = 0.f;
-          for (int c = lane; c < nc; c += 32) {
-            const float2 ms = p.part_ms[(size_t)(c0 + c) * bn + col];
-            if (ms.x != -INFINITY) S += ms.y * exp2f((ms.x - M) * kLog2e);
-          }
-#pragma unroll
-          for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-          float lv = -INFINITY;
-          int li = 0x7fffffff, cnt = 0;
-          for (int f0 = 0; f0 < nc * K; f0 += 32) {
-            const int f = f0 + lane;
-            float z[1] = {-INFINITY};
-            int id[1] = {0x7fffffff};
-            bool cand[1] = {false};
-            if (f < nc * K) {
-              const int c = f / K, j = f % K;
-              if (j < p.part_cnt[(size_t)(c0 + c) * bn + col]) {
-                z[0] = p.part_v[((size_t)(c0 + c) * bn + col) * K + j];
-                id[0] = p.part_i[((size_t)(c0 + c) * bn + col) * K + j];
-                cand[0] = true;
-              }
-            }
-            warp_topk_merge<1>(z, id, cand, lv, li, cnt, K);
-          }
-          const int row = m0 + col;
-          const float lse = M + logf(S);
-          if (lane < K) {
-            p.topk_ids[(size_t)row * K + lane] = lane < cnt ? li : -1;
-            p.topk_lp[(size_t)row * K + lane] = lane < cnt ? lv * p.inv_t - lse : -INFINITY;
-          }
-          if (lane == 0) {
-            if (p.row_max) p.row_max[row] = M;
-            if (p.row_sumexp) p.row_sumexp[row] = S;
-          }
-        }
-      }
-    }
+    if (!*reinterpret_cast<volatile int*>(&sh.epi_abort))
+      lm_publish_merge(p, E, &sh.flag, g, m0, ncol, threadIdx.x - 64, ew, lane);
   }
   cta_teardown(sh, tmem_cols, p.status);
+}
+
+// fp32 LM head on the CUDA cores (exact fp32 products and sums).  Same
+// schedule and epilogue as the tensor-core kernel; 128 threads, thread e
+// computes vocabulary row v0+e against 16 activation rows at a time from
+// shared-memory tiles of 32 K-elements.
+constexpr int kF32Kc = 32;
+__global__ void __launch_bounds__(kEpiThreads)
+    lmhead_topk_f32_kernel(const float* __restrict__ x, const float* __restrict__ w, int d,
+                           const LmParams p) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  __shared__ int flag;
+  float* Ws = reinterpret_cast<float*>(dsm);         // [128][kF32Kc + 1]
+  float* Xs = Ws + 128 * (kF32Kc + 1);                // [16][kF32Kc]
+  const LmEpi E = lm_epi_carve(reinterpret_cast<unsigned char*>(Xs + 16 * kF32Kc), p.bn, p.K, p.inv_t);
+  const int e = threadIdx.x, lane = e & 31, ew = e >> 5;
+  const int g = blockIdx.x / p.ctas_per_group, ci = blockIdx.x % p.ctas_per_group;
+  const int t0 = (int)((long long)ci * p.n_vtiles / p.ctas_per_group);
+  const int t1 = (int)((long long)(ci + 1) * p.n_vtiles / p.ctas_per_group);
+  const int m0 = g * p.bn, ncol = min(p.bn, p.M - m0);
+  for (int c = e; c < p.bn; c += kEpiThreads) {
+    E.col_m[c] = -INFINITY;
+    E.col_s[c] = 0.f;
+    E.col_c[c] = 0;
+  }
+  __syncthreads();
+  for (int t = t0; t < t1; ++t) {
+    const int v0 = t * 128;
+    const float bias_e = p.bias ? p.bias[v0 + e] : 0.f;
+    for (int c16 = 0; c16 * 16 < ncol; ++c16) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.f;
+      for (int k0 = 0; k0 < d; k0 += kF32Kc) {
+        __syncthreads();
+        for (int i = e; i < 128 * kF32Kc; i += kEpiThreads) {
+          const int r = i / kF32Kc, c = i % kF32Kc;
+          Ws[r * (kF32Kc + 1) + c] = w[(size_t)(v0 + r) * d + k0 + c];
+        }
+        for (int i = e; i < 16 * kF32Kc; i += kEpiThreads) {
+          const int r = i / kF32Kc, c = i % kF32Kc, m = m0 + c16 * 16 + r;
+          Xs[i] = (c16 * 16 + r < ncol) ? x[(size_t)m * d + k0 + c] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < kF32Kc; ++c) {
+          const float wv = Ws[e * (kF32Kc + 1) + c];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = fmaf(wv, Xs[j * kF32Kc + c], v[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] += bias_e;
+      lm_chunk(E, v, e, ew, lane, v0, c16, ncol);
+    }
+  }
+  named_bar(1, kEpiThreads);
+  lm_publish_merge(p, E, &flag, g, m0, ncol, e, ew, lane);
 }
 
 // ==================================================================== fuse_proj
@@ -632,6 +728,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   cta_teardown(sh, tmem_cols, p.status);
 }
 
+// fp32 fused projection on the CUDA cores (exact fp32): one warp per output
+// element g[m, o]; lanes stride the 3d inputs of the concatenation.
+__global__ void __launch_bounds__(256)
+    fuse_proj_f32_kernel(const float* __restrict__ hl, const float* __restrict__ hm,
+                         const float* __restrict__ hh, const float* __restrict__ w,
+                         const float* __restrict__ bias, float* __restrict__ g, int M, int d) {
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)M * d) return;
+  const int m = (int)(gw / d), o = (int)(gw % d);
+  const float* wr = w + (size_t)o * 3 * d;
+  float acc = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    acc = fmaf(wr[c], hl[(size_t)m * d + c], acc);
+    acc = fmaf(wr[d + c], hm[(size_t)m * d + c], acc);
+    acc = fmaf(wr[2 * d + c], hh[(size_t)m * d + c], acc);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) g[(size_t)m * d + o] = acc + (bias ? bias[o] : 0.f);
+}
+
 // ------------------------------------------------------------------ host side
 int pick_bn(int M, int* groups) {
   const int G = (M + 255) / 256;
@@ -691,13 +809,17 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
   if (cpg > n_vtiles) cpg = n_vtiles;
   const int n_ctas = cpg * G;
   const size_t extra = lm_epi_bytes(bn, k);
-  const int stages = pick_stages(bn, extra);
+  const int stages = dtype == EAGLE_BF16 ? pick_stages(bn, extra) : 2;
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
-  const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)bn * 128) + extra;
+  const size_t smem = dtype == EAGLE_BF16
+                          ? 1024 + (size_t)stages * (kTileA + (size_t)bn * 128) + extra
+                          : (size_t)(128 * (kF32Kc + 1) + 16 * kF32Kc) * 4 + extra;
+  if (smem > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;
 
   CUtensorMap mw, mx;
-  if (!make_tmap_2d(&mw, w_lm, esz, (uint64_t)V, (uint64_t)d, 128, (uint32_t)bke) ||
-      !make_tmap_2d(&mx, x, esz, (uint64_t)M, (uint64_t)d, (uint32_t)bn, (uint32_t)bke))
+  if (dtype == EAGLE_BF16 &&
+      (!make_tmap_2d(&mw, w_lm, esz, (uint64_t)V, (uint64_t)d, 128, (uint32_t)bke) ||
+       !make_tmap_2d(&mx, x, esz, (uint64_t)M, (uint64_t)d, (uint32_t)bn, (uint32_t)bke)))
     return EAGLE_ERR_CUDA;
 
   char* cur = static_cast<char*>(ws);
@@ -731,8 +853,8 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
     cudaFuncSetAttribute(lmhead_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     lmhead_topk_kernel<false><<<n_ctas, kThreads, smem, s>>>(mw, mx, p);
   } else {
-    cudaFuncSetAttribute(lmhead_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    lmhead_topk_kernel<true><<<n_ctas, kThreads, smem, s>>>(mw, mx, p);
+    cudaFuncSetAttribute(lmhead_topk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    lmhead_topk_f32_kernel<<<n_ctas, kEpiThreads, smem, s>>>((const float*)x, (const float*)w_lm, d, p);
   }
   note_launch();
   return last_launch_status();
@@ -784,8 +906,16 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   if (!aligned16(h_low) || !aligned16(h_mid) || !aligned16(h_high) || !aligned16(w_proj))
     return EAGLE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < eagle_fuse_proj_workspace_size(M, d, dtype)) return EAGLE_ERR_WORKSPACE;
-  const int esz = dtype == EAGLE_BF16 ? 2 : 4;
-  const int bke = 128 / esz;
+  if (dtype == EAGLE_FP32) {
+    const long long outs = (long long)M * d;
+    fuse_proj_f32_kernel<<<(unsigned)((outs + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        (const float*)h_low, (const float*)h_mid, (const float*)h_high, (const float*)w_proj, bias,
+        (float*)g, M, d);
+    note_launch();
+    return last_launch_status();
+  }
+  const int esz = 2;
+  const int bke = 64;
   int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
   const FpPlan f = fp_plan(M, d, esz, sms > kMaxCtas ? kMaxCtas : sms);
@@ -821,13 +951,8 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   p.status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.counters, 0, (size_t)f.n_tiles * 4, s) != cudaSuccess) return EAGLE_ERR_CUDA;
-  if (dtype == EAGLE_BF16) {
-    cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    fuse_proj_kernel<false><<<f.n_ctas, kThreads, smem, s>>>(mw, ml, mm, mh, p);
-  } else {
-    cudaFuncSetAttribute(fuse_proj_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    fuse_proj_kernel<true><<<f.n_ctas, kThreads, smem, s>>>(mw, ml, mm, mh, p);
-  }
+  cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  fuse_proj_kernel<false><<<f.n_ctas, kThreads, smem, s>>>(mw, ml, mm, mh, p);
   note_launch();
   return last_launch_status();
 }

@@ -92,7 +92,8 @@ uint64_t eagle_launch_count(void);
  *   bias                 : [d] fp32, or NULL
  *   g                    : [M, d]   output, dtype `dtype`
  * The concatenation is never materialised: the K loop walks the three inputs.
- * fp32 runs on the TF32 tensor-core kind; bf16 accumulates in fp32.
+ * bf16 runs on the tensor cores with fp32 accumulation; fp32 runs on the CUDA
+ * cores in exact fp32 arithmetic.
  * Limits: 1 <= M <= 4096, d % 128 == 0, d <= 16384.
  * ---------------------------------------------------------------------- */
 size_t eagle_fuse_proj_workspace_size(int M, int d, int dtype);
@@ -155,6 +156,8 @@ int eagle_tree_attn(const void* q, const void* k_tree, const void* v_tree,
  *   bias         : [V] fp32 or NULL
  *   topk_ids     : [M, k] int32;  topk_logprobs: [M, k] fp32
  *   row_max, row_sumexp : [M] fp32 or NULL
+ * bf16 runs on the tensor cores with fp32 accumulation; fp32 runs on the CUDA
+ * cores in exact fp32 arithmetic.
  * Limits: 1 <= M <= 2048, 1 <= k <= 32, k <= V, d % 64 == 0,
  * V % 128 == 0, temperature > 0.
  * ---------------------------------------------------------------------- */

@@ -133,4 +133,4 @@ def test_budget_zero_and_host_limits():
     flat = g.finalize(0, torch.tensor([5], dtype=torch.int32))
     assert flat["n_rows"][0] == 1 and flat["token"][0].tolist() == [9, -1, -1]
     with pytest.raises(b.EagleError):
-        g.step(3, torch.zeros((1, 2, 2), dtype=torch.int32), torch.zeros((1, 2, 2)))  # max_nodes too small
+        g.step(5, torch.zeros((1, 2, 2), dtype=torch.int32), torch.zeros((1, 2, 2)))  # max_nodes too small

@@ -37,8 +37,8 @@ def _lm_check(b, M, d, V, k, T, dtype, seed, rows=None, bias=False):
                              bias=None if bb is None else bb.numpy(), rows=rows)
     z = ref["z"]
     lse = ref["row_max"] + np.log(ref["row_sumexp"])
-    tol = 1e-2 if dtype == "fp32" else 1e-3
-    near = check_topk(ids[rows], lp[rows], z, lambda i, v: z[i, v] / T - lse[i], k, tol)
+    # fp32 accumulation error of z is ~1e-6 here; closer logits are near ties
+    near = check_topk(ids[rows], lp[rows], z, lambda i, v: z[i, v] / T - lse[i], k, 1e-4)
     assert np.abs(rm[rows] - ref["row_max"]).max() < 1e-3
     assert np.abs(np.log(rs[rows]) + rm[rows] - lse).max() < 1e-3
     return near
@@ -56,7 +56,7 @@ def _lm_check(b, M, d, V, k, T, dtype, seed, rows=None, bias=False):
 def test_lmhead_small(M, d, V, k, T, dtype):
     b = need_gpu()
     near = _lm_check(b, M, d, V, k, T, dtype, seed=M * 7 + k)
-    assert near <= max(2, M * k // 20)
+    assert near <= M * k // 4
 
 
 def test_lmhead_bias():
@@ -94,7 +94,7 @@ def _fp_check(b, M, d, dtype, seed, rows=None, bias=False):
     f = lambda t: t.float().numpy()[rows]
     ref = oracle.fuse_proj(f(hl), f(hm), f(hh), w.float().numpy(), None if bb is None else bb.numpy())
     err = rel_err(g.float().cpu().numpy()[rows], ref)
-    assert err < (1e-3 if dtype == "fp32" else REL_TOL), err
+    assert err < (1e-4 if dtype == "fp32" else REL_TOL), err
 
 
 @pytest.mark.parametrize("M,d,dtype", [(17, 256, "fp32"), (1, 128, "bf16"), (61, 512, "bf16"),

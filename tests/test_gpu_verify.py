@@ -71,11 +71,15 @@ def _stochastic_case(B, R, V, depth, T, seed):
     gen = synth.generator(seed)
     parent, tok = _trees(B, R, depth, V, gen)
     z = synth.target_logits((B, R, V), gen, std=1.0 if V < 100 else synth.LOGIT_STD)
-    # make the drafted tokens plausible under the target so walks go deep
+    # lift each drafted token near the top of its parent's target row so that
+    # acceptances happen at every depth
     zn = z.numpy()
+    rng = np.random.default_rng(seed)
+    top = zn.max(axis=2)
     for bb in range(B):
         for c in range(1, R):
-            zn[bb, int(parent[bb, c]), int(tok[bb, c])] += 3.0
+            r = int(parent[bb, c])
+            zn[bb, r, int(tok[bb, c])] = top[bb, r] + rng.uniform(-1.0, 2.0) * T
     return parent, tok, torch.from_numpy(zn)
 
 
