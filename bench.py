@@ -1,0 +1,504 @@
+"""Benchmark of the EAGLE tree-verify hot path on GB300.
+
+One step = one pass of every hot-path call over one batch:
+  draft round  depth x (LM-head top-k over the expanded parents' drafter rows
+               + one EAGLE-2 expansion step), then rerank/flatten
+  verify       tree attention (one target-layer-shaped call), fused EAGLE-3
+               projection of the verify rows, LM-head top-k of the verify
+               rows (k = 1: the target argmax), tree verification
+Metric: tree nodes verified per second (B * budget / step time); the step
+time in microseconds is reported beside it.
+
+Default workload: the LLaMA-3.1-8B-shaped batch-1 case (d 4096, 32/8 heads x
+128, V 128256, ctx 2048, depth 6, top-k 10, width 10, budget 60, greedy).
+Inputs are seeded synthetic tensors resident in HBM; weights ~ N(0, 0.02^2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference]
+Under torchrun each rank runs an independent replica (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from eagle_speculative_decoding_gb300 import binding as eb  # noqa: E402
+from eagle_speculative_decoding_gb300 import synth  # noqa: E402
+
+METRIC = "tree-verify step: tree nodes/s (B*budget / step time)"
+UNIT = "nodes/s"
+PROFILE = os.path.join(ROOT, "profiles", "lmhead_topk_llama8b.md")
+
+
+# --------------------------------------------------------------- workload
+class Workload:
+    """Device-resident inputs of one step plus pinned host copies of the
+    per-step inputs for the end-to-end measurement."""
+
+    def __init__(self, name, device, seed=0):
+        c = synth.CONFIGS[name]
+        self.name, self.c, self.dev = name, c, device
+        self.B, self.d, self.V = c["B"], c["d"], c["V"]
+        self.Hq, self.Hkv, self.D = c["Hq"], c["Hkv"], c["D"]
+        self.k, self.width, self.depth, self.N = c["topk"], c["width"], c["depth"], c["N"]
+        self.R = self.N + 1
+        self.T = c["temps"][0]
+        self.dt = synth.torch_dtype(c["dtype"])
+        B, d, V, R = self.B, self.d, self.V, self.R
+        g = synth.generator(seed, device)
+        gc = synth.generator(seed + 1)
+        nrm = lambda shape, std=1.0: synth.normal(shape, std, self.dt, g, device)
+        # model state (resident)
+        self.w_lm = nrm((V, d), synth.WEIGHT_STD)
+        self.w_proj = nrm((d, 3 * d), synth.WEIGHT_STD)
+        ctx = synth.ctx_lengths(c, gc)
+        kc, vc, table = synth.paged_kv(ctx.tolist(), self.Hkv, self.D, c["page"], self.dt, gc,
+                                       device=device)
+        self.k_cache, self.v_cache = kc, vc
+        self.block_table, self.ctx_lens = table.to(device), ctx.to(device)
+        # per-step inputs: drafter rows per depth, verify-row activations
+        self.P = [1 if s == 0 else self.width for s in range(self.depth)]
+        host = {}
+        host["draft_x"] = [synth.normal((B * p, d), 1.0, self.dt, gc) for p in self.P]
+        host["root"] = synth.random_tokens((B,), V, gc)
+        host["q"] = synth.normal((B, R, self.Hq, self.D), 1.0, self.dt, gc)
+        host["k_tree"] = synth.normal((B, R, self.Hkv, self.D), 1.0, self.dt, gc)
+        host["v_tree"] = synth.normal((B, R, self.Hkv, self.D), 1.0, self.dt, gc)
+        host["h"] = [synth.normal((B * R, d), 1.0, self.dt, gc) for _ in range(3)]
+        host["x_v"] = synth.normal((B * R, d), 1.0, self.dt, gc)
+        if self.T > 0:
+            host["logits"] = synth.target_logits((B, R, V), gc, device=device).cpu()
+        self.host = {k: ([t.pin_memory() for t in v] if isinstance(v, list) else v.pin_memory())
+                     for k, v in host.items()}
+        self.dev_in = {k: ([t.to(device) for t in v] if isinstance(v, list) else v.to(device))
+                       for k, v in self.host.items()}
+        # outputs / state
+        z = lambda *s, t=torch.int32: torch.zeros(s, dtype=t, device=device)
+        self.max_nodes = 1 + synth.n_candidates(c)
+        self.cand = [(z(B * p, self.k), z(B * p, self.k, t=torch.float32)) for p in self.P]
+        self.tree = dict(parent=z(B, self.max_nodes), token=z(B, self.max_nodes),
+                         logv=z(B, self.max_nodes, t=torch.float32), depth=z(B, self.max_nodes),
+                         count=z(B), frontier=z(B, self.width), nf=z(B))
+        self.flat = {n: z(B, R) for n in ("token", "parent_row", "depth", "node_id", "position")}
+        self.flat["mask"] = z(B, R, t=torch.int64)
+        self.flat["n_rows"] = z(B)
+        self.attn_out = torch.empty((B, R, self.Hq, self.D), dtype=self.dt, device=device)
+        self.g = torch.empty((B * R, d), dtype=self.dt, device=device)
+        self.amax = z(B * R, 1)
+        self.amax_lp = z(B * R, 1, t=torch.float32)
+        self.acc, self.path, self.out_tok = z(B), z(B, self.depth + 1), z(B, self.depth + 1)
+        self.status = z(1)
+        # workspaces (caller-owned scratch)
+        dt_code = eb.EAGLE_BF16 if self.dt == torch.bfloat16 else eb.EAGLE_FP32
+        lm_ws = max(eb.eagle_lmhead_topk_workspace_size(B * p, d, V, self.k, dt_code) for p in self.P)
+        lm_ws = max(lm_ws, eb.eagle_lmhead_topk_workspace_size(B * R, d, V, 1, dt_code))
+        self.ws_lm = eb.workspace(lm_ws, device)
+        self.ws_fp = eb.workspace(eb.eagle_fuse_proj_workspace_size(B * R, d, dt_code), device)
+        self.ws_attn = eb.workspace(eb.eagle_tree_attn_workspace_size(
+            B, R, self.Hq, self.Hkv, self.D, table.shape[1], c["page"], 0, dt_code), device)
+        self.ws_ver = eb.workspace(eb.eagle_tree_verify_workspace_size(B, R, V), device)
+
+    # ------------------------------------------------------------- step
+    def step(self, lm_events=None):
+        """Launch one step on the current stream.  ``lm_events``: list that
+        receives (start, end) CUDA events around each LM-head call."""
+        t, f, x = self.tree, self.flat, self.dev_in
+
+        def lm(xr, k, ids, lps):
+            if lm_events is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            eb.eagle_lmhead_topk(xr, self.w_lm, k, ids, lps, temperature=1.0, ws=self.ws_lm,
+                                 status=self.status)
+            if lm_events is not None:
+                e1.record()
+                lm_events.append((e0, e1, xr.shape[0], k))
+
+        for s in range(self.depth):
+            ids, lps = self.cand[s]
+            lm(x["draft_x"][s], self.k, ids, lps)
+            eb.eagle_tree_expand(s, self.width, ids, lps, x["root"], t["parent"], t["token"],
+                                 t["logv"], t["depth"], t["count"], t["frontier"], t["nf"],
+                                 status=self.status)
+        eb.eagle_tree_expand_finalize(self.N, t["parent"], t["token"], t["logv"], t["depth"],
+                                      t["count"], self.ctx_lens, f["token"], f["parent_row"],
+                                      f["depth"], f["mask"], f["node_id"], f["position"], f["n_rows"],
+                                      status=self.status)
+        eb.eagle_tree_attn(x["q"], x["k_tree"], x["v_tree"], self.k_cache, self.v_cache,
+                           self.block_table, self.ctx_lens, f["mask"], self.attn_out,
+                           ws=self.ws_attn, status=self.status)
+        eb.eagle_fuse_proj(x["h"][0], x["h"][1], x["h"][2], self.w_proj, self.g, ws=self.ws_fp,
+                           status=self.status)
+        lm(x["x_v"], 1, self.amax, self.amax_lp)
+        if self.T == 0:
+            eb.eagle_tree_verify(f["parent_row"], f["token"], 0.0, self.depth, self.acc, self.path,
+                                 self.out_tok, n_rows=f["n_rows"], target_argmax=self.amax.view(self.B, self.R),
+                                 V=self.V, ws=self.ws_ver, status=self.status)
+        else:
+            eb.eagle_tree_verify(f["parent_row"], f["token"], self.T, self.depth, self.acc, self.path,
+                                 self.out_tok, n_rows=f["n_rows"], target_logits=x["logits"],
+                                 seed=1234, ws=self.ws_ver, status=self.status)
+
+    def h2d(self):
+        """Copy this step's inputs from pinned host memory; returns bytes."""
+        n = 0
+        for k, v in self.host.items():
+            if isinstance(v, list):
+                for a, b in zip(self.dev_in[k], v):
+                    a.copy_(b, non_blocking=True)
+                    n += b.numel() * b.element_size()
+            else:
+                self.dev_in[k].copy_(v, non_blocking=True)
+                n += v.numel() * v.element_size()
+        return n
+
+    def d2h(self, host_out):
+        n = 0
+        for src, dst in zip((self.acc, self.path, self.out_tok), host_out):
+            dst.copy_(src, non_blocking=True)
+            n += src.numel() * src.element_size()
+        return n
+
+    def lm_bytes(self, M, k):
+        es = self.w_lm.element_size()
+        return self.V * self.d * es + M * self.d * es + M * k * 8
+
+
+# ------------------------------------------------------------ measurement
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[2:6]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes of the LM-head kernel from the committed ncu
+    summary, valid only while the kernel source hash matches the capture."""
+    src = os.path.join(ROOT, "eagle_speculative_decoding_gb300", "csrc", "gemm_tc.cu")
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if not os.path.exists(PROFILE):
+        return None
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("gemm_tc.cu sha256[:16]") != cur:
+        return None
+    try:
+        return float(vals["dram bytes per launch (verify-row call, M=61)"])
+    except (KeyError, ValueError):
+        return None
+
+
+def flush_l2(buf):
+    buf.add_(1)  # 256 MB read+write, larger than the 129 MB L2
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = Workload(args.workload, dev, seed=args.seed + 1000 * rank)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    st = eb.read_status(wl.status)
+    if st != 0:
+        raise RuntimeError(f"device status {eb.STATUS.get(st, st)} after warm-up")
+
+    # ---- device-resident timing (per-step events; L2 flushed between steps)
+    lm_events, step_events = [], []
+    n0 = eb.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            wl.step(lm_events)
+            e1.record(stream)
+            step_events.append((e0, e1))
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    launches = eb.launch_count() - n0
+    step_ms = [a.elapsed_time(b) for a, b in step_events]
+    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    nodes = wl.B * wl.N * world
+    value = nodes / (ms_per_step / 1e3)
+
+    # dominant kernel: the LM-head GEMM + top-k (reads the whole W_U per call)
+    lm_ms = [a.elapsed_time(b) for a, b, _, _ in lm_events]
+    lm_bytes = [wl.lm_bytes(M, k) for _, _, M, k in lm_events]
+    lm_avg_ms = sum(lm_ms) / len(lm_ms)
+    achieved = (sum(lm_bytes) / len(lm_bytes)) / (lm_avg_ms / 1e3) / 1e9
+    peaks, peak_kind = measured_peaks()
+
+    # ---- end to end through the public API: H2D of the step inputs, step,
+    # D2H of the accepted path / tokens, all inside the timed region
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (wl.acc, wl.path, wl.out_tok)]
+    barrier(world)
+    torch.cuda.synchronize()
+    e2e_ms, hb, db = [], 0, 0
+    for _ in range(args.steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        hb = wl.h2d()
+        wl.step()
+        db = wl.d2h(host_out)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = max_over_ranks(sum(e2e_ms), world)
+    e2e_value = nodes / (e2e_total / args.steps / 1e3)
+
+    st = eb.read_status(wl.status)
+    if st != 0:
+        raise RuntimeError(f"device status {eb.STATUS.get(st, st)}")
+    clocks = clk.summary()
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "step_us": round(ms_per_step * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dt == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+        "config": {"workload": wl.name, "batch": wl.B, "hidden": wl.d, "heads": f"{wl.Hq}/{wl.Hkv}x{wl.D}",
+                   "vocab": wl.V, "ctx": list(wl.c["ctx"]), "tree": f"depth {wl.depth}, top-k {wl.k}, "
+                   f"width {wl.width}, budget {wl.N}", "temperature": wl.T,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed between steps (256 MB write); W_U (1 GB) also exceeds L2"},
+        "gpu_launches": launches,
+        "roofline": {"kernel": "lmhead_topk_kernel (tcgen05 LM head + top-k)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
+                     "traffic": profile_traffic(), "avg_launch_us": round(lm_avg_ms * 1e3, 2),
+                     "launches_per_step": len(lm_events) // args.steps},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": hb,
+                "d2h_bytes_per_step": db},
+        "clocks": clocks,
+        "wall_s": round(t_wall, 3),
+    }
+    return res, wl
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+class OracleStep:
+    """The CPU oracle running one full step of the workload (test
+    infrastructure, used only for the CPU baseline and the reference arm)."""
+
+    def __init__(self, name, seed=0):
+        import numpy as np
+        import oracle
+        self.np, self.oracle = np, oracle
+        c = synth.CONFIGS[name]
+        self.c = c
+        B, d, V, width, depth, N = c["B"], c["d"], c["V"], c["width"], c["depth"], c["N"]
+        R = N + 1
+        gen = synth.generator(seed)
+        dt = synth.torch_dtype(c["dtype"])
+        f64 = lambda t: t.double().numpy()
+        self.w_lm = f64(synth.normal((V, d), synth.WEIGHT_STD, dt, gen))
+        self.w_proj = f64(synth.normal((d, 3 * d), synth.WEIGHT_STD, dt, gen))
+        self.ctx = synth.ctx_lengths(c, gen)
+        kc, vc, table = synth.paged_kv(self.ctx.tolist(), c["Hkv"], c["D"], c["page"], dt, gen)
+        self.kc, self.vc, self.table = f64(kc), f64(vc), table.numpy()
+        self.rows = [f64(synth.normal((B * (1 if s == 0 else width), d), 1.0, dt, gen))
+                     for s in range(depth)]
+        self.q = f64(synth.normal((B, R, c["Hq"], c["D"]), 1.0, dt, gen))
+        self.kt = f64(synth.normal((B, R, c["Hkv"], c["D"]), 1.0, dt, gen))
+        self.vt = f64(synth.normal((B, R, c["Hkv"], c["D"]), 1.0, dt, gen))
+        self.hs = [f64(synth.normal((B * R, d), 1.0, dt, gen)) for _ in range(3)]
+        self.xv = f64(synth.normal((B * R, d), 1.0, dt, gen))
+        self.T = c["temps"][0]
+        self.logits = synth.target_logits((B, R, V), gen).numpy() if self.T > 0 else None
+        self.nodes = B * N
+
+    def run(self):
+        """One step; returns its wall seconds."""
+        np, oracle, c = self.np, self.oracle, self.c
+        B, k, width, depth, N = c["B"], c["topk"], c["width"], c["depth"], c["N"]
+        R = N + 1
+        t0 = time.perf_counter()
+        sts = [oracle.tree_expand_init(7) for _ in range(B)]
+        for s in range(depth):
+            P = 1 if s == 0 else width
+            res = oracle.lmhead_topk(self.rows[s], self.w_lm, k)
+            for b in range(B):
+                n = len(sts[b]["frontier"])
+                oracle.tree_expand_step(sts[b], res["ids"][b * P:b * P + n],
+                                        res["logprobs"][b * P:b * P + n], width)
+        flats = [oracle.tree_expand_finalize(sts[b], N, int(self.ctx[b]), R_out=R) for b in range(B)]
+        mask = np.stack([f["mask"] for f in flats])
+        oracle.tree_attn(self.q, self.kt, self.vt, self.kc, self.vc, self.table, self.ctx.numpy(), mask)
+        oracle.fuse_proj(*self.hs, self.w_proj)
+        am = oracle.lmhead_topk(self.xv, self.w_lm, 1)["ids"].reshape(B, R)
+        parent = np.stack([f["parent_row"] for f in flats])
+        tok = np.stack([f["token"] for f in flats])
+        nr = [f["n_rows"] for f in flats]
+        if self.T == 0:
+            oracle.tree_verify(parent, tok, 0.0, depth, n_rows=nr, target_argmax=am)
+        else:
+            oracle.tree_verify(parent, tok, self.T, depth, n_rows=nr, target_logits=self.logits, seed=1234)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(name, budget_s=12.0):
+    """Oracle timed on a bounded sample: whole steps until ~budget_s of CPU work."""
+    o = OracleStep(name)
+    secs = [o.run()]
+    while sum(secs) < budget_s and len(secs) < 50:
+        secs.append(o.run())
+    per = sum(secs) / len(secs)
+    return {"value": round(o.nodes / per, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(secs)} full {name} step(s), {sum(secs):.1f} s of CPU time, "
+                      f"{per * 1e3:.0f} ms per step"}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed as the reference arm (rank 0 only): each step is
+    one full oracle step of the workload on the host cores."""
+    if rank != 0:
+        return None
+    o = OracleStep(args.workload)
+    for _ in range(args.warmup):
+        o.run()
+    secs = [o.run() for _ in range(args.steps)]
+    ms = 1e3 * sum(secs) / len(secs)
+    value = o.nodes / (ms / 1e3)
+    cores = cpu_cores()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"one full {args.workload} step per timed step"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res, wl = run_ours(args, rank, world)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            del wl
+            res["cpu_baseline"] = cpu_baseline(args.workload)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
