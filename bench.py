@@ -64,9 +64,8 @@ class Workload:
         self.w_lm = nrm((V, d), synth.WEIGHT_STD)
         self.w_proj = nrm((d, 3 * d), synth.WEIGHT_STD)
         ctx = synth.ctx_lengths(c, gc)
-        kc, vc, table = synth.paged_kv(ctx.tolist(), self.Hkv, self.D, c["page"], self.dt, gc,
-                                       device=device)
-        self.k_cache, self.v_cache = kc, vc
+        kc, vc, table = synth.paged_kv(ctx.tolist(), self.Hkv, self.D, c["page"], self.dt, gc)
+        self.k_cache, self.v_cache = kc.to(device), vc.to(device)
         self.block_table, self.ctx_lens = table.to(device), ctx.to(device)
         # per-step inputs: drafter rows per depth, verify-row activations
         self.P = [1 if s == 0 else self.width for s in range(self.depth)]
@@ -79,7 +78,7 @@ class Workload:
         host["h"] = [synth.normal((B * R, d), 1.0, self.dt, gc) for _ in range(3)]
         host["x_v"] = synth.normal((B * R, d), 1.0, self.dt, gc)
         if self.T > 0:
-            host["logits"] = synth.target_logits((B, R, V), gc, device=device).cpu()
+            host["logits"] = synth.target_logits((B, R, V), gc)
         self.host = {k: ([t.pin_memory() for t in v] if isinstance(v, list) else v.pin_memory())
                      for k, v in host.items()}
         self.dev_in = {k: ([t.to(device) for t in v] if isinstance(v, list) else v.to(device))
