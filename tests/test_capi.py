@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads without a GPU, exports every call that
+include/eagle.h declares, and validates arguments on the host (no GPU needed:
+every case below returns before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "eagle.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from eagle_speculative_decoding_gb300 import binding, build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    return binding.lib()
+
+
+def declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(eagle_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared()
+    for n in ("eagle_fuse_proj", "eagle_tree_attn", "eagle_lmhead_topk", "eagle_tree_expand",
+              "eagle_tree_expand_finalize", "eagle_tree_verify"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert L.eagle_status_string(0) == b"EAGLE_OK"
+    assert L.eagle_status_string(8) == b"EAGLE_ERR_TIMEOUT"
+    assert L.eagle_status_string(99) == b"EAGLE_ERR_UNKNOWN"
+
+
+def test_host_validation_without_gpu(L):
+    N = None
+    # verify: null pointers, negative sizes, sampled proposals at T = 0, deep trees
+    assert L.eagle_tree_verify(1, 4, 8, N, N, N, N, N, N, 1.0, 0, 0, 0, N, 2, N, N, N, N, 0, N, N) == 1
+    p = ctypes.c_void_p(16)
+    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, p, 0.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 1
+    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, p, 1.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 2
+    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 0, 0, 0, N, 65, p, p, p, N, 0, N, N) == 2
+    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 0, 0, 0, N, 2, p, p, p, N, 0, N, N) == 3
+    # lm head: k > 32 unsupported, k > V invalid, V not a multiple of 128
+    assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 33, 1.0, p, p, N, N, 1, N, 0, N, N) == 2
+    assert L.eagle_lmhead_topk(p, p, N, 4, 64, 128, 200, 1.0, p, p, N, N, 1, N, 0, N, N) == 1
+    assert L.eagle_lmhead_topk(p, p, N, 4, 64, 100, 1, 1.0, p, p, N, N, 1, N, 0, N, N) == 2
+    assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 1, 0.0, p, p, N, N, 1, N, 0, N, N) == 1
+    assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 1, 1.0, p, p, N, N, 1, N, 0, N, N) == 3
+    # fuse_proj: d not a multiple of 128
+    assert L.eagle_fuse_proj(p, p, p, p, N, p, 4, 100, 1, N, 0, N, N) == 2
+    assert L.eagle_fuse_proj(p, p, p, p, N, p, 4, 128, 1, N, 0, N, N) == 3
+    # attention: R > 64, D not in {64, 128}, page size != 16, Hq % Hkv
+    base = [p, p, p, p, p, 4, p, 2, p, p, p, N]
+    assert L.eagle_tree_attn(*base, 1, 65, 4, 2, 128, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 2
+    assert L.eagle_tree_attn(*base, 1, 8, 4, 2, 96, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 2
+    assert L.eagle_tree_attn(*base, 1, 8, 4, 2, 128, 32, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 2
+    assert L.eagle_tree_attn(*base, 1, 8, 5, 2, 128, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 1
+    # expand: width 0, k > 32, max_nodes too small for the step
+    assert L.eagle_tree_expand(1, 0, 0, 2, 16, p, p, p, p, p, p, p, p, p, p, N, N) == 1
+    assert L.eagle_tree_expand(1, 0, 2, 33, 64, p, p, p, p, p, p, p, p, p, p, N, N) == 2
+    assert L.eagle_tree_expand(1, 3, 2, 2, 12, p, p, p, p, p, p, p, p, p, p, N, N) == 1
+    assert L.eagle_tree_expand_finalize(1, 16, 8, 4, p, p, p, p, p, N, p, p, p, p, p, p, p, N, N) == 1
+    assert L.eagle_tree_expand_finalize(1, 16, 8, 65, p, p, p, p, p, N, p, p, p, p, p, p, p, N, N) == 2
+
+
+def test_workspace_queries(L):
+    assert L.eagle_lmhead_topk_workspace_size(61, 4096, 128256, 1, 1) > 0
+    assert L.eagle_fuse_proj_workspace_size(61, 4096, 1) > 0
+    assert L.eagle_tree_verify_workspace_size(4, 61, 128256) >= 4 * 61 * 12
