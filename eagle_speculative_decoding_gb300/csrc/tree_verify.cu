@@ -16,6 +16,9 @@
 //              stop row for the bonus token.
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace eagle {
@@ -316,6 +319,105 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
     stats = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
     amax = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
   }
+  const float inv_t = greedy ? 0.f : 1.f / temperature;
+  if (need_stats) {
+    verify_rowstats_kernel<<<(unsigned)(B * R), kStatThreads, 0, s>>>(
+        target_logits, n_rows, R, V, inv_t, greedy ? 1 : 0, stats, amax, dev_status);
+    note_launch();
+  }
+  const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
+  verify_walk_kernel<<<B, kWalkThreads, 0, s>>>(
+      R, V, parent_row, token, n_rows, target_logits, target_argmax, stats, amax, greedy ? 1 : 0,
+      inv_t, (uint32_t)seed, (uint32_t)(seed >> 32), 2u * off_hi, off_lo, uniforms_override,
+      max_depth, accept_len, path_rows, out_tokens, dev_status);
+  note_launch();
+  return last_launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// eagle_tree_verify_noalloc: the same verification for callers that cannot
+// allocate device memory (for instance a plugin whose host framework owns
+// every device allocation and hands it only the input and output tensors, or
+// a latency-critical loop that may not call cudaMalloc because of its implicit
+// device-wide synchronisation).  The row statistics that eagle_tree_verify
+// keeps in the caller's workspace live here in one library-owned buffer of
+// fixed capacity, allocated statically when the library is loaded.
+namespace eagle {
+namespace {
+
+constexpr int kNoAllocMaxRows = 65536;  // B * R rows of statistics
+constexpr size_t kNoAllocScratchBytes =
+    ((size_t)kNoAllocMaxRows * sizeof(RowStat) + 255) / 256 * 256 + (size_t)kNoAllocMaxRows * 4;
+
+// One copy per GPU that loads the library, kept until the process exits.
+// Every call on a device shares it: two calls whose kernels overlap on that
+// device (for example on two streams) race on it.  Nothing in it needs to
+// start at zero: every statistic is written before it is read.
+static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::atomic<void*> g_scratch_ptr[kNoAllocMaxDevices];
+std::mutex g_scratch_mu;
+
+// Device address of g_verify_scratch on the current device.  In host code the
+// symbol's name is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress once per device, with that device current.
+void* noalloc_scratch(eagle_status* st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    *st = EAGLE_ERR_CUDA;
+    return nullptr;
+  }
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || !p) {
+      *st = EAGLE_ERR_CUDA;
+      return nullptr;
+    }
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+}  // namespace
+}  // namespace eagle
+
+extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* parent_row,
+                                         const int32_t* token, const int32_t* n_rows,
+                                         const float* target_logits, const int32_t* target_argmax,
+                                         const float* draft_logits, float temperature,
+                                         int proposal_mode, uint64_t seed, uint64_t offset,
+                                         const float* uniforms_override, int max_depth,
+                                         int32_t* accept_len, int32_t* path_rows,
+                                         int32_t* out_tokens, int32_t* dev_status, void* stream) {
+  (void)draft_logits;
+  if (B <= 0 || R <= 0 || V < 2 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
+  if (!parent_row || !token || !accept_len || !path_rows || !out_tokens) return EAGLE_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || isinf(temperature)) return EAGLE_ERR_INVALID_ARG;
+  if (proposal_mode != EAGLE_PROPOSAL_DETERMINISTIC && proposal_mode != EAGLE_PROPOSAL_SAMPLED)
+    return EAGLE_ERR_INVALID_ARG;
+  const bool greedy = temperature == 0.f;
+  if (proposal_mode == EAGLE_PROPOSAL_SAMPLED) return greedy ? EAGLE_ERR_INVALID_ARG : EAGLE_ERR_UNSUPPORTED;
+  if (greedy && !target_logits && !target_argmax) return EAGLE_ERR_INVALID_ARG;
+  if (!greedy && !target_logits) return EAGLE_ERR_INVALID_ARG;
+  if (R > kMaxVerifyRows || max_depth > 64) return EAGLE_ERR_UNSUPPORTED;
+  if ((offset >> 63) != 0) return EAGLE_ERR_INVALID_ARG;
+  // the built-in scratch holds statistics for at most kNoAllocMaxRows rows
+  if ((long long)B * R > kNoAllocMaxRows) return EAGLE_ERR_WORKSPACE;
+  const bool need_stats = !greedy || !target_argmax;
+  RowStat* stats = nullptr;
+  int32_t* amax = nullptr;
+  if (need_stats) {
+    eagle_status st = EAGLE_OK;
+    char* base = static_cast<char*>(noalloc_scratch(&st));
+    if (!base) return st;
+    stats = reinterpret_cast<RowStat*>(base);
+    amax = reinterpret_cast<int32_t*>(base + ((size_t)kNoAllocMaxRows * sizeof(RowStat) + 255) / 256 * 256);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float inv_t = greedy ? 0.f : 1.f / temperature;
   if (need_stats) {
     verify_rowstats_kernel<<<(unsigned)(B * R), kStatThreads, 0, s>>>(

@@ -277,6 +277,33 @@ int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row, const int3
                       int32_t* path_rows, int32_t* out_tokens, void* ws, size_t ws_bytes,
                       int32_t* dev_status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * eagle_tree_verify_noalloc -- eagle_tree_verify without a workspace.
+ * The pages have no counterpart of this call: it exists for callers that
+ * cannot allocate device memory, such as a plugin whose host framework owns
+ * every device allocation and passes it only its input and output tensors,
+ * or a latency-critical loop that must not call cudaMalloc (which can
+ * synchronise the whole device).  Arguments, outputs and semantics are those
+ * of eagle_tree_verify minus `ws` / `ws_bytes`; the row statistics live in a
+ * fixed buffer inside the library instead.
+ *   Capacity: B * R <= 65536 rows; larger calls return EAGLE_ERR_WORKSPACE
+ *   without launching anything.  The buffer (768 KB) is a static device
+ *   array: every GPU that loads the library holds one copy until the process
+ *   exits, and no call allocates or frees memory.
+ *   The first call on a device looks up the buffer's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the buffer and it keeps the last call's
+ *   contents (no field needs to start at zero); calls whose kernels overlap
+ *   on the same device race on it, so serialise them (e.g. one stream).
+ * ---------------------------------------------------------------------- */
+int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* parent_row,
+                              const int32_t* token, const int32_t* n_rows,
+                              const float* target_logits, const int32_t* target_argmax,
+                              const float* draft_logits, float temperature, int proposal_mode,
+                              uint64_t seed, uint64_t offset, const float* uniforms_override,
+                              int max_depth, int32_t* accept_len, int32_t* path_rows,
+                              int32_t* out_tokens, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
