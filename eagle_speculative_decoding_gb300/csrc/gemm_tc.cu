@@ -34,10 +34,23 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr int kMaxAcc = 4;  // TMEM accumulator buffers (as many as 512 columns hold)
 constexpr int kTileA = 128 * 128;  // bytes of one A (weight) stage: 128 rows x 128 B
 constexpr int kMaxCtas = 256;      // upper bound used for workspace sizing
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared-memory ring of one GEMM: stage s holds the A tile at a0 + s*a_stride
+// (a_bytes of it loaded by TMA) and the B tile at b0 + s*b_stride (b_bytes).
+// The MMA always reads 128 A rows; rows past the loaded ones are don't-care
+// data that only reach accumulator rows the epilogue ignores.
+struct Ring {
+  uint32_t a0, a_stride, a_bytes;
+  uint32_t b0, b_stride, b_bytes;
+  int stages;
+  int n;     // MMA N (rows of the B tile)
+  int nbuf;  // TMEM accumulator buffers of n columns each
+};
 
 struct Seg {
   int a_row;  // first weight row of the tile
@@ -49,8 +62,8 @@ struct Seg {
 struct CtaShared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full[kMaxAcc];
+  uint64_t acc_empty[kMaxAcc];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;  // raised by any role whose bounded wait ran out
@@ -60,20 +73,23 @@ struct CtaShared {
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
 
-__host__ __device__ inline uint32_t tmem_cols_for(int bn) {
-  uint32_t need = 2u * (uint32_t)bn, c = 32;
+__host__ __device__ inline int acc_buffers_for(int n) {
+  const int b = 512 / n;
+  return b > kMaxAcc ? kMaxAcc : b;
+}
+__host__ __device__ inline uint32_t tmem_cols_for(int n) {
+  uint32_t need = (uint32_t)(acc_buffers_for(n) * n), c = 32;
   while (c < need) c <<= 1;
   return c;
 }
 
 // ------------------------------------------------------------ shared pipeline
 template <bool TF32, class Sched>
-__device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, uint32_t sA, uint32_t sB,
-                                             int stages, int bn) {
+__device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, const Ring& rg) {
   constexpr int kBke = TF32 ? 32 : 64;  // elements per 128-byte chunk
-  const uint64_t pol_w = l2_policy_evict_first();
-  const uint64_t pol_x = l2_policy_evict_last();
-  const uint32_t b_bytes = (uint32_t)bn * 128u;
+  const uint64_t pol_a = sc.a_policy();
+  const uint64_t pol_b = sc.b_policy();
+  const int stages = rg.stages;
   int it = 0;
   Seg sg;
   for (int si = 0; sc.seg(si, sg); ++si) {
@@ -82,9 +98,9 @@ __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, uin
       const uint32_t ph = (uint32_t)(it / stages) & 1u;
       if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u, &sh.abort_flag)) goto drain;
       const uint32_t fb = smem_u32(&sh.full[s]);
-      mbar_arrive_expect_tx(fb, (uint32_t)kTileA + b_bytes);
-      tma_load_2d(sA + s * kTileA, sc.map_a(), fb, kc * kBke, sg.a_row, pol_w);
-      tma_load_2d(sB + s * b_bytes, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_x);
+      mbar_arrive_expect_tx(fb, rg.a_bytes + rg.b_bytes);
+      tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
+      tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
     }
   }
   return;
@@ -103,22 +119,21 @@ drain:
 }
 
 template <bool TF32, class Sched>
-__device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, uint32_t sA, uint32_t sB,
-                                        int stages, int bn) {
-  const uint32_t idesc = mma_idesc(TF32 ? 2 : 1, 128, bn);
-  const uint32_t b_bytes = (uint32_t)bn * 128u;
+__device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, const Ring& rg) {
+  const uint32_t idesc = mma_idesc(TF32 ? 2 : 1, 128, rg.n);
+  const int stages = rg.stages;
   int it = 0, acc = 0;
   bool ok = true;
   Seg sg;
   for (int si = 0; ok && sc.seg(si, sg); ++si, ++acc) {
-    const int buf = acc & 1;
-    const uint32_t aph = (uint32_t)(acc >> 1) & 1u;
+    const int buf = acc % rg.nbuf;
+    const uint32_t aph = (uint32_t)(acc / rg.nbuf) & 1u;
     if (!mbar_wait(smem_u32(&sh.acc_empty[buf]), aph ^ 1u, &sh.abort_flag)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = sh.tmem_base + (uint32_t)(buf * bn);
+    const uint32_t d_tmem = sh.tmem_base + (uint32_t)(buf * rg.n);
     for (int kc = sg.k0; kc < sg.k1; ++kc, ++it) {
       const int s = it % stages;
       const uint32_t ph = (uint32_t)(it / stages) & 1u;
@@ -127,8 +142,8 @@ __device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, uint32_t
         break;
       }
       tc_fence_after();
-      const uint64_t da = smem_desc_sw128(sA + s * kTileA);
-      const uint64_t db = smem_desc_sw128(sB + s * b_bytes);
+      const uint64_t da = smem_desc_sw128(rg.a0 + s * rg.a_stride);
+      const uint64_t db = smem_desc_sw128(rg.b0 + s * rg.b_stride);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint32_t accum = (kc == sg.k0 && kk == 0) ? 0u : 1u;
@@ -170,7 +185,7 @@ __device__ __forceinline__ void cta_setup(CtaShared& sh, int stages, uint32_t tm
       mbar_init(smem_u32(&sh.full[s]), 1);
       mbar_init(smem_u32(&sh.empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxAcc; ++b) {
       mbar_init(smem_u32(&sh.acc_full[b]), 1);
       mbar_init(smem_u32(&sh.acc_empty[b]), 4);  // one arrive per epilogue warp
     }
@@ -201,373 +216,392 @@ __device__ __forceinline__ void cta_teardown(CtaShared& sh, uint32_t tmem_cols, 
 
 // ====================================================================== LM head
 struct LmParams {
-  int M, V, K, bn, groups, ctas_per_group, n_vtiles, nk, stages;
+  int M, V, K, groups, ctas_per_group, n_vtiles, nk, stages;
+  int tn;  // vocabulary rows per tile (MMA N, multiple of 16, <= 128)
+  int xr;  // activation rows loaded per stage (group rows rounded up to 16)
   float inv_t;
   const float* bias;
   int32_t* topk_ids;
   float* topk_lp;
   float* row_max;
   float* row_sumexp;
-  float2* part_ms;   // [cta][bn]       (max of z/T, sum exp)
-  float* part_v;     // [cta][bn][K]    top-k logits (z)
-  int* part_i;       // [cta][bn][K]
-  int* part_cnt;     // [cta][bn]
+  float2* part_ms;   // [cta][128]       (max of z/T, sum exp)
+  float* part_v;     // [cta][128][K]    sorted top-k logits (z)
+  int* part_i;       // [cta][128][K]
+  int* part_cnt;     // [cta][128]
   int* counters;     // [groups]
   int32_t* status;
 };
 
-template <bool TF32>
+// LM head, not swapped: the (up to) 128 activation rows of a group are the
+// MMA's M side (rows past M are zero-filled by TMA), 128 vocabulary rows of
+// W_U the N side, so TMEM lane e holds activation row e and each epilogue
+// thread scans its own row's logits with no cross-thread reduction.
 struct LmSched {
-  const CUtensorMap* mw;
   const CUtensorMap* mx;
-  int t0, t1, b_row, nk;
+  const CUtensorMap* mw;
+  int t0, t1, a_row, nk, tn;
+  bool w_reused;  // several activation groups read the same W tiles
   __device__ bool seg(int i, Seg& s) const {
     const int t = t0 + i;
     if (t >= t1) return false;
-    s.a_row = t * 128;
-    s.b_row = b_row;
+    s.a_row = a_row;
+    s.b_row = t * tn;
     s.k0 = 0;
     s.k1 = nk;
     s.tile = t;
     return true;
   }
-  __device__ const CUtensorMap* map_a() const { return mw; }
-  __device__ const CUtensorMap* map_b(int) const { return mx; }
-  __device__ int b_x(int kc) const { return kc * (TF32 ? 32 : 64); }
+  __device__ const CUtensorMap* map_a() const { return mx; }
+  __device__ const CUtensorMap* map_b(int) const { return mw; }
+  __device__ int b_x(int kc) const { return kc * 64; }
+  __device__ uint64_t a_policy() const { return l2_policy_evict_last(); }
+  __device__ uint64_t b_policy() const {
+    return w_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
+  }
 };
 
-// Insert-into-list merge of the candidates held by a warp.  Lane j < cnt holds
-// entry j of the column's sorted top-K list (lv, li).  Candidate values come
-// in per lane (up to 4 per lane, flagged by `cand`); the best remaining
-// candidate is inserted until none beats the list's K-th entry.
-template <int NPL>
-__device__ __forceinline__ void warp_topk_merge(float (&z)[NPL], int (&id)[NPL], bool (&cand)[NPL],
-                                                float& lv, int& li, int& cnt, int K) {
-  const int lane = threadIdx.x & 31;
-  float tv = -INFINITY;
-  int ti = 0x7fffffff;
-  if (cnt == K) {
-    tv = __shfl_sync(0xffffffffu, lv, K - 1);
-    ti = __shfl_sync(0xffffffffu, li, K - 1);
+// Running state of one activation row, held in registers by the thread that
+// owns the row: online max / sum-exp of z/T and the sorted top-K list (z
+// descending, id ascending) of the ids seen so far.  KMAX >= K is a
+// compile-time bound so the list lives in registers; entries past K are
+// The real list occupies the last K slots; the first KMAX - K slots hold +inf
+// sentinels that nothing displaces, so the K-th best is always slot KMAX - 1
+// (a static register index).  Insertion is a predicated compare-and-swap
+// pass, executed by the whole warp only when some lane holds a candidate.
+template <int KMAX>
+struct RowTopK {
+  float m, s;          // running max of z/T and sum of exp(z/T - m)
+  float av[KMAX];      // sorted top-K values (z)
+  int ai[KMAX];        // ... their ids
+  float tv;            // K-th best so far (-inf while fewer than K)
+  int ti;
+  bool nan_seen;
+};
+
+template <int KMAX>
+__device__ __forceinline__ void row_init(RowTopK<KMAX>& r, int K) {
+  r.m = -INFINITY;
+  r.s = 0.f;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) cand[i] = cand[i] && better(z[i], id[i], tv, ti);
+  for (int j = 0; j < KMAX; ++j) {
+    const bool sentinel = j < KMAX - K;
+    r.av[j] = sentinel ? INFINITY : -INFINITY;
+    r.ai[j] = sentinel ? -1 : 0x7fffffff;
   }
-  for (;;) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+  r.tv = -INFINITY;
+  r.ti = 0x7fffffff;
+  r.nan_seen = false;
+}
+
+// Fold 16 consecutive vocabulary ids id0.. (values v, the first `valid` of
+// them real; valid <= 0 for a lane without a row) into the row.  Must be
+// called by all 32 lanes of the warp together.
+template <int KMAX>
+__device__ __forceinline__ void row_chunk(RowTopK<KMAX>& r, const float (&v)[16], int id0, int valid,
+                                          float inv_t, int K) {
+  float y[16];
+  float cm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i)
-      if (cand[i] && better(z[i], id[i], bv, bi)) {
-        bv = z[i];
-        bi = id[i];
+  for (int j = 0; j < 16; ++j) {
+    y[j] = j < valid ? v[j] * inv_t : -INFINITY;
+    r.nan_seen |= (j < valid) && isnan(v[j]);
+    cm = fmaxf(cm, y[j]);
+  }
+  const float nm = fmaxf(r.m, cm);
+  if (nm != -INFINITY) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc += exp2f((y[j] - nm) * kLog2e);
+    r.s = r.s * exp2f((r.m - nm) * kLog2e) + acc;
+    r.m = nm;
+  }
+  // candidates: values that beat the current K-th best
+  unsigned cmask = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < valid && better(v[j], id0 + j, r.tv, r.ti)) cmask |= 1u << j;
+  // one candidate per lane per round, the whole warp in step
+  while (__any_sync(0xffffffffu, cmask != 0)) {
+    const int jc = cmask ? __ffs(cmask) - 1 : -1;
+    cmask &= cmask - 1;
+    float z = -INFINITY;
+    int id = 0x7fffffff;
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+      if (t == jc) {
+        z = v[t];
+        id = id0 + t;
       }
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+      const bool b = better(z, id, r.av[t], r.ai[t]);
+      const float oz = r.av[t];
+      const int oi = r.ai[t];
+      r.av[t] = b ? z : oz;
+      r.ai[t] = b ? id : oi;
+      z = b ? oz : z;
+      id = b ? oi : id;
+    }
+    r.tv = r.av[KMAX - 1];
+    r.ti = r.ai[KMAX - 1];
+  }
+}
+
+// Publish every row's partial state (running max / sum-exp and its sorted
+// top-K list) for lmhead_merge_kernel.
+template <int KMAX>
+__device__ __forceinline__ void lm_publish(const LmParams& p, const RowTopK<KMAX>& r, int nrow, int e) {
+  const int cta = blockIdx.x, K = p.K;
+  if (e < nrow) {
+    p.part_ms[(size_t)cta * 128 + e] = make_float2(r.m, r.s);
+    int cnt = 0;
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+      const int j = t - (KMAX - K);  // position in the reported list
+      if (j >= 0 && r.ai[t] != 0x7fffffff) {
+        p.part_v[((size_t)cta * 128 + e) * K + j] = r.av[t];
+        p.part_i[((size_t)cta * 128 + e) * K + j] = r.ai[t];
+        cnt = j + 1;
+      }
+    }
+    p.part_cnt[(size_t)cta * 128 + e] = cnt;
+  }
+}
+
+// Merge of the per-CTA partials: one warp per activation row.  Log-sum-exp by
+// max / rescale over the CTAs; top-K by K rounds of "best head among the
+// CTAs' sorted lists", the lists staged in this warp's shared memory.
+__global__ void __launch_bounds__(256) lmhead_merge_kernel(const LmParams p, int rows_per_cta) {
+  extern __shared__ __align__(16) unsigned char msm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x * rows_per_cta + warp;
+  if (warp >= rows_per_cta || m >= p.M) return;
+  const int K = p.K, g = m / 128, row = m % 128;
+  const int nc = p.ctas_per_group, G = p.groups;
+  const size_t per_warp = ((size_t)nc * (K * 8 + 4) + 15) / 16 * 16;
+  float* sv = reinterpret_cast<float*>(msm + warp * per_warp);
+  int* si = reinterpret_cast<int*>(sv + nc * K);
+  int* sc = si + nc * K;
+  float M = -INFINITY;
+  for (int c = lane; c < nc; c += 32) {
+    const int cnt = p.part_cnt[(size_t)(g + G * c) * 128 + row];
+    sc[c] = cnt;
+    const size_t base = ((size_t)(g + G * c) * 128 + row) * K;
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      sv[c * K + j] = p.part_v[base + j];
+      si[c * K + j] = p.part_i[base + j];
+    }
+    M = fmaxf(M, p.part_ms[(size_t)(g + G * c) * 128 + row].x);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = 0.f;
+  for (int c = lane; c < nc; c += 32) {
+    const float2 ms = p.part_ms[(size_t)(g + G * c) * 128 + row];
+    if (ms.x != -INFINITY) S += ms.y * exp2f((ms.x - M) * kLog2e);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  __syncwarp();
+  constexpr int kPer = kMaxCtas / 32;  // lists owned per lane
+  float hv[kPer];
+  int hi[kPer], hp[kPer], hc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = lane + 32 * i;
+    hp[i] = 0;
+    hc[i] = c < nc ? sc[c] : 0;
+    hv[i] = hc[i] > 0 ? sv[c * K] : -INFINITY;
+    hi[i] = hc[i] > 0 ? si[c * K] : 0x7fffffff;
+  }
+  const float lse = M + logf(S);
+  const size_t ob = (size_t)m * K;
+  for (int rnd = 0; rnd < K; ++rnd) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff, bs = -1;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (hp[i] < hc[i] && better(hv[i], hi[i], bv, bi)) {
+        bv = hv[i];
+        bi = hi[i];
+        bs = i;
+      }
+    int owner = bs >= 0 ? lane : 32;
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int ow = __shfl_xor_sync(0xffffffffu, owner, o);
       if (better(ov, oi, bv, bi)) {
         bv = ov;
         bi = oi;
+        owner = ow;
       }
     }
-    if (bi == 0x7fffffff) break;
-    const unsigned ahead = __ballot_sync(0xffffffffu, lane < cnt && better(lv, li, bv, bi));
-    const int pos = __popc(ahead);
-    const float nv = __shfl_up_sync(0xffffffffu, lv, 1);
-    const int ni = __shfl_up_sync(0xffffffffu, li, 1);
-    if (lane > pos) {
-      lv = nv;
-      li = ni;
-    }
-    if (lane == pos) {
-      lv = bv;
-      li = bi;
-    }
-    cnt = min(cnt + 1, K);
-#pragma unroll
-    for (int i = 0; i < NPL; ++i)
-      if (cand[i] && id[i] == bi && z[i] == bv) cand[i] = false;
-    if (cnt == K) {
-      tv = __shfl_sync(0xffffffffu, lv, K - 1);
-      ti = __shfl_sync(0xffffffffu, li, K - 1);
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) cand[i] = cand[i] && better(z[i], id[i], tv, ti);
-    }
-  }
-}
-
-// Per-column running state of the LM-head epilogue (one column = one
-// activation row): online max / sum-exp of z/T and a sorted top-K list.
-struct LmEpi {
-  float* T;      // [16][128] transpose buffer: 16 columns x 128 vocab rows
-  float* col_m;  // [bn]
-  float* col_s;  // [bn]
-  int* col_c;    // [bn] entries in the list
-  float* top_v;  // [bn][K]
-  int* top_i;    // [bn][K]
-  int K;
-  float inv_t;
-};
-
-__device__ __forceinline__ LmEpi lm_epi_carve(unsigned char* p, int bn, int K, float inv_t) {
-  LmEpi E;
-  E.T = reinterpret_cast<float*>(p);
-  E.col_m = E.T + 16 * 128;
-  E.col_s = E.col_m + bn;
-  E.col_c = reinterpret_cast<int*>(E.col_s + bn);
-  E.top_v = reinterpret_cast<float*>(E.col_c + bn);
-  E.top_i = reinterpret_cast<int*>(E.top_v + bn * K);
-  E.K = K;
-  E.inv_t = inv_t;
-  return E;
-}
-
-// Fold 16 columns of one 128-row vocabulary tile into the running state.
-// Called by the 128 epilogue threads together: thread e holds v[j] = z of
-// vocabulary row v0+e for column c16*16+j.  Warp ew then owns columns
-// ew*4..ew*4+3 of the chunk.
-__device__ __forceinline__ void lm_chunk(const LmEpi& E, const float (&v)[16], int e, int ew,
-                                         int lane, int v0, int c16, int ncol) {
-  const int K = E.K;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) E.T[j * 128 + e] = v[j];
-  named_bar(1, kEpiThreads);
-#pragma unroll 1
-  for (int jj = 0; jj < 4; ++jj) {
-    const int j = ew * 4 + jj, col = c16 * 16 + j;
-    if (col >= ncol) continue;
-    float z[4];
-    int id[4];
-    bool cand[4];
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      z[i] = E.T[j * 128 + lane + 32 * i];
-      id[i] = v0 + lane + 32 * i;
-      tmax = fmaxf(tmax, z[i] * E.inv_t);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-    float ts = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ts += exp2f((z[i] * E.inv_t - tmax) * kLog2e);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
-    int cnt = E.col_c[col];
-    float lv = lane < cnt ? E.top_v[col * K + lane] : -INFINITY;
-    int li = lane < cnt ? E.top_i[col * K + lane] : 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) cand[i] = !isnan(z[i]);
-    warp_topk_merge<4>(z, id, cand, lv, li, cnt, K);
-    if (lane < cnt) {
-      E.top_v[col * K + lane] = lv;
-      E.top_i[col * K + lane] = li;
-    }
     if (lane == 0) {
-      const float om = E.col_m[col];
-      const float nm = fmaxf(om, tmax);
-      E.col_s[col] = (om == -INFINITY ? 0.f : E.col_s[col] * exp2f((om - nm) * kLog2e)) +
-                     ts * exp2f((tmax - nm) * kLog2e);
-      E.col_m[col] = nm;
-      E.col_c[col] = cnt;
+      p.topk_ids[ob + rnd] = bi == 0x7fffffff ? -1 : bi;
+      p.topk_lp[ob + rnd] = bi == 0x7fffffff ? -INFINITY : bv * p.inv_t - lse;
     }
-    __syncwarp();
-  }
-  named_bar(1, kEpiThreads);
-}
-
-// Publish this CTA's per-column partial state; the last CTA of the group
-// (atomic ticket, no waiting) merges all partials of the group and writes the
-// final top-k ids, log-probs and row statistics.
-__device__ __forceinline__ void lm_publish_merge(const LmParams& p, const LmEpi& E, int* flag, int g,
-                                                 int m0, int ncol, int et, int ew, int lane) {
-  const int cta = blockIdx.x, bn = p.bn, K = p.K;
-  for (int c = et; c < ncol; c += kEpiThreads) {
-    p.part_ms[(size_t)cta * bn + c] = make_float2(E.col_m[c], E.col_s[c]);
-    p.part_cnt[(size_t)cta * bn + c] = E.col_c[c];
-  }
-  for (int x = et; x < ncol * K; x += kEpiThreads) {
-    p.part_v[(size_t)cta * bn * K + x] = E.top_v[x];
-    p.part_i[(size_t)cta * bn * K + x] = E.top_i[x];
-  }
-  __threadfence();
-  named_bar(1, kEpiThreads);
-  if (et == 0) *flag = (atomicAdd(&p.counters[g], 1) == p.ctas_per_group - 1) ? 1 : 0;
-  named_bar(1, kEpiThreads);
-  if (!*reinterpret_cast<volatile int*>(flag)) return;
-  __threadfence();
-  const int c0 = g * p.ctas_per_group, nc = p.ctas_per_group;
-  for (int col = ew; col < ncol; col += 4) {
-    float M = -INFINITY;
-    for (int c = lane; c < nc; c += 32) M = fmaxf(M, p.part_ms[(size_t)(c0 + c) * bn + col].x);
+    if (lane == owner && bs >= 0) {
 #pragma unroll
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float S = 0.f;
-    for (int c = lane; c < nc; c += 32) {
-      const float2 ms = p.part_ms[(size_t)(c0 + c) * bn + col];
-      if (ms.x != -INFINITY) S += ms.y * exp2f((ms.x - M) * kLog2e);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-    float lv = -INFINITY;
-    int li = 0x7fffffff, cnt = 0;
-    for (int f0 = 0; f0 < nc * K; f0 += 32) {
-      const int f = f0 + lane;
-      float z[1] = {-INFINITY};
-      int id[1] = {0x7fffffff};
-      bool cand[1] = {false};
-      if (f < nc * K) {
-        const int c = f / K, j = f % K;
-        if (j < p.part_cnt[(size_t)(c0 + c) * bn + col]) {
-          z[0] = p.part_v[((size_t)(c0 + c) * bn + col) * K + j];
-          id[0] = p.part_i[((size_t)(c0 + c) * bn + col) * K + j];
-          cand[0] = true;
+      for (int i = 0; i < kPer; ++i)
+        if (i == bs) {
+          const int c = lane + 32 * i;
+          ++hp[i];
+          if (hp[i] < hc[i]) {
+            hv[i] = sv[c * K + hp[i]];
+            hi[i] = si[c * K + hp[i]];
+          }
         }
-      }
-      warp_topk_merge<1>(z, id, cand, lv, li, cnt, K);
     }
-    const int row = m0 + col;
-    const float lse = M + logf(S);
-    if (lane < K) {
-      p.topk_ids[(size_t)row * K + lane] = lane < cnt ? li : -1;
-      p.topk_lp[(size_t)row * K + lane] = lane < cnt ? lv * p.inv_t - lse : -INFINITY;
-    }
-    if (lane == 0) {
-      if (p.row_max) p.row_max[row] = M;
-      if (p.row_sumexp) p.row_sumexp[row] = S;
-    }
+  }
+  if (lane == 0) {
+    if (p.row_max) p.row_max[m] = M;
+    if (p.row_sumexp) p.row_sumexp[m] = S;
   }
 }
 
-template <bool TF32>
+template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
-    lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+    lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                        const LmParams p) {
   __shared__ CtaShared sh;
   extern __shared__ unsigned char dsmem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bn = p.bn, stages = p.stages;
-  const uint32_t tmem_cols = tmem_cols_for(bn);
+  const int stages = p.stages, K = p.K;
+  const int tn = p.tn;  // vocabulary rows per tile (MMA N)
+  const uint32_t tmem_cols = tmem_cols_for(tn);
   const uint32_t base = align1024(smem_u32(dsmem));
-  const uint32_t sA = base, sB = sA + stages * kTileA;
   unsigned char* gbase = dsmem + (base - smem_u32(dsmem));
-  const LmEpi E = lm_epi_carve(gbase + stages * (kTileA + bn * 128), bn, p.K, p.inv_t);
+  // W tiles, then the activation tiles (only xr rows each are loaded), then
+  // slack so that the MMA's 128-row view of the last activation tile stays
+  // inside the allocation, then the per-row top-K lists
+  Ring rg;
+  rg.stages = stages;
+  rg.n = tn;
+  rg.nbuf = acc_buffers_for(tn);
+  rg.b0 = base;
+  rg.b_stride = kTileA;
+  rg.b_bytes = (uint32_t)tn * 128u;
+  rg.a0 = base + stages * kTileA;
+  rg.a_stride = rg.a_bytes = (uint32_t)p.xr * 128u;
+  (void)gbase;
 
-  const int g = blockIdx.x / p.ctas_per_group, ci = blockIdx.x % p.ctas_per_group;
-  LmSched<TF32> sc;
-  sc.mw = &map_w;
+  const int g = blockIdx.x % p.groups, ci = blockIdx.x / p.groups;
+  LmSched sc;
   sc.mx = &map_x;
+  sc.mw = &map_w;
   sc.t0 = (int)((long long)ci * p.n_vtiles / p.ctas_per_group);
   sc.t1 = (int)((long long)(ci + 1) * p.n_vtiles / p.ctas_per_group);
-  sc.b_row = g * bn;
+  sc.a_row = g * 128;
   sc.nk = p.nk;
-  const int m0 = g * bn;
-  const int ncol = min(bn, p.M - m0);
+  sc.tn = tn;
+  sc.w_reused = p.groups > 1;
+  const int m0 = g * 128;
+  const int nrow = min(128, p.M - m0);
 
   if (threadIdx.x == 0) {
-    tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_x);
-  }
-  for (int c = threadIdx.x; c < bn; c += kThreads) {
-    E.col_m[c] = -INFINITY;
-    E.col_s[c] = 0.f;
-    E.col_c[c] = 0;
+    tma_prefetch_desc(&map_w);
   }
   cta_setup(sh, stages, tmem_cols);
 
   if (warp == 0) {
-    if (lane == 0) run_producer<TF32>(sc, sh, sA, sB, stages, bn);
+    if (lane == 0) run_producer<false>(sc, sh, rg);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<TF32>(sc, sh, sA, sB, stages, bn);
+    if (lane == 0) run_mma<false>(sc, sh, rg);
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;           // TMEM lane quarter of this warp
-    const int e = q * 32 + lane;      // weight row inside the tile
-    const int ew = warp - 2;          // epilogue warp 0..3
+    const int q = warp & 3;       // TMEM lane quarter of this warp
+    const int e = q * 32 + lane;  // activation row inside the group
+    const bool valid = e < nrow;
+    RowTopK<KMAX> r;
+    row_init(r, K);
     int acc = 0;
     Seg sg;
     for (int si = 0; sc.seg(si, sg); ++si, ++acc) {
-      const int buf = acc & 1;
-      const uint32_t aph = (uint32_t)(acc >> 1) & 1u;
+      const int buf = acc % rg.nbuf;
+      const uint32_t aph = (uint32_t)(acc / rg.nbuf) & 1u;
       if (!epi_wait(sh, smem_u32(&sh.acc_full[buf]), aph)) break;
       tc_fence_after();
-      const int v0 = sg.tile * 128;
-      const float bias_e = p.bias ? p.bias[v0 + e] : 0.f;
-      const uint32_t taddr = sh.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * bn);
-      for (int c16 = 0; c16 * 16 < ncol; ++c16) {
+      const int v0 = sg.tile * tn;
+      const int vend = min(tn, p.V - v0);  // rows past V were zero-filled
+      const uint32_t taddr = sh.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * tn);
+#pragma unroll 1
+      for (int c16 = 0; c16 < tn / 16; ++c16) {
         float v[16];
         tmem_ld16(taddr + c16 * 16, v);
+        if (p.bias) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] += bias_e;
-        lm_chunk(E, v, e, ew, lane, v0, c16, ncol);
+          for (int j = 0; j < 16; ++j) v[j] += p.bias[min(v0 + c16 * 16 + j, p.V - 1)];
+        }
+        row_chunk(r, v, v0 + c16 * 16, valid ? vend - c16 * 16 : 0, p.inv_t, K);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
     }
+    if (r.nan_seen) set_status(p.status, EAGLE_ERR_NONFINITE);
     named_bar(1, kEpiThreads);
-    if (!*reinterpret_cast<volatile int*>(&sh.epi_abort))
-      lm_publish_merge(p, E, &sh.flag, g, m0, ncol, threadIdx.x - 64, ew, lane);
+    if (!*reinterpret_cast<volatile int*>(&sh.epi_abort)) lm_publish(p, r, nrow, e);
   }
   cta_teardown(sh, tmem_cols, p.status);
 }
 
-// fp32 LM head on the CUDA cores (exact fp32 products and sums).  Same
-// schedule and epilogue as the tensor-core kernel; 128 threads, thread e
-// computes vocabulary row v0+e against 16 activation rows at a time from
-// shared-memory tiles of 32 K-elements.
+// fp32 LM head on the CUDA cores (exact fp32 products and sums), same
+// schedule and epilogue: 128 threads, thread e owns activation row e of the
+// group; 16 vocabulary rows at a time from shared-memory tiles of 32 K-values.
 constexpr int kF32Kc = 32;
+template <int KMAX>
 __global__ void __launch_bounds__(kEpiThreads)
     lmhead_topk_f32_kernel(const float* __restrict__ x, const float* __restrict__ w, int d,
                            const LmParams p) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  __shared__ int flag;
-  float* Ws = reinterpret_cast<float*>(dsm);         // [128][kF32Kc + 1]
-  float* Xs = Ws + 128 * (kF32Kc + 1);                // [16][kF32Kc]
-  const LmEpi E = lm_epi_carve(reinterpret_cast<unsigned char*>(Xs + 16 * kF32Kc), p.bn, p.K, p.inv_t);
-  const int e = threadIdx.x, lane = e & 31, ew = e >> 5;
-  const int g = blockIdx.x / p.ctas_per_group, ci = blockIdx.x % p.ctas_per_group;
+  float* Xs = reinterpret_cast<float*>(dsm);        // [128][kF32Kc + 1]
+  float* Ws = Xs + 128 * (kF32Kc + 1);              // [16][kF32Kc]
+  const int e = threadIdx.x, K = p.K;
+  const int g = blockIdx.x % p.groups, ci = blockIdx.x / p.groups;
   const int t0 = (int)((long long)ci * p.n_vtiles / p.ctas_per_group);
   const int t1 = (int)((long long)(ci + 1) * p.n_vtiles / p.ctas_per_group);
-  const int m0 = g * p.bn, ncol = min(p.bn, p.M - m0);
-  for (int c = e; c < p.bn; c += kEpiThreads) {
-    E.col_m[c] = -INFINITY;
-    E.col_s[c] = 0.f;
-    E.col_c[c] = 0;
-  }
-  __syncthreads();
+  const int m0 = g * 128, nrow = min(128, p.M - m0);
+  RowTopK<KMAX> r;
+  row_init(r, K);
   for (int t = t0; t < t1; ++t) {
-    const int v0 = t * 128;
-    const float bias_e = p.bias ? p.bias[v0 + e] : 0.f;
-    for (int c16 = 0; c16 * 16 < ncol; ++c16) {
-      float v[16];
+    for (int v16 = 0; v16 < p.tn; v16 += 16) {
+      const int vb = t * p.tn + v16;
+      float acc[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = 0.f;
+      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
       for (int k0 = 0; k0 < d; k0 += kF32Kc) {
         __syncthreads();
         for (int i = e; i < 128 * kF32Kc; i += kEpiThreads) {
-          const int r = i / kF32Kc, c = i % kF32Kc;
-          Ws[r * (kF32Kc + 1) + c] = w[(size_t)(v0 + r) * d + k0 + c];
+          const int rr = i / kF32Kc, c = i % kF32Kc;
+          Xs[rr * (kF32Kc + 1) + c] = rr < nrow ? x[(size_t)(m0 + rr) * d + k0 + c] : 0.f;
         }
         for (int i = e; i < 16 * kF32Kc; i += kEpiThreads) {
-          const int r = i / kF32Kc, c = i % kF32Kc, m = m0 + c16 * 16 + r;
-          Xs[i] = (c16 * 16 + r < ncol) ? x[(size_t)m * d + k0 + c] : 0.f;
+          const int rr = i / kF32Kc, c = i % kF32Kc;
+          Ws[i] = vb + rr < p.V ? w[(size_t)(vb + rr) * d + k0 + c] : 0.f;
         }
         __syncthreads();
 #pragma unroll 4
         for (int c = 0; c < kF32Kc; ++c) {
-          const float wv = Ws[e * (kF32Kc + 1) + c];
+          const float xv = Xs[e * (kF32Kc + 1) + c];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = fmaf(wv, Xs[j * kF32Kc + c], v[j]);
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf(xv, Ws[j * kF32Kc + c], acc[j]);
         }
       }
+      if (p.bias) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] += bias_e;
-      lm_chunk(E, v, e, ew, lane, v0, c16, ncol);
+        for (int j = 0; j < 16; ++j) acc[j] += p.bias[min(vb + j, p.V - 1)];
+      }
+      row_chunk(r, acc, vb, e < nrow ? p.V - vb : 0, p.inv_t, K);
     }
   }
-  named_bar(1, kEpiThreads);
-  lm_publish_merge(p, E, &flag, g, m0, ncol, e, ew, lane);
+  if (r.nan_seen) set_status(p.status, EAGLE_ERR_NONFINITE);
+  __syncthreads();
+  lm_publish(p, r, nrow, e);
 }
 
 // ==================================================================== fuse_proj
@@ -611,6 +645,8 @@ struct FpSched {
   __device__ const CUtensorMap* map_a() const { return mw; }
   __device__ const CUtensorMap* map_b(int kc) const { return mx[kc / nkd]; }
   __device__ int b_x(int kc) const { return (kc % nkd) * (TF32 ? 32 : 64); }
+  __device__ uint64_t a_policy() const { return l2_policy_evict_first(); }
+  __device__ uint64_t b_policy() const { return l2_policy_evict_last(); }
 };
 
 template <bool TF32>
@@ -624,7 +660,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bn = p.bn, stages = p.stages;
   const uint32_t tmem_cols = tmem_cols_for(bn);
   const uint32_t base = align1024(smem_u32(dsmem));
-  const uint32_t sA = base, sB = sA + stages * kTileA;
+  Ring rg;
+  rg.stages = stages;
+  rg.n = bn;
+  rg.nbuf = acc_buffers_for(bn);
+  rg.a0 = base;
+  rg.a_stride = rg.a_bytes = kTileA;
+  rg.b0 = base + stages * kTileA;
+  rg.b_stride = rg.b_bytes = (uint32_t)bn * 128u;
 
   FpSched<TF32> sc;
   sc.mw = &map_w;
@@ -647,16 +690,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   cta_setup(sh, stages, tmem_cols);
 
   if (warp == 0) {
-    if (lane == 0) run_producer<TF32>(sc, sh, sA, sB, stages, bn);
+    if (lane == 0) run_producer<TF32>(sc, sh, rg);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<TF32>(sc, sh, sA, sB, stages, bn);
+    if (lane == 0) run_mma<TF32>(sc, sh, rg);
   } else {
     const int q = warp & 3, e = q * 32 + lane, et = threadIdx.x - 64;
     int acc = 0;
     Seg sg;
     for (int si = 0; sc.seg(si, sg); ++si, ++acc) {
-      const int buf = acc & 1;
-      const uint32_t aph = (uint32_t)(acc >> 1) & 1u;
+      const int buf = acc % rg.nbuf;
+      const uint32_t aph = (uint32_t)(acc / rg.nbuf) & 1u;
       if (!epi_wait(sh, smem_u32(&sh.acc_full[buf]), aph)) break;
       tc_fence_after();
       const int ot = sg.tile % p.n_otiles, gr = sg.tile / p.n_otiles;
@@ -758,14 +801,12 @@ int pick_bn(int M, int* groups) {
   return (per + 15) / 16 * 16;
 }
 
-int pick_stages(int bn, size_t extra) {
+int pick_stages(size_t stage, size_t extra) {
   const size_t budget = 227 * 1024 - 1024 - extra - 256;
-  const size_t stage = (size_t)kTileA + (size_t)bn * 128;
   int s = (int)(budget / stage);
   return s > kMaxStages ? kMaxStages : s;
 }
 
-size_t lm_epi_bytes(int bn, int K) { return 16 * 128 * 4 + (size_t)bn * (12 + 8 * (size_t)K); }
 
 }  // namespace
 }  // namespace eagle
@@ -777,11 +818,10 @@ extern "C" size_t eagle_lmhead_topk_workspace_size(int M, int d, int V, int k, i
   (void)V;
   (void)dtype;
   if (M <= 0 || k <= 0) return 0;
-  int G;
-  const int bn = pick_bn(M, &G);
-  const size_t n = (size_t)kMaxCtas * bn;
-  return round_up(n * 8, 256) + 2 * round_up(n * k * 4, 256) + round_up(n * 4, 256) +
-         round_up((size_t)G * 4, 256) + 1024;
+  const size_t G = (size_t)(M + 127) / 128;
+  const size_t n = (size_t)kMaxCtas * 128;  // one partial row per (CTA, group row)
+  (void)G;
+  return round_up(n * 8, 256) + 2 * round_up(n * k * 4, 256) + round_up(n * 4, 256) + 1024;
 }
 
 extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M, int d,
@@ -793,52 +833,51 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
     return EAGLE_ERR_INVALID_ARG;
   if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return EAGLE_ERR_INVALID_ARG;
   if (k > V) return EAGLE_ERR_INVALID_ARG;
-  if (M > 2048 || k > 32 || d % 64 || V % 128) return EAGLE_ERR_UNSUPPORTED;
+  if (M > 2048 || k > 32 || d % 64 || V % 16) return EAGLE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w_lm)) return EAGLE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < eagle_lmhead_topk_workspace_size(M, d, V, k, dtype)) return EAGLE_ERR_WORKSPACE;
-  const int esz = dtype == EAGLE_BF16 ? 2 : 4;
-  const int bke = 128 / esz;
-  int G;
-  const int bn = pick_bn(M, &G);
-  const int n_vtiles = V / 128;
+  const int G = (M + 127) / 128;
   int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
   sms = sms > kMaxCtas ? kMaxCtas : sms;
   int cpg = sms / G;
   if (cpg < 1) cpg = 1;
+  if (cpg > kMaxCtas / G) cpg = kMaxCtas / G;
+  // vocabulary rows per tile: 128 (fewer, larger K-chunks per byte of W_U
+  // measured faster than narrower tiles with better balance); narrower only
+  // when V is smaller than one tile per CTA
+  int tn = 128;
+  while (tn > 16 && (V + tn - 1) / tn < cpg) tn -= 16;
+  const int n_vtiles = (V + tn - 1) / tn;
   if (cpg > n_vtiles) cpg = n_vtiles;
   const int n_ctas = cpg * G;
-  const size_t extra = lm_epi_bytes(bn, k);
-  const int stages = dtype == EAGLE_BF16 ? pick_stages(bn, extra) : 2;
+  const size_t lists = 0;
+  const int rows_g = M < 128 ? M : 128;           // rows of the largest group
+  const int xr = (rows_g + 15) / 16 * 16;         // activation rows loaded per stage
+  const size_t xbytes = (size_t)xr * 128;
+  const int stages = dtype == EAGLE_BF16 ? pick_stages(kTileA + xbytes, lists + (kTileA - xbytes)) : 2;
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
   const size_t smem = dtype == EAGLE_BF16
-                          ? 1024 + (size_t)stages * (kTileA + (size_t)bn * 128) + extra
-                          : (size_t)(128 * (kF32Kc + 1) + 16 * kF32Kc) * 4 + extra;
-  if (smem > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;
-
-  CUtensorMap mw, mx;
-  if (dtype == EAGLE_BF16 &&
-      (!make_tmap_2d(&mw, w_lm, esz, (uint64_t)V, (uint64_t)d, 128, (uint32_t)bke) ||
-       !make_tmap_2d(&mx, x, esz, (uint64_t)M, (uint64_t)d, (uint32_t)bn, (uint32_t)bke)))
-    return EAGLE_ERR_CUDA;
+                          ? 1024 + (size_t)stages * (kTileA + xbytes) + (kTileA - xbytes) + lists
+                          : (size_t)(128 * (kF32Kc + 1) + 16 * kF32Kc) * 4 + lists;
 
   char* cur = static_cast<char*>(ws);
-  const size_t n = (size_t)kMaxCtas * bn;
+  const size_t n = (size_t)kMaxCtas * 128;
   LmParams p;
   p.part_ms = static_cast<float2*>(ws_carve(cur, n * 8));
   p.part_v = static_cast<float*>(ws_carve(cur, n * k * 4));
   p.part_i = static_cast<int*>(ws_carve(cur, n * k * 4));
   p.part_cnt = static_cast<int*>(ws_carve(cur, n * 4));
-  p.counters = static_cast<int*>(ws_carve(cur, (size_t)G * 4));
   p.M = M;
   p.V = V;
   p.K = k;
-  p.bn = bn;
   p.groups = G;
   p.ctas_per_group = cpg;
   p.n_vtiles = n_vtiles;
-  p.nk = d / bke;
+  p.nk = d / 64;
+  p.tn = tn;
   p.stages = stages;
+  p.xr = xr;
   p.inv_t = 1.f / temperature;
   p.bias = bias;
   p.topk_ids = topk_ids;
@@ -848,14 +887,32 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
   p.status = dev_status;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(p.counters, 0, (size_t)G * 4, s) != cudaSuccess) return EAGLE_ERR_CUDA;
   if (dtype == EAGLE_BF16) {
-    cudaFuncSetAttribute(lmhead_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    lmhead_topk_kernel<false><<<n_ctas, kThreads, smem, s>>>(mw, mx, p);
+    CUtensorMap mx, mw;
+    if (!make_tmap_2d(&mx, x, 2, (uint64_t)M, (uint64_t)d, (uint32_t)xr, 64) ||
+        !make_tmap_2d(&mw, w_lm, 2, (uint64_t)V, (uint64_t)d, (uint32_t)tn, 64))
+      return EAGLE_ERR_CUDA;
+    auto kern = k <= 1 ? lmhead_topk_kernel<1>
+                : k <= 4 ? lmhead_topk_kernel<4>
+                : k <= 16 ? lmhead_topk_kernel<16> : lmhead_topk_kernel<32>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<n_ctas, kThreads, smem, s>>>(mx, mw, p);
   } else {
-    cudaFuncSetAttribute(lmhead_topk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    lmhead_topk_f32_kernel<<<n_ctas, kEpiThreads, smem, s>>>((const float*)x, (const float*)w_lm, d, p);
+    auto kern = k <= 1 ? lmhead_topk_f32_kernel<1>
+                : k <= 4 ? lmhead_topk_f32_kernel<4>
+                : k <= 16 ? lmhead_topk_f32_kernel<16> : lmhead_topk_f32_kernel<32>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<n_ctas, kEpiThreads, smem, s>>>((const float*)x, (const float*)w_lm, d, p);
   }
+  note_launch();
+  // merge of the per-CTA partials: one warp per row, lists staged in shared memory
+  const size_t per_warp = ((size_t)cpg * (k * 8 + 4) + 15) / 16 * 16;
+  int rpc = (int)((200 * 1024) / per_warp);
+  rpc = rpc > 8 ? 8 : (rpc < 1 ? 1 : rpc);
+  const size_t msmem = (size_t)rpc * per_warp;
+  if (msmem > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;
+  cudaFuncSetAttribute(lmhead_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+  lmhead_merge_kernel<<<(M + rpc - 1) / rpc, rpc * 32, msmem, s>>>(p, rpc);
   note_launch();
   return last_launch_status();
 }
@@ -919,7 +976,7 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
   const FpPlan f = fp_plan(M, d, esz, sms > kMaxCtas ? kMaxCtas : sms);
-  const int stages = pick_stages(f.bn, 0);
+  const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
   const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
 

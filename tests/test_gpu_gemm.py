@@ -114,3 +114,4 @@ def test_fuse_proj_bias():
 def test_fuse_proj_full_size(M, d, rows):
     b = need_gpu()
     _fp_check(b, M, d, "bf16", seed=M * d % 1000, rows=rows)
+
