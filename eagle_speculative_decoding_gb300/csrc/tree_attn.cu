@@ -425,13 +425,16 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   pl.qtiles = (rows + pl.rows_per_cta - 1) / pl.rows_per_cta;
   const int max_blocks = max(1, (max_pages * 16 + kBlkKeys - 1) / kBlkKeys);
   if (num_splits > 0) {
-    pl.splits = num_splits;
+    pl.splits = min(num_splits, max_blocks);
   } else {
+    // enough CTAs for two waves of the SMs, but at least 8 key blocks (512
+    // keys) per split so the (O, lse) partials stay small beside the KV bytes
     const int base = pl.qtiles * B * Hkv;
     const int target = 2 * max(1, sm_count());
     pl.splits = base >= target ? 1 : (target + base - 1) / base;
+    pl.splits = min(pl.splits, max(1, max_blocks / 8));
   }
-  pl.splits = max(1, min(pl.splits, max_blocks));
+  pl.splits = max(1, pl.splits);
   return pl;
 }
 

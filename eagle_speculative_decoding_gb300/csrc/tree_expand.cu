@@ -8,10 +8,10 @@
 // and keep the verification budget) and 0x05C "Target Verification" (flatten
 // with ancestry-aware positions and a tree mask).
 //
-// One CTA per request.  Ranks are computed by counting, for each node, the
-// nodes with a smaller key: keys are unique (node ids differ), so the ranks
-// are a permutation and need no sort network.  log V is accumulated in fp32
-// with one correctly rounded addition per level.
+// One CTA per request.  A step ranks its (at most width*k) new nodes by
+// counting smaller keys (keys are unique: node ids differ); the final rerank
+// bitonic-sorts 64-bit order-preserving keys of all stored nodes.  log V is
+// accumulated in fp32 with one correctly rounded addition per level.
 #include <math.h>
 
 #include "common.cuh"
@@ -33,6 +33,50 @@ __device__ __forceinline__ bool key_less(float va, int da, int ia, float vb, int
   return ia < ib;
 }
 
+// Order-preserving 64-bit sort key of a node: ascending key = descending
+// log V, then ascending depth, then ascending node id.
+__device__ __forceinline__ unsigned long long node_key(float v, int d, int id) {
+  uint32_t f = __float_as_uint(v);
+  f = (f & 0x80000000u) ? ~f : (f | 0x80000000u);  // ascending as unsigned
+  return ((unsigned long long)(~f) << 32) | ((unsigned long long)(uint32_t)d << 16) |
+         (unsigned long long)(uint32_t)id;
+}
+
+// Exclusive prefix sum of 0/1 flags over n <= kMaxCand entries (block-wide).
+__device__ __forceinline__ int block_exclusive_scan(const int* flags, int* out, int n) {
+  __shared__ int s_warp[kExpandThreads / 32 * 2];
+  __shared__ int s_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kW = kExpandThreads / 32;
+  int pref[2], v[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = h * kExpandThreads + threadIdx.x;
+    v[h] = t < n ? flags[t] : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, v[h]);
+    pref[h] = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) s_warp[h * kW + warp] = __popc(bal);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int w = 0; w < 2 * kW; ++w) {
+      const int c = s_warp[w];
+      s_warp[w] = acc;
+      acc += c;
+    }
+    s_total = acc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = h * kExpandThreads + threadIdx.x;
+    if (t < n) out[t] = s_warp[h * kW + warp] + pref[h];
+  }
+  __syncthreads();
+  return s_total;
+}
+
 __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     int step, int width, int k, int max_nodes, const int32_t* __restrict__ cand_ids,
     const float* __restrict__ cand_lp, const int32_t* __restrict__ root_token,
@@ -47,55 +91,56 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
   float* nv_ = node_logv + (size_t)b * max_nodes;
   int32_t* nd_ = node_depth + (size_t)b * max_nodes;
 
-  __shared__ int s_par[64];       // expanded parent node ids (slot j)
+  __shared__ int s_par[64];  // expanded parent node ids (slot j)
   __shared__ float s_parv[64];
   __shared__ int s_pard[64];
-  __shared__ int s_npar, s_count0, s_bad;
+  __shared__ float s_mass[64];
   __shared__ int s_valid[kMaxCand];
   __shared__ int s_scan[kMaxCand];
   __shared__ float s_v[kMaxCand];
   __shared__ int s_id[kMaxCand];
-  __shared__ float s_mass[64];
+  __shared__ float s_lp[kMaxCand];
+  __shared__ int s_bad;
 
-  if (threadIdx.x == 0) {
-    s_bad = 0;
+  const int npar = step == 0 ? 1 : max(0, min(width, n_frontier[b]));
+  const int count0 = step == 0 ? 1 : node_count[b];
+  const int ncand = npar * k;
+  if (threadIdx.x == 0) s_bad = 0;
+  if (threadIdx.x < 64) s_mass[threadIdx.x] = 0.f;
+  // the expanded parents, loaded in parallel
+  if (threadIdx.x < npar) {
+    const int j = threadIdx.x;
     if (step == 0) {
+      s_par[0] = 0;
+      s_parv[0] = 0.f;
+      s_pard[0] = 0;
       np_[0] = -1;
       nt_[0] = root_token ? root_token[b] : -1;
       nv_[0] = 0.f;
       nd_[0] = 0;
-      s_npar = 1;
-      s_count0 = 1;
-      s_par[0] = 0;
-      s_parv[0] = 0.f;
-      s_pard[0] = 0;
     } else {
-      int np = n_frontier[b];
-      np = np < 0 ? 0 : (np > width ? width : np);
-      s_npar = np;
-      s_count0 = node_count[b];
-      for (int j = 0; j < np; ++j) {
-        int p = frontier[(size_t)b * width + j];
-        if (p < 0 || p >= s_count0) {
-          s_bad = EAGLE_ERR_BAD_TREE;
-          p = 0;
-        }
-        s_par[j] = p;
-        s_parv[j] = nv_[p];
-        s_pard[j] = nd_[p];
+      int p = frontier[(size_t)b * width + j];
+      if (p < 0 || p >= count0) {
+        atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
+        p = 0;
       }
+      s_par[j] = p;
+      s_parv[j] = nv_[p];
+      s_pard[j] = nd_[p];
     }
   }
-  if (threadIdx.x < 64) s_mass[threadIdx.x] = 0.f;
-  __syncthreads();
-  const int npar = s_npar, ncand = npar * k, count0 = s_count0;
-
-  // candidates: validity, duplicates, non-finite values, sibling mass
   for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
     const int j = t / k, i = t % k;
     const size_t src = ((size_t)b * P + j) * k + i;
-    const int id = cand_ids[src];
-    float lp = cand_lp[src];
+    s_id[t] = cand_ids[src];
+    s_lp[t] = cand_lp[src];
+  }
+  __syncthreads();
+  // validation (duplicates, non-finite values, sibling mass) and values
+  for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
+    const int j = t / k, i = t % k;
+    const int id = s_id[t];
+    float lp = s_lp[t];
     int valid = id >= 0;
     if (valid) {
       if (isnan(lp) || lp == INFINITY) {
@@ -103,14 +148,13 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
         valid = 0;
       }
       for (int i2 = 0; i2 < i; ++i2)
-        if (cand_ids[((size_t)b * P + j) * k + i2] == id) atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
+        if (s_id[j * k + i2] == id) atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
       lp = fminf(lp, 0.f);
       atomicAdd(&s_mass[j], expf(lp));
       // log V(child) = log V(parent) + log max(c, eps): one fp32 addition
       s_v[t] = __fadd_rn(s_parv[j], fmaxf(lp, kLogEps));
     }
     s_valid[t] = valid;
-    s_id[t] = id;
   }
   __syncthreads();
   if (threadIdx.x < npar && s_mass[threadIdx.x] > 1.f + kMassTol) atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
@@ -123,25 +167,15 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     }
     return;
   }
-  // exclusive scan of validity -> creation-ordered node ids (slot, then rank)
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int t = 0; t < ncand; ++t) {
-      s_scan[t] = acc;
-      acc += s_valid[t];
-    }
-    if (count0 + acc > max_nodes) s_bad = EAGLE_ERR_INVALID_ARG;
-    s_count0 = acc;  // reuse: number of new nodes
-  }
-  __syncthreads();
-  if (s_bad) {
+  // creation-ordered node ids (slot, then rank) via a block prefix sum
+  const int nnew = block_exclusive_scan(s_valid, s_scan, ncand);
+  if (count0 + nnew > max_nodes) {
     if (threadIdx.x == 0) {
-      set_status(dev_status, s_bad);
+      set_status(dev_status, EAGLE_ERR_INVALID_ARG);
       n_frontier[b] = 0;
     }
     return;
   }
-  const int nnew = s_count0;
   for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
     if (!s_valid[t]) continue;
     const int j = t / k;
@@ -150,17 +184,12 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     nt_[node] = s_id[t];
     nv_[node] = s_v[t];
     nd_[node] = s_pard[j] + 1;
-  }
-  // next frontier: the top-`width` new nodes by key (all at the same depth)
-  for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
-    if (!s_valid[t]) continue;
-    const int node = count0 + s_scan[t];
+    // next frontier: rank of this node among the new nodes (same depth)
     const float v = s_v[t];
     int rank = 0;
     for (int u = 0; u < ncand; ++u) {
       if (!s_valid[u] || u == t) continue;
-      const int nu = count0 + s_scan[u];
-      rank += key_less(s_v[u], 0, nu, v, 0, node) ? 1 : 0;
+      rank += key_less(s_v[u], 0, count0 + s_scan[u], v, 0, node) ? 1 : 0;
     }
     if (rank < width) frontier[(size_t)b * width + rank] = node;
   }
@@ -183,62 +212,76 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
   const int32_t* nt_ = node_token + (size_t)b * max_nodes;
   const float* nv_ = node_logv + (size_t)b * max_nodes;
   const int32_t* nd_ = node_depth + (size_t)b * max_nodes;
-  __shared__ float s_v[kMaxNodes];
-  __shared__ int s_d[kMaxNodes];
+  __shared__ unsigned long long s_key[kMaxNodes];
   __shared__ int s_row_of[kMaxNodes];
-  __shared__ int s_sel[64];
+  __shared__ int s_prow[64];
   __shared__ int s_bad;
   int count = node_count[b];
   count = count < 1 ? 1 : (count > max_nodes ? max_nodes : count);
-  const int nsel = min(budget, count - 1);
+  const int n = count - 1;  // candidates (the seed excluded)
+  const int nsel = min(budget, n);
   const int ctx = ctx_lens ? ctx_lens[b] : 0;
-  for (int n = threadIdx.x; n < count; n += kExpandThreads) {
-    s_v[n] = nv_[n];
-    s_d[n] = nd_[n];
-    s_row_of[n] = -1;
-  }
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = threadIdx.x; i < P; i += kExpandThreads)
+    s_key[i] = i < n ? node_key(nv_[i + 1], nd_[i + 1], i + 1) : ~0ull;
+  for (int i = threadIdx.x; i < count; i += kExpandThreads) s_row_of[i] = -1;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  for (int n = 1 + threadIdx.x; n < count; n += kExpandThreads) {
-    const float v = s_v[n];
-    const int d = s_d[n];
-    int rank = 0;
-    for (int u = 1; u < count; ++u) rank += key_less(s_v[u], s_d[u], u, v, d, n) ? 1 : 0;
-    if (rank < nsel) {
-      s_sel[rank] = n;
-      s_row_of[n] = rank + 1;
+  // bitonic sort of the keys (ascending)
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += kExpandThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const unsigned long long a = s_key[lo], c = s_key[hi];
+        if ((a > c) == up) {
+          s_key[lo] = c;
+          s_key[hi] = a;
+        }
+      }
+      __syncthreads();
     }
   }
+  for (int r = 1 + threadIdx.x; r <= nsel; r += kExpandThreads)
+    s_row_of[(int)(s_key[r - 1] & 0xFFFFu)] = r;
   if (threadIdx.x == 0) s_row_of[0] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // rows in key order; a parent always precedes its child
-    uint64_t m[64];
-    m[0] = 1ull;
-    const size_t o = (size_t)b * R;
-    token[o] = nt_[0];
-    parent_row[o] = -1;
-    depth[o] = 0;
-    mask[o] = 1ull;
-    node_id[o] = 0;
-    position[o] = ctx;
-    for (int r = 1; r <= nsel; ++r) {
-      const int n = s_sel[r - 1];
-      const int p = np_[n];
-      int pr = (p >= 0 && p < count) ? s_row_of[p] : -1;
-      if (pr < 0 || pr >= r) {
-        s_bad = 1;
-        pr = 0;
-      }
-      m[r] = m[pr] | (1ull << r);
-      token[o + r] = nt_[n];
-      parent_row[o + r] = pr;
-      depth[o + r] = s_d[n];
-      mask[o + r] = m[r];
-      node_id[o + r] = n;
-      position[o + r] = ctx + s_d[n];
+  // parent rows (a parent always precedes its child in key order)
+  for (int r = threadIdx.x; r < 64 && r <= nsel; r += kExpandThreads) {
+    if (r == 0) {
+      s_prow[0] = -1;
+      continue;
     }
-    for (int r = nsel + 1; r < R; ++r) {
+    const int nd = (int)(s_key[r - 1] & 0xFFFFu);
+    const int p = np_[nd];
+    int pr = (p >= 0 && p < count) ? s_row_of[p] : -1;
+    if (pr < 0 || pr >= r) {
+      atomicExch(&s_bad, 1);
+      pr = 0;
+    }
+    s_prow[r] = pr;
+  }
+  __syncthreads();
+  const size_t o = (size_t)b * R;
+  for (int r = threadIdx.x; r < R; r += kExpandThreads) {
+    if (r <= nsel) {
+      const int nd = r == 0 ? 0 : (int)(s_key[r - 1] & 0xFFFFu);
+      uint64_t m = 1ull << r;
+      int j = r, guard = 0;
+      while (j != 0 && guard++ < 64) {  // ancestry bits by walking the parent rows
+        j = s_prow[j];
+        m |= 1ull << j;
+      }
+      const int dd = r == 0 ? 0 : nd_[nd];
+      token[o + r] = nt_[nd];
+      parent_row[o + r] = s_prow[r];
+      depth[o + r] = dd;
+      mask[o + r] = m;
+      node_id[o + r] = nd;
+      position[o + r] = ctx + dd;
+    } else {
       token[o + r] = -1;
       parent_row[o + r] = -1;
       depth[o + r] = 0;
@@ -246,6 +289,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
       node_id[o + r] = -1;
       position[o + r] = ctx;
     }
+  }
+  if (threadIdx.x == 0) {
     n_rows[b] = nsel + 1;
     if (s_bad) set_status(dev_status, EAGLE_ERR_BAD_TREE);
   }
