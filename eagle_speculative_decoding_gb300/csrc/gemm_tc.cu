@@ -225,10 +225,10 @@ struct LmParams {
   float* topk_lp;
   float* row_max;
   float* row_sumexp;
-  float2* part_ms;   // [cta][128]       (max of z/T, sum exp)
-  float* part_v;     // [cta][128][K]    sorted top-k logits (z)
-  int* part_i;       // [cta][128][K]
-  int* part_cnt;     // [cta][128]
+  float2* part_ms;   // [M][cpg]       (max of z/T, sum exp) per row and CTA of its group
+  float* part_v;     // [M][cpg][K]    sorted top-k logits (z)
+  int* part_i;       // [M][cpg][K]
+  int* part_cnt;     // [M][cpg]
   int* counters;     // [groups]
   int32_t* status;
 };
@@ -352,60 +352,83 @@ __device__ __forceinline__ void row_chunk(RowTopK<KMAX>& r, const float (&v)[16]
 // top-K list) for lmhead_merge_kernel.
 template <int KMAX>
 __device__ __forceinline__ void lm_publish(const LmParams& p, const RowTopK<KMAX>& r, int nrow, int e) {
-  const int cta = blockIdx.x, K = p.K;
+  const int K = p.K;
+  const int g = blockIdx.x % p.groups, ci = blockIdx.x / p.groups;
+  const size_t slot = (size_t)(g * 128 + e) * p.ctas_per_group + ci;  // [row][cta]
   if (e < nrow) {
-    p.part_ms[(size_t)cta * 128 + e] = make_float2(r.m, r.s);
+    p.part_ms[slot] = make_float2(r.m, r.s);
     int cnt = 0;
 #pragma unroll
     for (int t = 0; t < KMAX; ++t) {
       const int j = t - (KMAX - K);  // position in the reported list
       if (j >= 0 && r.ai[t] != 0x7fffffff) {
-        p.part_v[((size_t)cta * 128 + e) * K + j] = r.av[t];
-        p.part_i[((size_t)cta * 128 + e) * K + j] = r.ai[t];
+        p.part_v[slot * K + j] = r.av[t];
+        p.part_i[slot * K + j] = r.ai[t];
         cnt = j + 1;
       }
     }
-    p.part_cnt[(size_t)cta * 128 + e] = cnt;
+    p.part_cnt[slot] = cnt;
   }
 }
 
-// Merge of the per-CTA partials: one warp per activation row.  Log-sum-exp by
-// max / rescale over the CTAs; top-K by K rounds of "best head among the
-// CTAs' sorted lists", the lists staged in this warp's shared memory.
-__global__ void __launch_bounds__(256) lmhead_merge_kernel(const LmParams p, int rows_per_cta) {
+// Merge of the per-CTA partials: one CTA per activation row.  All warps stage
+// the row's contiguous lists into shared memory with independent loads; warp
+// 0 then takes the log-sum-exp by max / rescale over the CTAs and the top-K by
+// K rounds of "best head among the CTAs' sorted lists".
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmParams p) {
   extern __shared__ __align__(16) unsigned char msm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.x * rows_per_cta + warp;
-  if (warp >= rows_per_cta || m >= p.M) return;
-  const int K = p.K, g = m / 128, row = m % 128;
-  const int nc = p.ctas_per_group, G = p.groups;
-  const size_t per_warp = ((size_t)nc * (K * 8 + 4) + 15) / 16 * 16;
-  float* sv = reinterpret_cast<float*>(msm + warp * per_warp);
-  int* si = reinterpret_cast<int*>(sv + nc * K);
-  int* sc = si + nc * K;
-  float M = -INFINITY;
-  for (int c = lane; c < nc; c += 32) {
-    const int cnt = p.part_cnt[(size_t)(g + G * c) * 128 + row];
-    sc[c] = cnt;
-    const size_t base = ((size_t)(g + G * c) * 128 + row) * K;
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      sv[c * K + j] = p.part_v[base + j];
-      si[c * K + j] = p.part_i[base + j];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int m = blockIdx.x;
+  const int K = p.K, nc = p.ctas_per_group, n = nc * K;
+  float* sv = reinterpret_cast<float*>(msm);
+  int* si = reinterpret_cast<int*>(sv + n);
+  int* sc = si + n;
+  // this row's partials are contiguous: [cta][K] values / ids, [cta] counts
+  const float* gv = p.part_v + (size_t)m * n;
+  const int* gi = p.part_i + (size_t)m * n;
+  const int* gc = p.part_cnt + (size_t)m * nc;
+  const float2* gms = p.part_ms + (size_t)m * nc;
+  constexpr int kU = 4;
+  for (int f0 = tid; f0 < n; f0 += kMergeThreads * kU) {
+    float v[kU];
+    int id[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int f = f0 + u * kMergeThreads;
+      v[u] = f < n ? __ldcg(gv + f) : 0.f;
+      id[u] = f < n ? __ldcg(gi + f) : 0;
     }
-    M = fmaxf(M, p.part_ms[(size_t)(g + G * c) * 128 + row].x);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int f = f0 + u * kMergeThreads;
+      if (f < n) {
+        sv[f] = v[u];
+        si[f] = id[u];
+      }
+    }
   }
+  for (int c = tid; c < nc; c += kMergeThreads) sc[c] = __ldcg(gc + c);
+  constexpr int kPer = kMaxCtas / 32;  // lists owned per lane of warp 0
+  float2 ms[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = lane + 32 * i;
+    ms[i] = tid < 32 && c < nc ? __ldcg(gms + c) : make_float2(-INFINITY, 0.f);
+  }
+  __syncthreads();
+  if (tid >= 32) return;
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) M = fmaxf(M, ms[i].x);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float S = 0.f;
-  for (int c = lane; c < nc; c += 32) {
-    const float2 ms = p.part_ms[(size_t)(g + G * c) * 128 + row];
-    if (ms.x != -INFINITY) S += ms.y * exp2f((ms.x - M) * kLog2e);
-  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (ms[i].x != -INFINITY) S += ms[i].y * exp2f((ms[i].x - M) * kLog2e);
 #pragma unroll
   for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-  __syncwarp();
-  constexpr int kPer = kMaxCtas / 32;  // lists owned per lane
   float hv[kPer];
   int hi[kPer], hp[kPer], hc[kPer];
 #pragma unroll
@@ -752,16 +775,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar(1, kEpiThreads);
         if (sh.flag) {
           __threadfence();
+          // sum the contributors' partials in slot order (deterministic):
+          // thread et owns float4s f = et + 128 i of the [ncol][128] tile
           const int ncontrib = c_last - c_first + 1;
-          const float* pbase = p.part + ((size_t)sg.tile * p.max_contrib * bn) * 128;
-          for (int col = 0; col < ncol; ++col) {
-            float s = 0.f;
-            for (int k = 0; k < ncontrib; ++k) s += pbase[((size_t)k * bn + col) * 128 + e];
-            const size_t idx = (size_t)(m0 + col) * p.d + o;
-            if (TF32)
-              reinterpret_cast<float*>(p.out)[idx] = s + bias_o;
-            else
-              reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16(s + bias_o);
+          const float4* pbase = reinterpret_cast<const float4*>(
+              p.part + ((size_t)sg.tile * p.max_contrib * bn) * 128);
+          const size_t slot4 = (size_t)bn * 32;  // float4s per contributor slot
+          for (int f0 = et; f0 < ncol * 32; f0 += kEpiThreads * 4) {
+            float4 acc4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < ncontrib; ++k) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int f = f0 + u * kEpiThreads;
+                if (f < ncol * 32) {
+                  const float4 x = pbase[(size_t)k * slot4 + f];
+                  acc4[u].x += x.x;
+                  acc4[u].y += x.y;
+                  acc4[u].z += x.z;
+                  acc4[u].w += x.w;
+                }
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int f = f0 + u * kEpiThreads;
+              if (f >= ncol * 32) continue;
+              const int col = f / 32, oo = ot * 128 + (f % 32) * 4;
+              const float b0 = p.bias ? p.bias[oo] : 0.f, b1 = p.bias ? p.bias[oo + 1] : 0.f;
+              const float b2 = p.bias ? p.bias[oo + 2] : 0.f, b3 = p.bias ? p.bias[oo + 3] : 0.f;
+              const size_t idx = (size_t)(m0 + col) * p.d + oo;
+              if (TF32) {
+                *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + idx) =
+                    make_float4(acc4[u].x + b0, acc4[u].y + b1, acc4[u].z + b2, acc4[u].w + b3);
+              } else {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc4[u].x + b0, acc4[u].y + b1);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc4[u].z + b2, acc4[u].w + b3);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + idx) = pk;
+              }
+            }
           }
         }
         named_bar(1, kEpiThreads);
@@ -818,9 +874,7 @@ extern "C" size_t eagle_lmhead_topk_workspace_size(int M, int d, int V, int k, i
   (void)V;
   (void)dtype;
   if (M <= 0 || k <= 0) return 0;
-  const size_t G = (size_t)(M + 127) / 128;
-  const size_t n = (size_t)kMaxCtas * 128;  // one partial row per (CTA, group row)
-  (void)G;
+  const size_t n = (size_t)((M + 127) / 128) * 128 * kMaxCtas;  // [row][cta of its group]
   return round_up(n * 8, 256) + 2 * round_up(n * k * 4, 256) + round_up(n * 4, 256) + 1024;
 }
 
@@ -862,7 +916,7 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
                           : (size_t)(128 * (kF32Kc + 1) + 16 * kF32Kc) * 4 + lists;
 
   char* cur = static_cast<char*>(ws);
-  const size_t n = (size_t)kMaxCtas * 128;
+  const size_t n = (size_t)G * 128 * kMaxCtas;
   LmParams p;
   p.part_ms = static_cast<float2*>(ws_carve(cur, n * 8));
   p.part_v = static_cast<float*>(ws_carve(cur, n * k * 4));
@@ -905,14 +959,12 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
     kern<<<n_ctas, kEpiThreads, smem, s>>>((const float*)x, (const float*)w_lm, d, p);
   }
   note_launch();
-  // merge of the per-CTA partials: one warp per row, lists staged in shared memory
-  const size_t per_warp = ((size_t)cpg * (k * 8 + 4) + 15) / 16 * 16;
-  int rpc = (int)((200 * 1024) / per_warp);
-  rpc = rpc > 8 ? 8 : (rpc < 1 ? 1 : rpc);
-  const size_t msmem = (size_t)rpc * per_warp;
+  // merge of the per-CTA partials: one CTA per row, lists staged in shared memory
+  const size_t msmem = (size_t)cpg * (k * 8 + 4);
   if (msmem > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;
-  cudaFuncSetAttribute(lmhead_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
-  lmhead_merge_kernel<<<(M + rpc - 1) / rpc, rpc * 32, msmem, s>>>(p, rpc);
+  if (msmem > 48 * 1024)
+    cudaFuncSetAttribute(lmhead_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+  lmhead_merge_kernel<<<M, kMergeThreads, msmem, s>>>(p);
   note_launch();
   return last_launch_status();
 }
