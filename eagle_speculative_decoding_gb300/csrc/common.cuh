@@ -28,7 +28,36 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t rows,
                   uint64_t cols, uint32_t box_rows, uint32_t box_cols);
 
+// Every kernel of the library is launched with programmatic stream
+// serialization (programmatic dependent launch): its CTAs may be scheduled
+// while the previous kernel on the stream is still finishing.  Each kernel
+// executes pdl_wait() before its first global-memory access (it returns once
+// the previous grid has completed and its writes are visible) and
+// pdl_trigger() only after that wait and after claiming its own shared memory
+// and TMEM, so at most two grids overlap and a dependent grid never holds a
+// resource that a running grid has yet to claim.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------- device side
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) {

@@ -195,6 +195,7 @@ __device__ __forceinline__ void cta_setup(CtaShared& sh, int stages, uint32_t tm
     sh.flag = 0;
     fence_mbar_init();
   }
+  pdl_wait();  // the previous grid (and its TMEM) is gone from here on
   if (warp == 1) {
     tmem_alloc(smem_u32(&sh.tmem_base), tmem_cols);
     tmem_relinquish();
@@ -202,6 +203,7 @@ __device__ __forceinline__ void cta_setup(CtaShared& sh, int stages, uint32_t tm
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();
 }
 
 __device__ __forceinline__ void cta_teardown(CtaShared& sh, uint32_t tmem_cols, int32_t* status) {
@@ -377,6 +379,8 @@ __device__ __forceinline__ void lm_publish(const LmParams& p, const RowTopK<KMAX
 // K rounds of "best head among the CTAs' sorted lists".
 constexpr int kMergeThreads = 256;
 __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char msm[];
   const int tid = threadIdx.x, lane = tid & 31;
   const int m = blockIdx.x;
@@ -581,6 +585,8 @@ template <int KMAX>
 __global__ void __launch_bounds__(kEpiThreads)
     lmhead_topk_f32_kernel(const float* __restrict__ x, const float* __restrict__ w, int d,
                            const LmParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char dsm[];
   float* Xs = reinterpret_cast<float*>(dsm);        // [128][kF32Kc + 1]
   float* Ws = Xs + 128 * (kF32Kc + 1);              // [16][kF32Kc]
@@ -833,6 +839,8 @@ __global__ void __launch_bounds__(256)
     fuse_proj_f32_kernel(const float* __restrict__ hl, const float* __restrict__ hm,
                          const float* __restrict__ hh, const float* __restrict__ w,
                          const float* __restrict__ bias, float* __restrict__ g, int M, int d) {
+  pdl_wait();
+  pdl_trigger();
   const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= (long long)M * d) return;
@@ -950,13 +958,13 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
                 : k <= 4 ? lmhead_topk_kernel<4>
                 : k <= 16 ? lmhead_topk_kernel<16> : lmhead_topk_kernel<32>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<n_ctas, kThreads, smem, s>>>(mx, mw, p);
+    launch(kern, n_ctas, kThreads, smem, s, mx, mw, p);
   } else {
     auto kern = k <= 1 ? lmhead_topk_f32_kernel<1>
                 : k <= 4 ? lmhead_topk_f32_kernel<4>
                 : k <= 16 ? lmhead_topk_f32_kernel<16> : lmhead_topk_f32_kernel<32>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<n_ctas, kEpiThreads, smem, s>>>((const float*)x, (const float*)w_lm, d, p);
+    launch(kern, n_ctas, kEpiThreads, smem, s, (const float*)x, (const float*)w_lm, d, p);
   }
   note_launch();
   // merge of the per-CTA partials: one CTA per row, lists staged in shared memory
@@ -964,7 +972,7 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
   if (msmem > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;
   if (msmem > 48 * 1024)
     cudaFuncSetAttribute(lmhead_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
-  lmhead_merge_kernel<<<M, kMergeThreads, msmem, s>>>(p);
+  launch(lmhead_merge_kernel, M, kMergeThreads, msmem, s, p);
   note_launch();
   return last_launch_status();
 }
@@ -1017,7 +1025,7 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   if (!ws || ws_bytes < eagle_fuse_proj_workspace_size(M, d, dtype)) return EAGLE_ERR_WORKSPACE;
   if (dtype == EAGLE_FP32) {
     const long long outs = (long long)M * d;
-    fuse_proj_f32_kernel<<<(unsigned)((outs + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    launch(fuse_proj_f32_kernel, (unsigned)((outs + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream),
         (const float*)h_low, (const float*)h_mid, (const float*)h_high, (const float*)w_proj, bias,
         (float*)g, M, d);
     note_launch();
@@ -1061,7 +1069,7 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.counters, 0, (size_t)f.n_tiles * 4, s) != cudaSuccess) return EAGLE_ERR_CUDA;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  fuse_proj_kernel<false><<<f.n_ctas, kThreads, smem, s>>>(mw, ml, mm, mh, p);
+  launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, ml, mm, mh, p);
   note_launch();
   return last_launch_status();
 }

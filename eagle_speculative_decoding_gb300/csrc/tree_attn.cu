@@ -89,6 +89,8 @@ __device__ __forceinline__ uint32_t swz(int row, int c) {
 
 template <int D>
 __global__ void __launch_bounds__(kMaxWarps * 32) tree_attn_bf16_kernel(const AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kChunks = D / 8;            // 16-byte chunks per key row
   constexpr int kTile = kBlkKeys * D * 2;   // bytes of one K (or V) tile
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -328,6 +330,8 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const float* __r
                                                                 int nrows, int splits,
                                                                 __nv_bfloat16* __restrict__ out,
                                                                 float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= nrows) return;
   const float* pl = part_lse + (size_t)row * splits;
@@ -360,6 +364,8 @@ __global__ void __launch_bounds__(256) tree_attn_f32_kernel(
     const uint64_t* __restrict__ tree_mask, float* __restrict__ out, float* __restrict__ lse,
     int B, int R, int Hq, int Hkv, int D, int max_pages, int num_pages, float scale,
     int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (gw >= B * R * Hq) return;
   const int h = gw % Hq, r = (gw / Hq) % R, b = gw / (Hq * R);
@@ -417,7 +423,23 @@ struct Plan {
   int nwarps, rows_per_cta, qtiles, splits;
 };
 
-Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
+template <int D>
+size_t attn_smem() {
+  return (size_t)kStages * 2 * kBlkKeys * D * 2;
+}
+
+// CTAs of the bf16 kernel that fit on one SM at once.
+int resident_per_sm(int D, int threads) {
+  const size_t sm = D == 128 ? attn_smem<128>() : attn_smem<64>();
+  auto kern = D == 128 ? tree_attn_bf16_kernel<128> : tree_attn_bf16_kernel<64>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, sm) != cudaSuccess || n < 1)
+    n = 1;
+  return n;
+}
+
+Plan make_plan(int B, int R, int Hq, int Hkv, int D, int max_pages, int num_splits) {
   Plan pl;
   const int rows = R * (Hq / Hkv);
   pl.nwarps = min(kMaxWarps, (rows + 15) / 16);
@@ -427,20 +449,25 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   if (num_splits > 0) {
     pl.splits = min(num_splits, max_blocks);
   } else {
-    // enough CTAs for two waves of the SMs, but at least 8 key blocks (512
-    // keys) per split so the (O, lse) partials stay small beside the KV bytes
-    const int base = pl.qtiles * B * Hkv;
-    const int target = 2 * max(1, sm_count());
-    pl.splits = base >= target ? 1 : (target + base - 1) / base;
-    pl.splits = min(pl.splits, max(1, max_blocks / 8));
+    // The split count that minimises waves x key blocks per CTA (the tree
+    // block included), plus a small charge per split for the (O, lse)
+    // partials and their merge.
+    const long long base = (long long)pl.qtiles * B * Hkv;
+    const long long slots = (long long)max(1, sm_count()) * resident_per_sm(D, pl.nwarps * 32);
+    double best = 1e300;
+    pl.splits = 1;
+    for (int sp = 1; sp <= min(max_blocks, 256); ++sp) {
+      const long long waves = (base * sp + slots - 1) / slots;
+      const int bps = (max_blocks + sp - 1) / sp;
+      const double cost = (double)waves * (bps + 1) + (sp > 1 ? 0.1 * sp : 0.0);
+      if (cost < best - 1e-9) {
+        best = cost;
+        pl.splits = sp;
+      }
+    }
   }
   pl.splits = max(1, pl.splits);
   return pl;
-}
-
-template <int D>
-size_t attn_smem() {
-  return (size_t)kStages * 2 * kBlkKeys * D * 2;
 }
 
 }  // namespace
@@ -453,7 +480,7 @@ extern "C" size_t eagle_tree_attn_workspace_size(int B, int R, int Hq, int Hkv, 
   (void)page_size;
   if (B <= 0 || R <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_pages <= 0) return 0;
   if (dtype != EAGLE_BF16 || Hq % Hkv) return 0;
-  const Plan pl = make_plan(B, R, Hq, Hkv, max_pages, num_splits);
+  const Plan pl = make_plan(B, R, Hq, Hkv, D, max_pages, num_splits);
   if (pl.splits == 1) return 0;
   const size_t rows = (size_t)B * R * Hq;
   return round_up(rows * pl.splits * D * 4, 256) + round_up(rows * pl.splits * 4, 256) + 512;
@@ -479,7 +506,7 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == EAGLE_FP32) {
     const int rows = B * R * Hq;
-    tree_attn_f32_kernel<<<(rows + 7) / 8, 256, 0, s>>>(
+    launch(tree_attn_f32_kernel, (rows + 7) / 8, 256, 0, s,
         (const float*)q, (const float*)k_tree, (const float*)v_tree, (const float*)k_cache,
         (const float*)v_cache, block_table, ctx_lens, tree_mask, (float*)out, lse, B, R, Hq, Hkv, D,
         max_pages, num_pages, scale, dev_status);
@@ -489,7 +516,7 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(out))
     return EAGLE_ERR_INVALID_ARG;
-  const Plan pl = make_plan(B, R, Hq, Hkv, max_pages, num_splits);
+  const Plan pl = make_plan(B, R, Hq, Hkv, D, max_pages, num_splits);
   if (pl.splits > 65535) return EAGLE_ERR_UNSUPPORTED;
   AttnParams p;
   p.q = (const __nv_bfloat16*)q;
@@ -529,20 +556,20 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   if (D == 128) {
     const size_t sm = attn_smem<128>();
     cudaFuncSetAttribute(tree_attn_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    tree_attn_bf16_kernel<128><<<grid, threads, sm, s>>>(p);
+    launch(tree_attn_bf16_kernel<128>, grid, threads, sm, s, p);
   } else {
     const size_t sm = attn_smem<64>();
     cudaFuncSetAttribute(tree_attn_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    tree_attn_bf16_kernel<64><<<grid, threads, sm, s>>>(p);
+    launch(tree_attn_bf16_kernel<64>, grid, threads, sm, s, p);
   }
   note_launch();
   if (pl.splits > 1) {
     const int rows = B * R * Hq;
     if (D == 128)
-      tree_attn_combine_kernel<128><<<(rows + 7) / 8, 256, 0, s>>>(p.part_o, p.part_lse, rows,
+      launch(tree_attn_combine_kernel<128>, (rows + 7) / 8, 256, 0, s, p.part_o, p.part_lse, rows,
                                                                   pl.splits, p.out, lse);
     else
-      tree_attn_combine_kernel<64><<<(rows + 7) / 8, 256, 0, s>>>(p.part_o, p.part_lse, rows,
+      launch(tree_attn_combine_kernel<64>, (rows + 7) / 8, 256, 0, s, p.part_o, p.part_lse, rows,
                                                                  pl.splits, p.out, lse);
     note_launch();
   }

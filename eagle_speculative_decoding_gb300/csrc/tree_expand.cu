@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     float* __restrict__ node_logv, int32_t* __restrict__ node_depth,
     int32_t* __restrict__ node_count, int32_t* __restrict__ frontier,
     int32_t* __restrict__ n_frontier, int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int P = step == 0 ? 1 : width;
   int32_t* np_ = node_parent + (size_t)b * max_nodes;
@@ -207,6 +209,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
     int32_t* __restrict__ parent_row, int32_t* __restrict__ depth, uint64_t* __restrict__ mask,
     int32_t* __restrict__ node_id, int32_t* __restrict__ position, int32_t* __restrict__ n_rows,
     int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int32_t* np_ = node_parent + (size_t)b * max_nodes;
   const int32_t* nt_ = node_token + (size_t)b * max_nodes;
@@ -315,7 +319,7 @@ extern "C" int eagle_tree_expand(int B, int step, int width, int k, int max_node
   if (width > 64 || k > 32 || width * k > kMaxCand || max_nodes > kMaxNodes || B > 65535)
     return EAGLE_ERR_UNSUPPORTED;
   if ((long long)max_nodes < 1LL + k + (long long)step * width * k) return EAGLE_ERR_INVALID_ARG;
-  expand_step_kernel<<<B, kExpandThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  launch(expand_step_kernel, B, kExpandThreads, 0, static_cast<cudaStream_t>(stream),
       step, width, k, max_nodes, cand_ids, cand_logprobs, root_token, node_parent, node_token,
       node_logv, node_depth, node_count, frontier, n_frontier, dev_status);
   note_launch();
@@ -335,7 +339,7 @@ extern "C" int eagle_tree_expand_finalize(int B, int max_nodes, int budget, int 
     return EAGLE_ERR_INVALID_ARG;
   if (R > 64 || max_nodes > kMaxNodes || B > 65535) return EAGLE_ERR_UNSUPPORTED;
   if (R < 1 + budget) return EAGLE_ERR_INVALID_ARG;
-  expand_finalize_kernel<<<B, kExpandThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  launch(expand_finalize_kernel, B, kExpandThreads, 0, static_cast<cudaStream_t>(stream),
       max_nodes, budget, R, node_parent, node_token, node_logv, node_depth, node_count, ctx_lens,
       token, parent_row, depth, mask, node_id, position, n_rows, dev_status);
   note_launch();

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kStatThreads) verify_rowstats_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ n_rows, int R, int V,
     float inv_t, int want_argmax, RowStat* __restrict__ stats, int32_t* __restrict__ amax,
     int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x % R, b = blockIdx.x / R;
   const int n = n_rows ? n_rows[b] : R;
   if (r >= n || r >= R) return;
@@ -124,6 +126,8 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
     uint32_t ctr2_accept, uint32_t ctr3, const float* __restrict__ uniforms_override,
     int max_depth, int32_t* __restrict__ accept_len, int32_t* __restrict__ path_rows,
     int32_t* __restrict__ out_tokens, int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   __shared__ int s_parent[kMaxVerifyRows];
   __shared__ int s_token[kMaxVerifyRows];
@@ -321,12 +325,12 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
   }
   const float inv_t = greedy ? 0.f : 1.f / temperature;
   if (need_stats) {
-    verify_rowstats_kernel<<<(unsigned)(B * R), kStatThreads, 0, s>>>(
+    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s,
         target_logits, n_rows, R, V, inv_t, greedy ? 1 : 0, stats, amax, dev_status);
     note_launch();
   }
   const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
-  verify_walk_kernel<<<B, kWalkThreads, 0, s>>>(
+  launch(verify_walk_kernel, B, kWalkThreads, 0, s,
       R, V, parent_row, token, n_rows, target_logits, target_argmax, stats, amax, greedy ? 1 : 0,
       inv_t, (uint32_t)seed, (uint32_t)(seed >> 32), 2u * off_hi, off_lo, uniforms_override,
       max_depth, accept_len, path_rows, out_tokens, dev_status);
@@ -420,12 +424,12 @@ extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* par
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float inv_t = greedy ? 0.f : 1.f / temperature;
   if (need_stats) {
-    verify_rowstats_kernel<<<(unsigned)(B * R), kStatThreads, 0, s>>>(
+    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s,
         target_logits, n_rows, R, V, inv_t, greedy ? 1 : 0, stats, amax, dev_status);
     note_launch();
   }
   const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
-  verify_walk_kernel<<<B, kWalkThreads, 0, s>>>(
+  launch(verify_walk_kernel, B, kWalkThreads, 0, s,
       R, V, parent_row, token, n_rows, target_logits, target_argmax, stats, amax, greedy ? 1 : 0,
       inv_t, (uint32_t)seed, (uint32_t)(seed >> 32), 2u * off_hi, off_lo, uniforms_override,
       max_depth, accept_len, path_rows, out_tokens, dev_status);
