@@ -29,6 +29,10 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous, never synchronise, keep no state between calls, and may be
  *     issued from several host threads on different streams and buffers.
+ *   - Kernels are launched with programmatic stream serialization: one may be
+ *     scheduled while the previous kernel on the stream is finishing, but it
+ *     reads and writes no global memory before that kernel has completed, so
+ *     stream order is unchanged for the caller.
  *   - Argument errors are detected on the host before anything is launched
  *     and returned as eagle_status.  Errors that only the device can see (a
  *     malformed tree, a non-finite value, a timed-out wait) are written to the
@@ -159,7 +163,7 @@ int eagle_tree_attn(const void* q, const void* k_tree, const void* v_tree,
  * bf16 runs on the tensor cores with fp32 accumulation; fp32 runs on the CUDA
  * cores in exact fp32 arithmetic.
  * Limits: 1 <= M <= 2048, 1 <= k <= 32, k <= V, d % 64 == 0,
- * V % 128 == 0, temperature > 0.
+ * V % 16 == 0, temperature > 0.
  * ---------------------------------------------------------------------- */
 size_t eagle_lmhead_topk_workspace_size(int M, int d, int V, int k, int dtype);
 int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M, int d,
