@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 10;
 constexpr int kMaxAcc = 4;  // TMEM accumulator buffers (as many as 512 columns hold)
 constexpr int kTileA = 128 * 128;  // bytes of one A (weight) stage: 128 rows x 128 B
 constexpr int kMaxCtas = 256;      // upper bound used for workspace sizing
@@ -90,17 +90,21 @@ __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, con
   const uint64_t pol_a = sc.a_policy();
   const uint64_t pol_b = sc.b_policy();
   const int stages = rg.stages;
-  int it = 0;
+  const uint32_t tx = rg.a_bytes + rg.b_bytes;
+  int it = 0, s = 0;  // iteration, its ring stage (it % stages) and phase
+  uint32_t ph = 0;
   Seg sg;
   for (int si = 0; sc.seg(si, sg); ++si) {
     for (int kc = sg.k0; kc < sg.k1; ++kc, ++it) {
-      const int s = it % stages;
-      const uint32_t ph = (uint32_t)(it / stages) & 1u;
       if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u, &sh.abort_flag)) goto drain;
       const uint32_t fb = smem_u32(&sh.full[s]);
-      mbar_arrive_expect_tx(fb, rg.a_bytes + rg.b_bytes);
+      mbar_arrive_expect_tx(fb, tx);
       tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
       tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
+      if (++s == stages) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
   }
   return;
@@ -122,21 +126,18 @@ template <bool TF32, class Sched>
 __device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, const Ring& rg) {
   const uint32_t idesc = mma_idesc(TF32 ? 2 : 1, 128, rg.n);
   const int stages = rg.stages;
-  int it = 0, acc = 0;
+  int s = 0, buf = 0;  // ring stage and accumulator buffer, with their phases
+  uint32_t ph = 0, aph = 0;
   bool ok = true;
   Seg sg;
-  for (int si = 0; ok && sc.seg(si, sg); ++si, ++acc) {
-    const int buf = acc % rg.nbuf;
-    const uint32_t aph = (uint32_t)(acc / rg.nbuf) & 1u;
+  for (int si = 0; ok && sc.seg(si, sg); ++si) {
     if (!mbar_wait(smem_u32(&sh.acc_empty[buf]), aph ^ 1u, &sh.abort_flag)) {
       ok = false;
       break;
     }
     tc_fence_after();
     const uint32_t d_tmem = sh.tmem_base + (uint32_t)(buf * rg.n);
-    for (int kc = sg.k0; kc < sg.k1; ++kc, ++it) {
-      const int s = it % stages;
-      const uint32_t ph = (uint32_t)(it / stages) & 1u;
+    for (int kc = sg.k0; kc < sg.k1; ++kc) {
       if (!mbar_wait(smem_u32(&sh.full[s]), ph, &sh.abort_flag)) {
         ok = false;
         break;
@@ -155,8 +156,16 @@ __device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, const Ri
           mma_bf16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, accum);
       }
       mma_commit(smem_u32(&sh.empty[s]));
+      if (++s == stages) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     if (ok) mma_commit(smem_u32(&sh.acc_full[buf]));
+    if (++buf == rg.nbuf) {
+      buf = 0;
+      aph ^= 1u;
+    }
   }
   if (!ok) {
     // drain: all MMAs issued so far complete before tensor memory is freed

@@ -7,13 +7,19 @@
 // Acceleration of Large Language Models via Training-Time Test", "Stage 2:
 // Verification".
 //
-// Two kernels:
+// Three kernels:
 //   rowstats : one CTA per (row, request): max and sum-exp of z/T (stochastic)
-//              or the argmax (greedy without a caller-provided argmax).
-//   walk     : one CTA per request: thread 0 walks the tree from the seed
-//              using the row statistics and the target logit of each child's
-//              token; then the whole CTA runs the exponential race over the
-//              stop row for the bonus token.
+//              or the argmax (greedy without a caller-provided argmax),
+//              streamed with 16-byte loads, four in flight per thread.
+//   walk     : one CTA per request: every per-row input of the walk (parents,
+//              tokens, row statistics or argmax, the target logit of each
+//              child's token at its parent row, the accept-test uniform) is
+//              gathered into shared memory in parallel, then one warp walks the
+//              tree from the seed without touching global memory.
+//   race     : (stochastic only) the exponential race for the bonus token at
+//              the stop row, split over 4096-id chunks of the vocabulary; each
+//              CTA reduces its chunk and the last CTA of a request (atomic
+//              ticket, no waiting) merges the chunk winners.
 #include <math.h>
 
 #include <atomic>
@@ -26,6 +32,8 @@ namespace {
 
 constexpr int kStatThreads = 256;
 constexpr int kWalkThreads = 512;
+constexpr int kRaceThreads = 256;
+constexpr int kRaceChunk = 4096;  // vocabulary ids per race CTA
 constexpr int kMaxVerifyRows = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -34,11 +42,36 @@ struct RowStat {
   float s;  // sum_v exp(z/T - m)
 };
 
+// Walk result of one request, read by the race kernel.
+struct VerifyReq {
+  int stop;    // row where the walk stopped; -1 = no race (bad tree)
+  int plen;    // rows on the accepted path (seed included)
+  int nexcl;   // tokens rejected at the stop row
+  int ticket;  // race CTAs of this request that have finished
+};
+
+struct RacePart {
+  float key;
+  int id;
+};
+
 __device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
   if (better(v2, i2, v, i)) {
     v = v2;
     i = i2;
   }
+}
+
+// Online max / sum-exp of four values of y = z/T.
+__device__ __forceinline__ void lse_add4(float& m, float& s, float y0, float y1, float y2, float y3) {
+  const float m4 = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+  if (m4 > m) {
+    s *= exp2f((m - m4) * kLog2e);
+    m = m4;
+  }
+  if (m != -INFINITY)
+    s += exp2f((y0 - m) * kLog2e) + exp2f((y1 - m) * kLog2e) + exp2f((y2 - m) * kLog2e) +
+         exp2f((y3 - m) * kLog2e);
 }
 
 __global__ void __launch_bounds__(kStatThreads) verify_rowstats_kernel(
@@ -56,14 +89,50 @@ __global__ void __launch_bounds__(kStatThreads) verify_rowstats_kernel(
   __shared__ int sh_i[kStatThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   bool nan_seen = false;
-  if (want_argmax) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int v = threadIdx.x; v < V; v += kStatThreads) {
-      const float x = z[v];
-      nan_seen |= isnan(x);
-      argmax_merge(bv, bi, x, v);
+  float m = -INFINITY, s = 0.f;     // stochastic: online max / sum-exp of z/T
+  float bv = -INFINITY;             // greedy: argmax (ties to the lower id)
+  int bi = 0x7fffffff;
+  auto take4 = [&](float z0, float z1, float z2, float z3, int y) {
+    nan_seen |= isnan(z0) | isnan(z1) | isnan(z2) | isnan(z3);
+    if (want_argmax) {
+      argmax_merge(bv, bi, z0, y);
+      argmax_merge(bv, bi, z1, y + 1);
+      argmax_merge(bv, bi, z2, y + 2);
+      argmax_merge(bv, bi, z3, y + 3);
+    } else {
+      lse_add4(m, s, z0 * inv_t, z1 * inv_t, z2 * inv_t, z3 * inv_t);
     }
+  };
+  if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) {
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+    const int n4 = V >> 2;
+    constexpr int kU = 4;  // 16-byte loads in flight per thread
+    for (int i0 = threadIdx.x; i0 < n4; i0 += kStatThreads * kU) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kStatThreads;
+        v[u] = i < n4 ? __ldcs(z4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kStatThreads;
+        if (i < n4) take4(v[u].x, v[u].y, v[u].z, v[u].w, 4 * i);
+      }
+    }
+  } else {
+    for (int y = threadIdx.x; y < V; y += kStatThreads) {
+      const float x = z[y];
+      nan_seen |= isnan(x);
+      if (want_argmax) {
+        argmax_merge(bv, bi, x, y);
+      } else {
+        const float yv = x * inv_t;
+        lse_add4(m, s, yv, -INFINITY, -INFINITY, -INFINITY);
+      }
+    }
+  }
+  if (want_argmax) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -80,18 +149,6 @@ __global__ void __launch_bounds__(kStatThreads) verify_rowstats_kernel(
       amax[(size_t)b * R + r] = bi;
     }
   } else {
-    // online max / sum-exp of y = z / T
-    float m = -INFINITY, s = 0.f;
-    for (int v = threadIdx.x; v < V; v += kStatThreads) {
-      const float y = z[v] * inv_t;
-      nan_seen |= isnan(y);
-      if (y > m) {
-        s = s * exp2f((m - y) * kLog2e) + 1.f;
-        m = y;
-      } else {
-        s += exp2f((y - m) * kLog2e);
-      }
-    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       const float om = __shfl_xor_sync(0xffffffffu, m, o);
@@ -125,95 +182,124 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
     const int32_t* __restrict__ ws_argmax, int greedy, float inv_t, uint32_t key0, uint32_t key1,
     uint32_t ctr2_accept, uint32_t ctr3, const float* __restrict__ uniforms_override,
     int max_depth, int32_t* __restrict__ accept_len, int32_t* __restrict__ path_rows,
-    int32_t* __restrict__ out_tokens, int32_t* dev_status) {
+    int32_t* __restrict__ out_tokens, VerifyReq* __restrict__ req, int32_t* __restrict__ excl_out,
+    int32_t* dev_status) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
   __shared__ int s_parent[kMaxVerifyRows];
   __shared__ int s_token[kMaxVerifyRows];
-  __shared__ int s_path[65];
+  __shared__ int s_amax[kMaxVerifyRows];      // greedy: argmax of row i
+  __shared__ float s_zt[kMaxVerifyRows];      // z[parent(i), token(i)]
+  __shared__ RowStat s_stat[kMaxVerifyRows];  // (max, sum-exp) of row i
+  __shared__ float s_u[kMaxVerifyRows];       // accept-test uniform of row i
   __shared__ int s_excl[kMaxVerifyRows];
-  __shared__ int s_nexcl, s_stop, s_plen, s_bad, s_bonus;
-  __shared__ float s_rv[kWalkThreads / 32];
-  __shared__ int s_ri[kWalkThreads / 32];
+  __shared__ int s_ch[kMaxVerifyRows];         // children of the current row
+  __shared__ int s_path[65];
+  __shared__ int s_nexcl, s_stop, s_plen, s_bad;
 
   const int n = n_rows ? n_rows[b] : R;
-  if (threadIdx.x == 0) {
-    s_bad = (n < 1 || n > R) ? 1 : 0;
-    s_nexcl = 0;
-  }
+  if (threadIdx.x == 0) s_bad = (n < 1 || n > R) ? 1 : 0;
   __syncthreads();
   const int nn = s_bad ? 1 : n;
+  const int32_t* am_src = target_argmax ? target_argmax : ws_argmax;
   for (int i = threadIdx.x; i < nn; i += kWalkThreads) {
-    const int p = parent_row[(size_t)b * R + i];
-    const int t = token[(size_t)b * R + i];
+    const size_t gi = (size_t)b * R + i;
+    const int p = parent_row[gi];
+    const int t = token[gi];
     s_parent[i] = p;
     s_token[i] = t;
     const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i && t >= 0 && t < V);
     if (!ok) atomicExch(&s_bad, 1);
+    if (greedy) {
+      s_amax[i] = am_src[gi];
+    } else {
+      s_stat[i] = stats[gi];
+      s_zt[i] = (i > 0 && ok) ? logits[((size_t)b * R + p) * V + t] : 0.f;
+      if (uniforms_override) {
+        s_u[i] = uniforms_override[gi];
+      } else {
+        const uint4 w =
+            philox4x32_10(make_uint4((uint32_t)i, (uint32_t)b, ctr2_accept, ctr3), key0, key1);
+        s_u[i] = bits_to_uniform(w.x);
+      }
+    }
   }
   __syncthreads();
 
-  if (threadIdx.x == 0) {
-    int plen = 1, cur = 0, bad = s_bad;
-    s_path[0] = 0;
+  // the walk, by warp 0: the children of the current row are found 32 rows at
+  // a time with ballots; the stochastic accept chain over them runs on lane 0
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int plen = 1, cur = 0, bad = s_bad, nex = 0;
+    if (lane == 0) s_path[0] = 0;
     while (!bad) {
       int accepted = -1;
       if (greedy) {
-        const int a = target_argmax ? target_argmax[(size_t)b * R + cur]
-                                    : ws_argmax[(size_t)b * R + cur];
-        for (int c = cur + 1; c < nn; ++c)
-          if (s_parent[c] == cur && s_token[c] == a) {
-            accepted = c;
-            break;
-          }
+        const int a = s_amax[cur];
+        for (int c0 = cur + 1; c0 < nn && accepted < 0; c0 += 32) {
+          const int c = c0 + lane;
+          const unsigned hit =
+              __ballot_sync(0xffffffffu, c < nn && s_parent[c] == cur && s_token[c] == a);
+          if (hit) accepted = c0 + __ffs(hit) - 1;
+        }
       } else {
-        const RowStat st = stats[(size_t)b * R + cur];
-        const float* z = logits + ((size_t)b * R + cur) * V;
-        float rem = 1.f;  // probability mass not yet rejected
-        s_nexcl = 0;
-        for (int c = cur + 1; c < nn; ++c) {
-          if (s_parent[c] != cur) continue;
-          const int t = s_token[c];
-          bool dup = false;
-          for (int e = 0; e < s_nexcl; ++e) dup |= (s_excl[e] == t);
-          const float pt = dup ? 0.f : exp2f((z[t] * inv_t - st.m) * kLog2e) / st.s;
-          const float ratio = pt / rem;
-          float u;
-          if (uniforms_override) {
-            u = uniforms_override[(size_t)b * R + c];
-          } else {
-            const uint4 w = philox4x32_10(make_uint4((uint32_t)c, (uint32_t)b, ctr2_accept, ctr3),
-                                          key0, key1);
-            u = bits_to_uniform(w.x);
-          }
-          if (u < ratio) {
-            accepted = c;
-            break;
-          }
-          if (!dup && rem - pt > 0.f) {
-            rem -= pt;
-            s_excl[s_nexcl++] = t;
+        int nch = 0;  // children of cur, in row order, into s_ch
+        for (int c0 = cur + 1; c0 < nn; c0 += 32) {
+          const int c = c0 + lane;
+          const bool is_child = c < nn && s_parent[c] == cur;
+          const unsigned m = __ballot_sync(0xffffffffu, is_child);
+          if (is_child) s_ch[nch + __popc(m & ((1u << lane) - 1u))] = c;
+          nch += __popc(m);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const RowStat st = s_stat[cur];
+          float rem = 1.f;  // probability mass not yet rejected
+          nex = 0;
+          for (int j = 0; j < nch; ++j) {
+            const int c = s_ch[j];
+            const int t = s_token[c];
+            bool dup = false;
+            for (int e = 0; e < nex; ++e) dup |= (s_excl[e] == t);
+            const float pt = dup ? 0.f : exp2f((s_zt[c] * inv_t - st.m) * kLog2e) / st.s;
+            const float ratio = pt / rem;
+            if (s_u[c] < ratio) {
+              accepted = c;
+              break;
+            }
+            if (!dup && rem - pt > 0.f) {
+              rem -= pt;
+              s_excl[nex++] = t;
+            }
           }
         }
+        accepted = __shfl_sync(0xffffffffu, accepted, 0);
+        nex = __shfl_sync(0xffffffffu, nex, 0);
+        __syncwarp();
       }
       if (accepted < 0) break;
       if (plen > max_depth) {
         bad = 2;
         break;
       }
-      s_path[plen++] = accepted;
+      if (lane == 0) s_path[plen] = accepted;
+      ++plen;
       cur = accepted;
     }
-    s_stop = cur;
-    s_plen = plen;
-    if (bad) s_bad = bad;
+    if (lane == 0) {
+      s_stop = cur;
+      s_plen = plen;
+      s_nexcl = greedy ? 0 : nex;
+      if (bad) s_bad = bad;
+    }
   }
   __syncthreads();
   if (s_bad) {
     if (threadIdx.x == 0) {
       set_status(dev_status, EAGLE_ERR_BAD_TREE);
       accept_len[b] = 0;
+      if (req) req[b] = VerifyReq{-1, 0, 0, 0};
     }
     for (int i = threadIdx.x; i <= max_depth; i += kWalkThreads) {
       path_rows[(size_t)b * (max_depth + 1) + i] = (i == 0) ? 0 : -1;
@@ -221,84 +307,150 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
     }
     return;
   }
-
-  const int stop = s_stop;
-  if (greedy) {
-    if (threadIdx.x == 0)
-      s_bonus = target_argmax ? target_argmax[(size_t)b * R + stop] : ws_argmax[(size_t)b * R + stop];
-  } else {
-    // exponential race over the ids not rejected at the stop row:
-    // bonus = argmax_y z_y/T - log(-log u_y)  (ties to the lower id)
-    const float* z = logits + ((size_t)b * R + stop) * V;
-    const int nex = s_nexcl;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    bool nan_seen = false;
-    const uint32_t ctr2_race = ctr2_accept + 1u;
-    for (int g = threadIdx.x; g * 4 < V; g += kWalkThreads) {
-      const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, ctr2_race, ctr3), key0, key1);
-      const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int y = g * 4 + j;
-        if (y >= V) break;
-        bool ex = false;
-        for (int e = 0; e < nex; ++e) ex |= (s_excl[e] == y);
-        if (ex) continue;
-        const float zy = z[y];
-        nan_seen |= isnan(zy);
-        const float u = bits_to_uniform(words[j]);
-        const float key = zy * inv_t - logf(-logf(u));
-        argmax_merge(bv, bi, key, y);
-      }
-    }
-    if (nan_seen) set_status(dev_status, EAGLE_ERR_NONFINITE);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      argmax_merge(bv, bi, ov, oi);
-    }
-    if ((threadIdx.x & 31) == 0) {
-      s_rv[threadIdx.x >> 5] = bv;
-      s_ri[threadIdx.x >> 5] = bi;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kWalkThreads / 32; ++w) argmax_merge(bv, bi, s_rv[w], s_ri[w]);
-      s_bonus = bi;
-    }
-  }
-  __syncthreads();
-  const int plen = s_plen;
+  const int plen = s_plen, stop = s_stop;
   for (int i = threadIdx.x; i <= max_depth; i += kWalkThreads) {
     const size_t o = (size_t)b * (max_depth + 1) + i;
     path_rows[o] = i < plen ? s_path[i] : -1;
-    out_tokens[o] = i + 1 < plen ? s_token[s_path[i + 1]] : (i + 1 == plen ? s_bonus : -1);
+    if (i + 1 < plen)
+      out_tokens[o] = s_token[s_path[i + 1]];
+    else if (i + 1 > plen)
+      out_tokens[o] = -1;
+    else if (greedy)
+      out_tokens[o] = s_amax[stop];  // the bonus token; the race writes it otherwise
+  }
+  if (!greedy) {
+    const int nex = s_nexcl;
+    for (int e = threadIdx.x; e < nex; e += kWalkThreads) excl_out[(size_t)b * R + e] = s_excl[e];
+    if (threadIdx.x == 0) req[b] = VerifyReq{stop, plen, nex, 0};
   }
   if (threadIdx.x == 0) accept_len[b] = plen - 1;
 }
 
-}  // namespace
-}  // namespace eagle
-
-using namespace eagle;
-
-extern "C" size_t eagle_tree_verify_workspace_size(int B, int R, int V) {
-  (void)V;
-  if (B <= 0 || R <= 0) return 0;
-  return round_up((size_t)B * R * sizeof(RowStat), 256) + round_up((size_t)B * R * 4, 256) + 512;
+// Exponential race over the ids not rejected at the stop row:
+// bonus = argmax_y z_y/T - log(-log u_y), ties to the lower id.
+__global__ void __launch_bounds__(kRaceThreads) verify_race_kernel(
+    int R, int V, const float* __restrict__ logits, VerifyReq* __restrict__ req,
+    const int32_t* __restrict__ excl, RacePart* __restrict__ part, float inv_t, uint32_t key0,
+    uint32_t key1, uint32_t ctr2_race, uint32_t ctr3, int max_depth,
+    int32_t* __restrict__ out_tokens, int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, cx = blockIdx.y, C = gridDim.y;
+  const VerifyReq q = req[b];
+  if (q.stop < 0) return;
+  const int lo = cx * kRaceChunk, hi = min(V, lo + kRaceChunk);
+  __shared__ uint32_t s_bits[kRaceChunk / 32];  // excluded ids of this chunk
+  __shared__ float s_rv[kRaceThreads / 32];
+  __shared__ int s_ri[kRaceThreads / 32];
+  __shared__ int s_last;
+  for (int i = threadIdx.x; i < kRaceChunk / 32; i += kRaceThreads) s_bits[i] = 0u;
+  __syncthreads();
+  for (int e = threadIdx.x; e < q.nexcl; e += kRaceThreads) {
+    const int y = excl[(size_t)b * R + e];
+    if (y >= lo && y < hi) atomicOr(&s_bits[(y - lo) >> 5], 1u << ((y - lo) & 31));
+  }
+  __syncthreads();
+  const float* z = logits + ((size_t)b * R + q.stop) * V;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  bool nan_seen = false;
+  for (int g = lo / 4 + threadIdx.x; g * 4 < hi; g += kRaceThreads) {
+    const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, ctr2_race, ctr3), key0, key1);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int y = g * 4 + j;
+      if (y >= hi) break;
+      if ((s_bits[(y - lo) >> 5] >> ((y - lo) & 31)) & 1u) continue;
+      const float zy = z[y];
+      nan_seen |= isnan(zy);
+      const float u = bits_to_uniform(words[j]);
+      argmax_merge(bv, bi, zy * inv_t - logf(-logf(u)), y);
+    }
+  }
+  if (nan_seen) set_status(dev_status, EAGLE_ERR_NONFINITE);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    argmax_merge(bv, bi, ov, oi);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_rv[threadIdx.x >> 5] = bv;
+    s_ri[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRaceThreads / 32; ++w) argmax_merge(bv, bi, s_rv[w], s_ri[w]);
+    part[(size_t)b * C + cx] = RacePart{bv, bi};
+    __threadfence();
+    s_last = atomicAdd(&req[b].ticket, 1) == C - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // the last chunk of this request to finish merges the chunk winners
+  __threadfence();
+  float mv = -INFINITY;
+  int mi = 0x7fffffff;
+  for (int c = threadIdx.x; c < C; c += kRaceThreads) {
+    const float pk = __ldcg(&part[(size_t)b * C + c].key);
+    const int pi = __ldcg(&part[(size_t)b * C + c].id);
+    argmax_merge(mv, mi, pk, pi);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, mv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, mi, o);
+    argmax_merge(mv, mi, ov, oi);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_rv[threadIdx.x >> 5] = mv;
+    s_ri[threadIdx.x >> 5] = mi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRaceThreads / 32; ++w) argmax_merge(mv, mi, s_rv[w], s_ri[w]);
+    out_tokens[(size_t)b * (max_depth + 1) + q.plen - 1] = mi;
+    req[b].ticket = 0;
+  }
 }
 
-extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
-                                 const int32_t* token, const int32_t* n_rows,
-                                 const float* target_logits, const int32_t* target_argmax,
-                                 const float* draft_logits, float temperature, int proposal_mode,
-                                 uint64_t seed, uint64_t offset, const float* uniforms_override,
-                                 int max_depth, int32_t* accept_len, int32_t* path_rows,
-                                 int32_t* out_tokens, void* ws, size_t ws_bytes,
-                                 int32_t* dev_status, void* stream) {
-  (void)draft_logits;
+int race_chunks(int V) { return (V + kRaceChunk - 1) / kRaceChunk; }
+
+// Workspace layout shared by eagle_tree_verify (caller buffer) and the
+// allocation-free variant (library buffer).
+struct VerifyScratch {
+  RowStat* stats;
+  int32_t* amax;
+  int32_t* excl;
+  VerifyReq* req;
+  RacePart* part;
+};
+
+
+size_t scratch_bytes(int B, int R, int V) {
+  return round_up((size_t)B * R * sizeof(RowStat), 256) + round_up((size_t)B * R * 4, 256) * 2 +
+         round_up((size_t)B * sizeof(VerifyReq), 256) +
+         round_up((size_t)B * race_chunks(V) * sizeof(RacePart), 256) + 256;
+}
+
+VerifyScratch carve_scratch(void* base, int B, int R, int V, bool race) {
+  char* cur = static_cast<char*>(base);
+  VerifyScratch w;
+  w.stats = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
+  w.amax = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
+  w.excl = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
+  w.req = static_cast<VerifyReq*>(ws_carve(cur, (size_t)B * sizeof(VerifyReq)));
+  w.part = race ? static_cast<RacePart*>(ws_carve(cur, (size_t)B * race_chunks(V) * sizeof(RacePart)))
+               : nullptr;
+  return w;
+}
+
+// Host-side argument checks common to both entry points.
+int verify_check(int B, int R, int V, const int32_t* parent_row, const int32_t* token,
+                 const float* target_logits, const int32_t* target_argmax, float temperature,
+                 int proposal_mode, uint64_t offset, int max_depth, const int32_t* accept_len,
+                 const int32_t* path_rows, const int32_t* out_tokens) {
   if (B <= 0 || R <= 0 || V < 2 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
   if (!parent_row || !token || !accept_len || !path_rows || !out_tokens) return EAGLE_ERR_INVALID_ARG;
   if (!(temperature >= 0.f) || isinf(temperature)) return EAGLE_ERR_INVALID_ARG;
@@ -310,32 +462,75 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
   if (!greedy && !target_logits) return EAGLE_ERR_INVALID_ARG;
   if (R > kMaxVerifyRows || max_depth > 64) return EAGLE_ERR_UNSUPPORTED;
   if ((offset >> 63) != 0) return EAGLE_ERR_INVALID_ARG;
-  const bool need_stats = !greedy || !target_argmax;
-  if (need_stats && (!ws || ws_bytes < eagle_tree_verify_workspace_size(B, R, V)))
-    return EAGLE_ERR_WORKSPACE;
   if ((long long)B * R > 2147483647LL) return EAGLE_ERR_UNSUPPORTED;
+  if (!greedy && race_chunks(V) > 65535) return EAGLE_ERR_UNSUPPORTED;
+  return EAGLE_OK;
+}
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* cur = static_cast<char*>(ws);
-  RowStat* stats = nullptr;
-  int32_t* amax = nullptr;
-  if (need_stats) {
-    stats = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
-    amax = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
-  }
+// Enqueues the kernels of one verification (arguments already checked).
+int verify_enqueue(int B, int R, int V, const int32_t* parent_row, const int32_t* token,
+                   const int32_t* n_rows, const float* target_logits,
+                   const int32_t* target_argmax, float temperature, uint64_t seed, uint64_t offset,
+                   const float* uniforms_override, int max_depth, int32_t* accept_len,
+                   int32_t* path_rows, int32_t* out_tokens, const VerifyScratch& w,
+                   int32_t* dev_status, cudaStream_t s) {
+  const bool greedy = temperature == 0.f;
+  const bool need_stats = !greedy || !target_argmax;
   const float inv_t = greedy ? 0.f : 1.f / temperature;
   if (need_stats) {
-    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s,
-        target_logits, n_rows, R, V, inv_t, greedy ? 1 : 0, stats, amax, dev_status);
+    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s, target_logits, n_rows, R,
+           V, inv_t, greedy ? 1 : 0, w.stats, w.amax, dev_status);
     note_launch();
   }
   const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
-  launch(verify_walk_kernel, B, kWalkThreads, 0, s,
-      R, V, parent_row, token, n_rows, target_logits, target_argmax, stats, amax, greedy ? 1 : 0,
-      inv_t, (uint32_t)seed, (uint32_t)(seed >> 32), 2u * off_hi, off_lo, uniforms_override,
-      max_depth, accept_len, path_rows, out_tokens, dev_status);
+  const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+  launch(verify_walk_kernel, B, kWalkThreads, 0, s, R, V, parent_row, token, n_rows, target_logits,
+         target_argmax, need_stats ? w.stats : nullptr, need_stats ? w.amax : nullptr,
+         greedy ? 1 : 0, inv_t, key0, key1, 2u * off_hi, off_lo, uniforms_override, max_depth,
+         accept_len, path_rows, out_tokens, greedy ? nullptr : w.req,
+         greedy ? nullptr : w.excl, dev_status);
   note_launch();
+  if (!greedy) {
+    launch(verify_race_kernel, dim3((unsigned)B, (unsigned)race_chunks(V)), kRaceThreads, 0, s, R,
+           V, target_logits, w.req, w.excl, w.part, inv_t, key0, key1, 2u * off_hi + 1u, off_lo,
+           max_depth, out_tokens, dev_status);
+    note_launch();
+  }
   return last_launch_status();
+}
+
+}  // namespace
+}  // namespace eagle
+
+using namespace eagle;
+
+extern "C" size_t eagle_tree_verify_workspace_size(int B, int R, int V) {
+  if (B <= 0 || R <= 0 || V < 2) return 0;
+  return scratch_bytes(B, R, V);
+}
+
+extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
+                                 const int32_t* token, const int32_t* n_rows,
+                                 const float* target_logits, const int32_t* target_argmax,
+                                 const float* draft_logits, float temperature, int proposal_mode,
+                                 uint64_t seed, uint64_t offset, const float* uniforms_override,
+                                 int max_depth, int32_t* accept_len, int32_t* path_rows,
+                                 int32_t* out_tokens, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, void* stream) {
+  (void)draft_logits;
+  const int chk = verify_check(B, R, V, parent_row, token, target_logits, target_argmax,
+                               temperature, proposal_mode, offset, max_depth, accept_len,
+                               path_rows, out_tokens);
+  if (chk != EAGLE_OK) return chk;
+  const bool need_ws = temperature != 0.f || !target_argmax;
+  VerifyScratch w{};
+  if (need_ws) {
+    if (!ws || ws_bytes < eagle_tree_verify_workspace_size(B, R, V)) return EAGLE_ERR_WORKSPACE;
+    w = carve_scratch(ws, B, R, V, temperature != 0.f);
+  }
+  return verify_enqueue(B, R, V, parent_row, token, n_rows, target_logits, target_argmax,
+                        temperature, seed, offset, uniforms_override, max_depth, accept_len,
+                        path_rows, out_tokens, w, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -349,9 +544,12 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
 namespace eagle {
 namespace {
 
-constexpr int kNoAllocMaxRows = 65536;  // B * R rows of statistics
+constexpr int kNoAllocMaxRows = 65536;    // B * R rows of statistics
+constexpr int kNoAllocMaxChunks = 65536;  // B * ceil(V / 4096) race chunks
 constexpr size_t kNoAllocScratchBytes =
-    ((size_t)kNoAllocMaxRows * sizeof(RowStat) + 255) / 256 * 256 + (size_t)kNoAllocMaxRows * 4;
+    (size_t)kNoAllocMaxRows * sizeof(RowStat) + (size_t)kNoAllocMaxRows * 4 * 2 +
+    (size_t)kNoAllocMaxRows * sizeof(VerifyReq) + (size_t)kNoAllocMaxChunks * sizeof(RacePart) +
+    5 * 256;
 
 // One copy per GPU that loads the library, kept until the process exits.
 // Every call on a device shares it: two calls whose kernels overlap on that
@@ -398,41 +596,23 @@ extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* par
                                          int32_t* accept_len, int32_t* path_rows,
                                          int32_t* out_tokens, int32_t* dev_status, void* stream) {
   (void)draft_logits;
-  if (B <= 0 || R <= 0 || V < 2 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
-  if (!parent_row || !token || !accept_len || !path_rows || !out_tokens) return EAGLE_ERR_INVALID_ARG;
-  if (!(temperature >= 0.f) || isinf(temperature)) return EAGLE_ERR_INVALID_ARG;
-  if (proposal_mode != EAGLE_PROPOSAL_DETERMINISTIC && proposal_mode != EAGLE_PROPOSAL_SAMPLED)
-    return EAGLE_ERR_INVALID_ARG;
-  const bool greedy = temperature == 0.f;
-  if (proposal_mode == EAGLE_PROPOSAL_SAMPLED) return greedy ? EAGLE_ERR_INVALID_ARG : EAGLE_ERR_UNSUPPORTED;
-  if (greedy && !target_logits && !target_argmax) return EAGLE_ERR_INVALID_ARG;
-  if (!greedy && !target_logits) return EAGLE_ERR_INVALID_ARG;
-  if (R > kMaxVerifyRows || max_depth > 64) return EAGLE_ERR_UNSUPPORTED;
-  if ((offset >> 63) != 0) return EAGLE_ERR_INVALID_ARG;
-  // the built-in scratch holds statistics for at most kNoAllocMaxRows rows
-  if ((long long)B * R > kNoAllocMaxRows) return EAGLE_ERR_WORKSPACE;
-  const bool need_stats = !greedy || !target_argmax;
-  RowStat* stats = nullptr;
-  int32_t* amax = nullptr;
-  if (need_stats) {
+  const int chk = verify_check(B, R, V, parent_row, token, target_logits, target_argmax,
+                               temperature, proposal_mode, offset, max_depth, accept_len,
+                               path_rows, out_tokens);
+  if (chk != EAGLE_OK) return chk;
+  // the built-in scratch holds kNoAllocMaxRows rows and kNoAllocMaxChunks
+  // race chunks
+  if ((long long)B * R > kNoAllocMaxRows ||
+      (temperature != 0.f && (long long)B * race_chunks(V) > kNoAllocMaxChunks))
+    return EAGLE_ERR_WORKSPACE;
+  VerifyScratch w{};
+  if (temperature != 0.f || !target_argmax) {
     eagle_status st = EAGLE_OK;
-    char* base = static_cast<char*>(noalloc_scratch(&st));
+    void* base = noalloc_scratch(&st);
     if (!base) return st;
-    stats = reinterpret_cast<RowStat*>(base);
-    amax = reinterpret_cast<int32_t*>(base + ((size_t)kNoAllocMaxRows * sizeof(RowStat) + 255) / 256 * 256);
+    w = carve_scratch(base, B, R, V, temperature != 0.f);
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const float inv_t = greedy ? 0.f : 1.f / temperature;
-  if (need_stats) {
-    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s,
-        target_logits, n_rows, R, V, inv_t, greedy ? 1 : 0, stats, amax, dev_status);
-    note_launch();
-  }
-  const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
-  launch(verify_walk_kernel, B, kWalkThreads, 0, s,
-      R, V, parent_row, token, n_rows, target_logits, target_argmax, stats, amax, greedy ? 1 : 0,
-      inv_t, (uint32_t)seed, (uint32_t)(seed >> 32), 2u * off_hi, off_lo, uniforms_override,
-      max_depth, accept_len, path_rows, out_tokens, dev_status);
-  note_launch();
-  return last_launch_status();
+  return verify_enqueue(B, R, V, parent_row, token, n_rows, target_logits, target_argmax,
+                        temperature, seed, offset, uniforms_override, max_depth, accept_len,
+                        path_rows, out_tokens, w, dev_status, static_cast<cudaStream_t>(stream));
 }

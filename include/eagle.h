@@ -288,10 +288,14 @@ int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row, const int3
  * every device allocation and passes it only its input and output tensors,
  * or a latency-critical loop that must not call cudaMalloc (which can
  * synchronise the whole device).  Arguments, outputs and semantics are those
- * of eagle_tree_verify minus `ws` / `ws_bytes`; the row statistics live in a
- * fixed buffer inside the library instead.
- *   Capacity: B * R <= 65536 rows; larger calls return EAGLE_ERR_WORKSPACE
- *   without launching anything.  The buffer (768 KB) is a static device
+ * of eagle_tree_verify minus `ws` / `ws_bytes`; the scratch that
+ * eagle_tree_verify keeps in `ws` lives in a fixed buffer inside the library
+ * instead.
+ *   Capacity: B * R <= 65536 rows and, when temperature > 0,
+ *   B * ceil(V / 4096) <= 65536 race chunks; larger calls return
+ *   EAGLE_ERR_WORKSPACE without launching anything.  The buffer (2.5 MB:
+ *   row statistics, argmax, rejected tokens, per-request walk results and
+ *   race partials) is a static device
  *   array: every GPU that loads the library holds one copy until the process
  *   exits, and no call allocates or frees memory.
  *   The first call on a device looks up the buffer's device address (with
