@@ -8,14 +8,12 @@
 // Generation" (each node attends only to its ancestors); "EAGLE-3: Scaling up
 // Inference Acceleration ...", "The Attention Mechanism Modifications".
 //
-// bf16 path: one CTA per (query tile, KV split, request x kv head).  All
-// query rows of one kv head (R tree rows x G grouped heads) share every K/V
-// byte the CTA stages, so each prefix byte leaves HBM once per query tile.
-// K/V pages are gathered through the block table with cp.async into a
-// 3-stage ring of XOR-swizzled shared tiles; warps run m16n8k16 bf16 MMAs with
-// an fp32 online softmax; the tree's own rows form one extra 64-key block
-// masked by the u64 ancestry bits.  KV splits write (O, lse) partials that a
-// second kernel merges.  fp32 path (small shapes): a warp per query row.
+// bf16 path: tcgen05 tensor-core kernel, one CTA per (query tile, KV split,
+// request x kv head).  All query rows of one kv head (R tree rows x G grouped
+// heads) share every K/V byte the CTA stages, so each prefix byte leaves HBM
+// once per query tile.  The tree's own rows form one extra key block masked by
+// the u64 ancestry bits.  KV splits write (O, lse) partials that a second
+// kernel merges.  fp32 path (small shapes): a warp per query row.
 #include <math.h>
 
 #include "common.cuh"
@@ -23,303 +21,498 @@
 namespace eagle {
 namespace {
 
-constexpr int kBlkKeys = 64;
-constexpr int kStages = 3;
-constexpr int kMaxWarps = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct AttnParams {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k_tree;
-  const __nv_bfloat16* v_tree;
-  const __nv_bfloat16* k_cache;
-  const __nv_bfloat16* v_cache;
-  const int32_t* block_table;
-  const int32_t* ctx_lens;
-  const uint64_t* tree_mask;
-  __nv_bfloat16* out;
-  float* lse;
-  float* part_o;    // [B*R*Hq, splits, D] (splits > 1)
-  float* part_lse;  // [B*R*Hq, splits]
-  int32_t* status;
-  int B, R, Hq, Hkv, G, max_pages, num_pages, splits, rows_per_cta;
-  float scale_log2;  // scale * log2(e)
-};
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// 2^x by the SFU's approximate base-2 exponential (subnormal results flush to
+// zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Byte offset of 16-byte chunk `c` of row `row` in a swizzled [64][D] bf16 tile.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int row, int c) {
-  return (uint32_t)(row * (D * 2) + ((c ^ (row & 7)) << 4));
-}
+// ----------------------------------------------------------------------------
+// tcgen05 path (bf16).  One CTA per (query tile of up to 128 rows, KV split,
+// request x kv head); 192 threads:
+//   warp 0     TMA producer: the Q tile once (3-D box [rows of r][G heads][64]),
+//              then per 128-key block 8 paged K boxes and 8 V boxes of 16 keys
+//              (3-D map over the pool viewed as [pages*16][Hkv][D]) or the
+//              tree's own K/V rows, into a 2-stage ring
+//   warp 1     MMA issuer (one thread): S = Q K^T (M 128, N 128, K D) into one
+//              of two TMEM S buffers, one block ahead; then O_j = P_j V_j
+//              (M 128, N D, K 128, V read MN-major) into one of two TMEM PV
+//              buffers
+//   warps 2-5  softmax, one thread per query row (TMEM lane): masked row max,
+//              P = exp2(S - m) rounded to bf16 into a 128-byte-swizzled shared
+//              tile (the A operand of P V), and O = O * exp2(m_old - m) + O_j
+//              in registers
+// Masked keys read as -inf through a select, so nothing a masked K row holds
+// reaches the softmax; V rows of a partly filled page or of the padded tree
+// block are zeroed in shared memory before P V reads them.
+namespace tc {
+constexpr int kBlk = 128;          // keys per block
+constexpr int kThreads = 192;
+constexpr int kBlkBytesHalf = kBlk * 128;  // one 64-column half of a K or V block
+constexpr float kRescaleLog2 = 8.f;        // O / l reference moves when the max grows by > 2^8
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+struct Params {
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  const uint64_t* tree_mask;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+  int B, R, Hq, Hkv, G, max_pages, num_pages, splits;
+  int nr;         // tree rows per query tile (rows per tile = nr * G <= 128)
+  int tr;         // tree keys loaded: R rounded up to 16
+  float scale_log2;
+};
+}  // namespace tc
 
 template <int D>
-__global__ void __launch_bounds__(kMaxWarps * 32) tree_attn_bf16_kernel(const AttnParams p) {
-  pdl_wait();
-  pdl_trigger();
-  constexpr int kChunks = D / 8;            // 16-byte chunks per key row
-  constexpr int kTile = kBlkKeys * D * 2;   // bytes of one K (or V) tile
-  extern __shared__ __align__(1024) unsigned char smem[];
+__global__ void __launch_bounds__(tc::kThreads, 1)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                        const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_kt,
+                        const __grid_constant__ CUtensorMap map_vt, const tc::Params p) {
+  using namespace tc;
+  constexpr int NH = D / 64;                         // 128-byte column halves of a row
+  constexpr uint32_t kTileQ = 128u * 128u * NH;      // 128 rows x D
+  constexpr uint32_t kTileKV = (uint32_t)kBlk * 128u * NH;
+  constexpr uint32_t kTileP = 128u * kBlk * 2u;      // 128 rows x 128 keys
+  constexpr uint32_t kColO = 2 * kBlk;               // O accumulator after the two S buffers
+  __shared__ Bars sb;
+  extern __shared__ unsigned char dsm[];
+  const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+  const uint32_t sQ = base, sK = sQ + kTileQ, sV = sK + 2 * kTileKV, sP = sV + 2 * kTileKV;
+  unsigned char* gbase = dsm + (base - smem_u32(dsm));
+
   const int qtile = blockIdx.x, split = blockIdx.y;
   const int b = blockIdx.z / p.Hkv, kvh = blockIdx.z % p.Hkv;
-  const int nthreads = blockDim.x, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  const int rows_total = p.R * p.G;
-  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sb.abort_flag;
 
-  const int ctx = p.ctx_lens[b];
-  const int nblk = (ctx + kBlkKeys - 1) / kBlkKeys;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+    mbar_init(smem_u32(&sb.q_full), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&sb.k_full[x]), 1);
+      mbar_init(smem_u32(&sb.v_full[x]), 1);
+      mbar_init(smem_u32(&sb.kv_empty[x]), 1);
+      mbar_init(smem_u32(&sb.s_full[x]), 1);
+      mbar_init(smem_u32(&sb.s_empty[x]), 4);
+      mbar_init(smem_u32(&sb.p_full[x]), 4);
+      mbar_init(smem_u32(&sb.pv_full[x]), 1);
+    }
+    mbar_init(smem_u32(&sb.drain), 1);
+    sb.abort_flag = 0;
+    fence_mbar_init();
+  }
+  pdl_wait();  // the previous grid (and its TMEM) is gone from here on
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sb.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem = sb.tmem_base;
+
+  // this CTA's key blocks: [blk_lo, blk_hi) of the prefix, then the tree block
+  int ctx = p.ctx_lens[b];
+  if (ctx < 0 || ctx > p.max_pages * 16) {
+    if (threadIdx.x == 0) set_status(p.status, EAGLE_ERR_BAD_KV);
+    ctx = ctx < 0 ? 0 : p.max_pages * 16;
+  }
+  const int nblk = (ctx + kBlk - 1) / kBlk;
   const int bps = (nblk + p.splits - 1) / p.splits;
   const int blk_lo = min(nblk, split * bps), blk_hi = min(nblk, blk_lo + bps);
-  const bool has_tree = split == 0;
-  const int n_iter = (blk_hi - blk_lo) + (has_tree ? 1 : 0);
+  const int n_ctx = blk_hi - blk_lo;
+  const int n_iter = n_ctx + (split == 0 ? 1 : 0);
+  const int rows_tile = p.nr * p.G, rows_total = p.R * p.G;
 
-  // ---- K/V block loader (iteration it -> stage it % kStages)
-  auto load_block = [&](int it) {
-    const int st = it % kStages;
-    const uint32_t kdst = sbase + st * 2 * kTile, vdst = kdst + kTile;
-    const bool tree_blk = it == (blk_hi - blk_lo);
-    const int kb = (blk_lo + it) * kBlkKeys;
-    for (int c = tid; c < kBlkKeys * kChunks; c += nthreads) {
-      const int row = c / kChunks, ch = c % kChunks;
-      const __nv_bfloat16 *ks = p.k_cache, *vs = p.v_cache;
-      int bytes = 0;
-      if (tree_blk) {
-        if (row < p.R) {
-          const size_t off = (((size_t)b * p.R + row) * p.Hkv + kvh) * D + ch * 8;
-          ks = p.k_tree + off;
-          vs = p.v_tree + off;
-          bytes = 16;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_kv = l2_policy_evict_normal();  // the other query tiles re-read it
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint32_t oob_row = (uint32_t)p.num_pages * 16u;  // a row past the pool: reads zeros
+    auto page_of = [&](int j) -> int {  // lane < 8: page id (or -1) of slot `lane` of block j
+      if (j >= n_ctx || lane >= 8) return -1;
+      const int key0 = (blk_lo + j) * kBlk + lane * 16;
+      if (key0 >= ctx) return -1;
+      const int pg = p.block_table[(size_t)b * p.max_pages + key0 / 16];
+      if (pg < 0 || pg >= p.num_pages) {
+        set_status(p.status, EAGLE_ERR_BAD_KV);
+        return -1;
+      }
+      return pg;
+    };
+    int issued = 0;
+    if (lane == 0 && n_iter > 0) {
+      mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)NH * rows_tile * 128u);
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+        tma_load_3d(sQ + h * 16384u, &map_q, smem_u32(&sb.q_full), h * 64, kvh * p.G,
+                    b * p.R + qtile * p.nr, pol_q);
+    }
+    int pg_next = page_of(0);
+    bool ok = true;
+    for (int j = 0; j < n_iter && ok; ++j) {
+      const int pg = pg_next;
+      if (j + 1 < n_iter) pg_next = page_of(j + 1);
+      const int st = j & 1;
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      if (lane == 0) ok = mbar_wait(smem_u32(&sb.kv_empty[st]), ph ^ 1u, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const uint32_t kd = sK + st * kTileKV, vd = sV + st * kTileKV;
+      const uint32_t kf = smem_u32(&sb.k_full[st]), vf = smem_u32(&sb.v_full[st]);
+      if (j < n_ctx) {
+        int rows[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int pq = __shfl_sync(0xffffffffu, pg, q);
+          rows[q] = pq >= 0 ? pq * 16 : (int)oob_row;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(kf, kTileKV);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              tma_load_3d(kd + h * kBlkBytesHalf + q * 2048u, &map_k, kf, h * 64, kvh, rows[q], pol_kv);
+          mbar_arrive_expect_tx(vf, kTileKV);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              tma_load_3d(vd + h * kBlkBytesHalf + q * 2048u, &map_v, vf, h * 64, kvh, rows[q], pol_kv);
+        }
+      } else if (lane == 0) {  // the tree block: rows of this request's tree K / V
+        const uint32_t bytes = (uint32_t)NH * p.tr * 128u;
+        mbar_arrive_expect_tx(kf, bytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tma_load_3d(kd + h * kBlkBytesHalf, &map_kt, kf, h * 64, kvh, b * p.R, pol_q);
+        mbar_arrive_expect_tx(vf, bytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tma_load_3d(vd + h * kBlkBytesHalf, &map_vt, vf, h * 64, kvh, b * p.R, pol_q);
+      }
+      issued = j + 1;
+    }
+    if (!ok && lane == 0) {
+      // wait (bounded) for the copies already issued into each stage
+      for (int j = max(0, issued - 2); j < issued; ++j) {
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        const unsigned long long t0 = globaltimer_ns();
+        while (!(mbar_try_wait(smem_u32(&sb.k_full[j & 1]), ph) &&
+                 mbar_try_wait(smem_u32(&sb.v_full[j & 1]), ph)) &&
+               globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+      if (n_iter > 0 && !mbar_try_wait(smem_u32(&sb.q_full), 0)) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&sb.q_full), 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = true;
+    if (n_iter > 0) {
+      if (lane == 0) ok = mbar_wait(smem_u32(&sb.q_full), 0, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    const uint32_t idesc_pv = mma_idesc_bmn(1, 128, D);
+    // S(j) = Q K_j^T into S buffer j & 1
+    auto issue_s = [&](int j) -> bool {
+      const int x = j & 1;
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      bool w = true;
+      if (lane == 0)
+        w = mbar_wait(smem_u32(&sb.k_full[x]), ph, abort_flag) &&
+            mbar_wait(smem_u32(&sb.s_empty[x]), ph ^ 1u, abort_flag);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!w) return false;
+      tc_fence_after();
+      const int n = j < n_ctx ? kBlk : p.tr;
+      const uint32_t idesc = mma_idesc(1, 128, n);
+      const uint32_t kd = sK + x * kTileKV;
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t) {
+          const uint32_t off = (uint32_t)(t >> 2) * 16384u + (uint32_t)(t & 3) * 32u;
+          mma_bf16(tmem + (uint32_t)(x * kBlk), smem_desc_sw128(sQ + off), smem_desc_sw128(kd + off),
+                   idesc, t > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sb.s_full[x]));
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && n_iter > 0) ok = issue_s(0);
+    for (int j = 0; ok && j < n_iter; ++j) {
+      if (j + 1 < n_iter && !(ok = issue_s(j + 1))) break;
+      const int x = j & 1;
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      if (lane == 0) ok = mbar_wait(smem_u32(&sb.v_full[x]), ph, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      // zero V rows [z0, z1) that hold no key: the unused tail of a partly
+      // filled page, or the padding of the tree block
+      int z0 = 0, z1 = 0, nk = kBlk;
+      if (j < n_ctx) {
+        const int valid = ctx - (blk_lo + j) * kBlk;
+        if (valid < kBlk) {
+          z0 = valid;
+          z1 = min(kBlk, (valid + 15) / 16 * 16);
         }
       } else {
-        const int key = kb + row;
-        if (key < ctx) {
-          int page = p.block_table[(size_t)b * p.max_pages + key / 16];
-          if (page < 0 || page >= p.num_pages) {
-            set_status(p.status, EAGLE_ERR_BAD_KV);
-          } else {
-            const size_t off = (((size_t)page * 16 + key % 16) * p.Hkv + kvh) * D + ch * 8;
-            ks = p.k_cache + off;
-            vs = p.v_cache + off;
-            bytes = 16;
+        z0 = p.R;
+        z1 = p.tr;
+        nk = p.tr;
+      }
+      if (z0 < z1) {
+        const uint32_t vd = sV + x * kTileKV;
+        for (int c = lane; c < (z1 - z0) * NH * 8; c += 32) {
+          const int row = z0 + c / (NH * 8), h = (c / 8) % NH, ch = c % 8;
+          *reinterpret_cast<uint4*>(gbase + (vd - base) + h * kBlkBytesHalf + row * 128 + ch * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) ok = mbar_wait(smem_u32(&sb.p_full[x]), ph, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t pd = sP + x * kTileP, vd = sV + x * kTileKV;
+        for (int t = 0; t < nk / 16; ++t) {
+          const uint32_t aoff = (uint32_t)(t >> 2) * 16384u + (uint32_t)(t & 3) * 32u;
+          mma_bf16(tmem + kColO, smem_desc_sw128(pd + aoff),
+                   smem_desc_sw128_mn(vd + (uint32_t)t * 2048u, kBlkBytesHalf), idesc_pv,
+                   (j > 0 || t > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sb.pv_full[x]));
+        mma_commit(smem_u32(&sb.kv_empty[x]));
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // drain: every MMA issued so far completes before tensor memory is freed
+      mma_commit(smem_u32(&sb.drain));
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&sb.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp & 3;            // TMEM lane quarter of this warp
+    const int i = q4 * 32 + lane;       // query row of the tile = TMEM lane
+    const int gi = qtile * rows_tile + i;
+    const bool row_ok = i < rows_tile && gi < rows_total;
+    const int r_i = row_ok ? gi / p.G : 0;
+    const uint64_t mrow = row_ok ? p.tree_mask[(size_t)b * p.R + r_i] : 0ull;
+    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_iter; ++j) {
+      const int x = j & 1;
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      if (lane == 0) ok = mbar_wait(smem_u32(&sb.s_full[x]), ph, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const bool tree = j >= n_ctx;
+      const int kb = (blk_lo + j) * kBlk;
+      // visible keys of this block as a 128-bit mask (all set for a full
+      // prefix block); a masked score reads as -inf through a select
+      uint64_t vis[2];
+      bool full = false;
+      if (tree) {
+        vis[0] = p.R >= 64 ? mrow : (mrow & ((1ull << p.R) - 1ull));
+        vis[1] = 0ull;
+      } else {
+        const int lim = ctx - kb;  // >= 1
+        full = lim >= kBlk;
+        vis[0] = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
+        vis[1] = lim >= 128 ? ~0ull : (lim <= 64 ? 0ull : ((1ull << (lim - 64)) - 1ull));
+      }
+      const uint32_t sa = tmem + lane_addr + (uint32_t)(x * kBlk);
+      // pass 1: block max of the raw scores (scale > 0 commutes with max)
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+      for (int c2 = 0; c2 < kBlk / 64; ++c2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_issue(sa + (uint32_t)(c2 * 64), r0);
+        tmem_ld32_issue(sa + (uint32_t)(c2 * 64 + 32), r1);
+        tmem_wait_ld();
+        const uint32_t w0 = (uint32_t)(vis[c2] & 0xffffffffull), w1 = (uint32_t)(vis[c2] >> 32);
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(r0[k]));
+            mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(r1[k]));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            mx[k & 7] = fmaxf(mx[k & 7], ((w0 >> k) & 1u) ? __uint_as_float(r0[k]) : -INFINITY);
+            mx[k & 7] = fmaxf(mx[k & 7], ((w1 >> k) & 1u) ? __uint_as_float(r1[k]) : -INFINITY);
           }
         }
       }
-      cp_async16(kdst + swz<D>(row, ch), ks, bytes);
-      cp_async16(vdst + swz<D>(row, ch), vs, bytes);
-    }
-  };
-
-  // ---- per-warp query rows and their tree masks
-  const int qrow0 = qtile * p.rows_per_cta + warp * 16;
-  const int i0 = qrow0 + gid, i1 = i0 + 8;
-  const uint64_t m_row0 = i0 < rows_total ? p.tree_mask[(size_t)b * p.R + i0 / p.G] : 0ull;
-  const uint64_t m_row1 = i1 < rows_total ? p.tree_mask[(size_t)b * p.R + i1 / p.G] : 0ull;
-  uint32_t qa[D / 16][4];
-  {
-    auto qptr = [&](int i) -> const uint32_t* {
-      const int r = i / p.G, g = i % p.G;
-      return reinterpret_cast<const uint32_t*>(p.q + (((size_t)b * p.R + r) * p.Hq + kvh * p.G + g) * D);
-    };
-    const uint32_t* q0 = i0 < rows_total ? qptr(i0) : nullptr;
-    const uint32_t* q1 = i1 < rows_total ? qptr(i1) : nullptr;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int w0 = kk * 8 + tig, w1 = w0 + 4;  // 32-bit words (2 bf16)
-      qa[kk][0] = q0 ? q0[w0] : 0u;
-      qa[kk][1] = q1 ? q1[w0] : 0u;
-      qa[kk][2] = q0 ? q0[w1] : 0u;
-      qa[kk][3] = q1 ? q1[w1] : 0u;
-    }
-  }
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-  // prologue
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < n_iter) load_block(s);
-    cp_async_commit();
-  }
-  for (int it = 0; it < n_iter; ++it) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    if (it + kStages - 1 < n_iter) load_block(it + kStages - 1);
-    cp_async_commit();
-    if (qrow0 >= rows_total) continue;
-
-    const int st = it % kStages;
-    const uint32_t ks = sbase + st * 2 * kTile, vs = ks + kTile;
-    const bool tree_blk = it == (blk_hi - blk_lo);
-    const int kb = (blk_lo + it) * kBlkKeys;
-
-    // S = Q K^T for 64 keys (8 n-tiles of 8 keys)
-    float s[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int k2 = 0; k2 < D / 32; ++k2) {
-        const int key = nt * 8 + (lane & 7);
-        const int ch = k2 * 4 + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ks + swz<D>(key, ch), b0, b1, b2, b3);
-        mma16816(s[nt], qa[2 * k2][0], qa[2 * k2][1], qa[2 * k2][2], qa[2 * k2][3], b0, b1);
-        mma16816(s[nt], qa[2 * k2 + 1][0], qa[2 * k2 + 1][1], qa[2 * k2 + 1][2], qa[2 * k2 + 1][3],
-                 b2, b3);
-      }
-    }
-    // mask, scale and block max
-    float bmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = nt * 8 + tig * 2 + (e & 1);
-        const int hr = e >> 1;  // 0: row gid, 1: row gid+8
-        bool valid;
-        if (tree_blk) {
-          const uint64_t m = hr ? m_row1 : m_row0;
-          valid = key < p.R && ((m >> key) & 1ull);
-        } else {
-          valid = kb + key < ctx;
+      const float bm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+      // m is the reference of O and l; it moves only when a block's max
+      // exceeds it by more than 2^8 (or when it is still -inf), and then O
+      // (all earlier P V complete) and l are rescaled by 2^(m_old - m_new)
+      // (TMEM loads and stores are warp-wide: a warp rescales when any of its
+      // rows needs it, with factor 1 for the others)
+      const bool need = bm > m + kRescaleLog2;
+      const bool resc = need && m != -INFINITY && j > 0;
+      if (__ballot_sync(0xffffffffu, resc)) {
+        const float alpha = resc ? ex2_approx(m - bm) : 1.f;
+        const int jp = j - 1;
+        bool w = true;
+        if (lane == 0)
+          w = mbar_wait(smem_u32(&sb.pv_full[jp & 1]), (uint32_t)(jp >> 1) & 1u, abort_flag);
+        w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!w) {
+          ok = false;
+          break;
         }
-        const float v = valid ? s[nt][e] * p.scale_log2 : -INFINITY;
-        s[nt][e] = v;
-        bmax[hr] = fmaxf(bmax[hr], v);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_issue(tmem + lane_addr + kColO + (uint32_t)(c * 32), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+          tmem_st32(tmem + lane_addr + kColO + (uint32_t)(c * 32), r);
+        }
+        tmem_wait_st();
+        l *= alpha;
+      }
+      if (need) m = bm;
+      // pass 2: P = 2^(S * scale_log2 - m) as bf16 into the swizzled P tile
+      const float neg_m = m == -INFINITY ? 0.f : -m;
+      unsigned char* prow = gbase + (sP - base) + x * kTileP + i * 128;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kBlk / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32_issue(sa + (uint32_t)(c * 32), r);
+        tmem_wait_ld();
+        const uint32_t w = (uint32_t)(vis[c >> 1] >> ((c & 1) * 32));
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float e0 = ex2_approx(fmaf(__uint_as_float(r[2 * k]), p.scale_log2, neg_m));
+          float e1 = ex2_approx(fmaf(__uint_as_float(r[2 * k + 1]), p.scale_log2, neg_m));
+          if (!full) {
+            e0 = ((w >> (2 * k)) & 1u) ? e0 : 0.f;
+            e1 = ((w >> (2 * k + 1)) & 1u) ? e1 : 0.f;
+          }
+          ls[k & 3] += e0 + e1;
+          pk[k] = pack_bf16(e0, e1);
+        }
+        // 32 keys = half of a 128-byte row of key-half c / 2: chunks 4 (c & 1) .. + 3
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ch = (c & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(prow + (c >> 1) * 16384 + ((ch ^ (i & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sb.s_empty[x]));
+        mbar_arrive(smem_u32(&sb.p_full[x]));
       }
     }
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      bmax[hr] = fmaxf(bmax[hr], __shfl_xor_sync(0xffffffffu, bmax[hr], 1));
-      bmax[hr] = fmaxf(bmax[hr], __shfl_xor_sync(0xffffffffu, bmax[hr], 2));
+    // O is final once the last P V completes
+    if (ok && n_iter > 0) {
+      const int jl = n_iter - 1;
+      if (lane == 0)
+        ok = mbar_wait(smem_u32(&sb.pv_full[jl & 1]), (uint32_t)(jl >> 1) & 1u, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      tc_fence_after();
     }
-    float alpha[2];
+    if (ok) {
+      const int r = r_i, h = kvh * p.G + gi % p.G;
+      const size_t row = ((size_t)b * p.R + r) * p.Hq + h;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const float mnew = fmaxf(mrow[hr], bmax[hr]);
-      alpha[hr] = (mrow[hr] == -INFINITY) ? 0.f : exp2f(mrow[hr] - mnew);
-      mrow[hr] = mnew;
-      lrow[hr] *= alpha[hr];
-    }
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_iter > 0) {
+          tmem_ld32_issue(tmem + lane_addr + kColO + (uint32_t)(c * 32), o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-    for (int dn = 0; dn < D / 8; ++dn) {
-      o[dn][0] *= alpha[0];
-      o[dn][1] *= alpha[0];
-      o[dn][2] *= alpha[1];
-      o[dn][3] *= alpha[1];
-    }
-    // P = exp2(S - m) -> bf16 A fragments; l accumulates the rounded P
-    uint32_t pa[4][4];
+          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        }
+        if (!row_ok) continue;
+        if (p.splits == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      float pv[4];
+          for (int u = 0; u < 4; ++u) {
+            const float* f = reinterpret_cast<const float*>(o + 8 * u);
+            dst[u] = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
+                                pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
+          }
+        } else {
+          float4* po = reinterpret_cast<float4*>(p.part_o + (row * p.splits + split) * D + c * 32);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float m = mrow[e >> 1];
-        pv[e] = (m == -INFINITY || s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - m);
+          for (int u = 0; u < 8; ++u) {
+            const float* f = reinterpret_cast<const float*>(o + 4 * u);
+            po[u] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+          }
+        }
       }
-      const uint32_t lo = pack_bf16(pv[0], pv[1]), hi = pack_bf16(pv[2], pv[3]);
-      const __nv_bfloat162 blo = *reinterpret_cast<const __nv_bfloat162*>(&lo);
-      const __nv_bfloat162 bhi = *reinterpret_cast<const __nv_bfloat162*>(&hi);
-      lrow[0] += __low2float(blo) + __high2float(blo);
-      lrow[1] += __low2float(bhi) + __high2float(bhi);
-      const int kk = nt >> 1;
-      if ((nt & 1) == 0) {
-        pa[kk][0] = lo;
-        pa[kk][1] = hi;
-      } else {
-        pa[kk][2] = lo;
-        pa[kk][3] = hi;
-      }
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        const int i = lane >> 3;
-        const int key = kk * 16 + (i & 1) * 8 + (lane & 7);
-        const int ch = dn * 2 + (i >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vs + swz<D>(key, ch), b0, b1, b2, b3);
-        mma16816(o[2 * dn], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-        mma16816(o[2 * dn + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+      if (row_ok) {
+        if (p.splits == 1) {
+          if (p.lse) p.lse[row] = lse;
+        } else {
+          p.part_lse[row * p.splits + split] = lse;
+        }
       }
     }
   }
-  cp_async_wait<0>();
-  if (qrow0 >= rows_total) return;
-
-  // finish: quad-reduce l, normalise, write
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
-    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
-  }
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int i = hr ? i1 : i0;
-    if (i >= rows_total) continue;
-    const int r = i / p.G, h = kvh * p.G + i % p.G;
-    const size_t row = ((size_t)b * p.R + r) * p.Hq + h;
-    const float l = lrow[hr];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float lse = l > 0.f ? (mrow[hr] + log2f(l)) * kLn2 : -INFINITY;
-    if (p.splits == 1) {
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        const int d = dn * 8 + tig * 2;
-        *reinterpret_cast<uint32_t*>(p.out + row * D + d) =
-            pack_bf16(o[dn][hr * 2] * inv, o[dn][hr * 2 + 1] * inv);
-      }
-      if (p.lse && tig == 0) p.lse[row] = lse;
-    } else {
-      float* po = p.part_o + (row * p.splits + split) * D;
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        const int d = dn * 8 + tig * 2;
-        *reinterpret_cast<float2*>(po + d) = make_float2(o[dn][hr * 2] * inv, o[dn][hr * 2 + 1] * inv);
-      }
-      if (tig == 0) p.part_lse[row * p.splits + split] = lse;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (sb.abort_flag && threadIdx.x == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -420,46 +613,36 @@ __global__ void __launch_bounds__(256) tree_attn_f32_kernel(
 }
 
 struct Plan {
-  int nwarps, rows_per_cta, qtiles, splits;
+  int nr, qtiles, splits;
 };
 
 template <int D>
-size_t attn_smem() {
-  return (size_t)kStages * 2 * kBlkKeys * D * 2;
+constexpr size_t tc_smem() {
+  return 1024 + (size_t)128 * 128 * (D / 64) + 4 * (size_t)tc::kBlk * 128 * (D / 64) +
+         2 * (size_t)128 * tc::kBlk * 2;
 }
 
-// CTAs of the bf16 kernel that fit on one SM at once.
-int resident_per_sm(int D, int threads) {
-  const size_t sm = D == 128 ? attn_smem<128>() : attn_smem<64>();
-  auto kern = D == 128 ? tree_attn_bf16_kernel<128> : tree_attn_bf16_kernel<64>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, sm) != cudaSuccess || n < 1)
-    n = 1;
-  return n;
-}
-
-Plan make_plan(int B, int R, int Hq, int Hkv, int D, int max_pages, int num_splits) {
+// Query tiles of nr tree rows x G heads (nr * G <= 128 MMA rows) and the KV
+// split count.  Auto splits: the count minimising (waves of CTAs, one per SM)
+// x (128-key blocks per CTA + the tree block + 2 blocks' worth of set-up),
+// plus a small charge per split for the (O, lse) partials and their merge.
+Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   Plan pl;
-  const int rows = R * (Hq / Hkv);
-  pl.nwarps = min(kMaxWarps, (rows + 15) / 16);
-  pl.rows_per_cta = pl.nwarps * 16;
-  pl.qtiles = (rows + pl.rows_per_cta - 1) / pl.rows_per_cta;
-  const int max_blocks = max(1, (max_pages * 16 + kBlkKeys - 1) / kBlkKeys);
+  const int G = Hq / Hkv;
+  pl.nr = 128 / G;
+  pl.qtiles = (R + pl.nr - 1) / pl.nr;
+  const int max_blocks = max(1, (max_pages * 16 + tc::kBlk - 1) / tc::kBlk);
   if (num_splits > 0) {
     pl.splits = min(num_splits, max_blocks);
   } else {
-    // The split count that minimises waves x key blocks per CTA (the tree
-    // block included), plus a small charge per split for the (O, lse)
-    // partials and their merge.
     const long long base = (long long)pl.qtiles * B * Hkv;
-    const long long slots = (long long)max(1, sm_count()) * resident_per_sm(D, pl.nwarps * 32);
+    const long long slots = max(1, sm_count());
     double best = 1e300;
     pl.splits = 1;
     for (int sp = 1; sp <= min(max_blocks, 256); ++sp) {
       const long long waves = (base * sp + slots - 1) / slots;
       const int bps = (max_blocks + sp - 1) / sp;
-      const double cost = (double)waves * (bps + 1) + (sp > 1 ? 0.1 * sp : 0.0);
+      const double cost = (double)waves * (bps + 3) + (sp > 1 ? 0.1 * sp : 0.0);
       if (cost < best - 1e-9) {
         best = cost;
         pl.splits = sp;
@@ -480,7 +663,7 @@ extern "C" size_t eagle_tree_attn_workspace_size(int B, int R, int Hq, int Hkv, 
   (void)page_size;
   if (B <= 0 || R <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_pages <= 0) return 0;
   if (dtype != EAGLE_BF16 || Hq % Hkv) return 0;
-  const Plan pl = make_plan(B, R, Hq, Hkv, D, max_pages, num_splits);
+  const Plan pl = make_plan(B, R, Hq, Hkv, max_pages, num_splits);
   if (pl.splits == 1) return 0;
   const size_t rows = (size_t)B * R * Hq;
   return round_up(rows * pl.splits * D * 4, 256) + round_up(rows * pl.splits * 4, 256) + 512;
@@ -516,14 +699,11 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(out))
     return EAGLE_ERR_INVALID_ARG;
-  const Plan pl = make_plan(B, R, Hq, Hkv, D, max_pages, num_splits);
-  if (pl.splits > 65535) return EAGLE_ERR_UNSUPPORTED;
-  AttnParams p;
-  p.q = (const __nv_bfloat16*)q;
-  p.k_tree = (const __nv_bfloat16*)k_tree;
-  p.v_tree = (const __nv_bfloat16*)v_tree;
-  p.k_cache = (const __nv_bfloat16*)k_cache;
-  p.v_cache = (const __nv_bfloat16*)v_cache;
+  const Plan pl = make_plan(B, R, Hq, Hkv, max_pages, num_splits);
+  if (pl.splits > 65535 || num_pages > (1 << 26) || (long long)B * R > (1LL << 30))
+    return EAGLE_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  tc::Params p;
   p.block_table = block_table;
   p.ctx_lens = ctx_lens;
   p.tree_mask = tree_mask;
@@ -536,11 +716,12 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   p.R = R;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.G = Hq / Hkv;
+  p.G = G;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.splits = pl.splits;
-  p.rows_per_cta = pl.rows_per_cta;
+  p.nr = pl.nr;
+  p.tr = (R + 15) / 16 * 16;
   p.scale_log2 = scale * kLog2e;
   if (pl.splits > 1) {
     if (!ws || ws_bytes < eagle_tree_attn_workspace_size(B, R, Hq, Hkv, D, max_pages, page_size,
@@ -551,16 +732,25 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
     p.part_o = static_cast<float*>(ws_carve(cur, rows * pl.splits * D * 4));
     p.part_lse = static_cast<float*>(ws_carve(cur, rows * pl.splits * 4));
   }
+  // tensor maps: q as [B*R][Hq][D], the pools as [pages*16][Hkv][D], the
+  // tree K/V as [B*R][Hkv][D]; boxes of 64 columns (128 bytes)
+  CUtensorMap mq, mk, mv, mkt, mvt;
+  const uint64_t hb = (uint64_t)D * 2;
+  if (!make_tmap_3d_bf16(&mq, q, D, Hq, (uint64_t)B * R, hb, hb * Hq, 64, G, pl.nr) ||
+      !make_tmap_3d_bf16(&mk, k_cache, D, Hkv, (uint64_t)num_pages * 16, hb, hb * Hkv, 64, 1, 16) ||
+      !make_tmap_3d_bf16(&mv, v_cache, D, Hkv, (uint64_t)num_pages * 16, hb, hb * Hkv, 64, 1, 16) ||
+      !make_tmap_3d_bf16(&mkt, k_tree, D, Hkv, (uint64_t)B * R, hb, hb * Hkv, 64, 1, p.tr) ||
+      !make_tmap_3d_bf16(&mvt, v_tree, D, Hkv, (uint64_t)B * R, hb, hb * Hkv, 64, 1, p.tr))
+    return EAGLE_ERR_CUDA;
   const dim3 grid(pl.qtiles, pl.splits, B * Hkv);
-  const int threads = pl.nwarps * 32;
   if (D == 128) {
-    const size_t sm = attn_smem<128>();
-    cudaFuncSetAttribute(tree_attn_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    launch(tree_attn_bf16_kernel<128>, grid, threads, sm, s, p);
+    constexpr size_t sm = tc_smem<128>();
+    cudaFuncSetAttribute(tree_attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    launch(tree_attn_tc_kernel<128>, grid, tc::kThreads, sm, s, mq, mk, mv, mkt, mvt, p);
   } else {
-    const size_t sm = attn_smem<64>();
-    cudaFuncSetAttribute(tree_attn_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    launch(tree_attn_bf16_kernel<64>, grid, threads, sm, s, p);
+    constexpr size_t sm = tc_smem<64>();
+    cudaFuncSetAttribute(tree_attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    launch(tree_attn_tc_kernel<64>, grid, tc::kThreads, sm, s, mq, mk, mv, mkt, mvt, p);
   }
   note_launch();
   if (pl.splits > 1) {

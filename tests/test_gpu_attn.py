@@ -50,6 +50,9 @@ def _ref(q, kt, vt, kc, vc, table, ctx, mask, sample=None):
     (2, 9, 32, 8, 128, 500, 900, 3),      # forced splits
     (1, 64, 16, 1, 128, 100, 100, 0),     # G = 16, R = 64
     (4, 5, 4, 4, 64, 33, 97, 2),          # MHA, D = 64
+    (2, 20, 12, 4, 128, 50, 400, 0),      # G = 3: 42 tree rows x 3 heads per tile
+    (3, 33, 10, 2, 64, 0, 260, 0),        # G = 5, rows spill into a second tile
+    (1, 61, 32, 8, 128, 2048, 2048, 16),  # many splits, full pages
 ])
 def test_bf16_small_cases(B, R, Hq, Hkv, D, lo, hi, splits):
     b = need_gpu()
@@ -92,7 +95,7 @@ def test_full_size_sampled(cfg):
     b = need_gpu()
     c = synth.CONFIGS[cfg]
     B, R = c["B"], c["N"] + 1
-    case = _case(hash(cfg) % 997, B, R, c["Hq"], c["Hkv"], c["D"], c["ctx"][0], c["ctx"][1], "bf16",
+    case = _case(sum(map(ord, cfg)), B, R, c["Hq"], c["Hkv"], c["D"], c["ctx"][0], c["ctx"][1], "bf16",
                  depth=c["depth"])
     out, lse, st = _gpu(b, *case)
     assert st == 0
