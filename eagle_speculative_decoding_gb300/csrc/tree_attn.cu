@@ -55,13 +55,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // reaches the softmax; V rows of a partly filled page or of the padded tree
 // block are zeroed in shared memory before P V reads them.
 namespace tc {
-constexpr int kBlk = 128;          // keys per block
-constexpr int kThreads = 192;
+constexpr int kBlk = 64;           // keys per block (4 pages)
+// threads: warp 0 TMA, warp 1 MMA, four softmax warps per query tile
 constexpr int kBlkBytesHalf = kBlk * 128;  // one 64-column half of a K or V block
+constexpr int kMaxStages = 8;
+// K/V ring depth: what the shared memory left by the Q tiles and the double
+// buffered P tiles holds
+template <int D>
+__host__ __device__ constexpr int kv_stages(int tpc) {
+  return D == 128 ? (tpc == 2 ? 3 : 5) : 8;
+}
 constexpr float kRescaleLog2 = 8.f;        // O / l reference moves when the max grows by > 2^8
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_full[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -78,13 +85,14 @@ struct Params {
   int32_t* status;
   int B, R, Hq, Hkv, G, max_pages, num_pages, splits;
   int nr;         // tree rows per query tile (rows per tile = nr * G <= 128)
+  int qtiles;     // query tiles of a (request, kv head)
   int tr;         // tree keys loaded: R rounded up to 16
   float scale_log2;
 };
 }  // namespace tc
 
-template <int D>
-__global__ void __launch_bounds__(tc::kThreads, 1)
+template <int D, int TPC>
+__global__ void __launch_bounds__(64 + 128 * TPC, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
@@ -94,16 +102,23 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   constexpr int NH = D / 64;                         // 128-byte column halves of a row
   constexpr uint32_t kTileQ = 128u * 128u * NH;      // 128 rows x D
   constexpr uint32_t kTileKV = (uint32_t)kBlk * 128u * NH;
-  constexpr uint32_t kTileP = 128u * kBlk * 2u;      // 128 rows x 128 keys
-  constexpr uint32_t kColO = 2 * kBlk;               // O accumulator after the two S buffers
+  constexpr uint32_t kTileP = 128u * kBlk * 2u;      // 128 rows x 64 keys
+  constexpr int kSt = kv_stages<D>(TPC);
+  // TMEM columns: S of tile t, buffer x at t * 2 kBlk + x kBlk; O of tile t at
+  // tpc * 2 kBlk + t D
+  constexpr uint32_t kColO = (uint32_t)(TPC * 2 * kBlk);
+  constexpr uint32_t tmem_cols = TPC == 2 ? 512u : 256u;
   __shared__ Bars sb;
   extern __shared__ unsigned char dsm[];
   const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
-  const uint32_t sQ = base, sK = sQ + kTileQ, sV = sK + 2 * kTileKV, sP = sV + 2 * kTileKV;
+  // P of tile t, buffer x at sP + (2 t + x) kTileP
+  const uint32_t sQ = base, sK = sQ + TPC * kTileQ, sV = sK + kSt * kTileKV,
+                 sP = sV + kSt * kTileKV;
   unsigned char* gbase = dsm + (base - smem_u32(dsm));
 
-  const int qtile = blockIdx.x, split = blockIdx.y;
+  const int cq = blockIdx.x, split = blockIdx.y;
   const int b = blockIdx.z / p.Hkv, kvh = blockIdx.z % p.Hkv;
+  const int nt = min(TPC, p.qtiles - TPC * cq);  // query tiles of this CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &sb.abort_flag;
 
@@ -112,13 +127,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
     mbar_init(smem_u32(&sb.q_full), 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kSt; ++x) {
       mbar_init(smem_u32(&sb.k_full[x]), 1);
       mbar_init(smem_u32(&sb.v_full[x]), 1);
       mbar_init(smem_u32(&sb.kv_empty[x]), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sb.s_full[x]), 1);
-      mbar_init(smem_u32(&sb.s_empty[x]), 4);
-      mbar_init(smem_u32(&sb.p_full[x]), 4);
+      mbar_init(smem_u32(&sb.s_empty[x]), 4 * nt);
+      mbar_init(smem_u32(&sb.p_full[x]), 4 * nt);
       mbar_init(smem_u32(&sb.pv_full[x]), 1);
     }
     mbar_init(smem_u32(&sb.drain), 1);
@@ -127,7 +144,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   }
   pdl_wait();  // the previous grid (and its TMEM) is gone from here on
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sb.tmem_base), 512);
+    tmem_alloc(smem_u32(&sb.tmem_base), tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -151,13 +168,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_kv = l2_policy_evict_normal();  // the other query tiles re-read it
+    const uint64_t pol_kv = l2_policy_evict_normal();  // other CTAs of the request re-read it
     const uint64_t pol_q = l2_policy_evict_first();
     const uint32_t oob_row = (uint32_t)p.num_pages * 16u;  // a row past the pool: reads zeros
-    auto page_of = [&](int j) -> int {  // lane < 8: page id (or -1) of slot `lane` of block j
-      if (j >= n_ctx || lane >= 8) return -1;
-      const int key0 = (blk_lo + j) * kBlk + lane * 16;
-      if (key0 >= ctx) return -1;
+    // page ids, 32 at a time (8 blocks of 4 pages): lane q holds page slot
+    // q of the group; the next group is loaded one group ahead
+    constexpr int kGrp = 32 / (kBlk / 16);  // blocks per group of 32 page ids
+    auto page_group = [&](int g) -> int {
+      const int key0 = (blk_lo + g * kGrp) * kBlk + lane * 16;
+      if (g * kGrp + lane / (kBlk / 16) >= n_ctx || key0 >= ctx) return -1;
       const int pg = p.block_table[(size_t)b * p.max_pages + key0 / 16];
       if (pg < 0 || pg >= p.num_pages) {
         set_status(p.status, EAGLE_ERR_BAD_KV);
@@ -167,41 +186,44 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     };
     int issued = 0;
     if (lane == 0 && n_iter > 0) {
-      mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)NH * rows_tile * 128u);
+      mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)(nt * NH * rows_tile) * 128u);
+      for (int t = 0; t < nt; ++t)
 #pragma unroll
-      for (int h = 0; h < NH; ++h)
-        tma_load_3d(sQ + h * 16384u, &map_q, smem_u32(&sb.q_full), h * 64, kvh * p.G,
-                    b * p.R + qtile * p.nr, pol_q);
+        for (int h = 0; h < NH; ++h)
+          tma_load_3d(sQ + t * kTileQ + h * 16384u, &map_q, smem_u32(&sb.q_full), h * 64,
+                      kvh * p.G, b * p.R + (TPC * cq + t) * p.nr, pol_q);
     }
-    int pg_next = page_of(0);
+    int pg_cur = page_group(0), pg_next = kGrp < n_ctx ? page_group(1) : -1;
     bool ok = true;
+    int st = 0;
+    uint32_t ph = 0;
     for (int j = 0; j < n_iter && ok; ++j) {
-      const int pg = pg_next;
-      if (j + 1 < n_iter) pg_next = page_of(j + 1);
-      const int st = j & 1;
-      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      if (j > 0 && j % kGrp == 0) {
+        pg_cur = pg_next;
+        pg_next = j + kGrp < n_ctx ? page_group(j / kGrp + 1) : -1;
+      }
       if (lane == 0) ok = mbar_wait(smem_u32(&sb.kv_empty[st]), ph ^ 1u, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const uint32_t kd = sK + st * kTileKV, vd = sV + st * kTileKV;
       const uint32_t kf = smem_u32(&sb.k_full[st]), vf = smem_u32(&sb.v_full[st]);
       if (j < n_ctx) {
-        int rows[8];
+        int rows[kBlk / 16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int pq = __shfl_sync(0xffffffffu, pg, q);
+        for (int q = 0; q < kBlk / 16; ++q) {
+          const int pq = __shfl_sync(0xffffffffu, pg_cur, (j % kGrp) * (kBlk / 16) + q);
           rows[q] = pq >= 0 ? pq * 16 : (int)oob_row;
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(kf, kTileKV);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
+          for (int q = 0; q < kBlk / 16; ++q)
 #pragma unroll
             for (int h = 0; h < NH; ++h)
               tma_load_3d(kd + h * kBlkBytesHalf + q * 2048u, &map_k, kf, h * 64, kvh, rows[q], pol_kv);
           mbar_arrive_expect_tx(vf, kTileKV);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
+          for (int q = 0; q < kBlk / 16; ++q)
 #pragma unroll
             for (int h = 0; h < NH; ++h)
               tma_load_3d(vd + h * kBlkBytesHalf + q * 2048u, &map_v, vf, h * 64, kvh, rows[q], pol_kv);
@@ -217,15 +239,19 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         for (int h = 0; h < NH; ++h)
           tma_load_3d(vd + h * kBlkBytesHalf, &map_vt, vf, h * 64, kvh, b * p.R, pol_q);
       }
+      if (++st == kSt) {
+        st = 0;
+        ph ^= 1u;
+      }
       issued = j + 1;
     }
     if (!ok && lane == 0) {
       // wait (bounded) for the copies already issued into each stage
-      for (int j = max(0, issued - 2); j < issued; ++j) {
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      for (int j = max(0, issued - kSt); j < issued; ++j) {
+        const uint32_t ph2 = (uint32_t)(j / kSt) & 1u;
         const unsigned long long t0 = globaltimer_ns();
-        while (!(mbar_try_wait(smem_u32(&sb.k_full[j & 1]), ph) &&
-                 mbar_try_wait(smem_u32(&sb.v_full[j & 1]), ph)) &&
+        while (!(mbar_try_wait(smem_u32(&sb.k_full[j % kSt]), ph2) &&
+                 mbar_try_wait(smem_u32(&sb.v_full[j % kSt]), ph2)) &&
                globaltimer_ns() - t0 < 100000000ull) {
         }
       }
@@ -243,26 +269,31 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     const uint32_t idesc_pv = mma_idesc_bmn(1, 128, D);
-    // S(j) = Q K_j^T into S buffer j & 1
+    // S(j) = Q_t K_j^T for each query tile t into S buffer j & 1
     auto issue_s = [&](int j) -> bool {
-      const int x = j & 1;
-      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+      const int x = j & 1, st = j % kSt;  // kSt is a compile-time constant
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u, kph = (uint32_t)(j / kSt) & 1u;
       bool w = true;
       if (lane == 0)
-        w = mbar_wait(smem_u32(&sb.k_full[x]), ph, abort_flag) &&
+        w = mbar_wait(smem_u32(&sb.k_full[st]), kph, abort_flag) &&
             mbar_wait(smem_u32(&sb.s_empty[x]), ph ^ 1u, abort_flag);
       w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (!w) return false;
       tc_fence_after();
       const int n = j < n_ctx ? kBlk : p.tr;
       const uint32_t idesc = mma_idesc(1, 128, n);
-      const uint32_t kd = sK + x * kTileKV;
+      const uint32_t kd = sK + st * kTileKV;
       if (lane == 0) {
+        for (int t = 0; t < nt; ++t) {
 #pragma unroll
-        for (int t = 0; t < D / 16; ++t) {
-          const uint32_t off = (uint32_t)(t >> 2) * 16384u + (uint32_t)(t & 3) * 32u;
-          mma_bf16(tmem + (uint32_t)(x * kBlk), smem_desc_sw128(sQ + off), smem_desc_sw128(kd + off),
-                   idesc, t > 0 ? 1u : 0u);
+          for (int k = 0; k < D / 16; ++k) {
+            // +32 bytes per 16 columns inside a 128-byte row; the next 64
+            // columns sit in the next half tile
+            const uint32_t qoff = (uint32_t)(k >> 2) * 16384u + (uint32_t)(k & 3) * 32u;
+            const uint32_t koff = (uint32_t)(k >> 2) * kBlkBytesHalf + (uint32_t)(k & 3) * 32u;
+            mma_bf16(tmem + (uint32_t)(t * 2 * kBlk + x * kBlk), smem_desc_sw128(sQ + t * kTileQ + qoff),
+                     smem_desc_sw128(kd + koff), idesc, k > 0 ? 1u : 0u);
+          }
         }
         mma_commit(smem_u32(&sb.s_full[x]));
       }
@@ -272,9 +303,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     if (ok && n_iter > 0) ok = issue_s(0);
     for (int j = 0; ok && j < n_iter; ++j) {
       if (j + 1 < n_iter && !(ok = issue_s(j + 1))) break;
-      const int x = j & 1;
-      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-      if (lane == 0) ok = mbar_wait(smem_u32(&sb.v_full[x]), ph, abort_flag);
+      const int x = j & 1, st = j % kSt;
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u, kph = (uint32_t)(j / kSt) & 1u;
+      if (lane == 0) ok = mbar_wait(smem_u32(&sb.v_full[st]), kph, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       // zero V rows [z0, z1) that hold no key: the unused tail of a partly
@@ -292,7 +323,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         nk = p.tr;
       }
       if (z0 < z1) {
-        const uint32_t vd = sV + x * kTileKV;
+        const uint32_t vd = sV + st * kTileKV;
         for (int c = lane; c < (z1 - z0) * NH * 8; c += 32) {
           const int row = z0 + c / (NH * 8), h = (c / 8) % NH, ch = c % 8;
           *reinterpret_cast<uint4*>(gbase + (vd - base) + h * kBlkBytesHalf + row * 128 + ch * 16) =
@@ -306,15 +337,16 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t pd = sP + x * kTileP, vd = sV + x * kTileKV;
-        for (int t = 0; t < nk / 16; ++t) {
-          const uint32_t aoff = (uint32_t)(t >> 2) * 16384u + (uint32_t)(t & 3) * 32u;
-          mma_bf16(tmem + kColO, smem_desc_sw128(pd + aoff),
-                   smem_desc_sw128_mn(vd + (uint32_t)t * 2048u, kBlkBytesHalf), idesc_pv,
-                   (j > 0 || t > 0) ? 1u : 0u);
+        const uint32_t vd = sV + st * kTileKV;
+        for (int t = 0; t < nt; ++t) {
+          for (int k = 0; k < nk / 16; ++k)  // 64 keys = one 128-byte row of P
+            mma_bf16(tmem + kColO + (uint32_t)(t * D),
+                     smem_desc_sw128(sP + (2 * t + x) * kTileP + (uint32_t)k * 32u),
+                     smem_desc_sw128_mn(vd + (uint32_t)k * 2048u, kBlkBytesHalf), idesc_pv,
+                     (j > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&sb.pv_full[x]));
-        mma_commit(smem_u32(&sb.kv_empty[x]));
+        mma_commit(smem_u32(&sb.kv_empty[st]));
       }
       __syncwarp();
     }
@@ -325,17 +357,27 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       while (!mbar_try_wait(smem_u32(&sb.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else {
+  } else if ((warp - 2) / 4 < nt) {
     // ------------------------------------------------------------ softmax
+    const int tq = (warp - 2) / 4;      // query tile of this warp group
     const int q4 = warp & 3;            // TMEM lane quarter of this warp
     const int i = q4 * 32 + lane;       // query row of the tile = TMEM lane
-    const int gi = qtile * rows_tile + i;
+    const int gi = (TPC * cq + tq) * rows_tile + i;
     const bool row_ok = i < rows_tile && gi < rows_total;
     const int r_i = row_ok ? gi / p.G : 0;
     const uint64_t mrow = row_ok ? p.tree_mask[(size_t)b * p.R + r_i] : 0ull;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    const uint32_t o_addr = tmem + lane_addr + kColO + (uint32_t)(tq * D);
+    unsigned char* prow0 = gbase + (sP - base) + 2 * tq * kTileP + i * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    auto wait_pv = [&](int jp) -> bool {  // P V of block jp complete
+      bool w = true;
+      if (lane == 0) w = mbar_wait(smem_u32(&sb.pv_full[jp & 1]), (uint32_t)(jp >> 1) & 1u, abort_flag);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (w) tc_fence_after();
+      return w;
+    };
     for (int j = 0; j < n_iter; ++j) {
       const int x = j & 1;
       const uint32_t ph = (uint32_t)(j >> 1) & 1u;
@@ -345,74 +387,60 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       tc_fence_after();
       const bool tree = j >= n_ctx;
       const int kb = (blk_lo + j) * kBlk;
-      // visible keys of this block as a 128-bit mask (all set for a full
+      // visible keys of this block as a 64-bit mask (all set for a full
       // prefix block); a masked score reads as -inf through a select
-      uint64_t vis[2];
+      uint64_t vis;
       bool full = false;
       if (tree) {
-        vis[0] = p.R >= 64 ? mrow : (mrow & ((1ull << p.R) - 1ull));
-        vis[1] = 0ull;
+        vis = p.R >= 64 ? mrow : (mrow & ((1ull << p.R) - 1ull));
       } else {
         const int lim = ctx - kb;  // >= 1
         full = lim >= kBlk;
-        vis[0] = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
-        vis[1] = lim >= 128 ? ~0ull : (lim <= 64 ? 0ull : ((1ull << (lim - 64)) - 1ull));
+        vis = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
       }
-      const uint32_t sa = tmem + lane_addr + (uint32_t)(x * kBlk);
+      // the block's 64 scores of this row, loaded once; the S buffer is free
+      // for S(j + 2) as soon as they are in registers
+      const uint32_t sa = tmem + lane_addr + (uint32_t)(tq * 2 * kBlk + x * kBlk);
+      uint32_t sr[kBlk];
+      tmem_ld32_issue(sa, sr);
+      tmem_ld32_issue(sa + 32u, sr + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sb.s_empty[x]));
       // pass 1: block max of the raw scores (scale > 0 commutes with max)
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c2 = 0; c2 < kBlk / 64; ++c2) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32_issue(sa + (uint32_t)(c2 * 64), r0);
-        tmem_ld32_issue(sa + (uint32_t)(c2 * 64 + 32), r1);
-        tmem_wait_ld();
-        const uint32_t w0 = (uint32_t)(vis[c2] & 0xffffffffull), w1 = (uint32_t)(vis[c2] >> 32);
-        if (full) {
+        for (int k = 0; k < kBlk; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]));
+      } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(r0[k]));
-            mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(r1[k]));
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            mx[k & 7] = fmaxf(mx[k & 7], ((w0 >> k) & 1u) ? __uint_as_float(r0[k]) : -INFINITY);
-            mx[k & 7] = fmaxf(mx[k & 7], ((w1 >> k) & 1u) ? __uint_as_float(r1[k]) : -INFINITY);
-          }
-        }
+        for (int k = 0; k < kBlk; ++k)
+          mx[k & 7] = fmaxf(mx[k & 7], ((vis >> k) & 1ull) ? __uint_as_float(sr[k]) : -INFINITY);
       }
       const float bm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
       // m is the reference of O and l; it moves only when a block's max
       // exceeds it by more than 2^8 (or when it is still -inf), and then O
-      // (all earlier P V complete) and l are rescaled by 2^(m_old - m_new)
-      // (TMEM loads and stores are warp-wide: a warp rescales when any of its
-      // rows needs it, with factor 1 for the others)
+      // and l are rescaled by 2^(m_old - m_new).  (TMEM loads and stores are
+      // warp-wide: a warp rescales when any of its rows needs it, with
+      // factor 1 for the others.)
       const bool need = bm > m + kRescaleLog2;
       const bool resc = need && m != -INFINITY && j > 0;
       if (__ballot_sync(0xffffffffu, resc)) {
+        // O must be stable: every earlier P V complete
+        if (!(ok = wait_pv(j - 1))) break;
         const float alpha = resc ? ex2_approx(m - bm) : 1.f;
-        const int jp = j - 1;
-        bool w = true;
-        if (lane == 0)
-          w = mbar_wait(smem_u32(&sb.pv_full[jp & 1]), (uint32_t)(jp >> 1) & 1u, abort_flag);
-        w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-        if (!w) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32_issue(tmem + lane_addr + kColO + (uint32_t)(c * 32), r);
+          tmem_ld32_issue(o_addr + (uint32_t)(c * 32), r);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-          tmem_st32(tmem + lane_addr + kColO + (uint32_t)(c * 32), r);
+          tmem_st32(o_addr + (uint32_t)(c * 32), r);
         }
         tmem_wait_st();
         l *= alpha;
@@ -420,14 +448,12 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (need) m = bm;
       // pass 2: P = 2^(S * scale_log2 - m) as bf16 into the swizzled P tile
       const float neg_m = m == -INFINITY ? 0.f : -m;
-      unsigned char* prow = gbase + (sP - base) + x * kTileP + i * 128;
+      unsigned char* prow = prow0 + x * kTileP;  // P(j - 2) in this buffer is consumed
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBlk / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32_issue(sa + (uint32_t)(c * 32), r);
-        tmem_wait_ld();
-        const uint32_t w = (uint32_t)(vis[c >> 1] >> ((c & 1) * 32));
+        const uint32_t* r = sr + c * 32;
+        const uint32_t w = (uint32_t)(vis >> (c * 32));
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -440,11 +466,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           ls[k & 3] += e0 + e1;
           pk[k] = pack_bf16(e0, e1);
         }
-        // 32 keys = half of a 128-byte row of key-half c / 2: chunks 4 (c & 1) .. + 3
+        // 32 keys = half of the row's 128 bytes: chunks 4 c .. 4 c + 3
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int ch = (c & 1) * 4 + u;
-          *reinterpret_cast<uint4*>(prow + (c >> 1) * 16384 + ((ch ^ (i & 7)) << 4)) =
+          const int ch = c * 4 + u;
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (i & 7)) << 4)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
@@ -452,19 +478,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sb.s_empty[x]));
-        mbar_arrive(smem_u32(&sb.p_full[x]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&sb.p_full[x]));
     }
     // O is final once the last P V completes
-    if (ok && n_iter > 0) {
-      const int jl = n_iter - 1;
-      if (lane == 0)
-        ok = mbar_wait(smem_u32(&sb.pv_full[jl & 1]), (uint32_t)(jl >> 1) & 1u, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      tc_fence_after();
-    }
+    if (ok && n_iter > 0) ok = wait_pv(n_iter - 1);
     if (ok) {
       const int r = r_i, h = kvh * p.G + gi % p.G;
       const size_t row = ((size_t)b * p.R + r) * p.Hq + h;
@@ -474,7 +491,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         if (n_iter > 0) {
-          tmem_ld32_issue(tmem + lane_addr + kColO + (uint32_t)(c * 32), o);
+          tmem_ld32_issue(o_addr + (uint32_t)(c * 32), o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -512,7 +529,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   if (sb.abort_flag && threadIdx.x == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
@@ -613,18 +630,19 @@ __global__ void __launch_bounds__(256) tree_attn_f32_kernel(
 }
 
 struct Plan {
-  int nr, qtiles, splits;
+  int nr, qtiles, tpc, splits;
 };
 
 template <int D>
-constexpr size_t tc_smem() {
-  return 1024 + (size_t)128 * 128 * (D / 64) + 4 * (size_t)tc::kBlk * 128 * (D / 64) +
-         2 * (size_t)128 * tc::kBlk * 2;
+size_t tc_smem(int tpc) {
+  return 1024 + (size_t)tpc * 128 * 128 * (D / 64) +
+         2 * (size_t)tc::kv_stages<D>(tpc) * tc::kBlk * 128 * (D / 64) +
+         (size_t)tpc * 2 * 128 * tc::kBlk * 2;
 }
 
 // Query tiles of nr tree rows x G heads (nr * G <= 128 MMA rows) and the KV
 // split count.  Auto splits: the count minimising (waves of CTAs, one per SM)
-// x (128-key blocks per CTA + the tree block + 2 blocks' worth of set-up),
+// x (64-key blocks per CTA + the tree block + 5 blocks' worth of set-up),
 // plus a small charge per split for the (O, lse) partials and their merge.
 Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   Plan pl;
@@ -632,17 +650,23 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   pl.nr = 128 / G;
   pl.qtiles = (R + pl.nr - 1) / pl.nr;
   const int max_blocks = max(1, (max_pages * 16 + tc::kBlk - 1) / tc::kBlk);
+  // two query tiles share each K/V block when the prefix is long enough
+  // (>= 4096 keys) for the splits to keep every SM busy anyway
+  pl.tpc = (pl.qtiles >= 2 && max_blocks >= 64) ? 2 : 1;
+#ifdef EXP_TPC
+  pl.tpc = pl.qtiles >= 2 ? EXP_TPC : 1;
+#endif
   if (num_splits > 0) {
     pl.splits = min(num_splits, max_blocks);
   } else {
-    const long long base = (long long)pl.qtiles * B * Hkv;
+    const long long base = (long long)((pl.qtiles + pl.tpc - 1) / pl.tpc) * B * Hkv;
     const long long slots = max(1, sm_count());
     double best = 1e300;
     pl.splits = 1;
     for (int sp = 1; sp <= min(max_blocks, 256); ++sp) {
       const long long waves = (base * sp + slots - 1) / slots;
       const int bps = (max_blocks + sp - 1) / sp;
-      const double cost = (double)waves * (bps + 3) + (sp > 1 ? 0.1 * sp : 0.0);
+      const double cost = (double)waves * (bps + 6) * pl.tpc + (sp > 1 ? 0.1 * sp : 0.0);
       if (cost < best - 1e-9) {
         best = cost;
         pl.splits = sp;
@@ -722,6 +746,7 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   p.splits = pl.splits;
   p.nr = pl.nr;
   p.tr = (R + 15) / 16 * 16;
+  p.qtiles = pl.qtiles;
   p.scale_log2 = scale * kLog2e;
   if (pl.splits > 1) {
     if (!ws || ws_bytes < eagle_tree_attn_workspace_size(B, R, Hq, Hkv, D, max_pages, page_size,
@@ -742,15 +767,21 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
       !make_tmap_3d_bf16(&mkt, k_tree, D, Hkv, (uint64_t)B * R, hb, hb * Hkv, 64, 1, p.tr) ||
       !make_tmap_3d_bf16(&mvt, v_tree, D, Hkv, (uint64_t)B * R, hb, hb * Hkv, 64, 1, p.tr))
     return EAGLE_ERR_CUDA;
-  const dim3 grid(pl.qtiles, pl.splits, B * Hkv);
+  const dim3 grid((pl.qtiles + pl.tpc - 1) / pl.tpc, pl.splits, B * Hkv);
+  auto run = [&](auto kern, size_t sm, int threads) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    launch(kern, grid, threads, sm, s, mq, mk, mv, mkt, mvt, p);
+  };
   if (D == 128) {
-    constexpr size_t sm = tc_smem<128>();
-    cudaFuncSetAttribute(tree_attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    launch(tree_attn_tc_kernel<128>, grid, tc::kThreads, sm, s, mq, mk, mv, mkt, mvt, p);
+    if (pl.tpc == 2)
+      run(tree_attn_tc_kernel<128, 2>, tc_smem<128>(2), 320);
+    else
+      run(tree_attn_tc_kernel<128, 1>, tc_smem<128>(1), 192);
   } else {
-    constexpr size_t sm = tc_smem<64>();
-    cudaFuncSetAttribute(tree_attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    launch(tree_attn_tc_kernel<64>, grid, tc::kThreads, sm, s, mq, mk, mv, mkt, mvt, p);
+    if (pl.tpc == 2)
+      run(tree_attn_tc_kernel<64, 2>, tc_smem<64>(2), 320);
+    else
+      run(tree_attn_tc_kernel<64, 1>, tc_smem<64>(1), 192);
   }
   note_launch();
   if (pl.splits > 1) {
