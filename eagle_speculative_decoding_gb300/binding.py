@@ -26,6 +26,7 @@ _SIGS = {
     "eagle_status_string": (ctypes.c_char_p, [_I]),
     "eagle_read_status": (_I, [_P, _P, _P]),
     "eagle_launch_count": (_U64, []),
+    "eagle_selftest_wait_timeout": (_I, [ctypes.c_uint, _P, _P]),
     "eagle_fuse_proj_workspace_size": (_Z, [_I, _I, _I]),
     "eagle_fuse_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
@@ -98,6 +99,13 @@ def workspace(nbytes, device=None):
 
 def launch_count():
     return int(lib().eagle_launch_count())
+
+
+def eagle_selftest_wait_timeout(limit_us, status, stream=None):
+    """Bounded-wait self-test: expects status[0] = EAGLE_ERR_TIMEOUT and
+    status[1] = 1 once the stream has run it."""
+    _check("eagle_selftest_wait_timeout",
+           lib().eagle_selftest_wait_timeout(int(limit_us), _ptr(status), _stream(stream)))
 
 
 def read_status(status, stream=None):

@@ -85,9 +85,46 @@ bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+// Self-test of the bounded wait every kernel uses: thread 0 waits on an
+// mbarrier that nothing ever arrives on, with a limit of limit_ns, and must
+// give up with EAGLE_ERR_TIMEOUT; thread 32 waits on a second such barrier
+// with the ordinary 2 s limit and must end early, through the abort flag the
+// first waiter raises (status[1] = 1).
+__global__ void __launch_bounds__(64) wait_selftest_kernel(unsigned long long limit_ns,
+                                                           int32_t* status) {
+  __shared__ uint64_t never_a, never_b;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&never_a), 1);
+    mbar_init(smem_u32(&never_b), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(smem_u32(&never_a), 0, &abort_flag, limit_ns)) set_status(status, EAGLE_ERR_TIMEOUT);
+  } else if (threadIdx.x == 32) {
+    const unsigned long long t0 = globaltimer_ns();
+    const bool done = mbar_wait(smem_u32(&never_b), 0, &abort_flag);
+    if (!done && abort_flag && globaltimer_ns() - t0 < kWaitLimitNs / 2) status[1] = 1;
+  }
+  __syncthreads();
+}
+}  // namespace
+
 }  // namespace eagle
 
 extern "C" {
+
+int eagle_selftest_wait_timeout(unsigned int limit_us, int32_t* dev_status, void* stream) {
+  if (!dev_status || limit_us == 0 || limit_us > 1000000u) return EAGLE_ERR_INVALID_ARG;
+  eagle::launch(eagle::wait_selftest_kernel, 1, 64, 0, static_cast<cudaStream_t>(stream),
+                (unsigned long long)limit_us * 1000ull, dev_status);
+  eagle::note_launch();
+  return eagle::last_launch_status();
+}
+
 
 const char* eagle_status_string(int status) {
   switch (status) {

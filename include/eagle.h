@@ -82,6 +82,16 @@ int eagle_read_status(const int32_t* dev_status, void* stream, int32_t* host_sta
  * benchmarks; incremented on every launch, never reset). */
 uint64_t eagle_launch_count(void);
 
+/* Self-test of the bounded waits (no counterpart in the pages): launches one
+ * CTA whose thread 0 waits on an mbarrier that nothing ever completes, with a
+ * limit of `limit_us` microseconds (1 .. 1,000,000), through the same bounded
+ * wait every kernel of the library uses.  Expected device result:
+ * dev_status[0] = EAGLE_ERR_TIMEOUT (the wait gave up) and dev_status[1] = 1
+ * (a second waiter of the CTA, on the ordinary 2 s limit, ended early through
+ * the abort flag the first one raised).  dev_status: [2] int32, zeroed by the
+ * caller.  The device stays usable; nothing else is touched. */
+int eagle_selftest_wait_timeout(unsigned int limit_us, int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------
  * eagle_fuse_proj -- EAGLE-3 multi-layer feature fusion.
  *   g[i, o] = sum_c W[o, c] h_low[i, c] + W[o, d+c] h_mid[i, c]

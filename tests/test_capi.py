@@ -52,12 +52,16 @@ def test_host_validation_without_gpu(L):
     assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, p, 1.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 2
     assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 0, 0, 0, N, 65, p, p, p, N, 0, N, N) == 2
     assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 0, 0, 0, N, 2, p, p, p, N, 0, N, N) == 3
-    # lm head: k > 32 unsupported, k > V invalid, V not a multiple of 128
+    # lm head: k > 32 unsupported, k > V invalid, V not a multiple of 16
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 33, 1.0, p, p, N, N, 1, N, 0, N, N) == 2
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 128, 200, 1.0, p, p, N, N, 1, N, 0, N, N) == 1
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 100, 1, 1.0, p, p, N, N, 1, N, 0, N, N) == 2
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 1, 0.0, p, p, N, N, 1, N, 0, N, N) == 1
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 1, 1.0, p, p, N, N, 1, N, 0, N, N) == 3
+    # bounded-wait self-test: the limit must be 1 .. 10^6 microseconds
+    assert L.eagle_selftest_wait_timeout(0, p, N) == 1
+    assert L.eagle_selftest_wait_timeout(1000001, p, N) == 1
+    assert L.eagle_selftest_wait_timeout(10, N, N) == 1
     # fuse_proj: d not a multiple of 128
     assert L.eagle_fuse_proj(p, p, p, p, N, p, 4, 100, 1, N, 0, N, N) == 2
     assert L.eagle_fuse_proj(p, p, p, p, N, p, 4, 128, 1, N, 0, N, N) == 3
