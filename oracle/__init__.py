@@ -38,6 +38,8 @@ from .eagle_oracle import (  # noqa: F401
     tree_expand_init,
     tree_expand_step,
     tree_verify,
+    tree_verify_stats,
+    verify_stats,
 )
 from .philox import (  # noqa: F401
     accept_uniforms, bits_to_uniform, philox4x32_10, race_uniforms, race_uniforms_batch)

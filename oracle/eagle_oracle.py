@@ -15,7 +15,7 @@ import math
 
 import numpy as np
 
-from .philox import accept_uniforms, race_uniforms
+from .philox import accept_uniforms, race_uniforms, race_uniforms_batch
 
 # ---------------------------------------------------------------------------
 # a1: EAGLE-3 multi-layer feature fusion
@@ -488,6 +488,136 @@ def tree_verify(parent_row, token, temperature, max_depth, n_rows=None,
                     top2 = np.sort(keyv)[-2:]
                     margins.append(("race", b, float(top2[1] - top2[0])))
                 toks.append(bonus)
+                break
+            if len(path) > max_depth:
+                raise ValueError("tree deeper than max_depth")
+            path.append(accepted)
+            toks.append(int(token[b, accepted]))
+            cur = accepted
+        accept_len[b] = len(path) - 1
+        path_rows[b, :len(path)] = path
+        out_tokens[b, :len(toks)] = toks
+    return dict(accept_len=accept_len, path_rows=path_rows, out_tokens=out_tokens,
+                margins=margins)
+
+
+# ---------------------------------------------------------------------------
+# K8 (follow-on): stochastic-verification statistics from the verification
+# LM head, so that verification never needs the [B, R, V] target logits
+# ---------------------------------------------------------------------------
+
+
+def verify_stats(x, w_lm, parent_row, token, temperature, race_k, seed=0, offset=0, bias=None,
+                 n_rows=None, race_u=None):
+    """Everything deterministic-proposal stochastic verification reads from
+    the target logits z = W_U a (+ b) of the verify rows, computed from the
+    verification LM head's inputs instead of from stored logits.
+
+    Rows are [B * R] (request-major).  The walk of [E1] "Verification Phase:
+    Multi-Round Speculative Sampling on Trees" (deterministic point-mass
+    proposals) reads, for the current row r: p(t) = exp(z_r[t]/T) / sum_v
+    exp(z_r[v]/T) for each child token t, and at the stop row the
+    exponential race over the ids not rejected there.  So it needs
+      row_max[r] = max_v z_r/T, row_sumexp[r] = sum_v exp(z_r/T - row_max[r]);
+      child_logit[c] = z[parent(c)][token(c)] for each row c >= 1 (0 for the
+        root and for rows past n_rows);
+      the race candidates of every row: the race_k ids of largest key
+        z_r[y]/T - log(-log u_{b,y}) (ties to the lower id), sorted, with their
+        keys.  The race's renormalisation constant is common to all allowed
+        ids, so the stop-row winner is the first candidate not rejected there;
+        race_k must exceed the number of children of any row.
+    Uniforms: oracle.philox race uniforms per (request, id), or race_u [B, V].
+    Returns dict(row_max [B*R], row_sumexp [B*R], child_logit [B*R],
+    race_ids [B*R, race_k] int64, race_keys [B*R, race_k], z [B*R, V]).
+    """
+    parent_row = np.asarray(parent_row)
+    token = np.asarray(token)
+    B, R = parent_row.shape
+    if not temperature > 0:
+        raise ValueError("temperature must be > 0")
+    x = np.asarray(x, np.float64)
+    w = np.asarray(w_lm, np.float64)
+    if x.shape[0] != B * R:
+        raise ValueError("x must hold B * R rows")
+    V = w.shape[0]
+    if not 1 <= race_k <= V:
+        raise ValueError("race_k must be in 1..V")
+    z = x @ w.T
+    if bias is not None:
+        z = z + np.asarray(bias, np.float64)[None, :]
+    y = z / temperature
+    row_max = y.max(axis=1)
+    row_sumexp = np.exp(y - row_max[:, None]).sum(axis=1)
+    ur = np.asarray(race_u, np.float64) if race_u is not None else race_uniforms_batch(seed, offset, B, V)
+    gumbel = -np.log(-np.log(ur))  # [B, V]
+    child_logit = np.zeros(B * R)
+    race_ids = np.zeros((B * R, race_k), np.int64)
+    race_keys = np.zeros((B * R, race_k))
+    vid = np.arange(V)
+    for b in range(B):
+        n = R if n_rows is None else int(n_rows[b])
+        for c in range(1, n):
+            child_logit[b * R + c] = z[b * R + int(parent_row[b, c]), int(token[b, c])]
+        for r in range(R):
+            key = y[b * R + r] + gumbel[b]
+            order = np.lexsort((vid, -key))[:race_k]
+            race_ids[b * R + r] = order
+            race_keys[b * R + r] = key[order]
+    return dict(row_max=row_max, row_sumexp=row_sumexp, child_logit=child_logit,
+                race_ids=race_ids, race_keys=race_keys, z=z)
+
+
+def tree_verify_stats(parent_row, token, temperature, max_depth, row_max, row_sumexp,
+                      child_logit, race_ids, n_rows=None, seed=0, offset=0, accept_u=None):
+    """Deterministic-proposal stochastic verification from verify_stats
+    outputs ([E1] "Verification Phase", the deterministic reading of
+    tree_verify): children of the current row are tried in row order; child c
+    with token t is accepted when u_c < p(t) / (1 - sum of p over the
+    distinct tokens already rejected at this row), p(t) = exp(child_logit[c]/T
+    - row_max) / row_sumexp; a repeated token has p = 0.  At the stop row the
+    bonus token is the first race candidate not rejected there.
+    Same outputs as tree_verify (accept_len, path_rows, out_tokens, margins).
+    """
+    parent_row = np.asarray(parent_row)
+    token = np.asarray(token)
+    B, R = parent_row.shape
+    if not temperature > 0:
+        raise ValueError("temperature must be > 0")
+    if accept_u is None:
+        accept_u = accept_uniforms(seed, offset, B, R)
+    accept_len = np.zeros(B, np.int64)
+    path_rows = np.full((B, max_depth + 1), -1, np.int64)
+    out_tokens = np.full((B, max_depth + 1), -1, np.int64)
+    margins = []
+    for b in range(B):
+        n = R if n_rows is None else int(n_rows[b])
+        if not 1 <= n <= R or parent_row[b, 0] != -1:
+            raise ValueError("row 0 must be the root and 1 <= n_rows <= R")
+        for i in range(1, n):
+            if not 0 <= parent_row[b, i] < i:
+                raise ValueError("parent_row must be topological")
+        cur, path, toks = 0, [0], []
+        while True:
+            children = [c for c in range(cur + 1, n) if parent_row[b, c] == cur]
+            rm, rs = float(row_max[b * R + cur]), float(row_sumexp[b * R + cur])
+            rejected, rem, accepted = [], 1.0, None
+            for c in children:
+                t = int(token[b, c])
+                pt = 0.0 if t in rejected else math.exp(child_logit[b * R + c] / temperature - rm) / rs
+                ratio = pt / rem
+                u = float(accept_u[b, c])
+                margins.append(("accept", b, abs(u - ratio)))
+                if u < ratio:
+                    accepted = c
+                    break
+                if t not in rejected and rem - pt > 0:
+                    rem -= pt
+                    rejected.append(t)
+            if accepted is None:
+                cands = [int(v) for v in race_ids[b * R + cur] if int(v) not in rejected]
+                if not cands:
+                    raise ValueError("race_k too small: every candidate was rejected")
+                toks.append(cands[0])
                 break
             if len(path) > max_depth:
                 raise ValueError("tree deeper than max_depth")
