@@ -508,7 +508,7 @@ def tree_verify(parent_row, token, temperature, max_depth, n_rows=None,
 
 
 def verify_stats(x, w_lm, parent_row, token, temperature, race_k, seed=0, offset=0, bias=None,
-                 n_rows=None, race_u=None):
+                 n_rows=None, race_u=None, rows=None):
     """Everything deterministic-proposal stochastic verification reads from
     the target logits z = W_U a (+ b) of the verify rows, computed from the
     verification LM head's inputs instead of from stored logits.
@@ -527,8 +527,9 @@ def verify_stats(x, w_lm, parent_row, token, temperature, race_k, seed=0, offset
         ids, so the stop-row winner is the first candidate not rejected there;
         race_k must exceed the number of children of any row.
     Uniforms: oracle.philox race uniforms per (request, id), or race_u [B, V].
+    rows: optional subset of row indices to compute (the others are NaN / -1).
     Returns dict(row_max [B*R], row_sumexp [B*R], child_logit [B*R],
-    race_ids [B*R, race_k] int64, race_keys [B*R, race_k], z [B*R, V]).
+    race_ids [B*R, race_k] int64, race_keys [B*R, race_k]).
     """
     parent_row = np.asarray(parent_row)
     token = np.asarray(token)
@@ -542,29 +543,39 @@ def verify_stats(x, w_lm, parent_row, token, temperature, race_k, seed=0, offset
     V = w.shape[0]
     if not 1 <= race_k <= V:
         raise ValueError("race_k must be in 1..V")
-    z = x @ w.T
-    if bias is not None:
-        z = z + np.asarray(bias, np.float64)[None, :]
-    y = z / temperature
-    row_max = y.max(axis=1)
-    row_sumexp = np.exp(y - row_max[:, None]).sum(axis=1)
-    ur = np.asarray(race_u, np.float64) if race_u is not None else race_uniforms_batch(seed, offset, B, V)
-    gumbel = -np.log(-np.log(ur))  # [B, V]
-    child_logit = np.zeros(B * R)
-    race_ids = np.zeros((B * R, race_k), np.int64)
-    race_keys = np.zeros((B * R, race_k))
+    bvec = None if bias is None else np.asarray(bias, np.float64)
+    todo = range(B * R) if rows is None else sorted(set(int(r) for r in rows))
+    need_b = sorted(set(r // R for r in todo))
+    if race_u is not None:
+        ur = {b: np.asarray(race_u, np.float64)[b] for b in need_b}
+    else:
+        ur = {b: race_uniforms(seed, offset, b, V) for b in need_b}
+    row_max = np.full(B * R, np.nan)
+    row_sumexp = np.full(B * R, np.nan)
+    child_logit = np.full(B * R, np.nan)
+    race_ids = np.full((B * R, race_k), -1, np.int64)
+    race_keys = np.full((B * R, race_k), np.nan)
     vid = np.arange(V)
-    for b in range(B):
+    for row in todo:
+        b, c = divmod(row, R)
+        z = w @ x[row]
+        if bvec is not None:
+            z = z + bvec
+        y = z / temperature
+        row_max[row] = y.max()
+        row_sumexp[row] = np.exp(y - row_max[row]).sum()
+        key = y - np.log(-np.log(ur[b]))
+        order = np.lexsort((vid, -key))[:race_k]
+        race_ids[row] = order
+        race_keys[row] = key[order]
         n = R if n_rows is None else int(n_rows[b])
-        for c in range(1, n):
-            child_logit[b * R + c] = z[b * R + int(parent_row[b, c]), int(token[b, c])]
-        for r in range(R):
-            key = y[b * R + r] + gumbel[b]
-            order = np.lexsort((vid, -key))[:race_k]
-            race_ids[b * R + r] = order
-            race_keys[b * R + r] = key[order]
+        if 1 <= c < n:
+            p, t = int(parent_row[b, c]), int(token[b, c])
+            child_logit[row] = float(np.dot(x[b * R + p], w[t])) + (0.0 if bvec is None else bvec[t])
+        else:
+            child_logit[row] = 0.0
     return dict(row_max=row_max, row_sumexp=row_sumexp, child_logit=child_logit,
-                race_ids=race_ids, race_keys=race_keys, z=z)
+                race_ids=race_ids, race_keys=race_keys)
 
 
 def tree_verify_stats(parent_row, token, temperature, max_depth, row_max, row_sumexp,
