@@ -77,8 +77,6 @@ class Workload:
         host["v_tree"] = synth.normal((B, R, self.Hkv, self.D), 1.0, self.dt, gc)
         host["h"] = [synth.normal((B * R, d), 1.0, self.dt, gc) for _ in range(3)]
         host["x_v"] = synth.normal((B * R, d), 1.0, self.dt, gc)
-        if self.T > 0:
-            host["logits"] = synth.target_logits((B, R, V), gc)
         self.host = {k: ([t.pin_memory() for t in v] if isinstance(v, list) else v.pin_memory())
                      for k, v in host.items()}
         self.dev_in = {k: ([t.to(device) for t in v] if isinstance(v, list) else v.to(device))
@@ -97,12 +95,20 @@ class Workload:
         self.g = torch.empty((B * R, d), dtype=self.dt, device=device)
         self.amax = z(B * R, 1)
         self.amax_lp = z(B * R, 1, t=torch.float32)
+        # stochastic verification reads statistics of the verification LM head
+        # (race candidates, row log-sum-exp, child logits), never [B, R, V] logits
+        self.race_k = self.k + 1  # > children of any node of a top-k tree
+        self.race_ids = z(B * R, self.race_k)
+        self.race_keys = z(B * R, self.race_k, t=torch.float32)
+        self.row_max = z(B * R, t=torch.float32)
+        self.row_sumexp = z(B * R, t=torch.float32)
+        self.child_logit = z(B * R, t=torch.float32)
         self.acc, self.path, self.out_tok = z(B), z(B, self.depth + 1), z(B, self.depth + 1)
         self.status = z(1)
         # workspaces (caller-owned scratch)
         dt_code = eb.EAGLE_BF16 if self.dt == torch.bfloat16 else eb.EAGLE_FP32
         lm_ws = max(eb.eagle_lmhead_topk_workspace_size(B * p, d, V, self.k, dt_code) for p in self.P)
-        lm_ws = max(lm_ws, eb.eagle_lmhead_topk_workspace_size(B * R, d, V, 1, dt_code))
+        lm_ws = max(lm_ws, eb.eagle_lmhead_topk_workspace_size(B * R, d, V, self.race_k, dt_code))
         self.ws_lm = eb.workspace(lm_ws, device)
         self.ws_fp = eb.workspace(eb.eagle_fuse_proj_workspace_size(B * R, d, dt_code), device)
         self.ws_attn = eb.workspace(eb.eagle_tree_attn_workspace_size(
@@ -115,15 +121,18 @@ class Workload:
         receives (start, end) CUDA events around each LM-head call."""
         t, f, x = self.tree, self.flat, self.dev_in
 
-        def lm(xr, k, ids, lps):
+        def timed(call, M, k):
             if lm_events is not None:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
-            eb.eagle_lmhead_topk(xr, self.w_lm, k, ids, lps, temperature=1.0, ws=self.ws_lm,
-                                 status=self.status)
+            call()
             if lm_events is not None:
                 e1.record()
-                lm_events.append((e0, e1, xr.shape[0], k))
+                lm_events.append((e0, e1, M, k))
+
+        def lm(xr, k, ids, lps):
+            timed(lambda: eb.eagle_lmhead_topk(xr, self.w_lm, k, ids, lps, temperature=1.0,
+                                               ws=self.ws_lm, status=self.status), xr.shape[0], k)
 
         for s in range(self.depth):
             ids, lps = self.cand[s]
@@ -140,15 +149,21 @@ class Workload:
                            ws=self.ws_attn, status=self.status)
         eb.eagle_fuse_proj(x["h"][0], x["h"][1], x["h"][2], self.w_proj, self.g, ws=self.ws_fp,
                            status=self.status)
-        lm(x["x_v"], 1, self.amax, self.amax_lp)
         if self.T == 0:
+            lm(x["x_v"], 1, self.amax, self.amax_lp)
             eb.eagle_tree_verify(f["parent_row"], f["token"], 0.0, self.depth, self.acc, self.path,
                                  self.out_tok, n_rows=f["n_rows"], target_argmax=self.amax.view(self.B, self.R),
                                  V=self.V, ws=self.ws_ver, status=self.status)
         else:
-            eb.eagle_tree_verify(f["parent_row"], f["token"], self.T, self.depth, self.acc, self.path,
-                                 self.out_tok, n_rows=f["n_rows"], target_logits=x["logits"],
-                                 seed=1234, ws=self.ws_ver, status=self.status)
+            timed(lambda: eb.eagle_lmhead_verify_stats(
+                x["x_v"], self.w_lm, f["parent_row"], f["token"], self.T, self.race_k,
+                self.race_ids, self.race_keys, self.row_max, self.row_sumexp, self.child_logit,
+                n_rows=f["n_rows"], seed=1234, ws=self.ws_lm, status=self.status),
+                self.B * self.R, self.race_k)
+            eb.eagle_tree_verify_stats(f["parent_row"], f["token"], self.T, self.depth, self.row_max,
+                                       self.row_sumexp, self.child_logit, self.race_ids, self.acc,
+                                       self.path, self.out_tok, self.V, n_rows=f["n_rows"],
+                                       seed=1234, status=self.status)
 
     def h2d(self):
         """Copy this step's inputs from pinned host memory; returns bytes."""
@@ -410,7 +425,6 @@ class OracleStep:
         self.hs = [f64(synth.normal((B * R, d), 1.0, dt, gen)) for _ in range(3)]
         self.xv = f64(synth.normal((B * R, d), 1.0, dt, gen))
         self.T = c["temps"][0]
-        self.logits = synth.target_logits((B, R, V), gen).numpy() if self.T > 0 else None
         self.nodes = B * N
 
     def run(self):
@@ -431,14 +445,17 @@ class OracleStep:
         mask = np.stack([f["mask"] for f in flats])
         oracle.tree_attn(self.q, self.kt, self.vt, self.kc, self.vc, self.table, self.ctx.numpy(), mask)
         oracle.fuse_proj(*self.hs, self.w_proj)
-        am = oracle.lmhead_topk(self.xv, self.w_lm, 1)["ids"].reshape(B, R)
         parent = np.stack([f["parent_row"] for f in flats])
         tok = np.stack([f["token"] for f in flats])
         nr = [f["n_rows"] for f in flats]
         if self.T == 0:
+            am = oracle.lmhead_topk(self.xv, self.w_lm, 1)["ids"].reshape(B, R)
             oracle.tree_verify(parent, tok, 0.0, depth, n_rows=nr, target_argmax=am)
         else:
-            oracle.tree_verify(parent, tok, self.T, depth, n_rows=nr, target_logits=self.logits, seed=1234)
+            st = oracle.verify_stats(self.xv, self.w_lm, parent, tok, self.T, k + 1, seed=1234,
+                                     n_rows=nr)
+            oracle.tree_verify_stats(parent, tok, self.T, depth, st["row_max"], st["row_sumexp"],
+                                     st["child_logit"], st["race_ids"], n_rows=nr, seed=1234)
         return time.perf_counter() - t0
 
 

@@ -42,6 +42,10 @@ _SIGS = {
                                _P, _P, _P, _Z, _P, _P]),
     "eagle_tree_verify_noalloc": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _F, _I, _U64, _U64, _P,
                                        _I, _P, _P, _P, _P, _P]),
+    "eagle_lmhead_verify_stats": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _U64, _U64, _I,
+                                       _P, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
+    "eagle_tree_verify_stats": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _F, _U64, _U64,
+                                     _P, _I, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -233,5 +237,37 @@ def eagle_tree_verify_noalloc(parent_row, token, temperature, max_depth, accept_
     _check("eagle_tree_verify_noalloc", lib().eagle_tree_verify_noalloc(
         B, R, V, _ptr(parent_row), _ptr(token), _ptr(n_rows), _ptr(target_logits),
         _ptr(target_argmax), None, float(temperature), proposal_mode, int(seed), int(offset),
+        _ptr(uniforms_override), max_depth, _ptr(accept_len), _ptr(path_rows), _ptr(out_tokens),
+        _ptr(status), _stream(stream)))
+
+
+# ------------------------------------------------------------------ K8
+def eagle_lmhead_verify_stats(x, w_lm, parent_row, token, temperature, race_k, race_ids,
+                              race_keys, row_max, row_sumexp, child_logit, n_rows=None, bias=None,
+                              seed=0, offset=0, ws=None, status=None, stream=None):
+    """Verification statistics from the LM head (rows of x: request-major
+    B*R); see include/eagle.h."""
+    B, R = parent_row.shape
+    M, d = x.shape
+    V = w_lm.shape[0]
+    dt = _dtype(x)
+    if ws is None:
+        ws = workspace(eagle_lmhead_topk_workspace_size(M, d, V, race_k, dt), x.device)
+    _check("eagle_lmhead_verify_stats", lib().eagle_lmhead_verify_stats(
+        _ptr(x), _ptr(w_lm), _ptr(bias), B, R, d, V, _ptr(parent_row), _ptr(token), _ptr(n_rows),
+        float(temperature), int(seed), int(offset), race_k, _ptr(race_ids), _ptr(race_keys),
+        _ptr(row_max), _ptr(row_sumexp), _ptr(child_logit), dt, _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+
+
+def eagle_tree_verify_stats(parent_row, token, temperature, max_depth, row_max, row_sumexp,
+                            child_logit, race_ids, accept_len, path_rows, out_tokens, V,
+                            n_rows=None, seed=0, offset=0, uniforms_override=None, status=None,
+                            stream=None):
+    B, R = parent_row.shape
+    race_k = race_ids.shape[-1]
+    _check("eagle_tree_verify_stats", lib().eagle_tree_verify_stats(
+        B, R, V, _ptr(parent_row), _ptr(token), _ptr(n_rows), _ptr(row_max), _ptr(row_sumexp),
+        _ptr(child_logit), _ptr(race_ids), race_k, float(temperature), int(seed), int(offset),
         _ptr(uniforms_override), max_depth, _ptr(accept_len), _ptr(path_rows), _ptr(out_tokens),
         _ptr(status), _stream(stream)))

@@ -231,9 +231,14 @@ struct LmParams {
   int tn;  // vocabulary rows per tile (MMA N, multiple of 16, <= 128)
   int xr;  // activation rows loaded per stage (group rows rounded up to 16)
   float inv_t;
+  // exponential-race mode (verification statistics): the top-K is taken over
+  // key = z/T - log(-log u_{b,y}) with u from Philox4x32-10 (key race_k0/1,
+  // counter (y >> 2, b, race_c2, race_c3), word y & 3), b = row / R
+  int race, R;
+  uint32_t race_k0, race_k1, race_c2, race_c3;
   const float* bias;
   int32_t* topk_ids;
-  float* topk_lp;
+  float* topk_lp;     // log-probs, or the race keys in race mode
   float* row_max;
   float* row_sumexp;
   float2* part_ms;   // [M][cpg]       (max of z/T, sum exp) per row and CTA of its group
@@ -275,7 +280,7 @@ struct LmSched {
 // Running state of one activation row, held in registers by the thread that
 // owns the row: online max / sum-exp of z/T and the sorted top-K list (z
 // descending, id ascending) of the ids seen so far.  KMAX >= K is a
-// compile-time bound so the list lives in registers; entries past K are
+// compile-time bound so the list lives in registers.
 // The real list occupies the last K slots; the first KMAX - K slots hold +inf
 // sentinels that nothing displaces, so the K-th best is always slot KMAX - 1
 // (a static register index).  Insertion is a predicated compare-and-swap
@@ -283,7 +288,7 @@ struct LmSched {
 template <int KMAX>
 struct RowTopK {
   float m, s;          // running max of z/T and sum of exp(z/T - m)
-  float av[KMAX];      // sorted top-K values (z)
+  float av[KMAX];      // sorted top-K values (z, or the race keys)
   int ai[KMAX];        // ... their ids
   float tv;            // K-th best so far (-inf while fewer than K)
   int ti;
@@ -305,12 +310,56 @@ __device__ __forceinline__ void row_init(RowTopK<KMAX>& r, int K) {
   r.nan_seen = false;
 }
 
+// -log(-log u) of one Philox word (u = (2 (x >> 9) + 1) 2^-24 in (0, 1)).
+__device__ __forceinline__ float gumbel_of(uint32_t x) { return -logf(-logf(bits_to_uniform(x))); }
+
+// Race noise g[j] = -log(-log u_{b,id0+j}) for this lane's request b and the
+// 16 ids id0.. (id0 a multiple of 16).  Rows of a warp are consecutive, so
+// they span few requests: lane L draws the four words of request
+// (first request + L / 4), ids id0 + 4 (L % 4) .., and the lanes gather their
+// own request's 16 values by shuffles (each Philox word drawn once per warp).
+// Must be called by all 32 lanes together.
+__device__ __forceinline__ void race_gumbel16(const LmParams& p, int grow, int id0, float (&g)[16],
+                                              int lane) {
+  const int b = min(grow, p.M - 1) / p.R;
+  const int b0 = __shfl_sync(0xffffffffu, b, 0);
+  const int nreq = __shfl_sync(0xffffffffu, b, 31) - b0 + 1;
+  if (nreq * 4 <= 32) {
+    float gw[4] = {0.f, 0.f, 0.f, 0.f};
+    if (lane < nreq * 4) {
+      const uint4 w = philox4x32_10(
+          make_uint4((uint32_t)(id0 >> 2) + (uint32_t)(lane & 3), (uint32_t)(b0 + (lane >> 2)),
+                     p.race_c2, p.race_c3),
+          p.race_k0, p.race_k1);
+      gw[0] = gumbel_of(w.x);
+      gw[1] = gumbel_of(w.y);
+      gw[2] = gumbel_of(w.z);
+      gw[3] = gumbel_of(w.w);
+    }
+    const int src = (b - b0) * 4;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) g[j] = __shfl_sync(0xffffffffu, gw[j & 3], src + (j >> 2));
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = philox4x32_10(
+          make_uint4((uint32_t)(id0 >> 2) + (uint32_t)q, (uint32_t)b, p.race_c2, p.race_c3),
+          p.race_k0, p.race_k1);
+      g[4 * q] = gumbel_of(w.x);
+      g[4 * q + 1] = gumbel_of(w.y);
+      g[4 * q + 2] = gumbel_of(w.z);
+      g[4 * q + 3] = gumbel_of(w.w);
+    }
+  }
+}
+
 // Fold 16 consecutive vocabulary ids id0.. (values v, the first `valid` of
-// them real; valid <= 0 for a lane without a row) into the row.  Must be
-// called by all 32 lanes of the warp together.
-template <int KMAX>
-__device__ __forceinline__ void row_chunk(RowTopK<KMAX>& r, const float (&v)[16], int id0, int valid,
-                                          float inv_t, int K) {
+// them real; valid <= 0 for a lane without a row) into the row: log-sum-exp
+// of z/T always; top-K of z, or with RACE of z/T + g (g from race_gumbel16).
+// Must be called by all 32 lanes of the warp together.
+template <int KMAX, bool RACE>
+__device__ __forceinline__ void row_chunk(RowTopK<KMAX>& r, float (&v)[16], const float (&g)[16],
+                                          int id0, int valid, float inv_t, int K) {
   float y[16];
   float cm = -INFINITY;
 #pragma unroll
@@ -326,6 +375,10 @@ __device__ __forceinline__ void row_chunk(RowTopK<KMAX>& r, const float (&v)[16]
     for (int j = 0; j < 16; ++j) acc += exp2f((y[j] - nm) * kLog2e);
     r.s = r.s * exp2f((r.m - nm) * kLog2e) + acc;
     r.m = nm;
+  }
+  if (RACE) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = y[j] + g[j];  // the race key replaces z below
   }
   // candidates: values that beat the current K-th best
   unsigned cmask = 0;
@@ -478,7 +531,7 @@ __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmPar
     }
     if (lane == 0) {
       p.topk_ids[ob + rnd] = bi == 0x7fffffff ? -1 : bi;
-      p.topk_lp[ob + rnd] = bi == 0x7fffffff ? -INFINITY : bv * p.inv_t - lse;
+      p.topk_lp[ob + rnd] = bi == 0x7fffffff ? -INFINITY : (p.race ? bv : bv * p.inv_t - lse);
     }
     if (lane == owner && bs >= 0) {
 #pragma unroll
@@ -573,7 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] += p.bias[min(v0 + c16 * 16 + j, p.V - 1)];
         }
-        row_chunk(r, v, v0 + c16 * 16, valid ? vend - c16 * 16 : 0, p.inv_t, K);
+        const int id0 = v0 + c16 * 16, nv = valid ? vend - c16 * 16 : 0;
+        float gk[16];
+        if (p.race) {
+          race_gumbel16(p, m0 + e, id0, gk, lane);
+          row_chunk<KMAX, true>(r, v, gk, id0, nv, p.inv_t, K);
+        } else {
+          row_chunk<KMAX, false>(r, v, gk, id0, nv, p.inv_t, K);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -634,7 +694,13 @@ __global__ void __launch_bounds__(kEpiThreads)
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[j] += p.bias[min(vb + j, p.V - 1)];
       }
-      row_chunk(r, acc, vb, e < nrow ? p.V - vb : 0, p.inv_t, K);
+      float gk[16];
+      if (p.race) {
+        race_gumbel16(p, m0 + e, vb, gk, e & 31);
+        row_chunk<KMAX, true>(r, acc, gk, vb, e < nrow ? p.V - vb : 0, p.inv_t, K);
+      } else {
+        row_chunk<KMAX, false>(r, acc, gk, vb, e < nrow ? p.V - vb : 0, p.inv_t, K);
+      }
     }
   }
   if (r.nan_seen) set_status(p.status, EAGLE_ERR_NONFINITE);
@@ -895,10 +961,19 @@ extern "C" size_t eagle_lmhead_topk_workspace_size(int M, int d, int V, int k, i
   return round_up(n * 8, 256) + 2 * round_up(n * k * 4, 256) + round_up(n * 4, 256) + 1024;
 }
 
-extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M, int d,
-                                 int V, int k, float temperature, int32_t* topk_ids,
-                                 float* topk_logprobs, float* row_max, float* row_sumexp, int dtype,
-                                 void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+namespace eagle {
+namespace {
+struct RaceCfg {
+  int R;
+  uint64_t seed, offset;
+};
+
+// The LM head proper: GEMM + per-CTA top-K / log-sum-exp partials, then the
+// merge.  race != nullptr selects the exponential-race keys.
+int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d, int V, int k,
+               float temperature, int32_t* topk_ids, float* topk_logprobs, float* row_max,
+               float* row_sumexp, int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
+               void* stream, const RaceCfg* race) {
   if (!x || !w_lm || !topk_ids || !topk_logprobs) return EAGLE_ERR_INVALID_ARG;
   if (M <= 0 || d <= 0 || V <= 0 || k <= 0 || !(temperature > 0.f) || isinf(temperature))
     return EAGLE_ERR_INVALID_ARG;
@@ -950,6 +1025,12 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
   p.stages = stages;
   p.xr = xr;
   p.inv_t = 1.f / temperature;
+  p.race = race ? 1 : 0;
+  p.R = race ? race->R : 1;
+  p.race_k0 = race ? (uint32_t)race->seed : 0u;
+  p.race_k1 = race ? (uint32_t)(race->seed >> 32) : 0u;
+  p.race_c2 = race ? 2u * (uint32_t)(race->offset >> 32) + 1u : 0u;
+  p.race_c3 = race ? (uint32_t)race->offset : 0u;
   p.bias = bias;
   p.topk_ids = topk_ids;
   p.topk_lp = topk_logprobs;
@@ -982,6 +1063,96 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
   if (msmem > 48 * 1024)
     cudaFuncSetAttribute(lmhead_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
   launch(lmhead_merge_kernel, M, kMergeThreads, msmem, s, p);
+  note_launch();
+  return last_launch_status();
+}
+
+// Target logit of each child's token at its parent row: one warp per tree
+// row c of request b, z = x[b R + parent(c)] . W_U[token(c)] (+ bias), fp32
+// accumulation of the exact products; 0 for the root and rows past n_rows.
+template <typename T>
+__global__ void __launch_bounds__(256) child_logit_kernel(
+    const T* __restrict__ x, const T* __restrict__ w, const float* __restrict__ bias,
+    const int32_t* __restrict__ parent_row, const int32_t* __restrict__ token,
+    const int32_t* __restrict__ n_rows, int B, int R, int d, int V, float* __restrict__ out,
+    int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)B * R) return;
+  const int b = (int)(gw / R), c = (int)(gw % R);
+  const int n = n_rows ? n_rows[b] : R;
+  float acc = 0.f;
+  bool ok = c > 0 && c < n && n <= R;
+  int pr = 0, t = 0;
+  if (ok) {
+    pr = parent_row[gw];
+    t = token[gw];
+    ok = pr >= 0 && pr < c && t >= 0 && t < V;
+    if (!ok && lane == 0) set_status(status, EAGLE_ERR_BAD_TREE);
+  }
+  if (ok) {
+    const T* xr = x + ((size_t)b * R + pr) * d;
+    const T* wr = w + (size_t)t * d;
+    if (sizeof(T) == 2) {
+      for (int c8 = lane; c8 < d / 8; c8 += 32) {
+        const uint4 xa = *reinterpret_cast<const uint4*>(xr + c8 * 8);
+        const uint4 wa = *reinterpret_cast<const uint4*>(wr + c8 * 8);
+        const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xa);
+        const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&wa);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 xf = __bfloat1622float2(xh[u]), wf = __bfloat1622float2(wh[u]);
+          acc = fmaf(xf.x, wf.x, acc);
+          acc = fmaf(xf.y, wf.y, acc);
+        }
+      }
+    } else {
+      for (int c1 = lane; c1 < d; c1 += 32) acc = fmaf((float)xr[c1], (float)wr[c1], acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) out[gw] = ok ? acc + (bias ? bias[t] : 0.f) : 0.f;
+}
+}  // namespace
+}  // namespace eagle
+
+extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M, int d,
+                                 int V, int k, float temperature, int32_t* topk_ids,
+                                 float* topk_logprobs, float* row_max, float* row_sumexp, int dtype,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return lmhead_run(x, w_lm, bias, M, d, V, k, temperature, topk_ids, topk_logprobs, row_max,
+                    row_sumexp, dtype, ws, ws_bytes, dev_status, stream, nullptr);
+}
+
+extern "C" int eagle_lmhead_verify_stats(const void* x, const void* w_lm, const float* bias, int B,
+                                         int R, int d, int V, const int32_t* parent_row,
+                                         const int32_t* token, const int32_t* n_rows,
+                                         float temperature, uint64_t seed, uint64_t offset,
+                                         int race_k, int32_t* race_ids, float* race_keys,
+                                         float* row_max, float* row_sumexp, float* child_logit,
+                                         int dtype, void* ws, size_t ws_bytes,
+                                         int32_t* dev_status, void* stream) {
+  if (B <= 0 || R <= 0 || !parent_row || !token || !row_max || !row_sumexp || !child_logit)
+    return EAGLE_ERR_INVALID_ARG;
+  if ((long long)B * R > 2048) return EAGLE_ERR_UNSUPPORTED;
+  if ((offset >> 63) != 0) return EAGLE_ERR_INVALID_ARG;
+  const RaceCfg rc{R, seed, offset};
+  const int st = lmhead_run(x, w_lm, bias, B * R, d, V, race_k, temperature, race_ids, race_keys,
+                            row_max, row_sumexp, dtype, ws, ws_bytes, dev_status, stream, &rc);
+  if (st != EAGLE_OK) return st;
+  const long long rows = (long long)B * R;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == EAGLE_BF16)
+    launch(child_logit_kernel<__nv_bfloat16>, (unsigned)((rows + 7) / 8), 256, 0, s,
+           (const __nv_bfloat16*)x, (const __nv_bfloat16*)w_lm, bias, parent_row, token, n_rows, B,
+           R, d, V, child_logit, dev_status);
+  else
+    launch(child_logit_kernel<float>, (unsigned)((rows + 7) / 8), 256, 0, s, (const float*)x,
+           (const float*)w_lm, bias, parent_row, token, n_rows, B, R, d, V, child_logit,
+           dev_status);
   note_launch();
   return last_launch_status();
 }

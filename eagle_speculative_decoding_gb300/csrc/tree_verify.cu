@@ -183,7 +183,12 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
     uint32_t ctr2_accept, uint32_t ctr3, const float* __restrict__ uniforms_override,
     int max_depth, int32_t* __restrict__ accept_len, int32_t* __restrict__ path_rows,
     int32_t* __restrict__ out_tokens, VerifyReq* __restrict__ req, int32_t* __restrict__ excl_out,
+    const float* __restrict__ st_max, const float* __restrict__ st_sumexp,
+    const float* __restrict__ child_logit, const int32_t* __restrict__ race_ids, int race_k,
     int32_t* dev_status) {
+  // statistics mode (race_ids != NULL): row max / sum-exp, the target logit
+  // of each child's token and each row's sorted race candidates come from
+  // the verification LM head; no logits are read
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -213,9 +218,14 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
     if (!ok) atomicExch(&s_bad, 1);
     if (greedy) {
       s_amax[i] = am_src[gi];
+    } else if (race_ids) {
+      s_stat[i] = RowStat{st_max[gi], st_sumexp[gi]};
+      s_zt[i] = child_logit[gi];
     } else {
       s_stat[i] = stats[gi];
       s_zt[i] = (i > 0 && ok) ? logits[((size_t)b * R + p) * V + t] : 0.f;
+    }
+    if (!greedy) {
       if (uniforms_override) {
         s_u[i] = uniforms_override[gi];
       } else {
@@ -308,6 +318,20 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
     return;
   }
   const int plen = s_plen, stop = s_stop;
+  if (!greedy && race_ids && threadIdx.x == 0) {
+    // the race winner at the stop row: its first candidate not rejected there
+    const int nex = s_nexcl;
+    int bonus = -1;
+    for (int j = 0; j < race_k && bonus < 0; ++j) {
+      const int y = race_ids[((size_t)b * R + stop) * race_k + j];
+      bool ex = y < 0;
+      for (int e = 0; e < nex; ++e) ex |= (s_excl[e] == y);
+      if (!ex) bonus = y;
+    }
+    if (bonus < 0) set_status(dev_status, EAGLE_ERR_INVALID_ARG);  // race_k too small
+    s_amax[stop] = bonus;
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i <= max_depth; i += kWalkThreads) {
     const size_t o = (size_t)b * (max_depth + 1) + i;
     path_rows[o] = i < plen ? s_path[i] : -1;
@@ -315,10 +339,10 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
       out_tokens[o] = s_token[s_path[i + 1]];
     else if (i + 1 > plen)
       out_tokens[o] = -1;
-    else if (greedy)
-      out_tokens[o] = s_amax[stop];  // the bonus token; the race writes it otherwise
+    else if (greedy || race_ids)
+      out_tokens[o] = s_amax[stop];  // the bonus token; the race kernel writes it otherwise
   }
-  if (!greedy) {
+  if (!greedy && !race_ids) {
     const int nex = s_nexcl;
     for (int e = threadIdx.x; e < nex; e += kWalkThreads) excl_out[(size_t)b * R + e] = s_excl[e];
     if (threadIdx.x == 0) req[b] = VerifyReq{stop, plen, nex, 0};
@@ -488,7 +512,8 @@ int verify_enqueue(int B, int R, int V, const int32_t* parent_row, const int32_t
          target_argmax, need_stats ? w.stats : nullptr, need_stats ? w.amax : nullptr,
          greedy ? 1 : 0, inv_t, key0, key1, 2u * off_hi, off_lo, uniforms_override, max_depth,
          accept_len, path_rows, out_tokens, greedy ? nullptr : w.req,
-         greedy ? nullptr : w.excl, dev_status);
+         greedy ? nullptr : w.excl, (const float*)nullptr, (const float*)nullptr,
+         (const float*)nullptr, (const int32_t*)nullptr, 0, dev_status);
   note_launch();
   if (!greedy) {
     launch(verify_race_kernel, dim3((unsigned)B, (unsigned)race_chunks(V)), kRaceThreads, 0, s, R,
@@ -615,4 +640,31 @@ extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* par
   return verify_enqueue(B, R, V, parent_row, token, n_rows, target_logits, target_argmax,
                         temperature, seed, offset, uniforms_override, max_depth, accept_len,
                         path_rows, out_tokens, w, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int eagle_tree_verify_stats(int B, int R, int V, const int32_t* parent_row,
+                                       const int32_t* token, const int32_t* n_rows,
+                                       const float* row_max, const float* row_sumexp,
+                                       const float* child_logit, const int32_t* race_ids,
+                                       int race_k, float temperature, uint64_t seed,
+                                       uint64_t offset, const float* uniforms_override,
+                                       int max_depth, int32_t* accept_len, int32_t* path_rows,
+                                       int32_t* out_tokens, int32_t* dev_status, void* stream) {
+  if (B <= 0 || R <= 0 || V < 2 || max_depth < 0 || race_k < 1) return EAGLE_ERR_INVALID_ARG;
+  if (!parent_row || !token || !row_max || !row_sumexp || !child_logit || !race_ids ||
+      !accept_len || !path_rows || !out_tokens)
+    return EAGLE_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || isinf(temperature)) return EAGLE_ERR_INVALID_ARG;
+  if (R > kMaxVerifyRows || max_depth > 64) return EAGLE_ERR_UNSUPPORTED;
+  if ((offset >> 63) != 0) return EAGLE_ERR_INVALID_ARG;
+  if ((long long)B * R > 2147483647LL) return EAGLE_ERR_UNSUPPORTED;
+  const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
+  launch(verify_walk_kernel, B, kWalkThreads, 0, static_cast<cudaStream_t>(stream), R, V,
+         parent_row, token, n_rows, (const float*)nullptr, (const int32_t*)nullptr,
+         (const RowStat*)nullptr, (const int32_t*)nullptr, 0, 1.f / temperature, (uint32_t)seed,
+         (uint32_t)(seed >> 32), 2u * off_hi, off_lo, uniforms_override, max_depth, accept_len,
+         path_rows, out_tokens, (VerifyReq*)nullptr, (int32_t*)nullptr, row_max, row_sumexp,
+         child_logit, race_ids, race_k, dev_status);
+  note_launch();
+  return last_launch_status();
 }

@@ -5,7 +5,8 @@ d 256, 4/2 heads x 64, V 1024, ctx 128, depth 4, top-k 4, budget 16), fp32:
   draft round : LM-head top-k on synthetic drafter rows + tree expansion per
                 depth, then rerank/flatten
   verify      : tree attention, fused projection, LM head (k = 1), greedy
-                and stochastic verification
+                and stochastic verification, and stochastic verification from
+                LM-head statistics
 """
 import numpy as np
 import torch
@@ -98,6 +99,27 @@ def run(device="cuda:0"):
                                n_rows=[ref_flat["n_rows"]], target_logits=logits.numpy(), seed=7)
     if min((m for _, _, m in ref_s["margins"]), default=1.0) > 1e-5:
         assert np.array_equal(toks.cpu().numpy(), ref_s["out_tokens"]), "stochastic verify"
+    # stochastic verification from LM-head statistics (no [B, R, V] logits)
+    rk = k + 1
+    xv = synth.normal((B * R, d), 1.0, dt, gen)
+    st_out = dict(ids=z32(B * R, rk), keys=z32(B * R, rk, t=torch.float32),
+                  m=z32(B * R, t=torch.float32), s=z32(B * R, t=torch.float32),
+                  c=z32(B * R, t=torch.float32))
+    b.eagle_lmhead_verify_stats(xv.to(dev), w_lm_d, flat["parent_row"], flat["token"], 1.0, rk,
+                                st_out["ids"], st_out["keys"], st_out["m"], st_out["s"],
+                                st_out["c"], n_rows=flat["n_rows"], seed=9, status=status)
+    b.eagle_tree_verify_stats(flat["parent_row"], flat["token"], 1.0, depth, st_out["m"],
+                              st_out["s"], st_out["c"], st_out["ids"], acc, path, toks, V,
+                              n_rows=flat["n_rows"], seed=9, status=status)
+    ref_st = oracle.verify_stats(xv.numpy(), w_lm.numpy(), ref_flat["parent_row"][None],
+                                 ref_flat["token"][None], 1.0, rk, seed=9, n_rows=[ref_flat["n_rows"]])
+    assert np.abs(st_out["m"].cpu().numpy() - ref_st["row_max"]).max() < 1e-3, "row max"
+    ref_w = oracle.tree_verify(ref_flat["parent_row"][None], ref_flat["token"][None], 1.0, depth,
+                               n_rows=[ref_flat["n_rows"]],
+                               target_logits=(xv.double() @ w_lm.double().T).reshape(B, R, V).numpy(),
+                               seed=9)
+    if min((m for _, _, m in ref_w["margins"]), default=1.0) > 1e-4:
+        assert np.array_equal(toks.cpu().numpy(), ref_w["out_tokens"]), "verify from statistics"
     torch.cuda.synchronize()
     assert int(status.item()) == 0, b.STATUS.get(int(status.item()))
     print("smoke ok: launches", b.launch_count())

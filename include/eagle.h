@@ -2,7 +2,8 @@
  * eagle.h -- C-ABI of the GB300 (sm_103a) EAGLE speculative-decoding hot path.
  *
  * One tree-verify round of EAGLE-family speculative decoding is served by
- * six calls:
+ * six calls (plus eagle_lmhead_verify_stats / eagle_tree_verify_stats, which
+ * serve stochastic verification without materialised logits):
  *   eagle_fuse_proj             EAGLE-3 fused feature g = W_proj [h_low; h_mid; h_high]
  *   eagle_tree_attn             tree-masked attention vs a paged KV cache + the tree rows
  *   eagle_lmhead_topk           LM-head GEMM with fused per-row top-k and log-softmax
@@ -290,6 +291,64 @@ int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row, const int3
                       const float* uniforms_override, int max_depth, int32_t* accept_len,
                       int32_t* path_rows, int32_t* out_tokens, void* ws, size_t ws_bytes,
                       int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_lmhead_verify_stats -- the verification LM head for stochastic
+ * verification: everything the deterministic-proposal walk of [E1]
+ * "Verification Phase: Multi-Round Speculative Sampling on Trees" reads from
+ * the target logits z = W_U a (+ b) of the B*R verify rows, without ever
+ * writing the [B, R, V] logits.  Rows are request-major (row = b*R + r).
+ *   row_max[row]    = max_v z/T;  row_sumexp[row] = sum_v exp(z/T - row_max)
+ *   child_logit[row]= z[b*R + parent_row(row)][token(row)] for tree rows
+ *                     1 <= r < n_rows[b]; 0 for the root and unused rows
+ *   race_ids / race_keys [row, race_k]: the race_k ids of largest
+ *                     key_y = z_y/T - log(-log u_{b,y}) (ties to the lower
+ *                     id), sorted, with their keys; u as in eagle_tree_verify
+ *                     (Philox word (y & 3) at counter (y >> 2, b,
+ *                     2*offset_hi + 1, offset_lo), key = seed).  The
+ *                     renormalisation of the race is common to all ids, so
+ *                     the stop row's bonus token is its first candidate not
+ *                     rejected there: race_k must exceed the number of
+ *                     children of any row (top-k trees: race_k = k + 1).
+ * No counterpart call on the pages: it fuses what [E1]'s verification reads
+ * into the LM head that produces the logits.
+ *   x : [B*R, d], w_lm : [V, d] (dtype `dtype`), bias : [V] fp32 or NULL
+ *   parent_row, token : [B, R] int32;  n_rows : [B] int32 or NULL (= R)
+ *   race_ids : [B*R, race_k] int32; race_keys : [B*R, race_k] fp32
+ *   row_max, row_sumexp, child_logit : [B*R] fp32
+ *   ws : eagle_lmhead_topk_workspace_size(B*R, d, V, race_k, dtype) bytes
+ * Device-detected: a parent or token out of range -> EAGLE_ERR_BAD_TREE;
+ * NaN logits -> EAGLE_ERR_NONFINITE.
+ * Limits: those of eagle_lmhead_topk with M = B*R and k = race_k; T > 0;
+ * offset < 2^63.
+ * ---------------------------------------------------------------------- */
+int eagle_lmhead_verify_stats(const void* x, const void* w_lm, const float* bias, int B, int R,
+                              int d, int V, const int32_t* parent_row, const int32_t* token,
+                              const int32_t* n_rows, float temperature, uint64_t seed,
+                              uint64_t offset, int race_k, int32_t* race_ids, float* race_keys,
+                              float* row_max, float* row_sumexp, float* child_logit, int dtype,
+                              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_verify_stats -- eagle_tree_verify for T > 0 with deterministic
+ * proposals, reading the outputs of eagle_lmhead_verify_stats instead of
+ * target logits.  Same walk, same accept uniforms (and uniforms_override),
+ * same outputs: child c of the current row r is accepted when
+ * u_c < p / (1 - mass of the distinct tokens already rejected at r), with
+ * p = exp(child_logit[c]/T - row_max[r]) / row_sumexp[r]; the bonus token at
+ * the stop row is its first race candidate not rejected there.  Needs no
+ * workspace (one kernel).
+ * Device-detected: as eagle_tree_verify; every race candidate of the stop row
+ * rejected (race_k too small) -> EAGLE_ERR_INVALID_ARG and bonus -1.
+ * Limits: R <= 1024, max_depth <= 64, T > 0, offset < 2^63.
+ * ---------------------------------------------------------------------- */
+int eagle_tree_verify_stats(int B, int R, int V, const int32_t* parent_row, const int32_t* token,
+                            const int32_t* n_rows, const float* row_max, const float* row_sumexp,
+                            const float* child_logit, const int32_t* race_ids, int race_k,
+                            float temperature, uint64_t seed, uint64_t offset,
+                            const float* uniforms_override, int max_depth, int32_t* accept_len,
+                            int32_t* path_rows, int32_t* out_tokens, int32_t* dev_status,
+                            void* stream);
 
 /* ------------------------------------------------------------------------
  * eagle_tree_verify_noalloc -- eagle_tree_verify without a workspace.
