@@ -38,6 +38,7 @@ from .eagle_oracle import (  # noqa: F401
     tree_expand_init,
     tree_expand_step,
     tree_verify,
+    tree_commit,
     tree_verify_stats,
     verify_stats,
 )

@@ -640,3 +640,66 @@ def tree_verify_stats(parent_row, token, temperature, max_depth, row_max, row_su
         out_tokens[b, :len(toks)] = toks
     return dict(accept_len=accept_len, path_rows=path_rows, out_tokens=out_tokens,
                 margins=margins)
+
+
+# ---------------------------------------------------------------------------
+# K9 (follow-on): publish the verified path
+# ---------------------------------------------------------------------------
+
+
+def tree_commit(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree, path_rows, accept_len,
+                features=None):
+    """Publish the verified path of each request ([M7.5] 0x05D "Feature And
+    KV Commit", the publish_verified_path transaction): the target K/V of the
+    accepted rows are appended to the committed prefix and their target
+    features are gathered for the next draft round; every other tree row is
+    discarded.  Rows are taken by their flat row index (the path from
+    verification), never by token id.
+
+    Reading: the accepted rows are path_rows[b, 0 .. accept_len[b]] -- row 0
+    (the root: the previous round's frontier token, whose K/V this verify
+    forward computed) and the accepted drafted rows, in path order.  They
+    land at positions ctx .. ctx + accept_len of the paged cache (page =
+    block_table[b, pos // 16], slot = pos % 16) and ctx grows by
+    accept_len + 1.  The new frontier (bonus) token is not one of the verified
+    rows: its K/V and feature need a later target append, so nothing is
+    written for it.
+
+    k_cache, v_cache [P, 16, Hkv, D]; block_table [B, max_pages];
+    ctx_lens [B]; k_tree, v_tree [B, R, Hkv, D]; path_rows [B, max_depth+1];
+    accept_len [B]; features [B*R, F] or None.
+    Returns dict(k_cache, v_cache (copies), ctx_lens [B],
+    features [B, max_depth+1, F] (zeros past accept_len) or None).
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    table = np.asarray(block_table)
+    ctx = np.array(ctx_lens, dtype=np.int64, copy=True)
+    path = np.asarray(path_rows)
+    acc = np.asarray(accept_len)
+    B, R = np.asarray(k_tree).shape[:2]
+    P = kc.shape[0]
+    out_f = None
+    if features is not None:
+        f = np.asarray(features)
+        out_f = np.zeros((B, path.shape[1], f.shape[1]), dtype=f.dtype)
+    for b in range(B):
+        n = int(acc[b]) + 1
+        if not 1 <= n <= path.shape[1]:
+            raise ValueError("accept_len out of range")
+        for i in range(n):
+            row = int(path[b, i])
+            if not 0 <= row < R:
+                raise ValueError("path row out of range")
+            pos = int(ctx[b]) + i
+            if pos // 16 >= table.shape[1]:
+                raise ValueError("no page for the committed position")
+            page = int(table[b, pos // 16])
+            if not 0 <= page < P:
+                raise ValueError("page id out of range")
+            kc[page, pos % 16] = k_tree[b, row]
+            vc[page, pos % 16] = v_tree[b, row]
+            if out_f is not None:
+                out_f[b, i] = f[b * R + row]
+        ctx[b] += n
+    return dict(k_cache=kc, v_cache=vc, ctx_lens=ctx, features=out_f)
