@@ -44,6 +44,8 @@ _SIGS = {
                                        _I, _P, _P, _P, _P, _P]),
     "eagle_lmhead_verify_stats": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _U64, _U64, _I,
                                        _P, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
+    "eagle_tree_commit": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P,
+                               _I, _P, _P, _P]),
     "eagle_tree_verify_stats": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _F, _U64, _U64,
                                      _P, _I, _P, _P, _P, _P, _P]),
 }
@@ -270,4 +272,18 @@ def eagle_tree_verify_stats(parent_row, token, temperature, max_depth, row_max, 
         B, R, V, _ptr(parent_row), _ptr(token), _ptr(n_rows), _ptr(row_max), _ptr(row_sumexp),
         _ptr(child_logit), _ptr(race_ids), race_k, float(temperature), int(seed), int(offset),
         _ptr(uniforms_override), max_depth, _ptr(accept_len), _ptr(path_rows), _ptr(out_tokens),
+        _ptr(status), _stream(stream)))
+
+
+# ------------------------------------------------------------------ K9
+def eagle_tree_commit(k_tree, v_tree, path_rows, accept_len, k_cache, v_cache, block_table,
+                      ctx_lens, features=None, features_out=None, status=None, stream=None):
+    """Publish the verified path into the paged cache (see include/eagle.h)."""
+    B, R, Hkv, D = k_tree.shape
+    max_depth = path_rows.shape[1] - 1
+    F = 0 if features is None else features.shape[1]
+    _check("eagle_tree_commit", lib().eagle_tree_commit(
+        B, R, Hkv, D, max_depth, _dtype(k_tree), _ptr(k_tree), _ptr(v_tree), _ptr(path_rows),
+        _ptr(accept_len), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(ctx_lens), _ptr(features), F, _ptr(features_out),
         _ptr(status), _stream(stream)))

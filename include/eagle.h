@@ -351,6 +351,37 @@ int eagle_tree_verify_stats(int B, int R, int V, const int32_t* parent_row, cons
                             void* stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_tree_commit -- publish the verified path.
+ * [M7.5] section 0x05D "Feature And KV Commit" (publish_verified_path):
+ * the target K/V of the accepted rows are appended to the committed prefix
+ * and their target features gathered for the next draft round; every other
+ * tree row is discarded.  Rows are taken by the flat row index of the
+ * verified path, never by token id.  The accepted rows of request b are
+ * path_rows[b, 0 .. accept_len[b]] (the root row -- the previous frontier
+ * token, computed by this verify forward -- then the accepted drafted rows);
+ * row i lands at position ctx_lens[b] + i (page block_table[b, pos / 16],
+ * slot pos % 16) and ctx_lens[b] grows by accept_len[b] + 1.  The new
+ * frontier token is not a verified row and needs a later target append.
+ *   k_tree, v_tree : [B, R, Hkv, D] dtype `dtype` (the verify forward's rows)
+ *   path_rows, accept_len : outputs of eagle_tree_verify ([B, max_depth+1], [B])
+ *   k_cache, v_cache : [num_pages, 16, Hkv, D], written in place
+ *   block_table : [B, max_pages] (the caller has mapped pages for the new
+ *                 positions);  ctx_lens : [B] int32, updated in place
+ *   features : [B*R, F] or NULL; features_out : [B, max_depth+1, F] or NULL
+ *                 (rows past accept_len are zeroed)
+ * Device-detected: accept_len or a path row out of range -> EAGLE_ERR_BAD_TREE;
+ * no room in the block table or a page id out of range -> EAGLE_ERR_BAD_KV;
+ * such a request is left untouched (nothing written, ctx_lens unchanged).
+ * Limits: max_depth <= 64; Hkv * D * element size and F * element size
+ * multiples of 16 bytes; 16-byte aligned arrays; num_pages <= 2^26.
+ * ---------------------------------------------------------------------- */
+int eagle_tree_commit(int B, int R, int Hkv, int D, int max_depth, int dtype, const void* k_tree,
+                      const void* v_tree, const int32_t* path_rows, const int32_t* accept_len,
+                      void* k_cache, void* v_cache, int num_pages, const int32_t* block_table,
+                      int max_pages, int32_t* ctx_lens, const void* features, int F,
+                      void* features_out, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * eagle_tree_verify_noalloc -- eagle_tree_verify without a workspace.
  * The pages have no counterpart of this call: it exists for callers that
  * cannot allocate device memory, such as a plugin whose host framework owns
