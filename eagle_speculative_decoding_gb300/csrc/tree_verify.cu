@@ -439,12 +439,192 @@ __global__ void __launch_bounds__(kRaceThreads) verify_race_kernel(
   }
 }
 
+// Sampled proposals ([E1] Algorithm 1 verbatim): the siblings under a row
+// were drawn i.i.d. from q = softmax(draft logits / T) of that row.  Child t
+// is accepted when u < p(t) / q(t), with p the current target distribution;
+// after a rejection p <- norm(max(0, p - q)) (p unchanged when that mass is
+// 0); if every child is rejected the bonus token is the exponential race
+// argmax_y log p(y) - log(-log u_y) over the final p.  The residual is never
+// stored: after r rejections at a row, p_r(y) is rebuilt from p_0(y) and
+// q(y) with the r normalising masses kept in shared memory, so each
+// rejection costs one vocabulary-wide pass for the next mass.  One CTA per
+// request; every thread runs the walk in step.
+__global__ void __launch_bounds__(kWalkThreads) verify_walk_sampled_kernel(
+    int R, int V, const int32_t* __restrict__ parent_row, const int32_t* __restrict__ token,
+    const int32_t* __restrict__ n_rows, const float* __restrict__ logits,
+    const float* __restrict__ draft, const RowStat* __restrict__ st_t,
+    const RowStat* __restrict__ st_d, float inv_t, uint32_t key0, uint32_t key1,
+    uint32_t ctr2_accept, uint32_t ctr3, const float* __restrict__ uniforms_override,
+    int max_depth, int32_t* __restrict__ accept_len, int32_t* __restrict__ path_rows,
+    int32_t* __restrict__ out_tokens, int32_t* dev_status) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int s_parent[kMaxVerifyRows];
+  __shared__ int s_token[kMaxVerifyRows];
+  __shared__ float s_u[kMaxVerifyRows];
+  __shared__ int s_ch[kMaxVerifyRows];
+  __shared__ float s_mass[kMaxVerifyRows];  // normalising masses of the rejections at this row
+  __shared__ int s_path[65];
+  __shared__ float s_rv[kWalkThreads / 32];
+  __shared__ int s_ri[kWalkThreads / 32];
+  __shared__ int s_bad, s_nch, s_acc;
+
+  const int n = n_rows ? n_rows[b] : R;
+  if (tid == 0) s_bad = (n < 1 || n > R) ? 1 : 0;
+  __syncthreads();
+  const int nn = s_bad ? 1 : n;
+  for (int i = tid; i < nn; i += kWalkThreads) {
+    const size_t gi = (size_t)b * R + i;
+    const int p = parent_row[gi], t = token[gi];
+    s_parent[i] = p;
+    s_token[i] = t;
+    if (!((i == 0) ? (p == -1) : (p >= 0 && p < i && t >= 0 && t < V))) atomicExch(&s_bad, 1);
+    if (uniforms_override) {
+      s_u[i] = uniforms_override[gi];
+    } else {
+      const uint4 w = philox4x32_10(make_uint4((uint32_t)i, (uint32_t)b, ctr2_accept, ctr3), key0, key1);
+      s_u[i] = bits_to_uniform(w.x);
+    }
+  }
+  __syncthreads();
+  // p_r(y) from the stored masses: p_0 = softmax(z/T), q = softmax(zd/T)
+  auto p_of = [&](float zy, float zdy, const RowStat& pt, const RowStat& qd, int nrej, float& q) {
+    float pv = exp2f((zy * inv_t - pt.m) * kLog2e) / pt.s;
+    q = exp2f((zdy * inv_t - qd.m) * kLog2e) / qd.s;
+    for (int r = 0; r < nrej; ++r)
+      if (s_mass[r] > 0.f) pv = fmaxf(0.f, pv - q) / s_mass[r];
+    return pv;
+  };
+  int bad = s_bad, cur = 0, plen = 1, nrej = 0;
+  if (tid == 0) s_path[0] = 0;
+  while (!bad) {
+    // the children of cur in row order (warp 0, by ballots)
+    if (warp == 0) {
+      int nch = 0;
+      for (int c0 = cur + 1; c0 < nn; c0 += 32) {
+        const int c = c0 + lane;
+        const bool is_child = c < nn && s_parent[c] == cur;
+        const unsigned m = __ballot_sync(0xffffffffu, is_child);
+        if (is_child) s_ch[nch + __popc(m & ((1u << lane) - 1u))] = c;
+        nch += __popc(m);
+      }
+      if (lane == 0) s_nch = nch;
+    }
+    __syncthreads();
+    const int nch = s_nch;
+    const float* z = logits + ((size_t)b * R + cur) * V;
+    const float* zd = draft + ((size_t)b * R + cur) * V;
+    const RowStat pt = st_t[(size_t)b * R + cur], qd = st_d[(size_t)b * R + cur];
+    int accepted = -1;
+    nrej = 0;
+    for (int j = 0; j < nch; ++j) {
+      if (tid == 0) {
+        const int c = s_ch[j], t = s_token[c];
+        float q;
+        const float pv = p_of(z[t], zd[t], pt, qd, nrej, q);
+        const float ratio = q > 0.f ? pv / q : (pv > 0.f ? INFINITY : 0.f);
+        s_acc = s_u[c] < ratio ? c : -1;
+      }
+      __syncthreads();
+      accepted = s_acc;
+      if (accepted >= 0) break;
+      // rejected: mass of max(0, p - q) for the next residual
+      float acc = 0.f;
+      for (int y = tid; y < V; y += kWalkThreads) {
+        float q;
+        const float pv = p_of(z[y], zd[y], pt, qd, nrej, q);
+        acc += fmaxf(0.f, pv - q);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) s_rv[warp] = acc;
+      __syncthreads();
+      if (tid == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < kWalkThreads / 32; ++w) tot += s_rv[w];
+        s_mass[nrej] = tot;
+      }
+      __syncthreads();
+      ++nrej;
+    }
+    if (accepted < 0) break;
+    if (plen > max_depth) {
+      bad = 2;
+      break;
+    }
+    if (tid == 0) s_path[plen] = accepted;
+    ++plen;
+    cur = accepted;
+    __syncthreads();
+  }
+  if (bad) {
+    if (tid == 0) {
+      set_status(dev_status, EAGLE_ERR_BAD_TREE);
+      accept_len[b] = 0;
+    }
+    for (int i = tid; i <= max_depth; i += kWalkThreads) {
+      path_rows[(size_t)b * (max_depth + 1) + i] = (i == 0) ? 0 : -1;
+      out_tokens[(size_t)b * (max_depth + 1) + i] = -1;
+    }
+    return;
+  }
+  // bonus: exponential race over the final residual at the stop row
+  {
+    const float* z = logits + ((size_t)b * R + cur) * V;
+    const float* zd = draft + ((size_t)b * R + cur) * V;
+    const RowStat pt = st_t[(size_t)b * R + cur], qd = st_d[(size_t)b * R + cur];
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    bool nan_seen = false;
+    for (int g = tid; g * 4 < V; g += kWalkThreads) {
+      const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, ctr2_accept + 1u, ctr3), key0, key1);
+      const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int y = g * 4 + k;
+        if (y >= V) break;
+        const float zy = z[y];
+        nan_seen |= isnan(zy);
+        float q;
+        const float pv = p_of(zy, zd[y], pt, qd, nrej, q);
+        if (pv > 0.f) argmax_merge(bv, bi, logf(pv) - logf(-logf(bits_to_uniform(words[k]))), y);
+      }
+    }
+    if (nan_seen) set_status(dev_status, EAGLE_ERR_NONFINITE);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      argmax_merge(bv, bi, ov, oi);
+    }
+    if (lane == 0) {
+      s_rv[warp] = bv;
+      s_ri[warp] = bi;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kWalkThreads / 32; ++w) argmax_merge(bv, bi, s_rv[w], s_ri[w]);
+      s_acc = bi == 0x7fffffff ? -1 : bi;
+    }
+    __syncthreads();
+  }
+  const int bonus = s_acc;
+  for (int i = tid; i <= max_depth; i += kWalkThreads) {
+    const size_t o = (size_t)b * (max_depth + 1) + i;
+    path_rows[o] = i < plen ? s_path[i] : -1;
+    out_tokens[o] = i + 1 < plen ? s_token[s_path[i + 1]] : (i + 1 == plen ? bonus : -1);
+  }
+  if (tid == 0) accept_len[b] = plen - 1;
+}
+
 int race_chunks(int V) { return (V + kRaceChunk - 1) / kRaceChunk; }
 
 // Workspace layout shared by eagle_tree_verify (caller buffer) and the
 // allocation-free variant (library buffer).
 struct VerifyScratch {
   RowStat* stats;
+  RowStat* stats_d;  // draft-logit row statistics (sampled proposals)
   int32_t* amax;
   int32_t* excl;
   VerifyReq* req;
@@ -453,7 +633,7 @@ struct VerifyScratch {
 
 
 size_t scratch_bytes(int B, int R, int V) {
-  return round_up((size_t)B * R * sizeof(RowStat), 256) + round_up((size_t)B * R * 4, 256) * 2 +
+  return round_up((size_t)B * R * sizeof(RowStat), 256) * 2 + round_up((size_t)B * R * 4, 256) * 2 +
          round_up((size_t)B * sizeof(VerifyReq), 256) +
          round_up((size_t)B * race_chunks(V) * sizeof(RacePart), 256) + 256;
 }
@@ -462,6 +642,7 @@ VerifyScratch carve_scratch(void* base, int B, int R, int V, bool race) {
   char* cur = static_cast<char*>(base);
   VerifyScratch w;
   w.stats = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
+  w.stats_d = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
   w.amax = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
   w.excl = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
   w.req = static_cast<VerifyReq*>(ws_carve(cur, (size_t)B * sizeof(VerifyReq)));
@@ -472,7 +653,8 @@ VerifyScratch carve_scratch(void* base, int B, int R, int V, bool race) {
 
 // Host-side argument checks common to both entry points.
 int verify_check(int B, int R, int V, const int32_t* parent_row, const int32_t* token,
-                 const float* target_logits, const int32_t* target_argmax, float temperature,
+                 const float* target_logits, const int32_t* target_argmax,
+                 const float* draft_logits, float temperature,
                  int proposal_mode, uint64_t offset, int max_depth, const int32_t* accept_len,
                  const int32_t* path_rows, const int32_t* out_tokens) {
   if (B <= 0 || R <= 0 || V < 2 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
@@ -481,7 +663,7 @@ int verify_check(int B, int R, int V, const int32_t* parent_row, const int32_t* 
   if (proposal_mode != EAGLE_PROPOSAL_DETERMINISTIC && proposal_mode != EAGLE_PROPOSAL_SAMPLED)
     return EAGLE_ERR_INVALID_ARG;
   const bool greedy = temperature == 0.f;
-  if (proposal_mode == EAGLE_PROPOSAL_SAMPLED) return greedy ? EAGLE_ERR_INVALID_ARG : EAGLE_ERR_UNSUPPORTED;
+  if (proposal_mode == EAGLE_PROPOSAL_SAMPLED && (greedy || !draft_logits)) return EAGLE_ERR_INVALID_ARG;
   if (greedy && !target_logits && !target_argmax) return EAGLE_ERR_INVALID_ARG;
   if (!greedy && !target_logits) return EAGLE_ERR_INVALID_ARG;
   if (R > kMaxVerifyRows || max_depth > 64) return EAGLE_ERR_UNSUPPORTED;
@@ -494,20 +676,33 @@ int verify_check(int B, int R, int V, const int32_t* parent_row, const int32_t* 
 // Enqueues the kernels of one verification (arguments already checked).
 int verify_enqueue(int B, int R, int V, const int32_t* parent_row, const int32_t* token,
                    const int32_t* n_rows, const float* target_logits,
-                   const int32_t* target_argmax, float temperature, uint64_t seed, uint64_t offset,
+                   const int32_t* target_argmax, const float* draft_logits, int proposal_mode,
+                   float temperature, uint64_t seed, uint64_t offset,
                    const float* uniforms_override, int max_depth, int32_t* accept_len,
                    int32_t* path_rows, int32_t* out_tokens, const VerifyScratch& w,
                    int32_t* dev_status, cudaStream_t s) {
   const bool greedy = temperature == 0.f;
   const bool need_stats = !greedy || !target_argmax;
   const float inv_t = greedy ? 0.f : 1.f / temperature;
+  const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
+  const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+  if (proposal_mode == EAGLE_PROPOSAL_SAMPLED) {
+    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s, target_logits, n_rows, R,
+           V, inv_t, 0, w.stats, w.amax, dev_status);
+    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s, draft_logits, n_rows, R,
+           V, inv_t, 0, w.stats_d, w.amax, dev_status);
+    launch(verify_walk_sampled_kernel, B, kWalkThreads, 0, s, R, V, parent_row, token, n_rows,
+           target_logits, draft_logits, (const RowStat*)w.stats, (const RowStat*)w.stats_d, inv_t,
+           key0, key1, 2u * off_hi, off_lo, uniforms_override, max_depth, accept_len, path_rows,
+           out_tokens, dev_status);
+    note_launch(3);
+    return last_launch_status();
+  }
   if (need_stats) {
     launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s, target_logits, n_rows, R,
            V, inv_t, greedy ? 1 : 0, w.stats, w.amax, dev_status);
     note_launch();
   }
-  const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
-  const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   launch(verify_walk_kernel, B, kWalkThreads, 0, s, R, V, parent_row, token, n_rows, target_logits,
          target_argmax, need_stats ? w.stats : nullptr, need_stats ? w.amax : nullptr,
          greedy ? 1 : 0, inv_t, key0, key1, 2u * off_hi, off_lo, uniforms_override, max_depth,
@@ -542,10 +737,9 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
                                  int max_depth, int32_t* accept_len, int32_t* path_rows,
                                  int32_t* out_tokens, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream) {
-  (void)draft_logits;
   const int chk = verify_check(B, R, V, parent_row, token, target_logits, target_argmax,
-                               temperature, proposal_mode, offset, max_depth, accept_len,
-                               path_rows, out_tokens);
+                               draft_logits, temperature, proposal_mode, offset, max_depth,
+                               accept_len, path_rows, out_tokens);
   if (chk != EAGLE_OK) return chk;
   const bool need_ws = temperature != 0.f || !target_argmax;
   VerifyScratch w{};
@@ -554,7 +748,8 @@ extern "C" int eagle_tree_verify(int B, int R, int V, const int32_t* parent_row,
     w = carve_scratch(ws, B, R, V, temperature != 0.f);
   }
   return verify_enqueue(B, R, V, parent_row, token, n_rows, target_logits, target_argmax,
-                        temperature, seed, offset, uniforms_override, max_depth, accept_len,
+                        draft_logits, proposal_mode, temperature, seed, offset, uniforms_override,
+                        max_depth, accept_len,
                         path_rows, out_tokens, w, dev_status, static_cast<cudaStream_t>(stream));
 }
 
@@ -572,9 +767,9 @@ namespace {
 constexpr int kNoAllocMaxRows = 65536;    // B * R rows of statistics
 constexpr int kNoAllocMaxChunks = 65536;  // B * ceil(V / 4096) race chunks
 constexpr size_t kNoAllocScratchBytes =
-    (size_t)kNoAllocMaxRows * sizeof(RowStat) + (size_t)kNoAllocMaxRows * 4 * 2 +
+    (size_t)kNoAllocMaxRows * sizeof(RowStat) * 2 + (size_t)kNoAllocMaxRows * 4 * 2 +
     (size_t)kNoAllocMaxRows * sizeof(VerifyReq) + (size_t)kNoAllocMaxChunks * sizeof(RacePart) +
-    5 * 256;
+    6 * 256;
 
 // One copy per GPU that loads the library, kept until the process exits.
 // Every call on a device shares it: two calls whose kernels overlap on that
@@ -620,10 +815,9 @@ extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* par
                                          const float* uniforms_override, int max_depth,
                                          int32_t* accept_len, int32_t* path_rows,
                                          int32_t* out_tokens, int32_t* dev_status, void* stream) {
-  (void)draft_logits;
   const int chk = verify_check(B, R, V, parent_row, token, target_logits, target_argmax,
-                               temperature, proposal_mode, offset, max_depth, accept_len,
-                               path_rows, out_tokens);
+                               draft_logits, temperature, proposal_mode, offset, max_depth,
+                               accept_len, path_rows, out_tokens);
   if (chk != EAGLE_OK) return chk;
   // the built-in scratch holds kNoAllocMaxRows rows and kNoAllocMaxChunks
   // race chunks
@@ -638,7 +832,8 @@ extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* par
     w = carve_scratch(base, B, R, V, temperature != 0.f);
   }
   return verify_enqueue(B, R, V, parent_row, token, n_rows, target_logits, target_argmax,
-                        temperature, seed, offset, uniforms_override, max_depth, accept_len,
+                        draft_logits, proposal_mode, temperature, seed, offset, uniforms_override,
+                        max_depth, accept_len,
                         path_rows, out_tokens, w, dev_status, static_cast<cudaStream_t>(stream));
 }
 

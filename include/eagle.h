@@ -260,8 +260,10 @@ int eagle_tree_expand_finalize(int B, int max_nodes, int budget, int R,
  *                      accept iff u < p(t), and a rejected token is removed
  *                      from p, which is renormalised.
  *   SAMPLED          : Algorithm 1 with p_hat = softmax(draft logits / T)
- *                      (children i.i.d. from it).  Not yet available on the
- *                      GPU: returns EAGLE_ERR_UNSUPPORTED.
+ *                      (children i.i.d. from it): accept iff u < p(t)/q(t);
+ *                      after a rejection p <- norm(max(0, p - q)) (unchanged
+ *                      when that mass is 0); the bonus is drawn from the
+ *                      final p.  Needs draft_logits [B, R, V] fp32 and T > 0.
  * The final draw is an exponential race argmax_y (z_y/T - log(-log u_y)) over
  * the ids not rejected at the stop row.
  * Uniforms: Philox4x32-10 (Salmon et al., SC'11), key = seed; accept test of

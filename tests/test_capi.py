@@ -45,11 +45,12 @@ def test_status_strings(L):
 
 def test_host_validation_without_gpu(L):
     N = None
-    # verify: null pointers, negative sizes, sampled proposals at T = 0, deep trees
+    # verify: null pointers, sampled proposals at T = 0 or without draft logits, deep trees, no ws
     assert L.eagle_tree_verify(1, 4, 8, N, N, N, N, N, N, 1.0, 0, 0, 0, N, 2, N, N, N, N, 0, N, N) == 1
     p = ctypes.c_void_p(16)
     assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, p, 0.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 1
-    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, p, 1.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 2
+    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 1
+    assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, p, 1.0, 1, 0, 0, N, 2, p, p, p, N, 0, N, N) == 3
     assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 0, 0, 0, N, 65, p, p, p, N, 0, N, N) == 2
     assert L.eagle_tree_verify(1, 4, 8, p, p, N, p, N, N, 1.0, 0, 0, 0, N, 2, p, p, p, N, 0, N, N) == 3
     # lm head: k > 32 unsupported, k > V invalid, V not a multiple of 16
