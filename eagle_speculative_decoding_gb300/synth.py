@@ -36,6 +36,10 @@ CONFIGS = {
                     N=8, depth=4, topk=2, width=2, temps=(1.0,), dtype="bf16"),
     "long4": dict(B=4, d=4096, Hq=32, Hkv=8, D=128, V=128256, ctx=(32768, 32768), page=16,
                   N=60, depth=8, topk=8, width=8, temps=(0.6,), dtype="bf16"),
+    # chain drafts of length 3 (top-1 at each depth: a degenerate tree), as in
+    # the serving-engine comparisons, at batch 64
+    "chain3": dict(B=64, d=4096, Hq=32, Hkv=8, D=128, V=128256, ctx=(1024, 4096), page=16,
+                   N=3, depth=3, topk=1, width=1, temps=(0.0,), dtype="bf16"),
 }
 
 WEIGHT_STD = 0.02      # W_proj, W_U ~ N(0, 0.02^2)

@@ -90,7 +90,7 @@ def test_bad_page_id_reported():
     assert st == 6
 
 
-@pytest.mark.parametrize("cfg", ["llama8b", "llama70b", "serve64", "long4"])
+@pytest.mark.parametrize("cfg", ["llama8b", "llama70b", "serve64", "long4", "chain3"])
 def test_full_size_sampled(cfg):
     b = need_gpu()
     c = synth.CONFIGS[cfg]

@@ -65,13 +65,13 @@ def test_numeric_example_on_gpu():
     assert int(g.status.item()) == 0
 
 
-@pytest.mark.parametrize("cfg", ["toy", "llama8b", "serve64", "long4"])
+@pytest.mark.parametrize("cfg", ["toy", "llama8b", "serve64", "long4", "chain3"])
 def test_random_trees_bit_exact(cfg):
     b = need_gpu()
     c = synth.CONFIGS[cfg]
     B, k, width, depth, N = c["B"], c["topk"], c["width"], c["depth"], c["N"]
     V = 5000
-    gen = synth.generator(hash(cfg) % 1000)
+    gen = synth.generator(sum(map(ord, cfg)))
     max_nodes = 1 + synth.n_candidates(c)
     R = N + 1
     roots = synth.random_tokens((B,), V, gen)
