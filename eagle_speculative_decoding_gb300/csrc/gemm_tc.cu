@@ -84,8 +84,32 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
 }
 
 // ------------------------------------------------------------ shared pipeline
+// Weight half of the first ring stages, issued by the producer thread before
+// the previous grid on the stream has finished (the weights are constants of
+// the model; only the activations depend on that grid).  Each stage's full
+// barrier expects both halves; the activation half follows after the wait.
+// Returns the number of stages pre-issued.
 template <bool TF32, class Sched>
-__device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, const Ring& rg) {
+__device__ __forceinline__ int prefetch_weights(const Sched& sc, CtaShared& sh, const Ring& rg) {
+  constexpr int kBke = TF32 ? 32 : 64;
+  int it = 0;
+  Seg sg;
+  for (int si = 0; it < rg.stages && sc.seg(si, sg); ++si) {
+    for (int kc = sg.k0; kc < sg.k1 && it < rg.stages; ++kc, ++it) {
+      const uint32_t fb = smem_u32(&sh.full[it]);
+      mbar_arrive_expect_tx(fb, rg.a_bytes + rg.b_bytes);
+      if (Sched::kWeightIsA)
+        tma_load_2d(rg.a0 + it * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, sc.a_policy());
+      else
+        tma_load_2d(rg.b0 + it * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, sc.b_policy());
+    }
+  }
+  return it;
+}
+
+template <bool TF32, class Sched>
+__device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, const Ring& rg,
+                                             int pre) {
   constexpr int kBke = TF32 ? 32 : 64;  // elements per 128-byte chunk
   const uint64_t pol_a = sc.a_policy();
   const uint64_t pol_b = sc.b_policy();
@@ -96,11 +120,18 @@ __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, con
   Seg sg;
   for (int si = 0; sc.seg(si, sg); ++si) {
     for (int kc = sg.k0; kc < sg.k1; ++kc, ++it) {
-      if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u, &sh.abort_flag)) goto drain;
       const uint32_t fb = smem_u32(&sh.full[s]);
-      mbar_arrive_expect_tx(fb, tx);
-      tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
-      tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
+      if (it < pre) {  // weight half already in flight: the activation half only
+        if (Sched::kWeightIsA)
+          tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
+        else
+          tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
+      } else {
+        if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u, &sh.abort_flag)) goto drain;
+        mbar_arrive_expect_tx(fb, tx);
+        tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
+        tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
+      }
       if (++s == stages) {
         s = 0;
         ph ^= 1u;
@@ -187,8 +218,10 @@ __device__ __forceinline__ bool epi_wait(CtaShared& sh, uint32_t bar, uint32_t p
 }
 
 // Kernel prologue/epilogue shared by both GEMMs.
-__device__ __forceinline__ void cta_setup(CtaShared& sh, int stages, uint32_t tmem_cols) {
-  const int warp = threadIdx.x >> 5;
+// CTA set-up in two halves: cta_init (thread 0: barriers) and cta_start (all
+// threads: wait for the previous grid, claim TMEM, then let dependents launch);
+// the producer may pre-issue weight loads in between (prefetch_weights).
+__device__ __forceinline__ void cta_init(CtaShared& sh, int stages) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&sh.full[s]), 1);
@@ -204,6 +237,9 @@ __device__ __forceinline__ void cta_setup(CtaShared& sh, int stages, uint32_t tm
     sh.flag = 0;
     fence_mbar_init();
   }
+}
+__device__ __forceinline__ void cta_start(CtaShared& sh, uint32_t tmem_cols) {
+  const int warp = threadIdx.x >> 5;
   pdl_wait();  // the previous grid (and its TMEM) is gone from here on
   if (warp == 1) {
     tmem_alloc(smem_u32(&sh.tmem_base), tmem_cols);
@@ -254,6 +290,7 @@ struct LmParams {
 // W_U the N side, so TMEM lane e holds activation row e and each epilogue
 // thread scans its own row's logits with no cross-thread reduction.
 struct LmSched {
+  static constexpr bool kWeightIsA = false;  // W_U is the B operand
   const CUtensorMap* mx;
   const CUtensorMap* mw;
   int t0, t1, a_row, nk, tn;
@@ -595,10 +632,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_x);
     tma_prefetch_desc(&map_w);
   }
-  cta_setup(sh, stages, tmem_cols);
+  cta_init(sh, stages);
+  int pre = 0;
+  if (threadIdx.x == 0) pre = prefetch_weights<false>(sc, sh, rg);
+  cta_start(sh, tmem_cols);
 
   if (warp == 0) {
-    if (lane == 0) run_producer<false>(sc, sh, rg);
+    if (lane == 0) run_producer<false>(sc, sh, rg, pre);
   } else if (warp == 1) {
     if (lane == 0) run_mma<false>(sc, sh, rg);
   } else {
@@ -730,6 +770,7 @@ __device__ inline int sk_owner(long long x, long long W, int n) {
 
 template <bool TF32>
 struct FpSched {
+  static constexpr bool kWeightIsA = true;  // W_proj is the A operand
   const CUtensorMap* mw;
   const CUtensorMap* mx[3];
   long long lo, hi;
@@ -791,10 +832,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_m);
     tma_prefetch_desc(&map_h);
   }
-  cta_setup(sh, stages, tmem_cols);
+  cta_init(sh, stages);
+  int pre = 0;
+  if (threadIdx.x == 0) pre = prefetch_weights<TF32>(sc, sh, rg);
+  cta_start(sh, tmem_cols);
 
   if (warp == 0) {
-    if (lane == 0) run_producer<TF32>(sc, sh, rg);
+    if (lane == 0) run_producer<TF32>(sc, sh, rg, pre);
   } else if (warp == 1) {
     if (lane == 0) run_mma<TF32>(sc, sh, rg);
   } else {

@@ -33,7 +33,10 @@
  *   - Kernels are launched with programmatic stream serialization: one may be
  *     scheduled while the previous kernel on the stream is finishing, but it
  *     reads and writes no global memory before that kernel has completed, so
- *     stream order is unchanged for the caller.
+ *     stream order is unchanged for the caller -- with one exception: the
+ *     weight matrices (w_lm of the LM-head calls, w_proj of eagle_fuse_proj)
+ *     may be read earlier.  They are constants of the model; do not write them
+ *     with a kernel on the same stream right before the call.
  *   - Argument errors are detected on the host before anything is launched
  *     and returned as eagle_status.  Errors that only the device can see (a
  *     malformed tree, a non-finite value, a timed-out wait) are written to the
