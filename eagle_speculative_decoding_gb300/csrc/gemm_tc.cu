@@ -281,7 +281,6 @@ struct LmParams {
   float* part_v;     // [M][cpg][K]    sorted top-k logits (z)
   int* part_i;       // [M][cpg][K]
   int* part_cnt;     // [M][cpg]
-  int* counters;     // [groups]
   int32_t* status;
 };
 
@@ -755,7 +754,6 @@ struct FpParams {
   const float* bias;
   void* out;
   float* part;    // [n_tiles][max_contrib][bn][128]
-  int* counters;  // [n_tiles]
   int32_t* status;
 };
 
@@ -793,6 +791,60 @@ struct FpSched {
   __device__ uint64_t a_policy() const { return l2_policy_evict_first(); }
   __device__ uint64_t b_policy() const { return l2_policy_evict_last(); }
 };
+
+// Sum of the stream-K partials of every tile that several CTAs share, in
+// contributor (slot) order, so the result does not depend on timing; one
+// thread per 4 outputs of a tile, all SMs at once.
+template <bool TF32>
+__global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int tile = blockIdx.y;
+  const long long x0 = (long long)tile * p.nk;
+  const int c_first = sk_owner(x0, p.W, p.n_ctas);
+  const int c_last = sk_owner(x0 + p.nk - 1, p.W, p.n_ctas);
+  if (c_first == c_last) return;  // one CTA held the whole tile and wrote it
+  const int ot = tile % p.n_otiles, gr = tile / p.n_otiles;
+  const int m0 = gr * p.bn, ncol = min(p.bn, p.M - m0);
+  const int f = blockIdx.x * 256 + threadIdx.x;  // float4 index in the [ncol][128] tile
+  if (f >= ncol * 32) return;
+  const int ncontrib = c_last - c_first + 1;
+  const float4* pbase = reinterpret_cast<const float4*>(p.part + ((size_t)tile * p.max_contrib * p.bn) * 128);
+  const size_t slot4 = (size_t)p.bn * 32;  // float4s per contributor slot
+  constexpr int kC = 8;  // contributors loaded per round
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < ncontrib; k0 += kC) {
+    float4 x[kC];
+#pragma unroll
+    for (int k = 0; k < kC; ++k)
+      x[k] = k0 + k < ncontrib ? __ldcg(pbase + (size_t)(k0 + k) * slot4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kC; ++k) {
+      acc.x += x[k].x;
+      acc.y += x[k].y;
+      acc.z += x[k].z;
+      acc.w += x[k].w;
+    }
+  }
+  const int col = f / 32, oo = ot * 128 + (f % 32) * 4;
+  if (p.bias) {
+    acc.x += p.bias[oo];
+    acc.y += p.bias[oo + 1];
+    acc.z += p.bias[oo + 2];
+    acc.w += p.bias[oo + 3];
+  }
+  const size_t idx = (size_t)(m0 + col) * p.d + oo;
+  if (TF32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + idx) = acc;
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + idx) = pk;
+  }
+}
 
 template <bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -842,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) run_mma<TF32>(sc, sh, rg);
   } else {
-    const int q = warp & 3, e = q * 32 + lane, et = threadIdx.x - 64;
+    const int q = warp & 3, e = q * 32 + lane;
     int acc = 0;
     Seg sg;
     for (int si = 0; sc.seg(si, sg); ++si, ++acc) {
@@ -875,10 +927,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
       } else {
-        // stream-K partial: write, then the last contributor of the tile reduces
+        // stream-K partial: write it; fuse_proj_reduce_kernel sums the
+        // contributors of the tile afterwards
         const long long x0 = (long long)sg.tile * p.nk;
         const int c_first = sk_owner(x0, p.W, p.n_ctas);
-        const int c_last = sk_owner(x0 + p.nk - 1, p.W, p.n_ctas);
         const int slot = blockIdx.x - c_first;
         float* part = p.part + (((size_t)sg.tile * p.max_contrib + slot) * bn) * 128;
         for (int c16 = 0; c16 * 16 < ncol; ++c16) {
@@ -893,59 +945,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
-        __threadfence();
-        named_bar(1, kEpiThreads);
-        if (et == 0)
-          sh.flag = (atomicAdd(&p.counters[sg.tile], sg.k1 - sg.k0) + (sg.k1 - sg.k0) == p.nk) ? 1 : 0;
-        named_bar(1, kEpiThreads);
-        if (sh.flag) {
-          __threadfence();
-          // sum the contributors' partials in slot order (deterministic):
-          // thread et owns float4s f = et + 128 i of the [ncol][128] tile
-          const int ncontrib = c_last - c_first + 1;
-          const float4* pbase = reinterpret_cast<const float4*>(
-              p.part + ((size_t)sg.tile * p.max_contrib * bn) * 128);
-          const size_t slot4 = (size_t)bn * 32;  // float4s per contributor slot
-          for (int f0 = et; f0 < ncol * 32; f0 += kEpiThreads * 4) {
-            float4 acc4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) acc4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int k = 0; k < ncontrib; ++k) {
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int f = f0 + u * kEpiThreads;
-                if (f < ncol * 32) {
-                  const float4 x = pbase[(size_t)k * slot4 + f];
-                  acc4[u].x += x.x;
-                  acc4[u].y += x.y;
-                  acc4[u].z += x.z;
-                  acc4[u].w += x.w;
-                }
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int f = f0 + u * kEpiThreads;
-              if (f >= ncol * 32) continue;
-              const int col = f / 32, oo = ot * 128 + (f % 32) * 4;
-              const float b0 = p.bias ? p.bias[oo] : 0.f, b1 = p.bias ? p.bias[oo + 1] : 0.f;
-              const float b2 = p.bias ? p.bias[oo + 2] : 0.f, b3 = p.bias ? p.bias[oo + 3] : 0.f;
-              const size_t idx = (size_t)(m0 + col) * p.d + oo;
-              if (TF32) {
-                *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + idx) =
-                    make_float4(acc4[u].x + b0, acc4[u].y + b1, acc4[u].z + b2, acc4[u].w + b3);
-              } else {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(acc4[u].x + b0, acc4[u].y + b1);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(acc4[u].z + b2, acc4[u].w + b3);
-                uint2 pk;
-                pk.x = *reinterpret_cast<uint32_t*>(&lo);
-                pk.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + idx) = pk;
-              }
-            }
-          }
-        }
-        named_bar(1, kEpiThreads);
       }
     }
   }
@@ -1230,8 +1229,7 @@ extern "C" size_t eagle_fuse_proj_workspace_size(int M, int d, int dtype) {
   size_t best = 0;
   for (int cap = 1; cap <= kMaxCtas; ++cap) {
     const FpPlan f = fp_plan(M, d, esz, cap);
-    const size_t sz = round_up((size_t)f.n_tiles * 4, 256) +
-                      round_up((size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4, 256) + 1024;
+    const size_t sz = round_up((size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4, 256) + 1024;
     best = sz > best ? sz : best;
   }
   return best;
@@ -1273,7 +1271,6 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
 
   char* cur = static_cast<char*>(ws);
   FpParams p;
-  p.counters = static_cast<int*>(ws_carve(cur, (size_t)f.n_tiles * 4));
   p.part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4));
   p.M = M;
   p.d = d;
@@ -1291,9 +1288,10 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   p.out = g;
   p.status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(p.counters, 0, (size_t)f.n_tiles * 4, s) != cudaSuccess) return EAGLE_ERR_CUDA;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, ml, mm, mh, p);
-  note_launch();
+  launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
+         256, 0, s, p);
+  note_launch(2);
   return last_launch_status();
 }
