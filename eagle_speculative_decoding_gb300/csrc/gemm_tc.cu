@@ -264,7 +264,7 @@ __device__ __forceinline__ void cta_teardown(CtaShared& sh, uint32_t tmem_cols, 
 // ====================================================================== LM head
 struct LmParams {
   int M, V, K, groups, ctas_per_group, n_vtiles, nk, stages;
-  int tn;  // vocabulary rows per tile (MMA N, multiple of 16, <= 128)
+  int tn;  // vocabulary rows per tile (MMA N, multiple of 16, <= 256)
   int xr;  // activation rows loaded per stage (group rows rounded up to 16)
   float inv_t;
   // exponential-race mode (verification statistics): the top-K is taken over
@@ -608,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   rg.n = tn;
   rg.nbuf = acc_buffers_for(tn);
   rg.b0 = base;
-  rg.b_stride = kTileA;
+  rg.b_stride = (uint32_t)tn * 128u;
   rg.b_bytes = (uint32_t)tn * 128u;
-  rg.a0 = base + stages * kTileA;
+  rg.a0 = base + stages * (uint32_t)tn * 128u;
   rg.a_stride = rg.a_bytes = (uint32_t)p.xr * 128u;
   (void)gbase;
 
@@ -1037,6 +1037,9 @@ int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d,
   // when V is smaller than one tile per CTA
   int tn = 128;
   while (tn > 16 && (V + tn - 1) / tn < cpg) tn -= 16;
+  // several activation groups re-read every W_U tile from L2: 256-row tiles
+  // (two 256-column TMEM buffers) cut that traffic per flop by a third
+  if (G >= 2 && dtype == EAGLE_BF16 && (V + 255) / 256 >= 4 * cpg) tn = 256;
   const int n_vtiles = (V + tn - 1) / tn;
   if (cpg > n_vtiles) cpg = n_vtiles;
   const int n_ctas = cpg * G;
@@ -1044,10 +1047,11 @@ int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d,
   const int rows_g = M < 128 ? M : 128;           // rows of the largest group
   const int xr = (rows_g + 15) / 16 * 16;         // activation rows loaded per stage
   const size_t xbytes = (size_t)xr * 128;
-  const int stages = dtype == EAGLE_BF16 ? pick_stages(kTileA + xbytes, lists + (kTileA - xbytes)) : 2;
+  const size_t wtile = (size_t)tn * 128;  // bytes of one W_U stage
+  const int stages = dtype == EAGLE_BF16 ? pick_stages(wtile + xbytes, lists + (kTileA - xbytes)) : 2;
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
   const size_t smem = dtype == EAGLE_BF16
-                          ? 1024 + (size_t)stages * (kTileA + xbytes) + (kTileA - xbytes) + lists
+                          ? 1024 + (size_t)stages * (wtile + xbytes) + (kTileA - xbytes) + lists
                           : (size_t)(128 * (kF32Kc + 1) + 16 * kF32Kc) * 4 + lists;
 
   char* cur = static_cast<char*>(ws);

@@ -52,6 +52,7 @@ def _lm_check(b, M, d, V, k, T, dtype, seed, rows=None, bias=False):
     (61, 1024, 8192, 1, 1.0, "bf16"),
     (100, 512, 4096, 32, 1.0, "bf16"),   # k = 32
     (300, 256, 2048, 2, 1.0, "bf16"),    # two activation groups
+    (300, 256, 65536, 3, 1.0, "bf16"),   # three groups, 256-row W_U tiles
 ])
 def test_lmhead_small(M, d, V, k, T, dtype):
     b = need_gpu()
