@@ -30,6 +30,7 @@ with no such pin say "parity unpinned" in their docstring (none at present).
 from .eagle_oracle import (  # noqa: F401
     LOG_EPS32,
     ancestor_mask,
+    draft_input,
     eagle2_tree,
     fuse_proj,
     lmhead_topk,

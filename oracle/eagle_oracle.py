@@ -44,6 +44,41 @@ def fuse_proj(h_low, h_mid, h_high, w_proj, bias=None):
     return g
 
 
+def draft_input(r, token_ids, embed, w_in, bias=None):
+    """Drafter input u = W_I [r; e(x)] (+ bias), fp64.
+
+    [M7.5] section 0x08B: after the feature fusion, the fused state r_t is
+    joined with the embedding of the sampled token and a second FC,
+    u_t = W_I [r_t; e(x_{t+1})] with W_I in R^{d x 2d}, feeds the draft
+    decoder.  [E3] section 3.4 ("Input representation", "Input projection FC
+    layer"): the k-wide feature and the k-wide token embedding from the target
+    model's own table are concatenated to 2k and projected back to k.  [E1]
+    "Draft Model Architecture" (FC layer): the same map with a bias,
+    h = FC([f; e]); [M7.5] section 0x03 "EAGLE-1 Tensor Path" writes it
+    u_t = W_F c_t + b_F.  The embedding is a plain row lookup in the frozen
+    table ([E1] "Draft Model Architecture", Embedding Layer).
+
+    Shapes: r [M, d]; token_ids [M] ints in [0, vocab); embed [vocab, d];
+    w_in [d, 2d] (out x in); bias [d] or None.  Returns [M, d] fp64.
+    """
+    r = np.asarray(r, np.float64)
+    ids = np.asarray(token_ids).astype(np.int64).reshape(-1)
+    table = np.asarray(embed, np.float64)
+    if r.ndim != 2 or ids.shape[0] != r.shape[0]:
+        raise ValueError("r must be [M, d] and token_ids [M]")
+    if ids.size and (ids.min() < 0 or ids.max() >= table.shape[0]):
+        raise ValueError("token id outside the embedding table")
+    e = table[ids]
+    x = np.concatenate([r, e], axis=1)
+    w = np.asarray(w_in, np.float64)
+    if w.shape != (r.shape[1], 2 * r.shape[1]) or table.shape[1] != r.shape[1]:
+        raise ValueError("w_in must be [d, 2d] and embed [vocab, d]")
+    u = x @ w.T
+    if bias is not None:
+        u = u + np.asarray(bias, np.float64)[None, :]
+    return u
+
+
 # ---------------------------------------------------------------------------
 # a5 helper: tree ancestry mask (flatten step)
 # ---------------------------------------------------------------------------
