@@ -29,6 +29,8 @@ _SIGS = {
     "eagle_selftest_wait_timeout": (_I, [ctypes.c_uint, _P, _P]),
     "eagle_fuse_proj_workspace_size": (_Z, [_I, _I, _I]),
     "eagle_fuse_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
+    "eagle_draft_input_workspace_size": (_Z, [_I, _I, _I]),
+    "eagle_draft_input": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "eagle_tree_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                              _I, _F, _I, _I, _P, _Z, _P, _P]),
@@ -134,6 +136,22 @@ def eagle_fuse_proj(h_low, h_mid, h_high, w_proj, g, bias=None, ws=None, status=
         _ptr(h_low), _ptr(h_mid), _ptr(h_high), _ptr(w_proj), _ptr(bias), _ptr(g), M, d, dt,
         _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
     return g
+
+
+def eagle_draft_input_workspace_size(M, d, dtype):
+    return int(lib().eagle_draft_input_workspace_size(M, d, dtype))
+
+
+def eagle_draft_input(r, token_ids, embed, w_in, u, bias=None, ws=None, status=None, stream=None):
+    """u = W_I [r; embed[token_ids]] (+ bias); token_ids int32 [M] on the device."""
+    M, d = r.shape
+    dt = _dtype(r)
+    if ws is None:
+        ws = workspace(eagle_draft_input_workspace_size(M, d, dt), r.device)
+    _check("eagle_draft_input", lib().eagle_draft_input(
+        _ptr(r), _ptr(token_ids), _ptr(embed), embed.shape[0], _ptr(w_in), _ptr(bias), _ptr(u), M, d,
+        dt, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return u
 
 
 # ------------------------------------------------------------------ a2

@@ -107,6 +107,19 @@ __device__ __forceinline__ int prefetch_weights(const Sched& sc, CtaShared& sh, 
   return it;
 }
 
+// Bounded wait for the copies a producer issued into each ring stage before it
+// gave up at iteration `it` (stage s last used by iteration i_s).
+__device__ __forceinline__ void drain_full(CtaShared& sh, int stages, int it) {
+  const int last = it - 1;
+  for (int s = 0; s < stages && s <= last; ++s) {
+    const int i_s = last - ((last - s) % stages);
+    const uint32_t ph = (uint32_t)(i_s / stages) & 1u;
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(&sh.full[s]), ph) && globaltimer_ns() - t0 < 100000000ull) {
+    }
+  }
+}
+
 template <bool TF32, class Sched>
 __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, const Ring& rg,
                                              int pre) {
@@ -140,17 +153,7 @@ __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, con
   }
   return;
 drain:
-  // wait (bounded) for the copies this thread issued into each stage
-  {
-    const int last = it - 1;
-    for (int s = 0; s < stages && s <= last; ++s) {
-      const int i_s = last - ((last - s) % stages);  // last iteration that used stage s
-      const uint32_t ph = (uint32_t)(i_s / stages) & 1u;
-      const unsigned long long t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_u32(&sh.full[s]), ph) && globaltimer_ns() - t0 < 100000000ull) {
-      }
-    }
-  }
+  drain_full(sh, stages, it);
 }
 
 template <bool TF32, class Sched>
@@ -846,6 +849,8 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
   }
 }
 
+// K = nk chunks over nk / nkd segments of width d, segment i read through
+// map_l, map_m, map_h in that order (two segments: map_h is unused).
 template <bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     fuse_proj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_l,
@@ -882,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_l);
     tma_prefetch_desc(&map_m);
-    tma_prefetch_desc(&map_h);
+    if (p.nk > 2 * p.nkd) tma_prefetch_desc(&map_h);
   }
   cta_init(sh, stages);
   int pre = 0;
@@ -973,6 +978,60 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) g[(size_t)m * d + o] = acc + (bias ? bias[o] : 0.f);
+}
+
+// fp32 drafter input FC on the CUDA cores (exact fp32): one warp per output
+// element u[m, o]; lanes stride the feature half and the embedding half of
+// the concatenation [r_m; embed[token_ids[m]]].  An id outside [0, vocab)
+// reads as a zero embedding and records EAGLE_ERR_BAD_TREE.
+__global__ void __launch_bounds__(256)
+    draft_input_f32_kernel(const float* __restrict__ r, const int32_t* __restrict__ ids,
+                           const float* __restrict__ embed, int vocab, const float* __restrict__ w,
+                           const float* __restrict__ bias, float* __restrict__ u, int M, int d,
+                           int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)M * d) return;
+  const int m = (int)(gw / d), o = (int)(gw % d);
+  const int id = ids[m];
+  const bool ok = id >= 0 && id < vocab;
+  if (!ok && lane == 0 && o == 0) set_status(status, EAGLE_ERR_BAD_TREE);
+  const float* wr = w + (size_t)o * 2 * d;
+  const float* er = embed + (size_t)(ok ? id : 0) * d;
+  float acc = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    acc = fmaf(wr[c], r[(size_t)m * d + c], acc);
+    if (ok) acc = fmaf(wr[d + c], er[c], acc);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) u[(size_t)m * d + o] = acc + (bias ? bias[o] : 0.f);
+}
+
+// Token-embedding lookup of the drafter input FC: out[m] = table[ids[m]]
+// (bf16 rows of d elements), 16 bytes per thread over all SMs, so the
+// projection then reads both halves of [r; e] through TMA.  An id outside
+// [0, n_rows) gives a zero row and records EAGLE_ERR_BAD_TREE.
+__global__ void __launch_bounds__(256)
+    embed_gather_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table, int n_rows,
+                        int M, int d, uint4* __restrict__ out, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int cpr = d / 8;  // 16-byte chunks per row
+  const long long n = (long long)M * cpr;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / cpr), c = (int)(i % cpr);
+    const int id = __ldg(ids + m);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (id >= 0 && id < n_rows)
+      v = __ldg(table + (size_t)id * cpr + c);
+    else if (c == 0)
+      set_status(status, EAGLE_ERR_BAD_TREE);
+    out[i] = v;
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -1209,13 +1268,14 @@ struct FpPlan {
   int bn, G, n_otiles, nk, nkd, n_tiles, n_ctas, max_contrib;
   long long W;
 };
-FpPlan fp_plan(int M, int d, int esz, int n_ctas_cap) {
+// nseg: K segments of width d (3 for the feature fusion, 2 for the drafter input)
+FpPlan fp_plan(int M, int d, int esz, int n_ctas_cap, int nseg) {
   FpPlan f;
   f.bn = pick_bn(M, &f.G);
   const int bke = 128 / esz;
   f.n_otiles = d / 128;
   f.nkd = d / bke;
-  f.nk = 3 * f.nkd;
+  f.nk = nseg * f.nkd;
   f.n_tiles = f.n_otiles * f.G;
   f.W = (long long)f.n_tiles * f.nk;
   f.n_ctas = (int)(f.W < n_ctas_cap ? f.W : n_ctas_cap);
@@ -1224,19 +1284,85 @@ FpPlan fp_plan(int M, int d, int esz, int n_ctas_cap) {
   if (f.max_contrib > f.n_ctas) f.max_contrib = f.n_ctas;
   return f;
 }
-}  // namespace
 
-extern "C" size_t eagle_fuse_proj_workspace_size(int M, int d, int dtype) {
+// gathered: room for the [M, d] looked-up embedding rows (drafter input FC)
+size_t fp_workspace(int M, int d, int dtype, int nseg, bool gathered) {
   if (M <= 0 || d <= 0 || d % 128) return 0;
   const int esz = dtype == EAGLE_BF16 ? 2 : 4;
   // sized for the largest grid the library launches (kMaxCtas CTAs)
   size_t best = 0;
   for (int cap = 1; cap <= kMaxCtas; ++cap) {
-    const FpPlan f = fp_plan(M, d, esz, cap);
-    const size_t sz = round_up((size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4, 256) + 1024;
+    const FpPlan f = fp_plan(M, d, esz, cap, nseg);
+    const size_t sz = round_up((size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4, 256) + 1024 +
+                      (gathered ? round_up((size_t)M * d * esz, 256) : 0);
     best = sz > best ? sz : best;
   }
   return best;
+}
+
+// bf16 tensor-core launch shared by both projections: xs[0..nseg) are the
+// [M, d] activation segments, read by TMA; with `ids` set the last segment is
+// first looked up from `table` ([n_rows, d]) into the workspace.
+int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const void* table, int n_rows,
+                   const void* w, const float* bias, void* out, int M, int d, void* ws, int32_t* dev_status,
+                   cudaStream_t s) {
+  constexpr int esz = 2, bke = 64;
+  int sms = sm_count();
+  if (sms <= 0) return EAGLE_ERR_CUDA;
+  const FpPlan f = fp_plan(M, d, esz, sms > kMaxCtas ? kMaxCtas : sms, nseg);
+  const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
+  if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
+  const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
+
+  char* cur = static_cast<char*>(ws);
+  float* part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4));
+  const void* seg[3] = {xs[0], xs[1], nseg > 2 ? xs[2] : xs[0]};
+  void* gathered = nullptr;
+  if (ids) {
+    gathered = ws_carve(cur, (size_t)M * d * esz);
+    seg[nseg - 1] = gathered;
+  }
+  CUtensorMap mw, mx[3];
+  if (!make_tmap_2d(&mw, w, esz, (uint64_t)d, (uint64_t)nseg * d, 128, (uint32_t)bke)) return EAGLE_ERR_CUDA;
+  for (int i = 0; i < 3; ++i)
+    if (!make_tmap_2d(&mx[i], seg[i], esz, (uint64_t)M, (uint64_t)d, (uint32_t)f.bn, (uint32_t)bke))
+      return EAGLE_ERR_CUDA;
+
+  if (ids) {
+    const long long chunks = (long long)M * (d / 8);
+    const long long blocks = (chunks + 255) / 256;
+    launch(embed_gather_kernel, (unsigned)(blocks < 4LL * sms ? blocks : 4LL * sms), 256, 0, s, ids,
+           static_cast<const uint4*>(table), n_rows, M, d, static_cast<uint4*>(gathered), dev_status);
+    note_launch();
+  }
+  FpParams p;
+  p.part = part;
+  p.M = M;
+  p.d = d;
+  p.bn = f.bn;
+  p.groups = f.G;
+  p.n_otiles = f.n_otiles;
+  p.nk = f.nk;
+  p.nkd = f.nkd;
+  p.n_tiles = f.n_tiles;
+  p.n_ctas = f.n_ctas;
+  p.max_contrib = f.max_contrib;
+  p.stages = stages;
+  p.W = f.W;
+  p.bias = bias;
+  p.out = out;
+  p.status = dev_status;
+  cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
+  launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
+         256, 0, s, p);
+  note_launch(2);
+  return last_launch_status();
+}
+}  // namespace
+
+extern "C" size_t eagle_fuse_proj_workspace_size(int M, int d, int dtype) {
+  return fp_workspace(M, d, dtype, 3, false);
 }
 
 extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void* h_high,
@@ -1257,45 +1383,33 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
     note_launch();
     return last_launch_status();
   }
-  const int esz = 2;
-  const int bke = 64;
-  int sms = sm_count();
-  if (sms <= 0) return EAGLE_ERR_CUDA;
-  const FpPlan f = fp_plan(M, d, esz, sms > kMaxCtas ? kMaxCtas : sms);
-  const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
-  if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
-  const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
+  const void* xs[3] = {h_low, h_mid, h_high};
+  return fp_launch_bf16(xs, 3, nullptr, nullptr, 0, w_proj, bias, g, M, d, ws, dev_status,
+                        static_cast<cudaStream_t>(stream));
+}
 
-  CUtensorMap mw, ml, mm, mh;
-  if (!make_tmap_2d(&mw, w_proj, esz, (uint64_t)d, (uint64_t)3 * d, 128, (uint32_t)bke) ||
-      !make_tmap_2d(&ml, h_low, esz, (uint64_t)M, (uint64_t)d, (uint32_t)f.bn, (uint32_t)bke) ||
-      !make_tmap_2d(&mm, h_mid, esz, (uint64_t)M, (uint64_t)d, (uint32_t)f.bn, (uint32_t)bke) ||
-      !make_tmap_2d(&mh, h_high, esz, (uint64_t)M, (uint64_t)d, (uint32_t)f.bn, (uint32_t)bke))
-    return EAGLE_ERR_CUDA;
+extern "C" size_t eagle_draft_input_workspace_size(int M, int d, int dtype) {
+  return fp_workspace(M, d, dtype, 2, true);
+}
 
-  char* cur = static_cast<char*>(ws);
-  FpParams p;
-  p.part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4));
-  p.M = M;
-  p.d = d;
-  p.bn = f.bn;
-  p.groups = f.G;
-  p.n_otiles = f.n_otiles;
-  p.nk = f.nk;
-  p.nkd = f.nkd;
-  p.n_tiles = f.n_tiles;
-  p.n_ctas = f.n_ctas;
-  p.max_contrib = f.max_contrib;
-  p.stages = stages;
-  p.W = f.W;
-  p.bias = bias;
-  p.out = g;
-  p.status = dev_status;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, ml, mm, mh, p);
-  launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
-         256, 0, s, p);
-  note_launch(2);
-  return last_launch_status();
+extern "C" int eagle_draft_input(const void* r, const int32_t* token_ids, const void* embed, int vocab,
+                                 const void* w_in, const float* bias, void* u, int M, int d, int dtype,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!r || !token_ids || !embed || !w_in || !u) return EAGLE_ERR_INVALID_ARG;
+  if (M <= 0 || d <= 0 || vocab <= 0) return EAGLE_ERR_INVALID_ARG;
+  if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return EAGLE_ERR_INVALID_ARG;
+  if (M > 4096 || d % 128 || d > 16384) return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned16(r) || !aligned16(embed) || !aligned16(w_in)) return EAGLE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < eagle_draft_input_workspace_size(M, d, dtype)) return EAGLE_ERR_WORKSPACE;
+  if (dtype == EAGLE_FP32) {
+    const long long outs = (long long)M * d;
+    launch(draft_input_f32_kernel, (unsigned)((outs + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream),
+           (const float*)r, token_ids, (const float*)embed, vocab, (const float*)w_in, bias, (float*)u, M, d,
+           dev_status);
+    note_launch();
+    return last_launch_status();
+  }
+  const void* xs[2] = {r, nullptr};
+  return fp_launch_bf16(xs, 2, token_ids, embed, vocab, w_in, bias, u, M, d, ws, dev_status,
+                        static_cast<cudaStream_t>(stream));
 }

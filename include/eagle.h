@@ -3,7 +3,9 @@
  *
  * One tree-verify round of EAGLE-family speculative decoding is served by
  * six calls (plus eagle_lmhead_verify_stats / eagle_tree_verify_stats, which
- * serve stochastic verification without materialised logits):
+ * serve stochastic verification without materialised logits, eagle_tree_commit
+ * which publishes the accepted path, and eagle_draft_input, the drafter's
+ * token-embedding input FC):
  *   eagle_fuse_proj             EAGLE-3 fused feature g = W_proj [h_low; h_mid; h_high]
  *   eagle_tree_attn             tree-masked attention vs a paged KV cache + the tree rows
  *   eagle_lmhead_topk           LM-head GEMM with fused per-row top-k and log-softmax
@@ -34,9 +36,10 @@
  *     scheduled while the previous kernel on the stream is finishing, but it
  *     reads and writes no global memory before that kernel has completed, so
  *     stream order is unchanged for the caller -- with one exception: the
- *     weight matrices (w_lm of the LM-head calls, w_proj of eagle_fuse_proj)
- *     may be read earlier.  They are constants of the model; do not write them
- *     with a kernel on the same stream right before the call.
+ *     weight matrices (w_lm of the LM-head calls, w_proj of eagle_fuse_proj,
+ *     w_in of eagle_draft_input) may be read earlier.  They are constants of
+ *     the model; do not write them with a kernel on the same stream right
+ *     before the call.
  *   - Argument errors are detected on the host before anything is launched
  *     and returned as eagle_status.  Errors that only the device can see (a
  *     malformed tree, a non-finite value, a timed-out wait) are written to the
@@ -119,6 +122,40 @@ int eagle_fuse_proj(const void* h_low, const void* h_mid, const void* h_high,
                     const void* w_proj, const float* bias, void* g, int M, int d,
                     int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_draft_input -- drafter input FC with the token-embedding lookup fused.
+ *   u[i, o] = sum_c W[o, c] r[i, c] + W[o, d+c] embed[token_ids[i], c]
+ *             (+ bias[o])
+ * [M7.5] section 0x08B (u_t = W_I [r_t; e(x_{t+1})], W_I in R^{d x 2d}: the
+ * fused state joined with the embedding of the sampled token); [E3] section
+ * 3.4 "Input projection FC layer" ([g; e] in R^{2k} projected back to k);
+ * [E1] "Draft Model Architecture" (FC layer with bias over [f; e], embedding
+ * table frozen from the target model); [M7.5] section 0x03 "EAGLE-1 Tensor
+ * Path" (u_t = W_F c_t + b_F).
+ *
+ *   r         : [M, d]      fused feature (or the drafter's own output a_t at
+ *                           drafted positions), dtype `dtype`
+ *   token_ids : [M] int32   token per row, in [0, vocab)
+ *   embed     : [vocab, d]  token-embedding table, dtype `dtype`
+ *   w_in      : [d, 2d]     row o = output feature o (out x in)
+ *   bias      : [d] fp32, or NULL
+ *   u         : [M, d]      output, dtype `dtype`
+ * The concatenation is never materialised: a lookup kernel over all SMs
+ * copies the M embedding rows into `ws`, and the K loop of the tensor-core
+ * projection then reads r and those rows through two tensor maps (weights
+ * stream as in eagle_fuse_proj).  bf16 runs on the tensor cores with fp32
+ * accumulation; fp32 on the CUDA cores in exact fp32 arithmetic, where the
+ * lookup is fused into the dot products.
+ * Device-detected: a token id outside [0, vocab) -> EAGLE_ERR_BAD_TREE (that
+ * row's embedding half reads as zeros).  w_in may be read before the previous
+ * kernel on the stream has completed (see the conventions above).
+ * Limits: 1 <= M <= 4096, d % 128 == 0, d <= 16384.
+ * ---------------------------------------------------------------------- */
+size_t eagle_draft_input_workspace_size(int M, int d, int dtype);
+int eagle_draft_input(const void* r, const int32_t* token_ids, const void* embed, int vocab,
+                      const void* w_in, const float* bias, void* u, int M, int d, int dtype,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * eagle_tree_attn -- attention of the tree rows against the committed prefix

@@ -28,7 +28,7 @@ def declared():
 def test_header_declares_the_hot_path_calls():
     names = declared()
     for n in ("eagle_fuse_proj", "eagle_tree_attn", "eagle_lmhead_topk", "eagle_tree_expand",
-              "eagle_tree_expand_finalize", "eagle_tree_verify"):
+              "eagle_tree_expand_finalize", "eagle_tree_verify", "eagle_draft_input"):
         assert n in names
 
 
@@ -66,6 +66,13 @@ def test_host_validation_without_gpu(L):
     # fuse_proj: d not a multiple of 128
     assert L.eagle_fuse_proj(p, p, p, p, N, p, 4, 100, 1, N, 0, N, N) == 2
     assert L.eagle_fuse_proj(p, p, p, p, N, p, 4, 128, 1, N, 0, N, N) == 3
+    # draft_input: null token ids, vocab 0, d not a multiple of 128, M too large, no ws
+    assert L.eagle_draft_input(p, N, p, 10, p, N, p, 4, 128, 1, N, 0, N, N) == 1
+    assert L.eagle_draft_input(p, p, p, 0, p, N, p, 4, 128, 1, N, 0, N, N) == 1
+    assert L.eagle_draft_input(p, p, p, 10, p, N, p, 4, 100, 1, N, 0, N, N) == 2
+    assert L.eagle_draft_input(p, p, p, 10, p, N, p, 4097, 128, 1, N, 0, N, N) == 2
+    assert L.eagle_draft_input(p, p, p, 10, p, N, p, 4, 128, 1, N, 0, N, N) == 3
+    assert L.eagle_draft_input_workspace_size(4, 128, 1) > 0
     # attention: R > 64, D not in {64, 128}, page size != 16, Hq % Hkv
     base = [p, p, p, p, p, 4, p, 2, p, p, p, N]
     assert L.eagle_tree_attn(*base, 1, 65, 4, 2, 128, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 2
