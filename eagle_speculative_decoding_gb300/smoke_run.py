@@ -80,6 +80,18 @@ def run(device="cuda:0"):
     ref_g = oracle.fuse_proj(*(h.numpy() for h in hs), w_proj.numpy())
     assert np.abs(g.cpu().numpy() - ref_g).max() < 1e-2 * (np.abs(ref_g).max() + 1), "fuse_proj"
 
+    # drafter input FC over the frontier rows, fp32 and bf16 (tensor cores)
+    w_in = synth.normal((d, 2 * d), synth.WEIGHT_STD, dt, gen)
+    toks = synth.random_tokens((B * width,), V, gen)
+    for ddt, tol in ((torch.float32, 1e-4), (torch.bfloat16, 2e-2)):
+        r_in = g[: B * width].to(ddt)
+        u = torch.empty((B * width, d), dtype=ddt, device=dev)
+        b.eagle_draft_input(r_in, toks.to(dev), w_lm.to(dev, ddt), w_in.to(dev, ddt), u, status=status)
+        ref_u = oracle.draft_input(r_in.float().cpu().numpy(), toks.numpy(), w_lm.to(ddt).float().numpy(),
+                                   w_in.to(ddt).float().numpy())
+        err = np.abs(u.float().cpu().numpy() - ref_u).max() / (np.abs(ref_u).max() + 1e-30)
+        assert err < tol, ("draft_input", ddt, err)
+
     am = torch.empty((B * R, 1), dtype=torch.int32, device=dev)
     amlp = torch.empty((B * R, 1), dtype=torch.float32, device=dev)
     b.eagle_lmhead_topk(g, w_lm_d, 1, am, amlp, status=status)
