@@ -31,9 +31,13 @@ from .eagle_oracle import (  # noqa: F401
     LOG_EPS32,
     ancestor_mask,
     draft_input,
+    draft_layer,
     eagle2_tree,
     fuse_proj,
     lmhead_topk,
+    rms_norm,
+    rope,
+    silu,
     tree_attn,
     tree_expand_finalize,
     tree_expand_init,

@@ -738,3 +738,101 @@ def tree_commit(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree, path_ro
                 out_f[b, i] = f[b * R + row]
         ctx[b] += n
     return dict(k_cache=kc, v_cache=vc, ctx_lens=ctx, features=out_f)
+
+
+# ---------------------------------------------------------------------------
+# drafter decoder layer (the step after the input FC)
+# ---------------------------------------------------------------------------
+# [E3] section 3.4 "The transformer decoder layer": one standard decoder layer
+# -- self-attention and a position-wise feed-forward sublayer, each with a
+# residual connection and normalisation.  The pages fix no further detail;
+# the reading taken is the form of the LLaMA-family targets the pages
+# evaluate ([E3] section 6, Limitation 6: pre-normalisation, SwiGLU, rotary
+# position embeddings, grouped-query attention): RMSNorm before each
+# sublayer, rotate-half RoPE on q and k, GQA attention, SwiGLU feed-forward,
+# no biases.  The attention is tree attention over the drafter's own KV
+# ([M7.5] 0x03C "The Drafter Has Its Own KV State"; 0x05B: the nodes of one
+# depth are expanded in one pass with tree attention, each node holding its
+# position and its draft-KV row).
+
+
+def rms_norm(x, w, eps):
+    """y = x / sqrt(mean(x^2) + eps) * w over the last axis, fp64."""
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(w, np.float64)
+
+
+def rope(x, positions, theta):
+    """Rotate-half rotary embedding of x [..., D] at integer positions
+    (broadcast over x.shape[:-1]): element pair (i, i + D/2) is rotated by
+    the angle position * theta^(-2i/D)."""
+    x = np.asarray(x, np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    inv = np.power(float(theta), -2.0 * np.arange(half) / D)
+    ang = np.asarray(positions, np.float64)[..., None] * inv
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def silu(x):
+    x = np.asarray(x, np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def draft_layer(x, weights, positions, k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree,
+                tree_mask, r0, Hq, Hkv, eps=1e-5, theta=500000.0, page_size=16, store=None):
+    """One drafter decoder layer over the B x W new tree nodes of one depth.
+
+    x [B*W, d] rows of the input (request-major).  weights: dict with
+    norm1 [d], qkv [(Hq + 2 Hkv) D, d] (q heads, then k heads, then v heads),
+    o [d, Hq D], norm2 [d], gu [2 I, d] (gate rows, then up rows), down [d, I].
+    positions [B, W].  The drafter's prefix K/V come from the paged cache;
+    k_tree / v_tree [B, Rmax, Hkv, D] hold the earlier nodes' rows, and the new
+    node j of request b takes row r0 + j; tree_mask [B, Rmax] (bit i of row r:
+    row i is visible).  ``store``: optional rounding applied wherever the
+    layer stores an intermediate tensor (identity by default).
+
+    Returns (out [B*W, d], k_new [B, W, Hkv, D], v_new [B, W, Hkv, D]).
+    """
+    st = store if store is not None else (lambda a: a)
+    x = np.asarray(x, np.float64)
+    positions = np.asarray(positions)
+    B, W = positions.shape
+    M, d = x.shape
+    D = np.asarray(weights["qkv"]).shape[0] // (Hq + 2 * Hkv)
+    Rmax = k_tree.shape[1]
+    if M != B * W or r0 < 0 or r0 + W > Rmax:
+        raise ValueError("x must be [B*W, d] and the new rows must fit the tree arrays")
+    h = st(rms_norm(x, weights["norm1"], eps))
+    qkv = st(h @ np.asarray(weights["qkv"], np.float64).T)
+    q = qkv[:, :Hq * D].reshape(M, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(M, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(M, Hkv, D)
+    pos = positions.reshape(M)[:, None]
+    q, k = st(rope(q, pos, theta)), st(rope(k, pos, theta))
+    kt = np.array(k_tree, np.float64)
+    vt = np.array(v_tree, np.float64)
+    qt = np.zeros((B, Rmax, Hq, D))
+    for b in range(B):
+        for j in range(W):
+            kt[b, r0 + j] = k[b * W + j]
+            vt[b, r0 + j] = v[b * W + j]
+            qt[b, r0 + j] = q[b * W + j]
+    want = [(b, r0 + j, hh) for b in range(B) for j in range(W) for hh in range(Hq)]
+    att = tree_attn(qt, kt, vt, k_cache, v_cache, block_table, ctx_lens, tree_mask,
+                    page_size=page_size, sample=want)
+    a = np.zeros((M, Hq, D))
+    for b in range(B):
+        for j in range(W):
+            for hh in range(Hq):
+                a[b * W + j, hh] = att[(b, r0 + j, hh)][0]
+    a = st(a.reshape(M, Hq * D))
+    x1 = st(x + a @ np.asarray(weights["o"], np.float64).T)
+    h2 = st(rms_norm(x1, weights["norm2"], eps))
+    I = np.asarray(weights["down"]).shape[1]
+    gu = st(h2 @ np.asarray(weights["gu"], np.float64).T)
+    act = st(silu(gu[:, :I]) * gu[:, I:])
+    out = st(x1 + act @ np.asarray(weights["down"], np.float64).T)
+    return out, k.reshape(B, W, Hkv, D), v.reshape(B, W, Hkv, D)
