@@ -30,6 +30,11 @@ _SIGS = {
     "eagle_fuse_proj_workspace_size": (_Z, [_I, _I, _I]),
     "eagle_fuse_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_draft_input_workspace_size": (_Z, [_I, _I, _I]),
+    "eagle_linear_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "eagle_linear": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P, _P]),
+    "eagle_draft_layer_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "eagle_draft_layer": (_I, [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P,
+                               _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_draft_input": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "eagle_tree_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
@@ -152,6 +157,50 @@ def eagle_draft_input(r, token_ids, embed, w_in, u, bias=None, ws=None, status=N
         _ptr(r), _ptr(token_ids), _ptr(embed), embed.shape[0], _ptr(w_in), _ptr(bias), _ptr(u), M, d,
         dt, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
     return u
+
+
+def eagle_linear_workspace_size(M, n_out, k_in, dtype):
+    return int(lib().eagle_linear_workspace_size(M, n_out, k_in, dtype))
+
+
+def eagle_linear(x, w, y, bias=None, residual=None, ws=None, status=None, stream=None):
+    """y = x w^T (+ bias) (+ residual)."""
+    M, k_in = x.shape
+    n_out = w.shape[0]
+    dt = _dtype(x)
+    if ws is None:
+        ws = workspace(eagle_linear_workspace_size(M, n_out, k_in, dt), x.device)
+    _check("eagle_linear", lib().eagle_linear(
+        _ptr(x), _ptr(w), _ptr(bias), _ptr(residual), _ptr(y), M, n_out, k_in, dt, _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+    return y
+
+
+def eagle_draft_layer_workspace_size(B, W, d, Hq, Hkv, D, I, Rmax, max_pages, dtype):
+    return int(lib().eagle_draft_layer_workspace_size(B, W, d, Hq, Hkv, D, I, Rmax, max_pages, dtype))
+
+
+def eagle_draft_layer(x, weights, positions, k_cache, v_cache, block_table, ctx_lens, q_tree, k_tree,
+                      v_tree, tree_mask, r0, out, eps=1e-5, theta=500000.0, ws=None, status=None,
+                      stream=None):
+    """The drafter's decoder layer over the B x W new nodes of one depth.
+    weights: dict norm1, qkv, o, norm2, gu, down (see include/eagle.h)."""
+    B, W = positions.shape
+    d = x.shape[1]
+    Rmax, Hq, D = q_tree.shape[1], q_tree.shape[2], q_tree.shape[3]
+    Hkv = k_tree.shape[2]
+    I = weights["down"].shape[1]
+    dt = _dtype(x)
+    if ws is None:
+        ws = workspace(eagle_draft_layer_workspace_size(B, W, d, Hq, Hkv, D, I, Rmax, block_table.shape[1], dt),
+                       x.device)
+    _check("eagle_draft_layer", lib().eagle_draft_layer(
+        _ptr(x), _ptr(weights["norm1"]), _ptr(weights["qkv"]), _ptr(weights["o"]), _ptr(weights["norm2"]),
+        _ptr(weights["gu"]), _ptr(weights["down"]), eps, theta, _ptr(positions), _ptr(k_cache),
+        _ptr(v_cache), k_cache.shape[0], _ptr(block_table), block_table.shape[1], _ptr(ctx_lens),
+        _ptr(q_tree), _ptr(k_tree), _ptr(v_tree), _ptr(tree_mask), r0, Rmax, _ptr(out), B, W, d, Hq, Hkv, D,
+        I, dt, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return out
 
 
 # ------------------------------------------------------------------ a2

@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libeagle_gb300.so")
-SOURCES = ["common.cu", "tree_verify.cu", "tree_expand.cu", "tree_attn.cu", "gemm_tc.cu", "tree_commit.cu"]
+SOURCES = ["common.cu", "tree_verify.cu", "tree_expand.cu", "tree_attn.cu", "gemm_tc.cu", "tree_commit.cu",
+           "draft_layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

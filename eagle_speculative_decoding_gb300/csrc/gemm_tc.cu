@@ -285,6 +285,7 @@ struct LmParams {
   int* part_i;       // [M][cpg][K]
   int* part_cnt;     // [M][cpg]
   int32_t* status;
+  const void* residual;  // [M, d] of the output dtype added to the result, or null
 };
 
 // LM head, not swapped: the (up to) 128 activation rows of a group are the
@@ -752,12 +753,13 @@ __global__ void __launch_bounds__(kEpiThreads)
 
 // ==================================================================== fuse_proj
 struct FpParams {
-  int M, d, bn, groups, n_otiles, nk, nkd, n_tiles, n_ctas, max_contrib, stages;
+  int M, d, bn, groups, n_otiles, nk, nkd, n_tiles, n_ctas, max_contrib, stages;  // d: output width
   long long W;  // total chunks = n_tiles * nk
   const float* bias;
   void* out;
   float* part;    // [n_tiles][max_contrib][bn][128]
   int32_t* status;
+  const void* residual;  // [M, d] of the output dtype added to the result, or null
 };
 
 __host__ __device__ inline long long sk_lo(long long c, long long W, int n) { return c * W / n; }
@@ -837,6 +839,23 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
     acc.w += p.bias[oo + 3];
   }
   const size_t idx = (size_t)(m0 + col) * p.d + oo;
+  if (p.residual) {
+    if (TF32) {
+      const float4 rv = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.residual) + idx);
+      acc.x += rv.x;
+      acc.y += rv.y;
+      acc.z += rv.z;
+      acc.w += rv.w;
+    } else {
+      const uint2 rv = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.residual) + idx);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rv.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rv.y));
+      acc.x += a.x;
+      acc.y += a.y;
+      acc.z += b.x;
+      acc.w += b.y;
+    }
+  }
   if (TF32) {
     *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + idx) = acc;
   } else {
@@ -921,10 +940,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = c16 * 16 + j;
             if (col < ncol) {
               const size_t idx = (size_t)(m0 + col) * p.d + o;
+              float y = v[j] + bias_o;
+              if (p.residual)
+                y += TF32 ? reinterpret_cast<const float*>(p.residual)[idx]
+                          : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.residual)[idx]);
               if (TF32)
-                reinterpret_cast<float*>(p.out)[idx] = v[j] + bias_o;
+                reinterpret_cast<float*>(p.out)[idx] = y;
               else
-                reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16(v[j] + bias_o);
+                reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16(y);
             }
           }
         }
@@ -1031,6 +1054,29 @@ __global__ void __launch_bounds__(256)
     else if (c == 0)
       set_status(status, EAGLE_ERR_BAD_TREE);
     out[i] = v;
+  }
+}
+
+// fp32 linear layer on the CUDA cores (exact fp32): one warp per output
+// element y[m, o] = sum_c w[o, c] x[m, c] (+ bias[o]) (+ residual[m, o]).
+__global__ void __launch_bounds__(256)
+    linear_f32_kernel(const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
+                      const float* residual, float* y, int M, int n_out, int k_in) {
+  pdl_wait();
+  pdl_trigger();
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)M * n_out) return;
+  const int m = (int)(gw / n_out), o = (int)(gw % n_out);
+  const float* wr = w + (size_t)o * k_in;
+  const float* xr = x + (size_t)m * k_in;
+  float acc = 0.f;
+  for (int c = lane; c < k_in; c += 32) acc = fmaf(wr[c], xr[c], acc);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    const size_t idx = (size_t)m * n_out + o;
+    y[idx] = acc + (bias ? bias[o] : 0.f) + (residual ? residual[idx] : 0.f);
   }
 }
 
@@ -1269,12 +1315,13 @@ struct FpPlan {
   long long W;
 };
 // nseg: K segments of width d (3 for the feature fusion, 2 for the drafter input)
-FpPlan fp_plan(int M, int d, int esz, int n_ctas_cap, int nseg) {
+// n_out output features (multiple of 128); nseg K segments of kseg inputs each
+FpPlan fp_plan(int M, int n_out, int kseg, int esz, int n_ctas_cap, int nseg) {
   FpPlan f;
   f.bn = pick_bn(M, &f.G);
   const int bke = 128 / esz;
-  f.n_otiles = d / 128;
-  f.nkd = d / bke;
+  f.n_otiles = n_out / 128;
+  f.nkd = kseg / bke;
   f.nk = nseg * f.nkd;
   f.n_tiles = f.n_otiles * f.G;
   f.W = (long long)f.n_tiles * f.nk;
@@ -1286,15 +1333,15 @@ FpPlan fp_plan(int M, int d, int esz, int n_ctas_cap, int nseg) {
 }
 
 // gathered: room for the [M, d] looked-up embedding rows (drafter input FC)
-size_t fp_workspace(int M, int d, int dtype, int nseg, bool gathered) {
-  if (M <= 0 || d <= 0 || d % 128) return 0;
+size_t fp_workspace(int M, int n_out, int kseg, int dtype, int nseg, bool gathered) {
+  if (M <= 0 || n_out <= 0 || kseg <= 0 || n_out % 128 || kseg % 64) return 0;
   const int esz = dtype == EAGLE_BF16 ? 2 : 4;
   // sized for the largest grid the library launches (kMaxCtas CTAs)
   size_t best = 0;
   for (int cap = 1; cap <= kMaxCtas; ++cap) {
-    const FpPlan f = fp_plan(M, d, esz, cap, nseg);
+    const FpPlan f = fp_plan(M, n_out, kseg, esz, cap, nseg);
     const size_t sz = round_up((size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4, 256) + 1024 +
-                      (gathered ? round_up((size_t)M * d * esz, 256) : 0);
+                      (gathered ? round_up((size_t)M * kseg * esz, 256) : 0);
     best = sz > best ? sz : best;
   }
   return best;
@@ -1304,41 +1351,42 @@ size_t fp_workspace(int M, int d, int dtype, int nseg, bool gathered) {
 // [M, d] activation segments, read by TMA; with `ids` set the last segment is
 // first looked up from `table` ([n_rows, d]) into the workspace.
 int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const void* table, int n_rows,
-                   const void* w, const float* bias, void* out, int M, int d, void* ws, int32_t* dev_status,
-                   cudaStream_t s) {
+                   const void* w, const float* bias, const void* residual, void* out, int M, int n_out,
+                   int kseg, void* ws, int32_t* dev_status, cudaStream_t s) {
   constexpr int esz = 2, bke = 64;
   int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
-  const FpPlan f = fp_plan(M, d, esz, sms > kMaxCtas ? kMaxCtas : sms, nseg);
+  const FpPlan f = fp_plan(M, n_out, kseg, esz, sms > kMaxCtas ? kMaxCtas : sms, nseg);
   const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
   const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
 
   char* cur = static_cast<char*>(ws);
   float* part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4));
-  const void* seg[3] = {xs[0], xs[1], nseg > 2 ? xs[2] : xs[0]};
+  const void* seg[3] = {xs[0], nseg > 1 ? xs[1] : xs[0], nseg > 2 ? xs[2] : xs[0]};
   void* gathered = nullptr;
   if (ids) {
-    gathered = ws_carve(cur, (size_t)M * d * esz);
+    gathered = ws_carve(cur, (size_t)M * kseg * esz);
     seg[nseg - 1] = gathered;
   }
   CUtensorMap mw, mx[3];
-  if (!make_tmap_2d(&mw, w, esz, (uint64_t)d, (uint64_t)nseg * d, 128, (uint32_t)bke)) return EAGLE_ERR_CUDA;
+  if (!make_tmap_2d(&mw, w, esz, (uint64_t)n_out, (uint64_t)nseg * kseg, 128, (uint32_t)bke))
+    return EAGLE_ERR_CUDA;
   for (int i = 0; i < 3; ++i)
-    if (!make_tmap_2d(&mx[i], seg[i], esz, (uint64_t)M, (uint64_t)d, (uint32_t)f.bn, (uint32_t)bke))
+    if (!make_tmap_2d(&mx[i], seg[i], esz, (uint64_t)M, (uint64_t)kseg, (uint32_t)f.bn, (uint32_t)bke))
       return EAGLE_ERR_CUDA;
 
   if (ids) {
-    const long long chunks = (long long)M * (d / 8);
+    const long long chunks = (long long)M * (kseg / 8);
     const long long blocks = (chunks + 255) / 256;
     launch(embed_gather_kernel, (unsigned)(blocks < 4LL * sms ? blocks : 4LL * sms), 256, 0, s, ids,
-           static_cast<const uint4*>(table), n_rows, M, d, static_cast<uint4*>(gathered), dev_status);
+           static_cast<const uint4*>(table), n_rows, M, kseg, static_cast<uint4*>(gathered), dev_status);
     note_launch();
   }
   FpParams p;
   p.part = part;
   p.M = M;
-  p.d = d;
+  p.d = n_out;
   p.bn = f.bn;
   p.groups = f.G;
   p.n_otiles = f.n_otiles;
@@ -1350,6 +1398,7 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.stages = stages;
   p.W = f.W;
   p.bias = bias;
+  p.residual = residual;
   p.out = out;
   p.status = dev_status;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1362,7 +1411,7 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
 }  // namespace
 
 extern "C" size_t eagle_fuse_proj_workspace_size(int M, int d, int dtype) {
-  return fp_workspace(M, d, dtype, 3, false);
+  return fp_workspace(M, d, d, dtype, 3, false);
 }
 
 extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void* h_high,
@@ -1384,12 +1433,12 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
     return last_launch_status();
   }
   const void* xs[3] = {h_low, h_mid, h_high};
-  return fp_launch_bf16(xs, 3, nullptr, nullptr, 0, w_proj, bias, g, M, d, ws, dev_status,
+  return fp_launch_bf16(xs, 3, nullptr, nullptr, 0, w_proj, bias, nullptr, g, M, d, d, ws, dev_status,
                         static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t eagle_draft_input_workspace_size(int M, int d, int dtype) {
-  return fp_workspace(M, d, dtype, 2, true);
+  return fp_workspace(M, d, d, dtype, 2, true);
 }
 
 extern "C" int eagle_draft_input(const void* r, const int32_t* token_ids, const void* embed, int vocab,
@@ -1410,6 +1459,33 @@ extern "C" int eagle_draft_input(const void* r, const int32_t* token_ids, const 
     return last_launch_status();
   }
   const void* xs[2] = {r, nullptr};
-  return fp_launch_bf16(xs, 2, token_ids, embed, vocab, w_in, bias, u, M, d, ws, dev_status,
+  return fp_launch_bf16(xs, 2, token_ids, embed, vocab, w_in, bias, nullptr, u, M, d, d, ws, dev_status,
                         static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t eagle_linear_workspace_size(int M, int n_out, int k_in, int dtype) {
+  return fp_workspace(M, n_out, k_in, dtype, 1, false);
+}
+
+extern "C" int eagle_linear(const void* x, const void* w, const float* bias, const void* residual, void* y,
+                            int M, int n_out, int k_in, int dtype, void* ws, size_t ws_bytes,
+                            int32_t* dev_status, void* stream) {
+  if (!x || !w || !y) return EAGLE_ERR_INVALID_ARG;
+  if (M <= 0 || n_out <= 0 || k_in <= 0) return EAGLE_ERR_INVALID_ARG;
+  if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return EAGLE_ERR_INVALID_ARG;
+  if (x == y) return EAGLE_ERR_INVALID_ARG;
+  if (M > 4096 || n_out % 128 || k_in % 64 || n_out > 65536 || k_in > 65536) return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)))
+    return EAGLE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < eagle_linear_workspace_size(M, n_out, k_in, dtype)) return EAGLE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == EAGLE_FP32) {
+    const long long outs = (long long)M * n_out;
+    launch(linear_f32_kernel, (unsigned)((outs + 7) / 8), 256, 0, s, (const float*)x, (const float*)w, bias,
+           (const float*)residual, (float*)y, M, n_out, k_in);
+    note_launch();
+    return last_launch_status();
+  }
+  const void* xs[1] = {x};
+  return fp_launch_bf16(xs, 1, nullptr, nullptr, 0, w, bias, residual, y, M, n_out, k_in, ws, dev_status, s);
 }

@@ -4,8 +4,9 @@
  * One tree-verify round of EAGLE-family speculative decoding is served by
  * six calls (plus eagle_lmhead_verify_stats / eagle_tree_verify_stats, which
  * serve stochastic verification without materialised logits, eagle_tree_commit
- * which publishes the accepted path, and eagle_draft_input, the drafter's
- * token-embedding input FC):
+ * which publishes the accepted path, and the drafter step: eagle_draft_input,
+ * the token-embedding input FC, and eagle_draft_layer, its decoder layer,
+ * built on eagle_linear):
  *   eagle_fuse_proj             EAGLE-3 fused feature g = W_proj [h_low; h_mid; h_high]
  *   eagle_tree_attn             tree-masked attention vs a paged KV cache + the tree rows
  *   eagle_lmhead_topk           LM-head GEMM with fused per-row top-k and log-softmax
@@ -158,6 +159,27 @@ int eagle_draft_input(const void* r, const int32_t* token_ids, const void* embed
                       void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_linear -- y = x W^T (+ bias) (+ residual): the weight-streaming
+ * tensor-core projection of eagle_fuse_proj for one input of any width.
+ * The projections of the drafter's decoder layer ([E3] section 3.4 "The
+ * transformer decoder layer") are made of it.
+ *
+ *   x        : [M, k_in]      activations, dtype `dtype` (must not alias y)
+ *   w        : [n_out, k_in]  weights (out x in)
+ *   bias     : [n_out] fp32, or NULL
+ *   residual : [M, n_out] dtype `dtype` added to the result, or NULL; may be y
+ *   y        : [M, n_out]
+ * bf16 on the tensor cores (fp32 accumulation, stream-K over the SMs), fp32
+ * on the CUDA cores in exact fp32.  w may be read before the previous kernel
+ * on the stream has completed (see the conventions above).
+ * Limits: 1 <= M <= 4096, n_out % 128 == 0, k_in % 64 == 0, both <= 65536.
+ * ---------------------------------------------------------------------- */
+size_t eagle_linear_workspace_size(int M, int n_out, int k_in, int dtype);
+int eagle_linear(const void* x, const void* w, const float* bias, const void* residual, void* y,
+                 int M, int n_out, int k_in, int dtype, void* ws, size_t ws_bytes,
+                 int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * eagle_tree_attn -- attention of the tree rows against the committed prefix
  * (read through a page table) plus the visible tree rows.
  *   For tree row r of request b and query head h (kv head h / (Hq/Hkv)):
@@ -193,6 +215,54 @@ int eagle_tree_attn(const void* q, const void* k_tree, const void* v_tree,
                     int Hq, int Hkv, int D, int page_size, float scale, int num_splits,
                     int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_draft_layer -- the drafter's decoder layer over the W new tree nodes
+ * of one depth of each of B requests (one pass for the whole depth).
+ * [E3] section 3.4 "The transformer decoder layer" (self-attention and a
+ * feed-forward sublayer, each with a residual connection and normalisation);
+ * the form is that of the LLaMA-family targets ([E3] section 6, Limitation 6:
+ * pre-normalisation, SwiGLU, rotary embeddings, grouped-query attention);
+ * the attention is tree attention over the drafter's own K/V ([M7.5]
+ * sections 0x03C, 0x05B).  With m = b * W + j:
+ *   h     = RMSNorm(x) * w_norm1             (x / sqrt(mean(x^2) + eps))
+ *   q,k,v = split(h W_qkv^T); q, k rotated (rotate-half RoPE: pair (i, i+D/2)
+ *           by positions[m] * theta^(-2i/D))
+ *   q_tree[b, r0+j], k_tree[b, r0+j], v_tree[b, r0+j] = q, k, v
+ *   a     = tree attention of row r0+j over the prefix (paged cache) and the
+ *           tree rows its mask row shows (as eagle_tree_attn, R = Rmax,
+ *           scale 1/sqrt(D))
+ *   x1    = x + a W_o^T
+ *   h2    = RMSNorm(x1) * w_norm2
+ *   out   = x1 + (silu(h2 Wg^T) * (h2 Wu^T)) W_down^T,  W_gu = [Wg; Wu]
+ *
+ *   x        : [B*W, d] dtype `dtype` (must not alias out)
+ *   w_norm1, w_norm2 : [d];  w_qkv : [(Hq + 2 Hkv) D, d] (q heads, k heads,
+ *              v heads);  w_o : [d, Hq D];  w_gu : [2 I, d] (gate rows then up
+ *              rows);  w_down : [d, I]; all dtype `dtype`, out x in
+ *   positions: [B, W] int32 (the nodes' positions: prefix length + depth)
+ *   k_cache, v_cache, num_pages, block_table, max_pages, ctx_lens: the
+ *              drafter's committed prefix, as for eagle_tree_attn
+ *   q_tree   : [B, Rmax, Hq, D], k_tree / v_tree : [B, Rmax, Hkv, D]: the
+ *              drafter's tree rows, owned by the caller for the whole round;
+ *              rows r0 .. r0+W-1 are written, the others are read (rows no
+ *              call has written yet must hold finite values: zero them once)
+ *   tree_mask: [B, Rmax] uint64, bit i of row r = row i visible to row r
+ *              (the new rows: their ancestors' rows and themselves)
+ *   out      : [B*W, d]
+ * Limits: B*W <= 4096, r0 + W <= Rmax <= 64, D in {64, 128}, Hq % Hkv == 0,
+ * d % 128 == 0, (Hq + 2 Hkv) D % 128 == 0, Hq D % 128 == 0, I % 64 == 0.
+ * ---------------------------------------------------------------------- */
+size_t eagle_draft_layer_workspace_size(int B, int W, int d, int Hq, int Hkv, int D, int I,
+                                        int Rmax, int max_pages, int dtype);
+int eagle_draft_layer(const void* x, const void* w_norm1, const void* w_qkv, const void* w_o,
+                      const void* w_norm2, const void* w_gu, const void* w_down, float eps,
+                      float theta, const int32_t* positions, const void* k_cache,
+                      const void* v_cache, int num_pages, const int32_t* block_table,
+                      int max_pages, const int32_t* ctx_lens, void* q_tree, void* k_tree,
+                      void* v_tree, const uint64_t* tree_mask, int r0, int Rmax, void* out,
+                      int B, int W, int d, int Hq, int Hkv, int D, int I, int dtype, void* ws,
+                      size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * eagle_lmhead_topk -- vocabulary logits and per-row top-k, fused.

@@ -34,6 +34,7 @@ from .eagle_oracle import (  # noqa: F401
     draft_layer,
     eagle2_tree,
     fuse_proj,
+    linear,
     lmhead_topk,
     rms_norm,
     rope,

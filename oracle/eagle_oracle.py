@@ -756,6 +756,17 @@ def tree_commit(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree, path_ro
 # position and its draft-KV row).
 
 
+def linear(x, w, bias=None, residual=None):
+    """y = x w^T (+ bias) (+ residual), fp64: the projections of the decoder
+    layer ([E3] section 3.4 "The transformer decoder layer")."""
+    y = np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
+    if bias is not None:
+        y = y + np.asarray(bias, np.float64)[None, :]
+    if residual is not None:
+        y = y + np.asarray(residual, np.float64)
+    return y
+
+
 def rms_norm(x, w, eps):
     """y = x / sqrt(mean(x^2) + eps) * w over the last axis, fp64."""
     x = np.asarray(x, np.float64)

@@ -73,6 +73,22 @@ def test_host_validation_without_gpu(L):
     assert L.eagle_draft_input(p, p, p, 10, p, N, p, 4097, 128, 1, N, 0, N, N) == 2
     assert L.eagle_draft_input(p, p, p, 10, p, N, p, 4, 128, 1, N, 0, N, N) == 3
     assert L.eagle_draft_input_workspace_size(4, 128, 1) > 0
+    # linear: x aliasing y, n_out not a multiple of 128, k_in not a multiple of 64, no ws
+    assert L.eagle_linear(p, p, N, N, p, 4, 128, 64, 1, N, 0, N, N) == 1
+    q = ctypes.c_void_p(32)
+    assert L.eagle_linear(p, p, N, N, q, 4, 100, 64, 1, N, 0, N, N) == 2
+    assert L.eagle_linear(p, p, N, N, q, 4, 128, 48, 1, N, 0, N, N) == 2
+    assert L.eagle_linear(p, p, N, N, q, 4, 128, 64, 1, N, 0, N, N) == 3
+    # draft layer: null pointer, rows past Rmax, D = 96, no ws
+    lay = lambda r0, Rmax, D, ws_b: L.eagle_draft_layer(
+        p, p, p, p, p, p, p, ctypes.c_float(1e-5), ctypes.c_float(5e5), p, p, p, 4, p, 2, p, p, p, p, p,
+        r0, Rmax, q, 1, 4, 256, 4, 2, D, 256, 1, N, ws_b, N, N)
+    assert lay(6, 8, 64, 0) == 2
+    assert lay(0, 8, 96, 0) == 2
+    assert lay(0, 8, 64, 0) == 3
+    assert L.eagle_draft_layer(N, p, p, p, p, p, p, ctypes.c_float(1e-5), ctypes.c_float(5e5), p, p, p, 4, p, 2,
+                               p, p, p, p, p, 0, 8, q, 1, 4, 256, 4, 2, 64, 256, 1, N, 0, N, N) == 1
+    assert L.eagle_draft_layer_workspace_size(1, 4, 256, 4, 2, 64, 256, 8, 2, 1) > 0
     # attention: R > 64, D not in {64, 128}, page size != 16, Hq % Hkv
     base = [p, p, p, p, p, 4, p, 2, p, p, p, N]
     assert L.eagle_tree_attn(*base, 1, 65, 4, 2, 128, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 2

@@ -151,3 +151,15 @@ def test_layer_zero_weight_residual_paths():
     assert np.abs(out2 - (x + (oracle.silu(gu[:, :I]) * gu[:, I:]) @ wts["down"].T)).max() < 1e-12
     with pytest.raises(ValueError):
         oracle.draft_layer(x, wts, pos, kc, vc, table, ctx, kt, vt, mask, 4, Hq, Hkv)
+
+
+def test_linear_bruteforce_bias_residual():
+    r = _rng(10)
+    x, w, b, res = r.normal(size=(3, 5)), r.normal(size=(4, 5)), r.normal(size=4), r.normal(size=(3, 4))
+    y = oracle.linear(x, w, b, res)
+    for i in range(3):
+        for o in range(4):
+            acc = b[o] + res[i, o]
+            for c in range(5):
+                acc += w[o, c] * x[i, c]
+            assert abs(y[i, o] - acc) < 1e-12
