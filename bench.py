@@ -318,6 +318,58 @@ def measure_draft_input(wl, calls, peak_gbs):
                       "(together larger than L2); the embedding table is W_U's shape"}
 
 
+def measure_draft_layer(wl, calls, peak_gbs):
+    """The drafter's decoder layer at this workload's draft-row shape (B
+    requests x width new nodes, the middle depth of a round), timed per call
+    with CUDA events.  Its weights (>= 416 MB) exceed L2, so back-to-back
+    calls stream them from HBM each time."""
+    B, W, d, dev, dt = wl.B, wl.width, wl.d, wl.dev, wl.dt
+    Hq, Hkv, D, I, R = wl.Hq, wl.Hkv, wl.D, synth.FFN_WIDTH[d], wl.R
+    g = synth.generator(11, dev)
+    nrm = lambda shape, std: synth.normal(shape, std, dt, g, dev)
+    wts = dict(norm1=nrm((d,), 1.0), qkv=nrm(((Hq + 2 * Hkv) * D, d), synth.WEIGHT_STD),
+               o=nrm((d, Hq * D), synth.WEIGHT_STD), norm2=nrm((d,), 1.0),
+               gu=nrm((2 * I, d), synth.WEIGHT_STD), down=nrm((d, I), synth.WEIGHT_STD))
+    x = nrm((B * W, d), 1.0)
+    r0 = min(1 + (wl.depth // 2) * W, R - W)
+    q_tree = torch.zeros((B, R, Hq, D), dtype=dt, device=dev)
+    k_tree, v_tree = nrm((B, R, Hkv, D), 1.0), nrm((B, R, Hkv, D), 1.0)
+    rows = torch.arange(R, device=dev)
+    masks = ((torch.ones(R, dtype=torch.int64, device=dev) << rows) | 1).repeat(B, 1)  # root + self
+    pos = (wl.ctx_lens[:, None] + wl.depth // 2 + 1).to(torch.int32).repeat(1, W).contiguous()
+    out = torch.empty_like(x)
+    dt_code = eb.EAGLE_BF16 if dt == torch.bfloat16 else eb.EAGLE_FP32
+    ws = eb.workspace(eb.eagle_draft_layer_workspace_size(B, W, d, Hq, Hkv, D, I, R, wl.block_table.shape[1],
+                                                          dt_code), dev)
+    call = lambda: eb.eagle_draft_layer(x, wts, pos, wl.k_cache, wl.v_cache, wl.block_table, wl.ctx_lens,
+                                        q_tree, k_tree, v_tree, masks, r0, out, ws=ws, status=wl.status)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    evs = []
+    torch.cuda._sleep(4_000_000)  # the host queues every call meanwhile
+    for _ in range(calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    st = eb.read_status(wl.status)
+    if st != 0:
+        raise RuntimeError(f"device status {eb.STATUS.get(st, st)} in the drafter layer")
+    us = sum(a.elapsed_time(b) for a, b in evs) / calls * 1e3
+    es = x.element_size()
+    w_bytes = sum(t.numel() for t in wts.values()) * es
+    kv_bytes = int(wl.ctx_lens.sum().item()) * Hkv * D * 2 * es
+    byts = w_bytes + kv_bytes + 2 * B * W * d * es
+    gbs = byts / us / 1e3
+    return {"call": "eagle_draft_layer", "rows": B * W, "hidden": d, "ffn": I, "avg_call_us": round(us, 2),
+            "bytes_per_call": byts, "achieved": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak_gbs, 4),
+            "bound": "hbm", "timing": f"CUDA events per call, {calls} calls; weights "
+                                      f"{w_bytes / 1e6:.0f} MB + drafter prefix K/V {kv_bytes / 1e6:.0f} MB"}
+
+
 def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -395,7 +447,8 @@ def run_ours(args, rank, world):
     if st != 0:
         raise RuntimeError(f"device status {eb.STATUS.get(st, st)}")
     clocks = clk.summary()
-    rows = {"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"])}
+    rows = {"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"]),
+            "draft_layer": measure_draft_layer(wl, max(min(args.steps, 50), 10), peaks["hbm_gbs"])}
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),

@@ -42,6 +42,10 @@ CONFIGS = {
                    N=3, depth=3, topk=1, width=1, temps=(0.0,), dtype="bf16"),
 }
 
+# feed-forward width of the drafter's decoder layer: the LLaMA-3 8B / 70B
+# intermediate sizes at d 4096 / 8192 (a toy value below)
+FFN_WIDTH = {256: 512, 4096: 14336, 8192: 28672}
+
 WEIGHT_STD = 0.02      # W_proj, W_U ~ N(0, 0.02^2)
 LOGIT_STD = 3.0        # target logits ~ N(0, 3^2) per row
 DRAFT_NOISE_STD = 0.5  # draft logits = target + N(0, 0.5^2)
