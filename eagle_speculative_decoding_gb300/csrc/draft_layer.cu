@@ -76,39 +76,64 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // RoPE (rotate-half: pair (i, i + D/2) turned by pos * theta^(-2i/D)) of the
 // q and k heads of one QKV row, written with the v heads into the drafter's
-// tree arrays at row r0 + j of request b (row m = b * W + j).  The angles are
-// taken in double precision (64 per row), so large positions lose nothing.
+// tree arrays at row r0 + j of request b (row m = b * W + j).  The angle is
+// formed in double precision so that large positions lose nothing: the
+// frequency theta^(-2i/D) = ratio^i by binary powering of ratio =
+// theta^(-2/D) (from the host), the product with the position, and its
+// reduction to [-pi, pi]; only the sine and cosine of the reduced angle are
+// taken in fp32.  (Double-precision transcendentals and division are slow
+// on this part.)  Each thread moves 16-byte vectors: a chunk of the first
+// half of a head and its partner chunk of the second half.
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
     rope_scatter_kernel(const T* __restrict__ qkv, const int32_t* __restrict__ positions, int W, int r0,
-                        int Rmax, int Hq, int Hkv, int D, double theta, T* __restrict__ q_tree,
+                        int Rmax, int Hq, int Hkv, int D, double ratio, T* __restrict__ q_tree,
                         T* __restrict__ k_tree, T* __restrict__ v_tree) {
   pdl_wait();
   pdl_trigger();
+  constexpr int kV = 16 / sizeof(T);  // elements per 16-byte vector
   __shared__ float cs[64], sn[64];
   const int m = blockIdx.x, b = m / W, j = m % W, half = D / 2;
   const double pos = (double)positions[m];
+  constexpr double kTwoPi = 6.283185307179586, kInvTwoPi = 0.15915494309189535;
   for (int i = threadIdx.x; i < half; i += kRowThreads) {
-    double s, c;
-    sincos(pos * pow(theta, -2.0 * i / D), &s, &c);
-    cs[i] = (float)c;
-    sn[i] = (float)s;
+    double f = 1.0, base = ratio;
+    for (int e = i; e; e >>= 1, base *= base)
+      if (e & 1) f *= base;
+    const double ang = pos * f;
+    const double red = fma(-rint(ang * kInvTwoPi), kTwoPi, ang);
+    float s, c;
+    sincosf((float)red, &s, &c);
+    cs[i] = c;
+    sn[i] = s;
   }
   __syncthreads();
   const T* row = qkv + (size_t)m * (Hq + 2 * Hkv) * D;
   const size_t trow = (size_t)b * Rmax + r0 + j;
-  // pairs of the q heads then the k heads
-  for (int t = threadIdx.x; t < (Hq + Hkv) * half; t += kRowThreads) {
-    const int h = t / half, i = t % half;
-    const T* src = row + (size_t)h * D;
-    const float x1 = to_f(src[i]), x2 = to_f(src[i + half]);
-    const float y1 = x1 * cs[i] - x2 * sn[i], y2 = x2 * cs[i] + x1 * sn[i];
+  // 16-byte vectors of the first half of each q / k head with their partners
+  const int vph = half / kV;  // vectors per half head
+  for (int t = threadIdx.x; t < (Hq + Hkv) * vph; t += kRowThreads) {
+    const int h = t / vph, i0 = (t % vph) * kV;
+    const T* src = row + (size_t)h * D + i0;
+    uint4 a = *reinterpret_cast<const uint4*>(src), bb = *reinterpret_cast<const uint4*>(src + half);
+    const T* x1 = reinterpret_cast<const T*>(&a);
+    const T* x2 = reinterpret_cast<const T*>(&bb);
+    uint4 ya, yb;
+    T* y1 = reinterpret_cast<T*>(&ya);
+    T* y2 = reinterpret_cast<T*>(&yb);
+#pragma unroll
+    for (int e = 0; e < kV; ++e) {
+      const float u = to_f(x1[e]), w = to_f(x2[e]), c = cs[i0 + e], sv = sn[i0 + e];
+      y1[e] = from_f<T>(u * c - w * sv);
+      y2[e] = from_f<T>(w * c + u * sv);
+    }
     T* dst = h < Hq ? q_tree + (trow * Hq + h) * D : k_tree + (trow * Hkv + (h - Hq)) * D;
-    dst[i] = from_f<T>(y1);
-    dst[i + half] = from_f<T>(y2);
+    *reinterpret_cast<uint4*>(dst + i0) = ya;
+    *reinterpret_cast<uint4*>(dst + i0 + half) = yb;
   }
-  for (int t = threadIdx.x; t < Hkv * D; t += kRowThreads)
-    v_tree[trow * Hkv * D + t] = row[(size_t)(Hq + Hkv) * D + t];
+  const uint4* vsrc = reinterpret_cast<const uint4*>(row + (size_t)(Hq + Hkv) * D);
+  uint4* vdst = reinterpret_cast<uint4*>(v_tree + trow * Hkv * D);
+  for (int t = threadIdx.x; t < Hkv * D / kV; t += kRowThreads) vdst[t] = vsrc[t];
 }
 
 // a[m] = attn[b, r0 + j] (Hq * D values), m = b * W + j.
@@ -198,6 +223,7 @@ extern "C" int eagle_draft_layer(const void* x, const void* w_norm1, const void*
   if (!(eps >= 0.f) || !(theta > 0.f) || x == out) return EAGLE_ERR_INVALID_ARG;
   if (B <= 0 || W <= 0 || r0 < 0 || num_pages <= 0 || max_pages <= 0) return EAGLE_ERR_INVALID_ARG;
   if (!layer_shape_ok(B, W, d, Hq, Hkv, D, I, Rmax, r0)) return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned16(q_tree) || !aligned16(k_tree) || !aligned16(v_tree)) return EAGLE_ERR_INVALID_ARG;
   const LayerWs L = layer_ws(B, W, d, Hq, Hkv, D, I, Rmax, max_pages, dtype);
   if (!ws || ws_bytes < L.total) return EAGLE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -229,14 +255,15 @@ extern "C" int eagle_draft_layer(const void* x, const void* w_norm1, const void*
     launch(rmsnorm_kernel<float>, M, kRowThreads, 0, s, (const float*)x, (const float*)w_norm1, eps, (float*)h, d);
   note_launch();
   // 2. qkv = h W_qkv^T;  3. RoPE, rows into the tree arrays
+  const double ratio = pow((double)theta, -2.0 / D);
   EAGLE_TRY(eagle_linear(h, w_qkv, nullptr, nullptr, qkv, M, nqkv, d, dtype, lin_ws, L.lin, dev_status, stream));
   if (bf)
     launch(rope_scatter_kernel<__nv_bfloat16>, M, kRowThreads, 0, s, (const __nv_bfloat16*)qkv, positions, W,
-           r0, Rmax, Hq, Hkv, D, (double)theta, (__nv_bfloat16*)q_tree, (__nv_bfloat16*)k_tree,
+           r0, Rmax, Hq, Hkv, D, ratio, (__nv_bfloat16*)q_tree, (__nv_bfloat16*)k_tree,
            (__nv_bfloat16*)v_tree);
   else
     launch(rope_scatter_kernel<float>, M, kRowThreads, 0, s, (const float*)qkv, positions, W, r0, Rmax, Hq, Hkv,
-           D, (double)theta, (float*)q_tree, (float*)k_tree, (float*)v_tree);
+           D, ratio, (float*)q_tree, (float*)k_tree, (float*)v_tree);
   note_launch();
   // 4. tree attention over the drafter's prefix and its tree rows
   EAGLE_TRY(eagle_tree_attn(q_tree, k_tree, v_tree, k_cache, v_cache, num_pages, block_table, max_pages,

@@ -4,6 +4,8 @@ Used by ``__graft_entry__.smoke()``.  Workload: the toy shape (batch 1,
 d 256, 4/2 heads x 64, V 1024, ctx 128, depth 4, top-k 4, budget 16), fp32:
   draft round : LM-head top-k on synthetic drafter rows + tree expansion per
                 depth, then rerank/flatten
+  drafter     : the input FC with the embedding lookup and the decoder layer
+                over the frontier rows (fp32 and bf16)
   verify      : tree attention, fused projection, LM head (k = 1), greedy
                 and stochastic verification, and stochastic verification from
                 LM-head statistics
@@ -91,6 +93,37 @@ def run(device="cuda:0"):
                                    w_in.to(ddt).float().numpy())
         err = np.abs(u.float().cpu().numpy() - ref_u).max() / (np.abs(ref_u).max() + 1e-30)
         assert err < tol, ("draft_input", ddt, err)
+
+    # drafter decoder layer over the frontier rows (rows 1..width of its tree,
+    # each below row 0), fp32 and bf16
+    Hq_, Hkv_, D_, I_ = c["Hq"], c["Hkv"], c["D"], synth.FFN_WIDTH[d]
+    Rm, r0 = 1 + width, 1
+    wl = dict(norm1=1 + 0.1 * synth.normal((d,), 1.0, dt, gen),
+              qkv=synth.normal(((Hq_ + 2 * Hkv_) * D_, d), 0.05, dt, gen),
+              o=synth.normal((d, Hq_ * D_), 0.05, dt, gen),
+              norm2=1 + 0.1 * synth.normal((d,), 1.0, dt, gen),
+              gu=synth.normal((2 * I_, d), 0.05, dt, gen), down=synth.normal((d, I_), 0.05, dt, gen))
+    par = np.array([-1] + [0] * width)
+    lmask = oracle.ancestor_mask(par)[None]
+    lpos = (ctx.numpy()[:, None] + 1).repeat(width, axis=1).astype(np.int32)
+    for ddt, tol in ((torch.float32, 1e-4), (torch.bfloat16, 2e-2)):
+        xin = g[: B * width].to(ddt)
+        kt0 = synth.normal((B, Rm, Hkv_, D_), 1.0, ddt, gen)
+        vt0 = synth.normal((B, Rm, Hkv_, D_), 1.0, ddt, gen)
+        qt_d = torch.zeros((B, Rm, Hq_, D_), dtype=ddt, device=dev)
+        kt_d, vt_d = kt0.to(dev), vt0.to(dev)
+        lo = torch.empty_like(xin)
+        b.eagle_draft_layer(xin, {k_: v_.to(dev, ddt) for k_, v_ in wl.items()}, torch.from_numpy(lpos).to(dev),
+                            kc.to(dev, ddt), vc.to(dev, ddt), table.to(dev), ctx.to(dev), qt_d, kt_d, vt_d,
+                            torch.from_numpy(lmask.view(np.int64)).to(dev), r0, lo, status=status)
+        store = None if ddt == torch.float32 else (
+            lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).double().numpy())
+        f64 = lambda t: t.to(ddt).double().cpu().numpy()
+        ref_l, _, _ = oracle.draft_layer(f64(xin), {k_: f64(v_) for k_, v_ in wl.items()}, lpos, f64(kc), f64(vc),
+                                         table.numpy(), ctx.numpy(), f64(kt0), f64(vt0), lmask, r0, Hq_, Hkv_,
+                                         store=store)
+        err = np.abs(lo.double().cpu().numpy() - ref_l).max() / (np.abs(ref_l).max() + 1e-30)
+        assert err < tol, ("draft_layer", ddt, err)
 
     am = torch.empty((B * R, 1), dtype=torch.int32, device=dev)
     amlp = torch.empty((B * R, 1), dtype=torch.float32, device=dev)
