@@ -39,6 +39,7 @@ from .eagle_oracle import (  # noqa: F401
     rms_norm,
     rope,
     silu,
+    static_tree_step,
     tree_attn,
     tree_expand_finalize,
     tree_expand_init,

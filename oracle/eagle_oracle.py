@@ -299,11 +299,19 @@ def tree_expand_step(st, cand_ids, cand_logprobs, width):
     parents = list(st["frontier"])
     if cand_ids.shape[0] < len(parents) or cand_lp.shape != cand_ids.shape:
         raise ValueError("need one candidate row per expandable parent")
+    new = _add_children(st, parents, cand_ids, cand_lp, [cand_ids.shape[1]] * len(parents))
+    st["frontier"] = sorted(new, key=lambda n: _key(st, n))[:width]
+    return list(st["frontier"])
+
+
+def _add_children(st, parents, cand_ids, cand_lp, limits):
+    """Store the children of each parent (ranks below its limit) with the
+    values and validation of ``tree_expand_step``; returns their node ids."""
     new = []
     for j, p in enumerate(parents):
         seen = set()
         mass = 0.0
-        for i in range(cand_ids.shape[1]):
+        for i in range(min(int(limits[j]), cand_ids.shape[1])):
             tok = int(cand_ids[j, i])
             if tok < 0:  # fewer than k alternatives for this parent
                 continue
@@ -325,7 +333,27 @@ def tree_expand_step(st, cand_ids, cand_logprobs, width):
             st["logv"].append(logv)
             st["depth"].append(st["depth"][p] + 1)
             new.append(n)
-    st["frontier"] = sorted(new, key=lambda n: _key(st, n))[:width]
+    return new
+
+
+def static_tree_step(st, cand_ids, cand_logprobs, fanout):
+    """One depth of a static draft tree (EAGLE-1, [E1] "Tree-Structured Draft
+    Generation": a fixed tree, the root branching into its top-4 tokens and
+    deeper nodes into fewer).  The tree is given depth by depth as the number
+    of children of each node of the current depth, in creation order:
+    frontier[j] takes the tokens of its top-``fanout[j]`` candidates (ranks
+    0 .. fanout[j]-1).  Values, depths, node ids and validation are those of
+    ``tree_expand_step``; the next frontier is every new node, in creation
+    order (no reranking: the shape is fixed)."""
+    cand_ids = np.asarray(cand_ids)
+    cand_lp = np.asarray(cand_logprobs, dtype=np.float32)
+    parents = list(st["frontier"])
+    fanout = [int(f) for f in fanout]
+    if len(fanout) < len(parents) or cand_ids.shape[0] < len(parents) or cand_lp.shape != cand_ids.shape:
+        raise ValueError("need one fan-out and one candidate row per node of the depth")
+    if any(f < 0 or f > cand_ids.shape[1] for f in fanout[:len(parents)]):
+        raise ValueError("a fan-out must lie in [0, k]")
+    st["frontier"] = _add_children(st, parents, cand_ids, cand_lp, fanout)
     return list(st["frontier"])
 
 
