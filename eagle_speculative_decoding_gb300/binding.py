@@ -42,6 +42,8 @@ _SIGS = {
     "eagle_lmhead_topk_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "eagle_lmhead_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
     "eagle_tree_expand": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "eagle_tree_expand_static": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                      _P]),
     "eagle_tree_expand_finalize": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P, _P, _P, _P]),
     "eagle_tree_verify_workspace_size": (_Z, [_I, _I, _I]),
@@ -256,6 +258,17 @@ def eagle_tree_expand(step, width, cand_ids, cand_logprobs, root_token, node_par
     k = cand_ids.shape[-1]
     _check("eagle_tree_expand", lib().eagle_tree_expand(
         B, step, width, k, max_nodes, _ptr(cand_ids), _ptr(cand_logprobs), _ptr(root_token),
+        _ptr(node_parent), _ptr(node_token), _ptr(node_logv), _ptr(node_depth), _ptr(node_count),
+        _ptr(frontier), _ptr(n_frontier), _ptr(status), _stream(stream)))
+
+
+def eagle_tree_expand_static(step, width, fanout, cand_ids, cand_logprobs, root_token, node_parent, node_token,
+                             node_logv, node_depth, node_count, frontier, n_frontier, status=None, stream=None):
+    """One depth of a static tree: frontier node j keeps its top-fanout[j] candidates."""
+    B, max_nodes = node_parent.shape
+    k = cand_ids.shape[-1]
+    _check("eagle_tree_expand_static", lib().eagle_tree_expand_static(
+        B, step, width, k, max_nodes, _ptr(fanout), _ptr(cand_ids), _ptr(cand_logprobs), _ptr(root_token),
         _ptr(node_parent), _ptr(node_token), _ptr(node_logv), _ptr(node_depth), _ptr(node_count),
         _ptr(frontier), _ptr(n_frontier), _ptr(status), _stream(stream)))
 

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     int32_t* __restrict__ node_parent, int32_t* __restrict__ node_token,
     float* __restrict__ node_logv, int32_t* __restrict__ node_depth,
     int32_t* __restrict__ node_count, int32_t* __restrict__ frontier,
-    int32_t* __restrict__ n_frontier, int32_t* dev_status) {
+    int32_t* __restrict__ n_frontier, const int32_t* __restrict__ fanout, int32_t* dev_status) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -103,12 +103,25 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
   __shared__ int s_id[kMaxCand];
   __shared__ float s_lp[kMaxCand];
   __shared__ int s_bad;
+  __shared__ int s_fan[64];  // static tree: children kept per parent slot
 
   const int npar = step == 0 ? 1 : max(0, min(width, n_frontier[b]));
   const int count0 = step == 0 ? 1 : node_count[b];
   const int ncand = npar * k;
   if (threadIdx.x == 0) s_bad = 0;
   if (threadIdx.x < 64) s_mass[threadIdx.x] = 0.f;
+  __syncthreads();  // the error word is reset before any thread can raise it
+  if (threadIdx.x < npar) {
+    int f = k;
+    if (fanout) {
+      f = fanout[threadIdx.x];
+      if (f < 0 || f > k) {
+        atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
+        f = 0;
+      }
+    }
+    s_fan[threadIdx.x] = f;
+  }
   // the expanded parents, loaded in parallel
   if (threadIdx.x < npar) {
     const int j = threadIdx.x;
@@ -143,7 +156,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     const int j = t / k, i = t % k;
     const int id = s_id[t];
     float lp = s_lp[t];
-    int valid = id >= 0;
+    int valid = id >= 0 && i < s_fan[j];
     if (valid) {
       if (isnan(lp) || lp == INFINITY) {
         atomicCAS(&s_bad, 0, EAGLE_ERR_NONFINITE);
@@ -186,16 +199,21 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     nt_[node] = s_id[t];
     nv_[node] = s_v[t];
     nd_[node] = s_pard[j] + 1;
-    // next frontier: rank of this node among the new nodes (same depth)
-    const float v = s_v[t];
-    int rank = 0;
-    for (int u = 0; u < ncand; ++u) {
-      if (!s_valid[u] || u == t) continue;
-      rank += key_less(s_v[u], 0, count0 + s_scan[u], v, 0, node) ? 1 : 0;
+    // next frontier: rank of this node among the new nodes (same depth) by
+    // key; a static tree keeps creation order
+    int rank = s_scan[t];
+    if (!fanout) {
+      const float v = s_v[t];
+      rank = 0;
+      for (int u = 0; u < ncand; ++u) {
+        if (!s_valid[u] || u == t) continue;
+        rank += key_less(s_v[u], 0, count0 + s_scan[u], v, 0, node) ? 1 : 0;
+      }
     }
     if (rank < width) frontier[(size_t)b * width + rank] = node;
   }
   if (threadIdx.x == 0) {
+    if (fanout && nnew > width) set_status(dev_status, EAGLE_ERR_BAD_TREE);  // a depth wider than the frontier
     n_frontier[b] = nnew < width ? nnew : width;
     node_count[b] = count0 + nnew;
   }
@@ -305,12 +323,12 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
 
 using namespace eagle;
 
-extern "C" int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
-                                 const int32_t* cand_ids, const float* cand_logprobs,
-                                 const int32_t* root_token, int32_t* node_parent,
-                                 int32_t* node_token, float* node_logv, int32_t* node_depth,
-                                 int32_t* node_count, int32_t* frontier, int32_t* n_frontier,
-                                 int32_t* dev_status, void* stream) {
+namespace {
+int expand_launch(int B, int step, int width, int k, int max_nodes, const int32_t* fanout,
+                  const int32_t* cand_ids, const float* cand_logprobs, const int32_t* root_token,
+                  int32_t* node_parent, int32_t* node_token, float* node_logv, int32_t* node_depth,
+                  int32_t* node_count, int32_t* frontier, int32_t* n_frontier, int32_t* dev_status,
+                  void* stream) {
   if (B <= 0 || step < 0 || width < 1 || k < 1 || max_nodes < 1) return EAGLE_ERR_INVALID_ARG;
   if (!cand_ids || !cand_logprobs || !node_parent || !node_token || !node_logv || !node_depth ||
       !node_count || !frontier || !n_frontier)
@@ -321,9 +339,33 @@ extern "C" int eagle_tree_expand(int B, int step, int width, int k, int max_node
   if ((long long)max_nodes < 1LL + k + (long long)step * width * k) return EAGLE_ERR_INVALID_ARG;
   launch(expand_step_kernel, B, kExpandThreads, 0, static_cast<cudaStream_t>(stream),
       step, width, k, max_nodes, cand_ids, cand_logprobs, root_token, node_parent, node_token,
-      node_logv, node_depth, node_count, frontier, n_frontier, dev_status);
+      node_logv, node_depth, node_count, frontier, n_frontier, fanout, dev_status);
   note_launch();
   return last_launch_status();
+}
+}  // namespace
+
+extern "C" int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
+                                 const int32_t* cand_ids, const float* cand_logprobs,
+                                 const int32_t* root_token, int32_t* node_parent,
+                                 int32_t* node_token, float* node_logv, int32_t* node_depth,
+                                 int32_t* node_count, int32_t* frontier, int32_t* n_frontier,
+                                 int32_t* dev_status, void* stream) {
+  return expand_launch(B, step, width, k, max_nodes, nullptr, cand_ids, cand_logprobs, root_token,
+                       node_parent, node_token, node_logv, node_depth, node_count, frontier, n_frontier,
+                       dev_status, stream);
+}
+
+extern "C" int eagle_tree_expand_static(int B, int step, int width, int k, int max_nodes,
+                                        const int32_t* fanout, const int32_t* cand_ids,
+                                        const float* cand_logprobs, const int32_t* root_token,
+                                        int32_t* node_parent, int32_t* node_token, float* node_logv,
+                                        int32_t* node_depth, int32_t* node_count, int32_t* frontier,
+                                        int32_t* n_frontier, int32_t* dev_status, void* stream) {
+  if (!fanout) return EAGLE_ERR_INVALID_ARG;
+  return expand_launch(B, step, width, k, max_nodes, fanout, cand_ids, cand_logprobs, root_token,
+                       node_parent, node_token, node_logv, node_depth, node_count, frontier, n_frontier,
+                       dev_status, stream);
 }
 
 extern "C" int eagle_tree_expand_finalize(int B, int max_nodes, int budget, int R,

@@ -11,6 +11,7 @@
  *   eagle_tree_attn             tree-masked attention vs a paged KV cache + the tree rows
  *   eagle_lmhead_topk           LM-head GEMM with fused per-row top-k and log-softmax
  *   eagle_tree_expand           one EAGLE-2 dynamic-tree expansion step
+ *                               (eagle_tree_expand_static: one depth of a fixed EAGLE-1 tree)
  *   eagle_tree_expand_finalize  EAGLE-2 global rerank + flatten (rows, mask, positions)
  *   eagle_tree_verify           lossless verification (greedy / rejection sampling)
  *
@@ -328,6 +329,30 @@ int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
                       int32_t* node_token, float* node_logv, int32_t* node_depth,
                       int32_t* node_count, int32_t* frontier, int32_t* n_frontier,
                       int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_expand_static -- one depth of a static (EAGLE-1) draft tree.
+ * [E1] "Tree-Structured Draft Generation" and its note on the tree used: a
+ * fixed tree whose root branches into its top-4 tokens and whose deeper
+ * nodes branch into fewer.  The shape is given depth by depth: node j of the
+ * current depth (frontier[b, j], creation order) keeps its top-fanout[j]
+ * candidates (ranks 0 .. fanout[j]-1).  Values, depths, node ids, validation
+ * and every argument are as for eagle_tree_expand, except that the next
+ * frontier is all the new nodes in creation order (no reranking), `width`
+ * is the frontier capacity (the widest depth), and
+ *   fanout : [P] int32 device, the same for every request (P = 1 at step 0,
+ *            else width), each in [0, k].
+ * Flatten a finished static tree with eagle_tree_expand_finalize and a
+ * budget of all its nodes.
+ * Device-detected: a fan-out outside [0, k], or more new nodes than `width`
+ * -> EAGLE_ERR_BAD_TREE (plus the checks of eagle_tree_expand).
+ * ---------------------------------------------------------------------- */
+int eagle_tree_expand_static(int B, int step, int width, int k, int max_nodes,
+                             const int32_t* fanout, const int32_t* cand_ids,
+                             const float* cand_logprobs, const int32_t* root_token,
+                             int32_t* node_parent, int32_t* node_token, float* node_logv,
+                             int32_t* node_depth, int32_t* node_count, int32_t* frontier,
+                             int32_t* n_frontier, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * eagle_tree_expand_finalize -- EAGLE-2 rerank, then flatten for verification.

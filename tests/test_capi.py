@@ -97,6 +97,9 @@ def test_host_validation_without_gpu(L):
     assert L.eagle_tree_attn(*base, 1, 8, 5, 2, 128, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 1
     # expand: width 0, k > 32, max_nodes too small for the step
     assert L.eagle_tree_expand(1, 0, 0, 2, 16, p, p, p, p, p, p, p, p, p, p, N, N) == 1
+    # static expansion: no fan-out array, width over 64
+    assert L.eagle_tree_expand_static(1, 0, 4, 2, 64, N, p, p, p, p, p, p, p, p, p, p, N, N) == 1
+    assert L.eagle_tree_expand_static(1, 0, 65, 2, 512, p, p, p, p, p, p, p, p, p, p, p, N, N) == 2
     assert L.eagle_tree_expand(1, 0, 2, 33, 64, p, p, p, p, p, p, p, p, p, p, N, N) == 2
     assert L.eagle_tree_expand(1, 3, 2, 2, 12, p, p, p, p, p, p, p, p, p, p, N, N) == 1
     assert L.eagle_tree_expand_finalize(1, 16, 8, 4, p, p, p, p, p, N, p, p, p, p, p, p, p, N, N) == 1

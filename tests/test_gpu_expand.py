@@ -134,3 +134,82 @@ def test_budget_zero_and_host_limits():
     assert flat["n_rows"][0] == 1 and flat["token"][0].tolist() == [9, -1, -1]
     with pytest.raises(b.EagleError):
         g.step(5, torch.zeros((1, 2, 2), dtype=torch.int32), torch.zeros((1, 2, 2)))  # max_nodes too small
+
+
+@pytest.mark.parametrize("schedule,k,B", [((4, 3, 2, 1), 4, 1), ((4, 3, 2, 1), 4, 3), ((2, 2, 2, 2, 1), 2, 5),
+                                          ((1, 1, 1), 1, 2), ((3, 0, 2), 3, 2)])
+def test_static_tree_bit_exact(schedule, k, B):
+    # a fixed tree grown depth by depth with the same fan-out for every node of
+    # a depth; node arrays and the flatten of the whole tree are bit-exact
+    b = need_gpu()
+    V = 3000
+    gen = synth.generator(sum(schedule) * 10 + k + B)
+    widths = [1]
+    for f in schedule:
+        widths.append(widths[-1] * f)
+    width = max(max(widths[1:]), 1)
+    n_nodes = sum(widths[1:])
+    max_nodes = 1 + k + len(schedule) * width * k
+    roots = synth.random_tokens((B,), V, gen)
+    d = "cuda"
+    z = lambda *s, dt=torch.int32: torch.zeros(s, dtype=dt, device=d)
+    parent, token, logv, depth = z(B, max_nodes), z(B, max_nodes), z(B, max_nodes, dt=torch.float32), z(B, max_nodes)
+    count, frontier, nf, status = z(B), z(B, width), z(B), z(1)
+    sts = [oracle.tree_expand_init(int(roots[i])) for i in range(B)]
+    for s, f in enumerate(schedule):
+        P = 1 if s == 0 else width
+        ids = torch.full((B, P, k), -1, dtype=torch.int32)
+        lps = torch.full((B, P, k), -math.inf, dtype=torch.float32)
+        for i in range(B):
+            npar = len(sts[i]["frontier"])
+            ci, cl = synth.draft_candidates(npar, k, V, gen)
+            ids[i, :npar], lps[i, :npar] = ci, cl
+        fan = torch.full((P,), f, dtype=torch.int32, device=d)
+        b.eagle_tree_expand_static(s, width, fan, ids.to(d), lps.to(d), roots.to(d), parent, token, logv, depth,
+                                   count, frontier, nf, status=status)
+        for i in range(B):
+            npar = len(sts[i]["frontier"])
+            oracle.static_tree_step(sts[i], ids[i, :npar].numpy(), lps[i, :npar].numpy(), [f] * npar)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i in range(B):
+        n = len(sts[i]["parent"])
+        assert n == 1 + n_nodes
+        assert int(count[i]) == n
+        assert parent[i, :n].cpu().tolist() == sts[i]["parent"]
+        assert token[i, :n].cpu().tolist() == sts[i]["token"]
+        assert np.array_equal(logv[i, :n].cpu().numpy(), np.array(sts[i]["logv"], np.float32))
+        assert depth[i, :n].cpu().tolist() == sts[i]["depth"]
+        nfi = int(nf[i])
+        assert frontier[i, :nfi].cpu().tolist() == sts[i]["frontier"][:width]
+    if n_nodes + 1 <= 64:
+        R = n_nodes + 1
+        ctx = torch.randint(0, 500, (B,), generator=gen, dtype=torch.int32)
+        out = {n: torch.zeros((B, R), dtype=torch.int32, device=d)
+               for n in ("token", "parent_row", "depth", "node_id", "position")}
+        out["mask"] = torch.zeros((B, R), dtype=torch.int64, device=d)
+        out["n_rows"] = torch.zeros(B, dtype=torch.int32, device=d)
+        b.eagle_tree_expand_finalize(n_nodes, parent, token, logv, depth, count, ctx.to(d), out["token"],
+                                     out["parent_row"], out["depth"], out["mask"], out["node_id"],
+                                     out["position"], out["n_rows"], status=status)
+        torch.cuda.synchronize()
+        for i in range(B):
+            ref = oracle.tree_expand_finalize(sts[i], n_nodes, int(ctx[i]), R_out=R)
+            for key in ("token", "parent_row", "depth", "node_id", "position"):
+                assert np.array_equal(out[key][i].cpu().numpy(), ref[key]), key
+            assert np.array_equal(out["mask"][i].cpu().numpy().view(np.uint64), ref["mask"])
+
+
+def test_static_tree_bad_fanout_flags():
+    b = need_gpu()
+    d = "cuda"
+    z = lambda *s, dt=torch.int32: torch.zeros(s, dtype=dt, device=d)
+    parent, token, logv, depth = z(1, 64), z(1, 64), z(1, 64, dt=torch.float32), z(1, 64)
+    count, frontier, nf, status = z(1), z(1, 4), z(1), z(1)
+    ids = torch.tensor([[[5, 6, 7]]], dtype=torch.int32, device=d)
+    lps = torch.log(torch.tensor([[[0.5, 0.2, 0.1]]], device=d))
+    fan = torch.tensor([4], dtype=torch.int32, device=d)  # more than k = 3
+    b.eagle_tree_expand_static(0, 4, fan, ids, lps, torch.tensor([1], dtype=torch.int32, device=d), parent,
+                               token, logv, depth, count, frontier, nf, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
