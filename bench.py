@@ -77,10 +77,34 @@ class Workload:
         host["v_tree"] = synth.normal((B, R, self.Hkv, self.D), 1.0, self.dt, gc)
         host["h"] = [synth.normal((B * R, d), 1.0, self.dt, gc) for _ in range(3)]
         host["x_v"] = synth.normal((B * R, d), 1.0, self.dt, gc)
-        self.host = {k: ([t.pin_memory() for t in v] if isinstance(v, list) else v.pin_memory())
-                     for k, v in host.items()}
-        self.dev_in = {k: ([t.to(device) for t in v] if isinstance(v, list) else v.to(device))
-                       for k, v in self.host.items()}
+        # the per-step inputs live in one pinned host buffer and one device
+        # buffer (256-byte aligned slots), so a step's upload is one copy
+        flat = [t for v in host.values() for t in (v if isinstance(v, list) else [v])]
+        offs, n = [], 0
+        for t in flat:
+            offs.append(n)
+            n += -(-t.numel() * t.element_size() // 256) * 256
+        self.host_buf = torch.empty(n, dtype=torch.uint8).pin_memory()
+        self.dev_buf = torch.empty(n, dtype=torch.uint8, device=device)
+
+        def slot(buf, t, off):
+            nb = t.numel() * t.element_size()
+            return buf[off:off + nb].view(t.dtype).view(t.shape)
+
+        it = iter(range(len(flat)))
+        self.host, self.dev_in = {}, {}
+        for k, v in host.items():
+            ts = v if isinstance(v, list) else [v]
+            hs, ds = [], []
+            for t in ts:
+                i = next(it)
+                h = slot(self.host_buf, t, offs[i])
+                h.copy_(t)
+                hs.append(h)
+                ds.append(slot(self.dev_buf, t, offs[i]))
+            self.host[k] = hs if isinstance(v, list) else hs[0]
+            self.dev_in[k] = ds if isinstance(v, list) else ds[0]
+        self.dev_buf.copy_(self.host_buf)
         # outputs / state
         z = lambda *s, t=torch.int32: torch.zeros(s, dtype=t, device=device)
         self.max_nodes = 1 + synth.n_candidates(c)
@@ -166,17 +190,10 @@ class Workload:
                                        seed=1234, status=self.status)
 
     def h2d(self):
-        """Copy this step's inputs from pinned host memory; returns bytes."""
-        n = 0
-        for k, v in self.host.items():
-            if isinstance(v, list):
-                for a, b in zip(self.dev_in[k], v):
-                    a.copy_(b, non_blocking=True)
-                    n += b.numel() * b.element_size()
-            else:
-                self.dev_in[k].copy_(v, non_blocking=True)
-                n += v.numel() * v.element_size()
-        return n
+        """Copy this step's inputs from pinned host memory (one copy of the
+        packed input buffer); returns the bytes copied."""
+        self.dev_buf.copy_(self.host_buf, non_blocking=True)
+        return self.host_buf.numel()
 
     def d2h(self, host_out):
         n = 0
