@@ -653,9 +653,6 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   // two query tiles share each K/V block when the prefix is long enough
   // (>= 4096 keys) for the splits to keep every SM busy anyway
   pl.tpc = (pl.qtiles >= 2 && max_blocks >= 64) ? 2 : 1;
-#ifdef EXP_TPC
-  pl.tpc = pl.qtiles >= 2 ? EXP_TPC : 1;
-#endif
   if (num_splits > 0) {
     pl.splits = min(num_splits, max_blocks);
   } else {
