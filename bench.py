@@ -131,6 +131,7 @@ class Workload:
         self.status = z(1)
         # workspaces (caller-owned scratch)
         dt_code = eb.EAGLE_BF16 if self.dt == torch.bfloat16 else eb.EAGLE_FP32
+        self.dt_code = dt_code
         lm_ws = max(eb.eagle_lmhead_topk_workspace_size(B * p, d, V, self.k, dt_code) for p in self.P)
         lm_ws = max(lm_ws, eb.eagle_lmhead_topk_workspace_size(B * R, d, V, self.race_k, dt_code))
         self.ws_lm = eb.workspace(lm_ws, device)
@@ -155,8 +156,15 @@ class Workload:
                 lm_events.append((e0, e1, M, k))
 
         def lm(xr, k, ids, lps):
-            timed(lambda: eb.eagle_lmhead_topk(xr, self.w_lm, k, ids, lps, temperature=1.0,
-                                               ws=self.ws_lm, status=self.status), xr.shape[0], k)
+            if lm_events is None:
+                eb.eagle_lmhead_topk(xr, self.w_lm, k, ids, lps, temperature=1.0, ws=self.ws_lm,
+                                     status=self.status)
+                return
+            # the same kernels as eagle_lmhead_topk, with events around the GEMM alone
+            timed(lambda: eb.eagle_lmhead_topk_partial(xr, self.w_lm, k, self.ws_lm, temperature=1.0,
+                                                       status=self.status), xr.shape[0], k)
+            eb.eagle_lmhead_topk_merge(xr.shape[0], self.d, self.V, ids, lps, self.ws_lm, dtype=self.dt_code,
+                                       temperature=1.0, status=self.status)
 
         for s in range(self.depth):
             ids, lps = self.cand[s]
@@ -179,11 +187,10 @@ class Workload:
                                  self.out_tok, n_rows=f["n_rows"], target_argmax=self.amax.view(self.B, self.R),
                                  V=self.V, ws=self.ws_ver, status=self.status)
         else:
-            timed(lambda: eb.eagle_lmhead_verify_stats(
+            eb.eagle_lmhead_verify_stats(
                 x["x_v"], self.w_lm, f["parent_row"], f["token"], self.T, self.race_k,
                 self.race_ids, self.race_keys, self.row_max, self.row_sumexp, self.child_logit,
-                n_rows=f["n_rows"], seed=1234, ws=self.ws_lm, status=self.status),
-                self.B * self.R, self.race_k)
+                n_rows=f["n_rows"], seed=1234, ws=self.ws_lm, status=self.status)
             eb.eagle_tree_verify_stats(f["parent_row"], f["token"], self.T, self.depth, self.row_max,
                                        self.row_sumexp, self.child_logit, self.race_ids, self.acc,
                                        self.path, self.out_tok, self.V, n_rows=f["n_rows"],
@@ -420,8 +427,9 @@ def run_ours(args, rank, world):
     launches = eb.launch_count() - n0
 
     # ---- the dominant kernel's launch durations: a second pass of the same
-    # steps with CUDA events around every LM-head call (events between kernels
-    # stop the next kernel's early launch, so this pass is not the one timed)
+    # steps with CUDA events around every LM-head GEMM launch (events between
+    # kernels stop the next kernel's early launch, so this pass is not the one
+    # timed)
     lm_events = []
     barrier(world)
     torch.cuda.synchronize()
@@ -485,8 +493,10 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
                      "traffic": profile_traffic(), "avg_launch_us": round(lm_avg_ms * 1e3, 2),
                      "launches_per_step": len(lm_events) // args.steps,
-                     "timing": "CUDA events around each LM-head call (main kernel + partial "
-                               "merge) over a second pass of the timed steps"},
+                     "timing": "CUDA events around each launch of the LM-head GEMM kernel "
+                               "(eagle_lmhead_topk_partial; its partial merge follows outside the "
+                               "events) in a second pass of the timed steps; the statistics-mode "
+                               "verification call of T > 0 workloads is not among them"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": hb,
                 "d2h_bytes_per_step": db},
         "clocks": clocks,

@@ -41,6 +41,8 @@ _SIGS = {
                              _I, _F, _I, _I, _P, _Z, _P, _P]),
     "eagle_lmhead_topk_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "eagle_lmhead_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
+    "eagle_lmhead_topk_partial": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P, _P]),
+    "eagle_lmhead_topk_merge": (_I, [_I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
     "eagle_tree_expand": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "eagle_tree_expand_static": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       _P]),
@@ -248,6 +250,24 @@ def eagle_lmhead_topk(x, w_lm, k, topk_ids, topk_logprobs, temperature=1.0, bias
         _ptr(topk_logprobs), _ptr(row_max), _ptr(row_sumexp), dt, _ptr(ws), ws.numel(),
         _ptr(status), _stream(stream)))
     return topk_ids, topk_logprobs
+
+
+def eagle_lmhead_topk_partial(x, w_lm, k, ws, temperature=1.0, bias=None, status=None, stream=None):
+    """First half of eagle_lmhead_topk: the GEMM, partials left in ws."""
+    M, d = x.shape
+    V = w_lm.shape[0]
+    _check("eagle_lmhead_topk_partial", lib().eagle_lmhead_topk_partial(
+        _ptr(x), _ptr(w_lm), _ptr(bias), M, d, V, k, float(temperature), _dtype(x), _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+
+
+def eagle_lmhead_topk_merge(M, d, V, topk_ids, topk_logprobs, ws, dtype=EAGLE_BF16, temperature=1.0,
+                            row_max=None, row_sumexp=None, status=None, stream=None):
+    """Second half of eagle_lmhead_topk: merge the partials a partial call left in ws."""
+    k = topk_ids.shape[-1]
+    _check("eagle_lmhead_topk_merge", lib().eagle_lmhead_topk_merge(
+        M, d, V, k, float(temperature), _ptr(topk_ids), _ptr(topk_logprobs), _ptr(row_max), _ptr(row_sumexp),
+        dtype, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
 
 
 # ------------------------------------------------------------------ a4 / a5

@@ -1118,17 +1118,22 @@ struct RaceCfg {
 
 // The LM head proper: GEMM + per-CTA top-K / log-sum-exp partials, then the
 // merge.  race != nullptr selects the exponential-race keys.
+// phase: kBoth, or only the GEMM + per-CTA partials (kPartial, into ws), or
+// only the merge of partials a kPartial call left in ws (kMerge).
+enum LmPhase { kBoth = 0, kPartial = 1, kMerge = 2 };
+
 int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d, int V, int k,
                float temperature, int32_t* topk_ids, float* topk_logprobs, float* row_max,
                float* row_sumexp, int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
-               void* stream, const RaceCfg* race) {
-  if (!x || !w_lm || !topk_ids || !topk_logprobs) return EAGLE_ERR_INVALID_ARG;
+               void* stream, const RaceCfg* race, LmPhase phase = kBoth) {
+  if (phase != kMerge && (!x || !w_lm)) return EAGLE_ERR_INVALID_ARG;
+  if (phase != kPartial && (!topk_ids || !topk_logprobs)) return EAGLE_ERR_INVALID_ARG;
   if (M <= 0 || d <= 0 || V <= 0 || k <= 0 || !(temperature > 0.f) || isinf(temperature))
     return EAGLE_ERR_INVALID_ARG;
   if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return EAGLE_ERR_INVALID_ARG;
   if (k > V) return EAGLE_ERR_INVALID_ARG;
   if (M > 2048 || k > 32 || d % 64 || V % 16) return EAGLE_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(w_lm)) return EAGLE_ERR_INVALID_ARG;
+  if (phase != kMerge && (!aligned16(x) || !aligned16(w_lm))) return EAGLE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < eagle_lmhead_topk_workspace_size(M, d, V, k, dtype)) return EAGLE_ERR_WORKSPACE;
   const int G = (M + 127) / 128;
   int sms = sm_count();
@@ -1191,7 +1196,9 @@ int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d,
   p.status = dev_status;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == EAGLE_BF16) {
+  if (phase == kMerge) {
+    // nothing to launch here but the merge below
+  } else if (dtype == EAGLE_BF16) {
     CUtensorMap mx, mw;
     if (!make_tmap_2d(&mx, x, 2, (uint64_t)M, (uint64_t)d, (uint32_t)xr, 64) ||
         !make_tmap_2d(&mw, w_lm, 2, (uint64_t)V, (uint64_t)d, (uint32_t)tn, 64))
@@ -1208,7 +1215,8 @@ int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d,
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     launch(kern, n_ctas, kEpiThreads, smem, s, (const float*)x, (const float*)w_lm, d, p);
   }
-  note_launch();
+  if (phase != kMerge) note_launch();
+  if (phase == kPartial) return last_launch_status();
   // merge of the per-CTA partials: one CTA per row, lists staged in shared memory
   const size_t msmem = (size_t)cpg * (k * 8 + 4);
   if (msmem > 227 * 1024) return EAGLE_ERR_UNSUPPORTED;
@@ -1277,6 +1285,20 @@ extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* b
                                  void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
   return lmhead_run(x, w_lm, bias, M, d, V, k, temperature, topk_ids, topk_logprobs, row_max,
                     row_sumexp, dtype, ws, ws_bytes, dev_status, stream, nullptr);
+}
+
+extern "C" int eagle_lmhead_topk_partial(const void* x, const void* w_lm, const float* bias, int M, int d,
+                                         int V, int k, float temperature, int dtype, void* ws,
+                                         size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return lmhead_run(x, w_lm, bias, M, d, V, k, temperature, nullptr, nullptr, nullptr, nullptr, dtype, ws,
+                    ws_bytes, dev_status, stream, nullptr, kPartial);
+}
+
+extern "C" int eagle_lmhead_topk_merge(int M, int d, int V, int k, float temperature, int32_t* topk_ids,
+                                       float* topk_logprobs, float* row_max, float* row_sumexp, int dtype,
+                                       void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return lmhead_run(nullptr, nullptr, nullptr, M, d, V, k, temperature, topk_ids, topk_logprobs, row_max,
+                    row_sumexp, dtype, ws, ws_bytes, dev_status, stream, nullptr, kMerge);
 }
 
 extern "C" int eagle_lmhead_verify_stats(const void* x, const void* w_lm, const float* bias, int B,

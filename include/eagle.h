@@ -293,6 +293,19 @@ int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M,
                       float* topk_logprobs, float* row_max, float* row_sumexp, int dtype,
                       void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* The same call in two halves (same arguments, same `ws`, in stream order):
+ * eagle_lmhead_topk_partial runs the GEMM and leaves each CTA's partial
+ * lists and log-sum-exp terms in `ws`; eagle_lmhead_topk_merge turns them
+ * into topk_ids / topk_logprobs / row_max / row_sumexp.  Together they launch
+ * exactly the kernels of eagle_lmhead_topk (lets a caller time or overlap the
+ * GEMM on its own). */
+int eagle_lmhead_topk_partial(const void* x, const void* w_lm, const float* bias, int M, int d,
+                              int V, int k, float temperature, int dtype, void* ws,
+                              size_t ws_bytes, int32_t* dev_status, void* stream);
+int eagle_lmhead_topk_merge(int M, int d, int V, int k, float temperature, int32_t* topk_ids,
+                            float* topk_logprobs, float* row_max, float* row_sumexp, int dtype,
+                            void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------
  * eagle_tree_expand -- one EAGLE-2 expansion step for B requests.
  * [M7.5] section 0x06A "Path Value Derivation" and 0x06B "Expansion And

@@ -59,6 +59,10 @@ def test_host_validation_without_gpu(L):
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 100, 1, 1.0, p, p, N, N, 1, N, 0, N, N) == 2
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 1, 0.0, p, p, N, N, 1, N, 0, N, N) == 1
     assert L.eagle_lmhead_topk(p, p, N, 4, 64, 256, 1, 1.0, p, p, N, N, 1, N, 0, N, N) == 3
+    # split LM head: partial without x, merge without outputs, merge without ws
+    assert L.eagle_lmhead_topk_partial(N, p, N, 4, 64, 256, 1, ctypes.c_float(1.0), 1, p, 1 << 30, N, N) == 1
+    assert L.eagle_lmhead_topk_merge(4, 64, 256, 1, ctypes.c_float(1.0), N, p, N, N, 1, p, 1 << 30, N, N) == 1
+    assert L.eagle_lmhead_topk_merge(4, 64, 256, 1, ctypes.c_float(1.0), p, p, N, N, 1, N, 0, N, N) == 3
     # bounded-wait self-test: the limit must be 1 .. 10^6 microseconds
     assert L.eagle_selftest_wait_timeout(0, p, N) == 1
     assert L.eagle_selftest_wait_timeout(1000001, p, N) == 1

@@ -65,6 +65,34 @@ def test_lmhead_bias():
     _lm_check(b, 9, 256, 2048, 5, 1.0, "bf16", seed=3, bias=True)
 
 
+@pytest.mark.parametrize("M,d,V,k,dtype", [(10, 4096, 128256, 10, "bf16"), (300, 256, 4096, 3, "bf16"),
+                                           (7, 128, 1024, 4, "fp32")])
+def test_lmhead_partial_then_merge_equals_one_call(M, d, V, k, dtype):
+    # the two halves launch the same kernels: outputs are bit-identical
+    b = need_gpu()
+    gen = synth.generator(M + V)
+    dt = synth.torch_dtype(dtype)
+    x = synth.normal((M, d), 1.0, dt, gen).cuda()
+    w = synth.normal((V, d), synth.WEIGHT_STD, dt, gen).cuda()
+    code = b.EAGLE_BF16 if dtype == "bf16" else b.EAGLE_FP32
+    ws = b.workspace(b.eagle_lmhead_topk_workspace_size(M, d, V, k, code), "cuda")
+    outs = []
+    for split in (False, True):
+        ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+        lps = torch.empty((M, k), dtype=torch.float32, device="cuda")
+        mx = torch.empty(M, dtype=torch.float32, device="cuda")
+        se = torch.empty(M, dtype=torch.float32, device="cuda")
+        if split:
+            b.eagle_lmhead_topk_partial(x, w, k, ws, temperature=0.8)
+            b.eagle_lmhead_topk_merge(M, d, V, ids, lps, ws, dtype=code, temperature=0.8, row_max=mx, row_sumexp=se)
+        else:
+            b.eagle_lmhead_topk(x, w, k, ids, lps, temperature=0.8, row_max=mx, row_sumexp=se, ws=ws)
+        torch.cuda.synchronize()
+        outs.append([t.cpu() for t in (ids, lps, mx, se)])
+    for a, c in zip(*outs):
+        assert torch.equal(a, c)
+
+
 @pytest.mark.parametrize("M,d,k,T,rows", [
     (10, 4096, 10, 1.0, None),                  # llama8b draft rows, width 10
     (61, 4096, 1, 1.0, [0, 17, 33, 60]),        # llama8b verify rows
