@@ -290,8 +290,8 @@ def profile_traffic():
         return None
     vals = {}
     for line in open(PROFILE):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
+        if ": " in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].rsplit(": ", 1)  # keys may hold ':' themselves
             vals[k.strip()] = v.strip()
     if vals.get("gemm_tc.cu sha256[:16]") != cur:
         return None
