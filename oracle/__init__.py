@@ -32,6 +32,7 @@ from .eagle_oracle import (  # noqa: F401
     ancestor_mask,
     draft_input,
     draft_layer,
+    draft_rows,
     eagle2_tree,
     fuse_proj,
     linear,

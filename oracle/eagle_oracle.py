@@ -875,3 +875,42 @@ def draft_layer(x, weights, positions, k_cache, v_cache, block_table, ctx_lens, 
     act = st(silu(gu[:, :I]) * gu[:, I:])
     out = st(x1 + act @ np.asarray(weights["down"], np.float64).T)
     return out, k.reshape(B, W, Hkv, D), v.reshape(B, W, Hkv, D)
+
+
+def draft_rows(step, width, st, node_row, row_mask, ctx_len, prev, root_token=None):
+    """Bookkeeping of one drafter pass over the nodes of one depth ([M7.5]
+    0x05B: the nodes of a depth are expanded in one pass, each holding its
+    token, parent index, position and draft-KV row; [E3] "Input
+    representation": a drafted node's feature input is the drafter's own
+    output at its parent, the target's fused feature only at the root).
+
+    Reading: the root is processed first (step 0, row 0, feature input = the
+    target feature g, its token the seed token); at step s >= 1 slot j of the
+    frontier (the nodes the expansion step s - 1 chose) takes row
+    1 + (s - 1) * width + j, sees its parent's row and the rows that row sees,
+    sits at position ctx + depth, and its feature input is the drafter output
+    of its parent's slot at step s - 1 (``prev`` rows, slot order).
+
+    st: the expansion store (parent / token / depth / frontier), or None at
+    step 0.  node_row: dict node -> row (updated); row_mask: dict row -> bits
+    (updated).  Returns (rows, tokens, positions, feature inputs [n, d])."""
+    prev = np.asarray(prev, np.float64)
+    if step == 0:
+        node_row[0] = 0
+        row_mask[0] = 1
+        return [0], [int(root_token)], [int(ctx_len)], prev[:1].copy()
+    rows, toks, pos, feats = [], [], [], []
+    r0_prev = 0 if step == 1 else 1 + (step - 2) * width
+    for j, n in enumerate(st["frontier"]):
+        p = st["parent"][n]
+        if p not in node_row:
+            raise ValueError("a frontier node whose parent the drafter has not processed")
+        prow = node_row[p]
+        row = 1 + (step - 1) * width + j
+        node_row[n] = row
+        row_mask[row] = row_mask[prow] | (1 << row)
+        rows.append(row)
+        toks.append(int(st["token"][n]))
+        pos.append(int(ctx_len) + int(st["depth"][n]))
+        feats.append(prev[prow - r0_prev])
+    return rows, toks, pos, np.asarray(feats).reshape(len(rows), prev.shape[1])
