@@ -33,6 +33,8 @@ _SIGS = {
     "eagle_linear_workspace_size": (_Z, [_I, _I, _I, _I]),
     "eagle_linear": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_draft_layer_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "eagle_draft_rows": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                              _P, _P]),
     "eagle_draft_layer": (_I, [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P,
                                _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _Z, _P, _P]),
     "eagle_draft_input": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
@@ -205,6 +207,19 @@ def eagle_draft_layer(x, weights, positions, k_cache, v_cache, block_table, ctx_
         _ptr(q_tree), _ptr(k_tree), _ptr(v_tree), _ptr(tree_mask), r0, Rmax, _ptr(out), B, W, d, Hq, Hkv, D,
         I, dt, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
     return out
+
+
+def eagle_draft_rows(step, width, ctx_lens, node_row, row_mask, prev, r_in, tokens, positions, root_token=None,
+                     frontier=None, n_frontier=None, node_parent=None, node_token=None, node_depth=None,
+                     status=None, stream=None):
+    """Bookkeeping of one drafter pass (see include/eagle.h)."""
+    B, max_nodes = node_row.shape
+    Rmax = row_mask.shape[1]
+    d = prev.shape[-1]
+    _check("eagle_draft_rows", lib().eagle_draft_rows(
+        B, step, width, Rmax, max_nodes, d, _dtype(prev), _ptr(root_token), _ptr(frontier), _ptr(n_frontier),
+        _ptr(node_parent), _ptr(node_token), _ptr(node_depth), _ptr(ctx_lens), _ptr(node_row), _ptr(row_mask),
+        _ptr(prev), _ptr(r_in), _ptr(tokens), _ptr(positions), _ptr(status), _stream(stream)))
 
 
 # ------------------------------------------------------------------ a2

@@ -162,6 +162,79 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
+// Bookkeeping of one drafter pass (one CTA per request): which draft-KV row
+// each node of the depth takes, the rows it sees, its position, token and
+// feature input.  Step 0 is the root: row 0, position ctx, the seed token and
+// the target feature prev[b].  At step s >= 1, frontier slot j takes row
+// r0 = 1 + (s - 1) * width + j, sees its parent's row and what that row sees,
+// sits at ctx + depth, and reads the drafter output of its parent's slot of
+// the previous pass, prev[b * W_prev + (row(parent) - r0_prev)].  Empty
+// slots get token 0, position ctx, zero features and a row that sees only
+// itself.  A parent that the previous pass did not process, or a node id out
+// of range, records EAGLE_ERR_BAD_TREE and reads as an empty slot.
+constexpr int kRowsMaxWidth = 64;
+__global__ void __launch_bounds__(kRowThreads)
+    draft_rows_kernel(int step, int width, int Rmax, int max_nodes, int vec_per_row,
+                      const int32_t* __restrict__ root_token, const int32_t* __restrict__ frontier,
+                      const int32_t* __restrict__ n_frontier, const int32_t* __restrict__ node_parent,
+                      const int32_t* __restrict__ node_token, const int32_t* __restrict__ node_depth,
+                      const int32_t* __restrict__ ctx_lens, int32_t* __restrict__ node_row,
+                      uint64_t* __restrict__ row_mask, const uint4* __restrict__ prev, uint4* __restrict__ r_in,
+                      int32_t* __restrict__ tokens, int32_t* __restrict__ positions, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_src[kRowsMaxWidth];  // feature row of prev per slot, -1: zeros
+  const int b = blockIdx.x;
+  const int W = step == 0 ? 1 : width;
+  const int ctx = ctx_lens[b];
+  int32_t* nrow = node_row + (size_t)b * max_nodes;
+  uint64_t* rmask = row_mask + (size_t)b * Rmax;
+  if (step == 0) {
+    // a new round: no node has a row yet; unused rows see only themselves
+    for (int n = threadIdx.x; n < max_nodes; n += kRowThreads) nrow[n] = n == 0 ? 0 : -1;
+    for (int r = threadIdx.x; r < Rmax; r += kRowThreads) rmask[r] = 1ull << r;
+    if (threadIdx.x == 0) {
+      tokens[b] = root_token[b];
+      positions[b] = ctx;
+      s_src[0] = b;
+    }
+  } else if (threadIdx.x < W) {
+    const int j = threadIdx.x;
+    const int W_prev = step == 1 ? 1 : width;
+    const int r0_prev = step == 1 ? 0 : 1 + (step - 2) * width;
+    const int row = 1 + (step - 1) * width + j;
+    const int nf = n_frontier[b];
+    int src = -1, tok = 0, pos = ctx;
+    uint64_t m = 1ull << row;
+    if (j < nf) {
+      const int n = frontier[(size_t)b * width + j];
+      const int p = (n > 0 && n < max_nodes) ? node_parent[(size_t)b * max_nodes + n] : -1;
+      const int prow = (p >= 0 && p < max_nodes) ? nrow[p] : -1;
+      if (prow >= r0_prev && prow < r0_prev + W_prev) {
+        nrow[n] = row;
+        m |= rmask[prow];
+        tok = node_token[(size_t)b * max_nodes + n];
+        pos = ctx + node_depth[(size_t)b * max_nodes + n];
+        src = b * W_prev + (prow - r0_prev);
+      } else {
+        set_status(status, EAGLE_ERR_BAD_TREE);
+      }
+    }
+    rmask[row] = m;
+    tokens[(size_t)b * width + j] = tok;
+    positions[(size_t)b * width + j] = pos;
+    s_src[j] = src;
+  }
+  __syncthreads();
+  // feature inputs, 16-byte vectors
+  for (int t = threadIdx.x; t < W * vec_per_row; t += kRowThreads) {
+    const int j = t / vec_per_row, v = t % vec_per_row;
+    const int src = s_src[j];
+    r_in[((size_t)b * W + j) * vec_per_row + v] =
+        src >= 0 ? prev[(size_t)src * vec_per_row + v] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 struct LayerWs {
   size_t h, qkv, attn, a, x1, h2, gu, act, lin, att, total;
 };
@@ -298,5 +371,29 @@ extern "C" int eagle_draft_layer(const void* x, const void* w_norm1, const void*
   note_launch();
   EAGLE_TRY(eagle_linear(act, w_down, nullptr, x1, out, M, d, I, dtype, lin_ws, L.lin, dev_status, stream));
 #undef EAGLE_TRY
+  return last_launch_status();
+}
+
+extern "C" int eagle_draft_rows(int B, int step, int width, int Rmax, int max_nodes, int d, int dtype,
+                                const int32_t* root_token, const int32_t* frontier, const int32_t* n_frontier,
+                                const int32_t* node_parent, const int32_t* node_token,
+                                const int32_t* node_depth, const int32_t* ctx_lens, int32_t* node_row,
+                                uint64_t* row_mask, const void* prev, void* r_in, int32_t* tokens,
+                                int32_t* positions, int32_t* dev_status, void* stream) {
+  if (B <= 0 || step < 0 || width < 1 || Rmax < 1 || max_nodes < 1 || d <= 0) return EAGLE_ERR_INVALID_ARG;
+  if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return EAGLE_ERR_INVALID_ARG;
+  if (!ctx_lens || !node_row || !row_mask || !prev || !r_in || !tokens || !positions)
+    return EAGLE_ERR_INVALID_ARG;
+  if (step == 0 && !root_token) return EAGLE_ERR_INVALID_ARG;
+  if (step > 0 && (!frontier || !n_frontier || !node_parent || !node_token || !node_depth))
+    return EAGLE_ERR_INVALID_ARG;
+  const int es = dtype == EAGLE_BF16 ? 2 : 4;
+  if (width > kRowsMaxWidth || Rmax > 64 || (d * es) % 16 || B > 65535) return EAGLE_ERR_UNSUPPORTED;
+  if (step > 0 && 1LL + (long long)step * width > Rmax) return EAGLE_ERR_INVALID_ARG;
+  if (!aligned16(prev) || !aligned16(r_in)) return EAGLE_ERR_INVALID_ARG;
+  launch(draft_rows_kernel, B, kRowThreads, 0, static_cast<cudaStream_t>(stream), step, width, Rmax, max_nodes,
+         d * es / 16, root_token, frontier, n_frontier, node_parent, node_token, node_depth, ctx_lens, node_row,
+         row_mask, static_cast<const uint4*>(prev), static_cast<uint4*>(r_in), tokens, positions, dev_status);
+  note_launch();
   return last_launch_status();
 }

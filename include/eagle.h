@@ -254,6 +254,44 @@ int eagle_tree_attn(const void* q, const void* k_tree, const void* v_tree,
  * Limits: B*W <= 4096, r0 + W <= Rmax <= 64, D in {64, 128}, Hq % Hkv == 0,
  * d % 128 == 0, (Hq + 2 Hkv) D % 128 == 0, Hq D % 128 == 0, I % 64 == 0.
  * ---------------------------------------------------------------------- */
+/* ------------------------------------------------------------------------
+ * eagle_draft_rows -- bookkeeping of one drafter pass of a draft round:
+ * which draft-KV row each node of the depth takes, the rows it sees, its
+ * position, token and feature input, for eagle_draft_input and
+ * eagle_draft_layer.  [M7.5] section 0x05B (the nodes of a depth are expanded
+ * in one pass; each keeps its token, parent, position and draft-KV row);
+ * [E3] section 3.4 "Input representation" (a drafted node's feature is the
+ * drafter's own output at its parent; the target feature only at the root).
+ *   step 0 : the root: row 0, position ctx_lens[b], token root_token[b],
+ *            feature prev[b] (the target's fused feature g, [B, d]); also
+ *            starts the round (node_row = -1 except node 0, every row of
+ *            row_mask sees only itself).
+ *   step s : frontier slot j of request b (the nodes eagle_tree_expand step
+ *            s - 1 chose) takes row 1 + (s - 1) * width + j, row_mask[b, row]
+ *            = row_mask[b, row(parent)] | (1 << row), position = ctx + depth,
+ *            token = node_token, feature = prev[b * W_prev + slot of the
+ *            parent] where prev = the previous pass's eagle_draft_layer
+ *            output [B * W_prev, d] (W_prev = 1 after step 0, else width).
+ *            Slots past n_frontier[b]: token 0, position ctx, zero feature,
+ *            a row that sees only itself.
+ *   node_row : [B, max_nodes] int32 state; row_mask : [B, Rmax] uint64 state
+ *   r_in     : [B * W, d] out (dtype `dtype`), tokens : [B * W] int32 out,
+ *   positions: [B, W] int32 out, W = 1 at step 0, else width.
+ * The layer call of the pass then uses r0 = 0 (step 0) or
+ * 1 + (step - 1) * width, and R = Rmax.
+ * Device-detected: a node whose parent the previous pass did not process,
+ * or a node id out of range -> EAGLE_ERR_BAD_TREE (the slot reads as empty).
+ * Limits: width <= 64, 1 + step * width <= Rmax <= 64, d * element size a
+ * multiple of 16 bytes.
+ * ---------------------------------------------------------------------- */
+int eagle_draft_rows(int B, int step, int width, int Rmax, int max_nodes, int d, int dtype,
+                     const int32_t* root_token, const int32_t* frontier,
+                     const int32_t* n_frontier, const int32_t* node_parent,
+                     const int32_t* node_token, const int32_t* node_depth,
+                     const int32_t* ctx_lens, int32_t* node_row, uint64_t* row_mask,
+                     const void* prev, void* r_in, int32_t* tokens, int32_t* positions,
+                     int32_t* dev_status, void* stream);
+
 size_t eagle_draft_layer_workspace_size(int B, int W, int d, int Hq, int Hkv, int D, int I,
                                         int Rmax, int max_pages, int dtype);
 int eagle_draft_layer(const void* x, const void* w_norm1, const void* w_qkv, const void* w_o,

@@ -93,6 +93,12 @@ def test_host_validation_without_gpu(L):
     assert L.eagle_draft_layer(N, p, p, p, p, p, p, ctypes.c_float(1e-5), ctypes.c_float(5e5), p, p, p, 4, p, 2,
                                p, p, p, p, p, 0, 8, q, 1, 4, 256, 4, 2, 64, 256, 1, N, 0, N, N) == 1
     assert L.eagle_draft_layer_workspace_size(1, 4, 256, 4, 2, 64, 256, 8, 2, 1) > 0
+    # draft rows: step 0 without root tokens, width over 64, rows past Rmax
+    rows = lambda step, width, Rmax, root: L.eagle_draft_rows(1, step, width, Rmax, 64, 256, 1, root, p, p, p, p,
+                                                              p, p, p, p, p, q, p, p, N, N)
+    assert rows(0, 4, 8, N) == 1
+    assert rows(1, 65, 64, p) == 2
+    assert rows(2, 4, 8, p) == 1
     # attention: R > 64, D not in {64, 128}, page size != 16, Hq % Hkv
     base = [p, p, p, p, p, 4, p, 2, p, p, p, N]
     assert L.eagle_tree_attn(*base, 1, 65, 4, 2, 128, 16, ctypes.c_float(0.1), 0, 1, N, 0, N, N) == 2
