@@ -394,6 +394,94 @@ def measure_draft_layer(wl, calls, peak_gbs):
                                       f"{w_bytes / 1e6:.0f} MB + drafter prefix K/V {kv_bytes / 1e6:.0f} MB"}
 
 
+def measure_draft_round(wl, rounds, peak_gbs):
+    """A whole EAGLE draft round at this workload's shape, timed with CUDA
+    events around each round: per depth, eagle_draft_rows -> eagle_draft_input
+    -> eagle_draft_layer -> eagle_lmhead_topk -> eagle_tree_expand, the root
+    pass first, then depth - 1 passes over width nodes per request (the last
+    expansion's nodes are not drafted from).  The drafter's prefix is the
+    workload's KV cache; its embedding table is W_U's shape."""
+    B, d, dev, dt = wl.B, wl.d, wl.dev, wl.dt
+    Hq, Hkv, D, I, W, k, depth = wl.Hq, wl.Hkv, wl.D, synth.FFN_WIDTH[d], wl.width, wl.k, wl.depth
+    Rmax = 1 + (depth - 1) * W
+    if Rmax > 64:
+        return None
+    g = synth.generator(13, dev)
+    nrm = lambda shape, std: synth.normal(shape, std, dt, g, dev)
+    wts = dict(norm1=nrm((d,), 1.0), qkv=nrm(((Hq + 2 * Hkv) * D, d), synth.WEIGHT_STD),
+               o=nrm((d, Hq * D), synth.WEIGHT_STD), norm2=nrm((d,), 1.0),
+               gu=nrm((2 * I, d), synth.WEIGHT_STD), down=nrm((d, I), synth.WEIGHT_STD))
+    w_in = nrm((d, 2 * d), synth.WEIGHT_STD)
+    g_root = nrm((B, d), 1.0)
+    z = lambda *s_, t=torch.int32: torch.zeros(s_, dtype=t, device=dev)
+    max_nodes = 1 + synth.n_candidates(wl.c)
+    tree = dict(parent=z(B, max_nodes), token=z(B, max_nodes), logv=z(B, max_nodes, t=torch.float32),
+                depth=z(B, max_nodes), count=z(B), frontier=z(B, W), nf=z(B))
+    node_row, row_mask = z(B, max_nodes), z(B, Rmax, t=torch.int64)
+    q_tree = torch.zeros((B, Rmax, Hq, D), dtype=dt, device=dev)
+    k_tree, v_tree = torch.zeros((B, Rmax, Hkv, D), dtype=dt, device=dev), torch.zeros((B, Rmax, Hkv, D), dtype=dt, device=dev)
+    bufs = {}
+    for Wp in {1, W}:
+        bufs[Wp] = dict(r=torch.empty((B * Wp, d), dtype=dt, device=dev), tok=z(B * Wp), pos=z(B, Wp),
+                        u=torch.empty((B * Wp, d), dtype=dt, device=dev), ids=z(B * Wp, k),
+                        lps=z(B * Wp, k, t=torch.float32))
+    a_out = [torch.empty((B * (1 if s == 0 else W), d), dtype=dt, device=dev) for s in range(depth)]
+    dt_code = eb.EAGLE_BF16 if dt == torch.bfloat16 else eb.EAGLE_FP32
+    ws_in = eb.workspace(eb.eagle_draft_input_workspace_size(B * W, d, dt_code), dev)
+    ws_layer = eb.workspace(max(eb.eagle_draft_layer_workspace_size(B, Wp, d, Hq, Hkv, D, I, Rmax,
+                                                                     wl.block_table.shape[1], dt_code)
+                                for Wp in (1, W)), dev)
+    root = wl.dev_in["root"]
+
+    def one_round():
+        prev = g_root
+        for s in range(depth):
+            Wp = 1 if s == 0 else W
+            bf = bufs[Wp]
+            eb.eagle_draft_rows(s, W, wl.ctx_lens, node_row, row_mask, prev, bf["r"], bf["tok"], bf["pos"],
+                                root_token=root, frontier=tree["frontier"], n_frontier=tree["nf"],
+                                node_parent=tree["parent"], node_token=tree["token"], node_depth=tree["depth"],
+                                status=wl.status)
+            eb.eagle_draft_input(bf["r"], bf["tok"], wl.w_lm, w_in, bf["u"], ws=ws_in, status=wl.status)
+            eb.eagle_draft_layer(bf["u"], wts, bf["pos"], wl.k_cache, wl.v_cache, wl.block_table, wl.ctx_lens,
+                                 q_tree, k_tree, v_tree, row_mask, 0 if s == 0 else 1 + (s - 1) * W, a_out[s],
+                                 ws=ws_layer, status=wl.status)
+            eb.eagle_lmhead_topk(a_out[s], wl.w_lm, k, bf["ids"], bf["lps"], temperature=1.0, ws=wl.ws_lm,
+                                 status=wl.status)
+            eb.eagle_tree_expand(s, W, bf["ids"].view(B, Wp, k), bf["lps"].view(B, Wp, k), root, tree["parent"],
+                                 tree["token"], tree["logv"], tree["depth"], tree["count"], tree["frontier"],
+                                 tree["nf"], status=wl.status)
+            prev = a_out[s]
+
+    for _ in range(2):
+        one_round()
+    torch.cuda.synchronize()
+    evs = []
+    torch.cuda._sleep(20_000_000)  # the host queues the rounds meanwhile
+    for _ in range(rounds):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        one_round()
+        e1.record()
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    st = eb.read_status(wl.status)
+    if st != 0:
+        raise RuntimeError(f"device status {eb.STATUS.get(st, st)} in the draft round")
+    us = sum(a.elapsed_time(b) for a, b in evs) / rounds * 1e3
+    es = wl.w_lm.element_size()
+    w_bytes = (sum(t.numel() for t in wts.values()) + w_in.numel() + wl.w_lm.numel()) * es
+    kv_bytes = int(wl.ctx_lens.sum().item()) * Hkv * D * 2 * es
+    byts = depth * (w_bytes + kv_bytes)
+    gbs = byts / us / 1e3
+    nodes = B * (k + (depth - 1) * W * k)
+    return {"call": "draft round (rows, input FC, decoder layer, LM head, expansion per depth)",
+            "depth": depth, "avg_round_us": round(us, 1), "draft_nodes_per_round": nodes,
+            "bytes_per_round": byts, "achieved": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak_gbs, 4),
+            "bound": "hbm", "timing": f"CUDA events per round, {rounds} rounds; per depth the drafter's weights, "
+                                      "W_U and the drafter prefix K/V stream once"}
+
+
 def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -473,7 +561,8 @@ def run_ours(args, rank, world):
         raise RuntimeError(f"device status {eb.STATUS.get(st, st)}")
     clocks = clk.summary()
     rows = {"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"]),
-            "draft_layer": measure_draft_layer(wl, max(min(args.steps, 50), 10), peaks["hbm_gbs"])}
+            "draft_layer": measure_draft_layer(wl, max(min(args.steps, 50), 10), peaks["hbm_gbs"]),
+            "draft_round": measure_draft_round(wl, max(min(args.steps // 10, 10), 3), peaks["hbm_gbs"])}
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
