@@ -37,20 +37,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ----------------------------------------------------------------------------
-// tcgen05 path (bf16).  One CTA per (query tile of up to 128 rows, KV split,
-// request x kv head); 192 threads:
-//   warp 0     TMA producer: the Q tile once (3-D box [rows of r][G heads][64]),
-//              then per 128-key block 8 paged K boxes and 8 V boxes of 16 keys
-//              (3-D map over the pool viewed as [pages*16][Hkv][D]) or the
-//              tree's own K/V rows, into a 2-stage ring
-//   warp 1     MMA issuer (one thread): S = Q K^T (M 128, N 128, K D) into one
-//              of two TMEM S buffers, one block ahead; then O_j = P_j V_j
-//              (M 128, N D, K 128, V read MN-major) into one of two TMEM PV
-//              buffers
-//   warps 2-5  softmax, one thread per query row (TMEM lane): masked row max,
-//              P = exp2(S - m) rounded to bf16 into a 128-byte-swizzled shared
-//              tile (the A operand of P V), and O = O * exp2(m_old - m) + O_j
-//              in registers
+// tcgen05 path (bf16).  One CTA per (one or two query tiles of up to 128
+// rows, KV split, request x kv head); 64 + 128 * TPC threads:
+//   warp 0     TMA producer: the Q tiles once (3-D box [rows of r][G heads]
+//              [64]), then per 64-key block 4 paged K boxes and 4 V boxes of
+//              16 keys per 64-column half (3-D map over the pool viewed as
+//              [pages*16][Hkv][D]) or the tree's own K/V rows, into a ring of
+//              kv_stages(TPC) stages
+//   warp 1     MMA issuer (one thread): S = Q K^T (M 128, N 64, K D) into one
+//              of two TMEM S buffers per tile, one block ahead; then
+//              O += P V (M 128, N D, K 64, V read MN-major) into the tile's
+//              TMEM O accumulator.  Two commits per block: S ready, and P V
+//              done (which also frees the K/V stage)
+//   4 warps per query tile: softmax, one thread per query row (TMEM lane):
+//              the block's 64 scores loaded once, masked row max, P =
+//              exp2(S - m) rounded to bf16 into a double-buffered
+//              128-byte-swizzled shared tile (the A operand of P V), and O
+//              rescaled in TMEM only when the row max grows by more than 2^8
 // Masked keys read as -inf through a select, so nothing a masked K row holds
 // reaches the softmax; V rows of a partly filled page or of the padded tree
 // block are zeroed in shared memory before P V reads them.
@@ -69,7 +72,7 @@ constexpr float kRescaleLog2 = 8.f;        // O / l reference moves when the max
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_full[2];
+  uint64_t s_full[2], s_empty[2], p_full[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -136,7 +139,6 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       mbar_init(smem_u32(&sb.s_full[x]), 1);
       mbar_init(smem_u32(&sb.s_empty[x]), 4 * nt);
       mbar_init(smem_u32(&sb.p_full[x]), 4 * nt);
-      mbar_init(smem_u32(&sb.pv_full[x]), 1);
     }
     mbar_init(smem_u32(&sb.drain), 1);
     sb.abort_flag = 0;
@@ -345,7 +347,8 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
                      smem_desc_sw128_mn(vd + (uint32_t)k * 2048u, kBlkBytesHalf), idesc_pv,
                      (j > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(smem_u32(&sb.pv_full[x]));
+        // one commit per block for P V: its completion frees the K/V stage
+        // and is what the softmax warps wait for before touching O
         mma_commit(smem_u32(&sb.kv_empty[st]));
       }
       __syncwarp();
@@ -373,7 +376,11 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
     bool ok = true;
     auto wait_pv = [&](int jp) -> bool {  // P V of block jp complete
       bool w = true;
-      if (lane == 0) w = mbar_wait(smem_u32(&sb.pv_full[jp & 1]), (uint32_t)(jp >> 1) & 1u, abort_flag);
+      // P V(jp) completes the phase jp / kSt of its stage's kv_empty barrier;
+      // the stage cannot be reused (a later phase) before this warp has
+      // finished block jp + kSt - 1 > jp, so the parity is unambiguous
+      if (lane == 0)
+        w = mbar_wait(smem_u32(&sb.kv_empty[jp % kSt]), (uint32_t)(jp / kSt) & 1u, abort_flag);
       w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (w) tc_fence_after();
       return w;
