@@ -141,10 +141,22 @@ class Workload:
         self.ws_ver = eb.workspace(eb.eagle_tree_verify_workspace_size(B, R, V), device)
 
     # ------------------------------------------------------------- step
-    def step(self, lm_events=None):
+    def step(self, lm_events=None, row_events=None):
         """Launch one step on the current stream.  ``lm_events``: list that
-        receives (start, end) CUDA events around each LM-head call."""
+        receives (start, end) CUDA events around each LM-head GEMM launch;
+        ``row_events``: dict name -> list of (start, end) around every other
+        call of the step."""
         t, f, x = self.tree, self.flat, self.dev_in
+
+        def rt(name, call):
+            if row_events is None:
+                call()
+                return
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            row_events.setdefault(name, []).append((e0, e1))
 
         def timed(call, M, k):
             if lm_events is not None:
@@ -169,32 +181,32 @@ class Workload:
         for s in range(self.depth):
             ids, lps = self.cand[s]
             lm(x["draft_x"][s], self.k, ids, lps)
-            eb.eagle_tree_expand(s, self.width, ids, lps, x["root"], t["parent"], t["token"],
-                                 t["logv"], t["depth"], t["count"], t["frontier"], t["nf"],
-                                 status=self.status)
-        eb.eagle_tree_expand_finalize(self.N, t["parent"], t["token"], t["logv"], t["depth"],
-                                      t["count"], self.ctx_lens, f["token"], f["parent_row"],
-                                      f["depth"], f["mask"], f["node_id"], f["position"], f["n_rows"],
-                                      status=self.status)
-        eb.eagle_tree_attn(x["q"], x["k_tree"], x["v_tree"], self.k_cache, self.v_cache,
-                           self.block_table, self.ctx_lens, f["mask"], self.attn_out,
-                           ws=self.ws_attn, status=self.status)
-        eb.eagle_fuse_proj(x["h"][0], x["h"][1], x["h"][2], self.w_proj, self.g, ws=self.ws_fp,
-                           status=self.status)
+            rt("tree_expand", lambda: eb.eagle_tree_expand(
+                s, self.width, ids, lps, x["root"], t["parent"], t["token"], t["logv"], t["depth"],
+                t["count"], t["frontier"], t["nf"], status=self.status))
+        rt("tree_expand_finalize", lambda: eb.eagle_tree_expand_finalize(
+            self.N, t["parent"], t["token"], t["logv"], t["depth"], t["count"], self.ctx_lens, f["token"],
+            f["parent_row"], f["depth"], f["mask"], f["node_id"], f["position"], f["n_rows"], status=self.status))
+        rt("tree_attn", lambda: eb.eagle_tree_attn(
+            x["q"], x["k_tree"], x["v_tree"], self.k_cache, self.v_cache, self.block_table, self.ctx_lens,
+            f["mask"], self.attn_out, ws=self.ws_attn, status=self.status))
+        rt("fuse_proj", lambda: eb.eagle_fuse_proj(x["h"][0], x["h"][1], x["h"][2], self.w_proj, self.g,
+                                                   ws=self.ws_fp, status=self.status))
         if self.T == 0:
             lm(x["x_v"], 1, self.amax, self.amax_lp)
-            eb.eagle_tree_verify(f["parent_row"], f["token"], 0.0, self.depth, self.acc, self.path,
-                                 self.out_tok, n_rows=f["n_rows"], target_argmax=self.amax.view(self.B, self.R),
-                                 V=self.V, ws=self.ws_ver, status=self.status)
+            rt("tree_verify", lambda: eb.eagle_tree_verify(
+                f["parent_row"], f["token"], 0.0, self.depth, self.acc, self.path, self.out_tok,
+                n_rows=f["n_rows"], target_argmax=self.amax.view(self.B, self.R), V=self.V, ws=self.ws_ver,
+                status=self.status))
         else:
-            eb.eagle_lmhead_verify_stats(
+            rt("lmhead_verify_stats", lambda: eb.eagle_lmhead_verify_stats(
                 x["x_v"], self.w_lm, f["parent_row"], f["token"], self.T, self.race_k,
                 self.race_ids, self.race_keys, self.row_max, self.row_sumexp, self.child_logit,
-                n_rows=f["n_rows"], seed=1234, ws=self.ws_lm, status=self.status)
-            eb.eagle_tree_verify_stats(f["parent_row"], f["token"], self.T, self.depth, self.row_max,
-                                       self.row_sumexp, self.child_logit, self.race_ids, self.acc,
-                                       self.path, self.out_tok, self.V, n_rows=f["n_rows"],
-                                       seed=1234, status=self.status)
+                n_rows=f["n_rows"], seed=1234, ws=self.ws_lm, status=self.status))
+            rt("tree_verify_stats", lambda: eb.eagle_tree_verify_stats(
+                f["parent_row"], f["token"], self.T, self.depth, self.row_max, self.row_sumexp,
+                self.child_logit, self.race_ids, self.acc, self.path, self.out_tok, self.V, n_rows=f["n_rows"],
+                seed=1234, status=self.status))
 
     def h2d(self):
         """Copy this step's inputs from pinned host memory (one copy of the
@@ -299,6 +311,54 @@ def profile_traffic():
         return float(vals["dram bytes per launch (verify-row call, M=61)"])
     except (KeyError, ValueError):
         return None
+
+
+def row_rooflines(wl, steps, peaks):
+    """Per-call timing of every other call of the step (CUDA events around
+    each call in a separate pass; events between kernels stop the next
+    kernel's early launch, so these are per-call upper bounds), with the
+    roofline of the calls that stream or contract: algorithmic bytes for
+    the fused projection and the attention, flops for the statistics-mode
+    verification LM head; the expansion, finalize and verification walks are
+    latency-bound and report their time only."""
+    ev = {}
+    torch.cuda.synchronize()
+    torch.cuda._sleep(4_000_000)  # the host stays ahead of the GPU
+    for _ in range(steps):
+        wl.step(row_events=ev)
+    torch.cuda.synchronize()
+    es = wl.w_lm.element_size()
+    M = wl.B * wl.R
+    ctx_sum = int(wl.ctx_lens.sum().item())
+    out = {}
+    for name, lst in ev.items():
+        us = sum(a.elapsed_time(b) for a, b in lst) / len(lst) * 1e3
+        row = {"avg_call_us": round(us, 2), "calls_per_step": len(lst) // steps}
+        if name in ("fuse_proj", "tree_attn"):
+            if name == "fuse_proj":
+                byts = 3 * wl.d * wl.d * es + 4 * M * wl.d * es
+                flops = 2 * M * 3 * wl.d * wl.d
+            else:  # prefix K/V, tree K/V, Q and O; Q K^T and P V over every key of each row
+                byts = (ctx_sum + M) * wl.Hkv * wl.D * 2 * es + 2 * M * wl.Hq * wl.D * es
+                flops = 4 * wl.R * wl.Hq * wl.D * (ctx_sum + wl.B * wl.R)
+            # the bound is whichever floor is higher: the byte stream or the contraction
+            if byts / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
+                gbs = byts / us / 1e3
+                row.update(bound="hbm", bytes_per_call=byts, achieved=round(gbs, 1), unit="GB/s",
+                           frac=round(gbs / peaks["hbm_gbs"], 4))
+            else:
+                tfs = flops / us / 1e6
+                row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
+                           frac=round(tfs / peaks["bf16_tflops"], 4))
+        elif name == "lmhead_verify_stats":
+            flops = 2 * M * wl.d * wl.V
+            tfs = flops / us / 1e6
+            row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
+                       frac=round(tfs / peaks["bf16_tflops"], 4))
+        else:
+            row.update(bound="latency")
+        out[name] = row
+    return out
 
 
 def measure_draft_input(wl, calls, peak_gbs):
@@ -560,9 +620,13 @@ def run_ours(args, rank, world):
     if st != 0:
         raise RuntimeError(f"device status {eb.STATUS.get(st, st)}")
     clocks = clk.summary()
-    rows = {"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"]),
+    rows = row_rooflines(wl, max(min(args.steps, 50), 3), peaks)
+    rows["lmhead_topk"] = {"avg_call_us": round(lm_avg_ms * 1e3, 2), "bound": "hbm", "achieved": round(achieved, 1),
+                           "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                           "timing": "the GEMM launch; see roofline"}
+    rows.update({"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"]),
             "draft_layer": measure_draft_layer(wl, max(min(args.steps, 50), 10), peaks["hbm_gbs"]),
-            "draft_round": measure_draft_round(wl, max(min(args.steps // 10, 10), 3), peaks["hbm_gbs"])}
+            "draft_round": measure_draft_round(wl, max(min(args.steps // 10, 10), 3), peaks["hbm_gbs"])})
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
