@@ -38,18 +38,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // ----------------------------------------------------------------------------
 // tcgen05 path (bf16).  One CTA per (one or two query tiles of up to 128
-// rows, KV split, request x kv head); 64 + 128 * TPC threads:
-//   warp 0     TMA producer: the Q tiles once (3-D box [rows of r][G heads]
+// rows, KV split, request x kv head); 128 + 128 * TPC threads:
+//   warp 1     allocates the tensor memory; warps 0-1 have no other role, so
+//              that the producer and the MMA issuer sit on the sub-partitions
+//              of lane quarters 2 and 3, the quarters that have no query rows
+//              when a tile holds 64 rows or fewer (short trees, batch 64): the
+//              single MMA-issuing thread then shares its issue slots with an
+//              idle warp instead of a busy softmax warp
+//   warp 2     TMA producer: the Q tiles once (3-D box [rows of r][G heads]
 //              [64]), then per 64-key block 4 paged K boxes and 4 V boxes of
 //              16 keys per 64-column half (3-D map over the pool viewed as
 //              [pages*16][Hkv][D]) or the tree's own K/V rows, into a ring of
 //              kv_stages(TPC) stages
-//   warp 1     MMA issuer (one thread): S = Q K^T (M 128, N 64, K D) into one
+//   warp 3     MMA issuer (one thread): S = Q K^T (M 128, N 64, K D) into one
 //              of two TMEM S buffers per tile, one block ahead; then
 //              O += P V (M 128, N D, K 64, V read MN-major) into the tile's
 //              TMEM O accumulator.  Two commits per block: S ready, and P V
 //              done (which also frees the K/V stage)
-//   4 warps per query tile: softmax, one thread per query row (TMEM lane):
+//   warps 4.. (4 per query tile): softmax, one thread per query row (TMEM lane;
+//              a quarter without query rows only keeps the barrier protocol):
 //              the block's 64 scores loaded once, masked row max, P =
 //              exp2(S - m) rounded to bf16 into a double-buffered
 //              128-byte-swizzled shared tile (the A operand of P V), and O
@@ -59,7 +66,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // block are zeroed in shared memory before P V reads them.
 namespace tc {
 constexpr int kBlk = 64;           // keys per block (4 pages)
-// threads: warp 0 TMA, warp 1 MMA, four softmax warps per query tile
 constexpr int kBlkBytesHalf = kBlk * 128;  // one 64-column half of a K or V block
 constexpr int kMaxStages = 8;
 // K/V ring depth: what the shared memory left by the Q tiles and the double
@@ -95,7 +101,7 @@ struct Params {
 }  // namespace tc
 
 template <int D, int TPC>
-__global__ void __launch_bounds__(64 + 128 * TPC, 1)
+__global__ void __launch_bounds__(128 + 128 * TPC, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
   const int n_iter = n_ctx + (split == 0 ? 1 : 0);
   const int rows_tile = p.nr * p.G, rows_total = p.R * p.G;
 
-  if (warp == 0) {
+  if (warp == 2) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_kv = l2_policy_evict_normal();  // other CTAs of the request re-read it
     const uint64_t pol_q = l2_policy_evict_first();
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
     bool ok = true;
     if (n_iter > 0) {
@@ -271,6 +277,7 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     const uint32_t idesc_pv = mma_idesc_bmn(1, 128, D);
+    const uint64_t dq0 = smem_desc_sw128(sQ), dp0 = smem_desc_sw128(sP);
     // S(j) = Q_t K_j^T for each query tile t into S buffer j & 1
     auto issue_s = [&](int j) -> bool {
       const int x = j & 1, st = j % kSt;  // kSt is a compile-time constant
@@ -284,17 +291,21 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       tc_fence_after();
       const int n = j < n_ctx ? kBlk : p.tr;
       const uint32_t idesc = mma_idesc(1, 128, n);
-      const uint32_t kd = sK + st * kTileKV;
       if (lane == 0) {
+        // The MMA thread shares its issue slots with a busy softmax warp, so
+        // the loop is kept to a few instructions per MMA: base descriptors
+        // once, then constant offsets in the descriptors' address field
+        // (bytes >> 4): +32 bytes per 16 columns inside a 128-byte row, the
+        // next 64 columns in the next half tile
+        const uint64_t dk = smem_desc_sw128(sK + st * kTileKV);
         for (int t = 0; t < nt; ++t) {
+          const uint64_t dq = dq0 + (uint64_t)((t * kTileQ) >> 4);
+          const uint32_t dt = tmem + (uint32_t)(t * 2 * kBlk + x * kBlk);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            // +32 bytes per 16 columns inside a 128-byte row; the next 64
-            // columns sit in the next half tile
-            const uint32_t qoff = (uint32_t)(k >> 2) * 16384u + (uint32_t)(k & 3) * 32u;
-            const uint32_t koff = (uint32_t)(k >> 2) * kBlkBytesHalf + (uint32_t)(k & 3) * 32u;
-            mma_bf16(tmem + (uint32_t)(t * 2 * kBlk + x * kBlk), smem_desc_sw128(sQ + t * kTileQ + qoff),
-                     smem_desc_sw128(kd + koff), idesc, k > 0 ? 1u : 0u);
+            const uint32_t qoff = ((uint32_t)(k >> 2) * 16384u + (uint32_t)(k & 3) * 32u) >> 4;
+            const uint32_t koff = ((uint32_t)(k >> 2) * kBlkBytesHalf + (uint32_t)(k & 3) * 32u) >> 4;
+            mma_bf16(dt, dq + qoff, dk + koff, idesc, k > 0 ? 1u : 0u);
           }
         }
         mma_commit(smem_u32(&sb.s_full[x]));
@@ -339,13 +350,14 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t vd = sV + st * kTileKV;
+        const uint64_t dv = smem_desc_sw128_mn(sV + st * kTileKV, kBlkBytesHalf);
         for (int t = 0; t < nt; ++t) {
-          for (int k = 0; k < nk / 16; ++k)  // 64 keys = one 128-byte row of P
-            mma_bf16(tmem + kColO + (uint32_t)(t * D),
-                     smem_desc_sw128(sP + (2 * t + x) * kTileP + (uint32_t)k * 32u),
-                     smem_desc_sw128_mn(vd + (uint32_t)k * 2048u, kBlkBytesHalf), idesc_pv,
-                     (j > 0 || k > 0) ? 1u : 0u);
+          const uint64_t dp = dp0 + (uint64_t)(((2 * t + x) * kTileP) >> 4);
+          const uint32_t dt = tmem + kColO + (uint32_t)(t * D);
+          // 64 keys = one 128-byte row of P: +32 bytes of P and 16 rows
+          // (2048 bytes) of V per MMA
+          for (int k = 0; k < nk / 16; ++k)
+            mma_bf16(dt, dp + (uint32_t)k * 2u, dv + (uint32_t)k * 128u, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
         // one commit per block for P V: its completion frees the K/V stage
         // and is what the softmax warps wait for before touching O
@@ -360,13 +372,17 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       while (!mbar_try_wait(smem_u32(&sb.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else if ((warp - 2) / 4 < nt) {
+  } else if (warp >= 4 && (warp - 4) / 4 < nt) {
     // ------------------------------------------------------------ softmax
-    const int tq = (warp - 2) / 4;      // query tile of this warp group
+    const int tq = (warp - 4) / 4;      // query tile of this warp group
     const int q4 = warp & 3;            // TMEM lane quarter of this warp
     const int i = q4 * 32 + lane;       // query row of the tile = TMEM lane
     const int gi = (TPC * cq + tq) * rows_tile + i;
     const bool row_ok = i < rows_tile && gi < rows_total;
+    // a quarter with no query row keeps only the barrier protocol: its P rows
+    // and O rows feed nothing that is written out
+    const int tile_rows = min(rows_tile, rows_total - (TPC * cq + tq) * rows_tile);
+    const bool quad_live = q4 * 32 < tile_rows;
     const int r_i = row_ok ? gi / p.G : 0;
     const uint64_t mrow = row_ok ? p.tree_mask[(size_t)b * p.R + r_i] : 0ull;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
@@ -392,6 +408,14 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
+      if (!quad_live) {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&sb.s_empty[x]));
+          mbar_arrive(smem_u32(&sb.p_full[x]));
+        }
+        continue;
+      }
       const bool tree = j >= n_ctx;
       const int kb = (blk_lo + j) * kBlk;
       // visible keys of this block as a 64-bit mask (all set for a full
@@ -488,8 +512,8 @@ __global__ void __launch_bounds__(64 + 128 * TPC, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sb.p_full[x]));
     }
     // O is final once the last P V completes
-    if (ok && n_iter > 0) ok = wait_pv(n_iter - 1);
-    if (ok) {
+    if (ok && quad_live && n_iter > 0) ok = wait_pv(n_iter - 1);
+    if (ok && quad_live) {
       const int r = r_i, h = kvh * p.G + gi % p.G;
       const size_t row = ((size_t)b * p.R + r) * p.Hq + h;
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -778,14 +802,14 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   };
   if (D == 128) {
     if (pl.tpc == 2)
-      run(tree_attn_tc_kernel<128, 2>, tc_smem<128>(2), 320);
+      run(tree_attn_tc_kernel<128, 2>, tc_smem<128>(2), 384);
     else
-      run(tree_attn_tc_kernel<128, 1>, tc_smem<128>(1), 192);
+      run(tree_attn_tc_kernel<128, 1>, tc_smem<128>(1), 256);
   } else {
     if (pl.tpc == 2)
-      run(tree_attn_tc_kernel<64, 2>, tc_smem<64>(2), 320);
+      run(tree_attn_tc_kernel<64, 2>, tc_smem<64>(2), 384);
     else
-      run(tree_attn_tc_kernel<64, 1>, tc_smem<64>(1), 192);
+      run(tree_attn_tc_kernel<64, 1>, tc_smem<64>(1), 256);
   }
   note_launch();
   if (pl.splits > 1) {
