@@ -351,10 +351,17 @@ def row_rooflines(wl, steps, peaks):
                 row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
                            frac=round(tfs / peaks["bf16_tflops"], 4))
         elif name == "lmhead_verify_stats":
+            # W_U once plus the activation rows; 2 M d V flops
+            byts = wl.V * wl.d * es + M * wl.d * es
             flops = 2 * M * wl.d * wl.V
-            tfs = flops / us / 1e6
-            row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
-                       frac=round(tfs / peaks["bf16_tflops"], 4))
+            if byts / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
+                gbs = byts / us / 1e3
+                row.update(bound="hbm", bytes_per_call=byts, achieved=round(gbs, 1), unit="GB/s",
+                           frac=round(gbs / peaks["hbm_gbs"], 4))
+            else:
+                tfs = flops / us / 1e6
+                row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
+                           frac=round(tfs / peaks["bf16_tflops"], 4))
         else:
             row.update(bound="latency")
         out[name] = row

@@ -323,6 +323,21 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32:
+// relative error about 2^-22; results below 2^-126 flush to zero, -inf -> 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Maximum that returns NaN when either input is NaN (PTX max.NaN.f32).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
 // (value, id) ordering used by every top-k: larger value first, then lower id.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);

@@ -393,60 +393,102 @@ __device__ __forceinline__ void race_gumbel16(const LmParams& p, int grow, int i
   }
 }
 
+// Insert (z, id) into the sorted list; id is larger than every listed id.
+// Slot t is beaten iff z is larger, or (unless PLAIN: no slot is empty) equal
+// while the slot is empty; the beaten slots form a suffix, which shifts down
+// by one with z at its head.
+template <int KMAX, bool PLAIN>
+__device__ __forceinline__ void list_insert(RowTopK<KMAX>& r, float z, int id) {
+  float pv = 0.f;
+  int pi = 0;
+  bool pb = false;
+#pragma unroll
+  for (int t = 0; t < KMAX; ++t) {
+    const float ov = r.av[t];
+    const int oi = r.ai[t];
+    const bool b = PLAIN ? z > ov : (z > ov || (z == ov && oi == 0x7fffffff));
+    r.av[t] = b ? (pb ? pv : z) : ov;
+    r.ai[t] = b ? (pb ? pi : id) : oi;
+    pv = ov;
+    pi = oi;
+    pb = b;
+  }
+}
+
 // Fold 16 consecutive vocabulary ids id0.. (values v, the first `valid` of
 // them real; valid <= 0 for a lane without a row) into the row: log-sum-exp
 // of z/T always; top-K of z, or with RACE of z/T + g (g from race_gumbel16).
+// A row's ids arrive in strictly increasing order (its CTA's tiles, then the
+// 16-column chunks, in order), so a new id loses every tie with a listed one:
+// it beats a slot iff its value is larger, or equal while the slot is still
+// empty (id 0x7fffffff).  Against a list sorted by (value desc, id asc) that
+// test is monotone along the slots, so a candidate's insertion is one
+// independent compare per slot, not a chain through the list.
 // Must be called by all 32 lanes of the warp together.
 template <int KMAX, bool RACE>
 __device__ __forceinline__ void row_chunk(RowTopK<KMAX>& r, float (&v)[16], const float (&g)[16],
                                           int id0, int valid, float inv_t, int K) {
-  float y[16];
-  float cm = -INFINITY;
+  // chunk maximum of z/T: multiplying by inv_t > 0 is monotone in fp32, so
+  // max(z) inv_t is exactly max(z inv_t); the NaN-propagating maximum also
+  // tells whether any real column is NaN
+  float vm = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    y[j] = j < valid ? v[j] * inv_t : -INFINITY;
-    r.nan_seen |= (j < valid) && isnan(v[j]);
-    cm = fmaxf(cm, y[j]);
+  for (int j = 0; j < 16; ++j) vm = fmax_nan(vm, j < valid ? v[j] : -INFINITY);
+  const bool nan = isnan(vm);
+  r.nan_seen |= nan;
+  if (nan) {  // rare: the maximum over the real columns that are not NaN
+    vm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) vm = fmaxf(vm, j < valid ? v[j] : -INFINITY);
   }
-  const float nm = fmaxf(r.m, cm);
+  const float nm = fmaxf(r.m, vm * inv_t);
   if (nm != -INFINITY) {
-    float acc = 0.f;
+    // exp(z/T - m) = 2^(z log2e/T - m log2e): one fused multiply-add per id
+    const float sl = inv_t * kLog2e, ml = nm * kLog2e;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc += exp2f((y[j] - nm) * kLog2e);
-    r.s = r.s * exp2f((r.m - nm) * kLog2e) + acc;
+    for (int j = 0; j < 16; j += 2) {
+      const float e0 = ex2_approx(fmaf(v[j], sl, -ml)), e1 = ex2_approx(fmaf(v[j + 1], sl, -ml));
+      a0 += j < valid ? e0 : 0.f;
+      a1 += j + 1 < valid ? e1 : 0.f;
+    }
+    r.s = r.s * ex2_approx((r.m - nm) * kLog2e) + (a0 + a1);
     r.m = nm;
   }
   if (RACE) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = y[j] + g[j];  // the race key replaces z below
+    for (int j = 0; j < 16; ++j) v[j] = v[j] * inv_t + g[j];  // the race key replaces z below
   }
-  // candidates: values that beat the current K-th best
+  // candidates: values that beat the current K-th slot
+  const bool full = r.ti != 0x7fffffff;
   unsigned cmask = 0;
 #pragma unroll
   for (int j = 0; j < 16; ++j)
-    if (j < valid && better(v[j], id0 + j, r.tv, r.ti)) cmask |= 1u << j;
+    if (j < valid && (v[j] > r.tv || (!full && v[j] == r.tv))) cmask |= 1u << j;
   // one candidate per lane per round, the whole warp in step
   while (__any_sync(0xffffffffu, cmask != 0)) {
     const int jc = cmask ? __ffs(cmask) - 1 : -1;
     cmask &= cmask - 1;
-    float z = -INFINITY;
-    int id = 0x7fffffff;
+    // v[jc] by a 4-level select on the bits of jc; a lane without a
+    // candidate re-inserts an empty slot (-inf beats only empty slots)
+    float z;
+    {
+      float h[8], q[4], w[2];
 #pragma unroll
-    for (int t = 0; t < 16; ++t)
-      if (t == jc) {
-        z = v[t];
-        id = id0 + t;
-      }
+      for (int t = 0; t < 8; ++t) h[t] = (jc & 8) ? v[t + 8] : v[t];
 #pragma unroll
-    for (int t = 0; t < KMAX; ++t) {
-      const bool b = better(z, id, r.av[t], r.ai[t]);
-      const float oz = r.av[t];
-      const int oi = r.ai[t];
-      r.av[t] = b ? z : oz;
-      r.ai[t] = b ? id : oi;
-      z = b ? oz : z;
-      id = b ? oi : id;
+      for (int t = 0; t < 4; ++t) q[t] = (jc & 4) ? h[t + 4] : h[t];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) w[t] = (jc & 2) ? q[t + 2] : q[t];
+      z = jc < 0 ? -INFINITY : ((jc & 1) ? w[1] : w[0]);
     }
+    const int id = jc < 0 ? 0x7fffffff : id0 + jc;
+    // once every candidate lane's list is full no slot is empty, and the
+    // slot test is the plain value compare
+    if (__all_sync(0xffffffffu, jc < 0 || r.ti != 0x7fffffff))
+      list_insert<KMAX, true>(r, z, id);
+    else
+      list_insert<KMAX, false>(r, z, id);
     r.tv = r.av[KMAX - 1];
     r.ti = r.ai[KMAX - 1];
   }
@@ -1205,12 +1247,16 @@ int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d,
       return EAGLE_ERR_CUDA;
     auto kern = k <= 1 ? lmhead_topk_kernel<1>
                 : k <= 4 ? lmhead_topk_kernel<4>
+                : k <= 8 ? lmhead_topk_kernel<8>
+                : k <= 12 ? lmhead_topk_kernel<12>
                 : k <= 16 ? lmhead_topk_kernel<16> : lmhead_topk_kernel<32>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     launch(kern, n_ctas, kThreads, smem, s, mx, mw, p);
   } else {
     auto kern = k <= 1 ? lmhead_topk_f32_kernel<1>
                 : k <= 4 ? lmhead_topk_f32_kernel<4>
+                : k <= 8 ? lmhead_topk_f32_kernel<8>
+                : k <= 12 ? lmhead_topk_f32_kernel<12>
                 : k <= 16 ? lmhead_topk_f32_kernel<16> : lmhead_topk_f32_kernel<32>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     launch(kern, n_ctas, kEpiThreads, smem, s, (const float*)x, (const float*)w_lm, d, p);

@@ -65,6 +65,54 @@ def test_lmhead_bias():
     _lm_check(b, 9, 256, 2048, 5, 1.0, "bf16", seed=3, bias=True)
 
 
+@pytest.mark.parametrize("dtype,k", [("bf16", 8), ("bf16", 3), ("fp32", 8)])
+def test_lmhead_masked_vocabulary(dtype, k):
+    """Degenerate rows: a -inf bias masks all but three ids (spread over the
+    CTAs' vocabulary slices), so a top-8 list must end with masked ids.  They
+    tie at -inf and are listed by ascending id after the three finite ones,
+    with log-prob -inf, as the oracle orders them."""
+    b = need_gpu()
+    M, d, V = 20, 256, 4096
+    gen = synth.generator(41 + k)
+    dt = synth.torch_dtype(dtype)
+    x = synth.normal((M, d), 1.0, dt, gen)
+    w = synth.normal((V, d), synth.WEIGHT_STD, dt, gen)
+    bias = torch.full((V,), float("-inf"))
+    allowed = [4000, 1234, 77]
+    bias[allowed] = 0.0
+    ids, lp, rm, rs, st = _lm_gpu(b, x, w, k, 1.0, bias)
+    assert st == 0
+    ref = oracle.lmhead_topk(x.float().numpy(), w.float().numpy(), k, bias=bias.numpy())
+    assert np.array_equal(ids, ref["ids"])
+    fin = np.isfinite(ref["logprobs"])
+    assert fin.sum(axis=1).tolist() == [min(k, 3)] * M
+    assert np.all(np.isneginf(lp[~fin]))
+    assert np.abs(lp[fin] - ref["logprobs"][fin]).max() < 1e-3
+    assert np.abs(rm - ref["row_max"]).max() < 1e-3
+
+
+def test_lmhead_nan_logit_sets_status_and_is_never_listed():
+    """A NaN logit (here from a NaN bias entry) raises EAGLE_ERR_NONFINITE;
+    the NaN id never enters a list, so the ids equal the oracle's with that id
+    masked."""
+    b = need_gpu()
+    M, d, V, k = 12, 256, 4096, 8
+    gen = synth.generator(43)
+    x = synth.normal((M, d), 1.0, torch.bfloat16, gen)
+    w = synth.normal((V, d), synth.WEIGHT_STD, torch.bfloat16, gen)
+    ref0 = oracle.lmhead_topk(x.float().numpy(), w.float().numpy(), k)
+    bad = int(ref0["ids"][0, 0])  # row 0's best id
+    bias = torch.zeros(V)
+    bias[bad] = float("nan")
+    ids, _, _, _, st = _lm_gpu(b, x, w, k, 1.0, bias)
+    assert st == 7  # EAGLE_ERR_NONFINITE
+    masked = bias.clone()
+    masked[bad] = float("-inf")
+    ref = oracle.lmhead_topk(x.float().numpy(), w.float().numpy(), k, bias=masked.numpy())
+    assert not np.any(ids == bad)
+    check_topk(ids, np.zeros_like(ids, dtype=np.float32), ref["z"], lambda i, v: 0.0, k, 1e-4)
+
+
 @pytest.mark.parametrize("M,d,V,k,dtype", [(10, 4096, 128256, 10, "bf16"), (300, 256, 4096, 3, "bf16"),
                                            (7, 128, 1024, 4, "fp32")])
 def test_lmhead_partial_then_merge_equals_one_call(M, d, V, k, dtype):
