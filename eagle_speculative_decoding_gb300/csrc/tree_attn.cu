@@ -24,13 +24,6 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// 2^x by the SFU's approximate base-2 exponential (subnormal results flush to
-// zero; 2^-inf = 0).
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -39,22 +32,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // ----------------------------------------------------------------------------
 // tcgen05 path (bf16).  One CTA per (one or two query tiles of up to 128
 // rows, KV split, request x kv head); 128 + 128 * TPC threads:
-//   warp 1     allocates the tensor memory; warps 0-1 have no other role, so
-//              that the producer and the MMA issuer sit on the sub-partitions
-//              of lane quarters 2 and 3, the quarters that have no query rows
-//              when a tile holds 64 rows or fewer (short trees, batch 64): the
-//              single MMA-issuing thread then shares its issue slots with an
-//              idle warp instead of a busy softmax warp
+//   warp 1     allocates the tensor memory, then issues the P V MMAs (one
+//              thread); warp 0 has no role, so that the producer and the S
+//              issuer sit on the sub-partitions of lane quarters 2 and 3, the
+//              quarters that have no query rows when a tile holds 64 rows or
+//              fewer (short trees, batch 64)
 //   warp 2     TMA producer: the Q tiles once (3-D box [rows of r][G heads]
 //              [64]), then per 64-key block 4 paged K boxes and 4 V boxes of
 //              16 keys per 64-column half (3-D map over the pool viewed as
 //              [pages*16][Hkv][D]) or the tree's own K/V rows, into a ring of
 //              kv_stages(TPC) stages
-//   warp 3     MMA issuer (one thread): S = Q K^T (M 128, N 64, K D) into one
-//              of two TMEM S buffers per tile, one block ahead; then
-//              O += P V (M 128, N D, K 64, V read MN-major) into the tile's
-//              TMEM O accumulator.  Two commits per block: S ready, and P V
-//              done (which also frees the K/V stage)
+//   warp 3     S issuer (one thread): S = Q K^T (M 128, N 64, K D) into one
+//              of two TMEM S buffers per tile, up to two blocks ahead; warp 1
+//              issues O += P V (M 128, N D, K 64, V read MN-major) into the
+//              tile's TMEM O accumulator as soon as P is ready.  Two issuing
+//              threads, because one thread issues an MMA only every ≈ 50
+//              cycles; the commits: S ready, and P V done (which also frees
+//              the K/V stage)
 //   warps 4.. (4 per query tile): softmax, one thread per query row (TMEM lane;
 //              a quarter without query rows only keeps the barrier protocol):
 //              the block's 64 scores loaded once, masked row max, P =
@@ -79,7 +73,7 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2], p_full[2];
-  uint64_t drain;
+  uint64_t drain, drain_pv;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -147,6 +141,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       mbar_init(smem_u32(&sb.p_full[x]), 4 * nt);
     }
     mbar_init(smem_u32(&sb.drain), 1);
+    mbar_init(smem_u32(&sb.drain_pv), 1);
     sb.abort_flag = 0;
     fence_mbar_init();
   }
@@ -270,14 +265,13 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     bool ok = true;
     if (n_iter > 0) {
       if (lane == 0) ok = mbar_wait(smem_u32(&sb.q_full), 0, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
-    const uint32_t idesc_pv = mma_idesc_bmn(1, 128, D);
-    const uint64_t dq0 = smem_desc_sw128(sQ), dp0 = smem_desc_sw128(sP);
+    const uint64_t dq0 = smem_desc_sw128(sQ);
     // S(j) = Q_t K_j^T for each query tile t into S buffer j & 1
     auto issue_s = [&](int j) -> bool {
       const int x = j & 1, st = j % kSt;  // kSt is a compile-time constant
@@ -313,9 +307,25 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       __syncwarp();
       return true;
     };
-    if (ok && n_iter > 0) ok = issue_s(0);
+    for (int j = 0; ok && j < n_iter; ++j) ok = issue_s(j);
+    if (lane == 0) {
+      // drain (always: after an abort elsewhere no consumer may have waited
+      // for the last S): every S MMA completes before tensor memory is freed
+      mma_commit(smem_u32(&sb.drain));
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&sb.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ P V issuer
+    // A second MMA-issuing thread: O += P V of block j goes out as soon as P
+    // of block j is ready, without queuing behind the S MMAs of later blocks
+    // (S(j) is complete before P(j) exists, so the K/V stage that P V's
+    // commit frees holds nothing an S MMA still reads)
+    bool ok = true;
+    const uint32_t idesc_pv = mma_idesc_bmn(1, 128, D);
+    const uint64_t dp0 = smem_desc_sw128(sP);
     for (int j = 0; ok && j < n_iter; ++j) {
-      if (j + 1 < n_iter && !(ok = issue_s(j + 1))) break;
       const int x = j & 1, st = j % kSt;
       const uint32_t ph = (uint32_t)(j >> 1) & 1u, kph = (uint32_t)(j / kSt) & 1u;
       if (lane == 0) ok = mbar_wait(smem_u32(&sb.v_full[st]), kph, abort_flag);
@@ -365,11 +375,11 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       }
       __syncwarp();
     }
-    if (!ok && lane == 0) {
-      // drain: every MMA issued so far completes before tensor memory is freed
-      mma_commit(smem_u32(&sb.drain));
+    if (lane == 0) {
+      // drain: every P V MMA completes before tensor memory is freed
+      mma_commit(smem_u32(&sb.drain_pv));
       const unsigned long long t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_u32(&sb.drain), 0) && globaltimer_ns() - t0 < 100000000ull) {
+      while (!mbar_try_wait(smem_u32(&sb.drain_pv), 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
   } else if (warp >= 4 && (warp - 4) / 4 < nt) {
@@ -393,8 +403,9 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     auto wait_pv = [&](int jp) -> bool {  // P V of block jp complete
       bool w = true;
       // P V(jp) completes the phase jp / kSt of its stage's kv_empty barrier;
-      // the stage cannot be reused (a later phase) before this warp has
-      // finished block jp + kSt - 1 > jp, so the parity is unambiguous
+      // the next phase needs P V(jp + kSt), hence P(jp + kSt), which this
+      // warp writes only after every wait on jp (jp >= j - 2, kSt >= 3), so
+      // the parity is unambiguous
       if (lane == 0)
         w = mbar_wait(smem_u32(&sb.kv_empty[jp % kSt]), (uint32_t)(jp / kSt) & 1u, abort_flag);
       w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
@@ -410,10 +421,13 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       tc_fence_after();
       if (!quad_live) {
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&sb.s_empty[x]));
-          mbar_arrive(smem_u32(&sb.p_full[x]));
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&sb.s_empty[x]));
+        // p_full of block j only after P V(j - 2): the S thread runs up to
+        // two blocks ahead of P V, so without this wait the arrivals of a
+        // warp with no rows for block j + 2 could complete block j's phase
+        // before the warps with rows have written P(j)
+        if (j >= 2 && !(ok = wait_pv(j - 2))) break;
+        if (lane == 0) mbar_arrive(smem_u32(&sb.p_full[x]));
         continue;
       }
       const bool tree = j >= n_ctx;
@@ -477,9 +491,13 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         l *= alpha;
       }
       if (need) m = bm;
-      // pass 2: P = 2^(S * scale_log2 - m) as bf16 into the swizzled P tile
+      // pass 2: P = 2^(S * scale_log2 - m) as bf16 into the swizzled P tile,
+      // once P V(j - 2) has read this buffer (the P V thread commits it
+      // separately from the S MMAs, so S(j) being complete says nothing
+      // about it)
+      if (j >= 2 && !(ok = wait_pv(j - 2))) break;
       const float neg_m = m == -INFINITY ? 0.f : -m;
-      unsigned char* prow = prow0 + x * kTileP;  // P(j - 2) in this buffer is consumed
+      unsigned char* prow = prow0 + x * kTileP;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBlk / 32; ++c) {
