@@ -33,15 +33,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // tcgen05 path (bf16).  One CTA per (one or two query tiles of up to 128
 // rows, KV split, request x kv head); 128 + 128 * TPC threads:
 //   warp 1     allocates the tensor memory, then issues the P V MMAs (one
-//              thread); warp 0 has no role, so that the producer and the S
-//              issuer sit on the sub-partitions of lane quarters 2 and 3, the
-//              quarters that have no query rows when a tile holds 64 rows or
-//              fewer (short trees, batch 64)
+//              thread); with one query tile warp 0 has no role, so that the
+//              producer and the S issuer sit on the sub-partitions of lane
+//              quarters 2 and 3, the quarters that have no query rows when a
+//              tile holds 64 rows or fewer (short trees, batch 64)
 //   warp 2     TMA producer: the Q tiles once (3-D box [rows of r][G heads]
 //              [64]), then per 64-key block 4 paged K boxes and 4 V boxes of
 //              16 keys per 64-column half (3-D map over the pool viewed as
 //              [pages*16][Hkv][D]) or the tree's own K/V rows, into a ring of
-//              kv_stages(TPC) stages
+//              kv_stages(TPC) stages; with two query tiles warp 0 loads Q and
+//              K (its stages freed by S) and warp 2 only V (freed by P V)
 //   warp 3     S issuer (one thread): S = Q K^T (M 128, N 64, K D) into one
 //              of two TMEM S buffers per tile, up to two blocks ahead; warp 1
 //              issues O += P V (M 128, N D, K 64, V read MN-major) into the
@@ -71,7 +72,7 @@ __host__ __device__ constexpr int kv_stages(int tpc) {
 constexpr float kRescaleLog2 = 8.f;        // O / l reference moves when the max grows by > 2^8
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
+  uint64_t k_full[kMaxStages], v_full[kMaxStages], k_empty[kMaxStages], kv_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2], p_full[2];
   uint64_t drain, drain_pv;
   uint32_t tmem_base;
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
   constexpr uint32_t kTileKV = (uint32_t)kBlk * 128u * NH;
   constexpr uint32_t kTileP = 128u * kBlk * 2u;      // 128 rows x 64 keys
   constexpr int kSt = kv_stages<D>(TPC);
+  constexpr bool kSplitLoad = TPC == 2;  // separate K and V producers (see the producers)
   // TMEM columns: S of tile t, buffer x at t * 2 kBlk + x kBlk; O of tile t at
   // tpc * 2 kBlk + t D
   constexpr uint32_t kColO = (uint32_t)(TPC * 2 * kBlk);
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     for (int x = 0; x < kSt; ++x) {
       mbar_init(smem_u32(&sb.k_full[x]), 1);
       mbar_init(smem_u32(&sb.v_full[x]), 1);
+      mbar_init(smem_u32(&sb.k_empty[x]), 1);
       mbar_init(smem_u32(&sb.kv_empty[x]), 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -169,8 +172,14 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
   const int n_iter = n_ctx + (split == 0 ? 1 : 0);
   const int rows_tile = p.nr * p.G, rows_total = p.R * p.G;
 
-  if (warp == 2) {
-    // ------------------------------------------------------------ producer
+  if (warp == 2 || (kSplitLoad && warp == 0)) {
+    // ------------------------------------------------------------ producers
+    // With two query tiles (a 3-stage ring) warp 0 loads Q and the K blocks
+    // and warp 2 the V blocks: a K stage is released as soon as S of its
+    // block is complete, a V stage only after P V, so the K loads run ahead
+    // of the V loads by the softmax of a block.  With one tile (5 stages)
+    // warp 2 loads everything and a stage is released after P V.
+    const bool kload = !kSplitLoad || warp == 0, vload = !kSplitLoad || warp == 2;
     const uint64_t pol_kv = l2_policy_evict_normal();  // other CTAs of the request re-read it
     const uint64_t pol_q = l2_policy_evict_first();
     const uint32_t oob_row = (uint32_t)p.num_pages * 16u;  // a row past the pool: reads zeros
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       return pg;
     };
     int issued = 0;
-    if (lane == 0 && n_iter > 0) {
+    if (kload && lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)(nt * NH * rows_tile) * 128u);
       for (int t = 0; t < nt; ++t)
 #pragma unroll
@@ -205,7 +214,8 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         pg_cur = pg_next;
         pg_next = j + kGrp < n_ctx ? page_group(j / kGrp + 1) : -1;
       }
-      if (lane == 0) ok = mbar_wait(smem_u32(&sb.kv_empty[st]), ph ^ 1u, abort_flag);
+      if (lane == 0)
+        ok = mbar_wait(smem_u32(vload ? &sb.kv_empty[st] : &sb.k_empty[st]), ph ^ 1u, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const uint32_t kd = sK + st * kTileKV, vd = sV + st * kTileKV;
@@ -218,29 +228,31 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
           rows[q] = pq >= 0 ? pq * 16 : (int)oob_row;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(kf, kTileKV);
 #pragma unroll
-          for (int q = 0; q < kBlk / 16; ++q)
+          for (int o = 0; o < 2; ++o) {
+            if (!(o == 0 ? kload : vload)) continue;
+            const uint32_t dst = o == 0 ? kd : vd, fb = o == 0 ? kf : vf;
+            const CUtensorMap* map = o == 0 ? &map_k : &map_v;
+            mbar_arrive_expect_tx(fb, kTileKV);
 #pragma unroll
-            for (int h = 0; h < NH; ++h)
-              tma_load_3d(kd + h * kBlkBytesHalf + q * 2048u, &map_k, kf, h * 64, kvh, rows[q], pol_kv);
-          mbar_arrive_expect_tx(vf, kTileKV);
+            for (int q = 0; q < kBlk / 16; ++q)
 #pragma unroll
-          for (int q = 0; q < kBlk / 16; ++q)
-#pragma unroll
-            for (int h = 0; h < NH; ++h)
-              tma_load_3d(vd + h * kBlkBytesHalf + q * 2048u, &map_v, vf, h * 64, kvh, rows[q], pol_kv);
+              for (int h = 0; h < NH; ++h)
+                tma_load_3d(dst + h * kBlkBytesHalf + q * 2048u, map, fb, h * 64, kvh, rows[q], pol_kv);
+          }
         }
       } else if (lane == 0) {  // the tree block: rows of this request's tree K / V
         const uint32_t bytes = (uint32_t)NH * p.tr * 128u;
-        mbar_arrive_expect_tx(kf, bytes);
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          tma_load_3d(kd + h * kBlkBytesHalf, &map_kt, kf, h * 64, kvh, b * p.R, pol_q);
-        mbar_arrive_expect_tx(vf, bytes);
+        for (int o = 0; o < 2; ++o) {
+          if (!(o == 0 ? kload : vload)) continue;
+          const uint32_t dst = o == 0 ? kd : vd, fb = o == 0 ? kf : vf;
+          const CUtensorMap* map = o == 0 ? &map_kt : &map_vt;
+          mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          tma_load_3d(vd + h * kBlkBytesHalf, &map_vt, vf, h * 64, kvh, b * p.R, pol_q);
+          for (int h = 0; h < NH; ++h)
+            tma_load_3d(dst + h * kBlkBytesHalf, map, fb, h * 64, kvh, b * p.R, pol_q);
+        }
       }
       if (++st == kSt) {
         st = 0;
@@ -253,12 +265,12 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       for (int j = max(0, issued - kSt); j < issued; ++j) {
         const uint32_t ph2 = (uint32_t)(j / kSt) & 1u;
         const unsigned long long t0 = globaltimer_ns();
-        while (!(mbar_try_wait(smem_u32(&sb.k_full[j % kSt]), ph2) &&
-                 mbar_try_wait(smem_u32(&sb.v_full[j % kSt]), ph2)) &&
+        while (!((!kload || mbar_try_wait(smem_u32(&sb.k_full[j % kSt]), ph2)) &&
+                 (!vload || mbar_try_wait(smem_u32(&sb.v_full[j % kSt]), ph2))) &&
                globaltimer_ns() - t0 < 100000000ull) {
         }
       }
-      if (n_iter > 0 && !mbar_try_wait(smem_u32(&sb.q_full), 0)) {
+      if (kload && n_iter > 0 && !mbar_try_wait(smem_u32(&sb.q_full), 0)) {
         const unsigned long long t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&sb.q_full), 0) && globaltimer_ns() - t0 < 100000000ull) {
         }
@@ -303,6 +315,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
           }
         }
         mma_commit(smem_u32(&sb.s_full[x]));
+        if (kSplitLoad) mma_commit(smem_u32(&sb.k_empty[st]));  // the K stage is free once S is complete
       }
       __syncwarp();
       return true;
