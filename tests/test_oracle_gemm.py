@@ -80,3 +80,26 @@ def test_lmhead_bias_and_temperature():
         oracle.lmhead_topk(x, w, 0)
     with pytest.raises(ValueError):
         oracle.lmhead_topk(x, w, 2, temperature=0.0)
+
+
+def test_lmhead_masked_ids_follow_by_ascending_id():
+    """A -inf bias removes an id from the softmax: the normaliser is the one
+    of the allowed ids alone, and a list longer than the allowed set ends with
+    masked ids in ascending order at log-prob -inf (the (z desc, id asc)
+    order with z = -inf for all of them)."""
+    d, V, k = 6, 24, 6
+    x, w = _rand((2, d), 14), _rand((V, d), 15)
+    allowed = [19, 4, 11]
+    bias = np.full(V, -np.inf)
+    bias[allowed] = 0.0
+    res = oracle.lmhead_topk(x, w, k, bias=bias)
+    for i in range(2):
+        z = {v: float(x[i] @ w[v]) for v in allowed}
+        fin = sorted(allowed, key=lambda v: (-z[v], v))
+        masked = [v for v in range(V) if v not in allowed][:k - len(allowed)]
+        assert res["ids"][i].tolist() == fin + masked
+        lse = math.log(sum(math.exp(z[v]) for v in allowed))
+        for j, v in enumerate(fin):
+            assert abs(res["logprobs"][i, j] - (z[v] - lse)) < 1e-12
+        assert np.all(np.isneginf(res["logprobs"][i, len(allowed):]))
+        assert abs(res["row_max"][i] + math.log(res["row_sumexp"][i]) - lse) < 1e-12
