@@ -855,6 +855,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.steps is None:
         args.steps = 20 if args.impl == "reference" else 1000
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:
