@@ -120,3 +120,25 @@ def test_workspace_queries(L):
     assert L.eagle_lmhead_topk_workspace_size(61, 4096, 128256, 1, 1) > 0
     assert L.eagle_fuse_proj_workspace_size(61, 4096, 1) > 0
     assert L.eagle_tree_verify_workspace_size(4, 61, 128256) >= 4 * 61 * 12
+
+
+def _declared_arity():
+    """Parameter count of every call the header declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for m in re.finditer(r"\b(eagle_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Every call the Python binding marshals passes exactly as many
+    arguments as the header's prototype declares."""
+    from eagle_speculative_decoding_gb300 import binding
+    arity = _declared_arity()
+    for name, (_, args) in binding._SIGS.items():
+        assert name in arity, name
+        assert len(args) == arity[name], (name, len(args), arity[name])
