@@ -240,61 +240,85 @@ class Workload:
 
 # ------------------------------------------------------------ measurement
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling during the timed region."""
-    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi clock / throttle-reason sampling, running from before the
+    first warm-up step to after the last GPU measurement.  Each sample is
+    stamped with the host clock, so the samples of one window (a timed
+    region) can be picked out; a window too short to hold a sample (20 steps
+    of about 1 ms) falls back to the samples taken under load during the
+    whole GPU run, and the summary says which."""
+    Q = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index):
-        self.index, self.proc, self.lines = index, None, []
+        self.index, self.proc, self.samples = index, None, []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
-            t0 = time.perf_counter()  # let the sampler start before the timed region
-            while not self.lines and time.perf_counter() - t0 < 3.0:
+            t0 = time.perf_counter()  # let the sampler start before any GPU work
+            while not self.samples and time.perf_counter() - t0 < 3.0:
                 time.sleep(0.01)
-            self.lines.clear()
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc:
+            time.sleep(0.1)  # one more sample after the last measurement
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 6:
-                continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[2:6]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+    @classmethod
+    def parse(cls, line):
+        """(sm_mhz, max_mhz, util %, set of active reasons) or None."""
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 7:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        try:
+            sm, mx = float(f[0]), float(f[1])
+        except ValueError:
+            return None
+        try:
+            util = float(f[2])
+        except ValueError:
+            util = None
+        reasons = {nm for nm, v in zip(cls.REASONS, f[3:7]) if v.lower() == "active"}
+        return sm, mx, util, reasons
+
+    def summary(self, t0=None, t1=None):
+        """Clock record of the window [t0, t1] (host perf_counter times), or
+        of every sample taken under load when the window holds none."""
+        rows = [(t, self.parse(ln)) for t, ln in self.samples]
+        rows = [(t, r) for t, r in rows if r is not None]
+        window = [r for t, r in rows if t0 is not None and t0 <= t <= t1]
+        kind = "timed region"
+        if not window:
+            window = [r for _, r in rows if r[2] is None or r[2] >= 50.0]
+            kind = "whole GPU run, samples at >= 50 % utilisation (the timed region is shorter " \
+                   "than the sampling period)"
+        if not window:
+            window = [r for _, r in rows]
+            kind = "whole GPU run, all samples"
+        if not window:
+            return None
+        reasons = sorted(set().union(*(r[3] for r in window)))
+        return {"sm_mhz": statistics.median(r[0] for r in window),
+                "sm_max_mhz": max(r[1] for r in window), "reasons": reasons,
+                "samples": len(window), "window": kind}
 
 
 def measured_peaks():
@@ -302,7 +326,22 @@ def measured_peaks():
     if os.path.exists(p):
         with open(p) as fh:
             return json.load(fh), "measured"
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def bound_row(byts, flops, us, peaks):
+    """Roofline of one call: the higher of its byte floor (HBM copy peak) and
+    its flop floor.  Calls are timed inside a pass of whole steps, so a
+    tensor-bound call is held to the sustained bf16 peak (the GEMM rate under
+    the power cap), not the burst."""
+    tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    if byts / (peaks["hbm_gbs"] * 1e9) >= flops / (tc * 1e12):
+        gbs = byts / us / 1e3
+        return dict(bound="hbm", bytes_per_call=byts, flops_per_call=flops, achieved=round(gbs, 1),
+                    unit="GB/s", peak=peaks["hbm_gbs"], frac=round(gbs / peaks["hbm_gbs"], 4))
+    tfs = flops / us / 1e6
+    return dict(bound="tensor", bytes_per_call=byts, flops_per_call=flops, achieved=round(tfs, 1),
+                unit="TFLOP/s", peak=tc, peak_kind="sustained", frac=round(tfs / tc, 4))
 
 
 def profile_traffic():
@@ -346,34 +385,15 @@ def row_rooflines(wl, steps, peaks):
     for name, lst in ev.items():
         us = sum(a.elapsed_time(b) for a, b in lst) / len(lst) * 1e3
         row = {"avg_call_us": round(us, 2), "calls_per_step": len(lst) // steps}
-        if name in ("fuse_proj", "tree_attn"):
-            if name == "fuse_proj":
-                byts = 3 * wl.d * wl.d * es + 4 * M * wl.d * es
-                flops = 2 * M * 3 * wl.d * wl.d
-            else:  # prefix K/V, tree K/V, Q and O; Q K^T and P V over every key of each row
-                byts = (ctx_sum + M) * wl.Hkv * wl.D * 2 * es + 2 * M * wl.Hq * wl.D * es
-                flops = 4 * wl.R * wl.Hq * wl.D * (ctx_sum + wl.B * wl.R)
-            # the bound is whichever floor is higher: the byte stream or the contraction
-            if byts / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
-                gbs = byts / us / 1e3
-                row.update(bound="hbm", bytes_per_call=byts, achieved=round(gbs, 1), unit="GB/s",
-                           frac=round(gbs / peaks["hbm_gbs"], 4))
-            else:
-                tfs = flops / us / 1e6
-                row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
-                           frac=round(tfs / peaks["bf16_tflops"], 4))
+        if name == "fuse_proj":
+            row.update(bound_row(3 * wl.d * wl.d * es + 4 * M * wl.d * es, 2 * M * 3 * wl.d * wl.d, us, peaks))
+        elif name == "tree_attn":
+            # prefix K/V, tree K/V, Q and O; Q K^T and P V over every key of each row
+            row.update(bound_row((ctx_sum + M) * wl.Hkv * wl.D * 2 * es + 2 * M * wl.Hq * wl.D * es,
+                                 4 * wl.R * wl.Hq * wl.D * (ctx_sum + wl.B * wl.R), us, peaks))
         elif name == "lmhead_verify_stats":
             # W_U once plus the activation rows; 2 M d V flops
-            byts = wl.V * wl.d * es + M * wl.d * es
-            flops = 2 * M * wl.d * wl.V
-            if byts / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
-                gbs = byts / us / 1e3
-                row.update(bound="hbm", bytes_per_call=byts, achieved=round(gbs, 1), unit="GB/s",
-                           frac=round(gbs / peaks["hbm_gbs"], 4))
-            else:
-                tfs = flops / us / 1e6
-                row.update(bound="tensor", flops_per_call=flops, achieved=round(tfs, 1), unit="TFLOP/s",
-                           frac=round(tfs / peaks["bf16_tflops"], 4))
+            row.update(bound_row(wl.V * wl.d * es + M * wl.d * es, 2 * M * wl.d * wl.V, us, peaks))
         else:
             row.update(bound="latency")
         out[name] = row
@@ -561,23 +581,23 @@ def measure_draft_round(wl, rounds, peak_gbs):
                                       "W_U and the drafter prefix K/V stream once"}
 
 
-def run_ours(args, rank, world):
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    wl = Workload(args.workload, dev, seed=args.seed + 1000 * rank)
-    stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        wl.step()
-    torch.cuda.synchronize()
-    st = eb.read_status(wl.status)
-    if st != 0:
-        raise RuntimeError(f"device status {eb.STATUS.get(st, st)} after warm-up")
+def workload_config(name, world):
+    """The ``config`` object of both arms' JSON lines for one workload."""
+    c = synth.CONFIGS[name]
+    es = 2 if c["dtype"] == "bf16" else 4
+    return {"workload": name, "batch": c["B"], "hidden": c["d"],
+            "heads": f"{c['Hq']}/{c['Hkv']}x{c['D']}", "vocab": c["V"], "ctx": list(c["ctx"]),
+            "tree": f"depth {c['depth']}, top-k {c['topk']}, width {c['width']}, budget {c['N']}",
+            "temperature": c["temps"][0], "parallelism": f"replicas x{world}",
+            "l2": "not flushed: inputs larger than L2 (each step streams W_U, "
+                  f"{c['V'] * c['d'] * es / 1e9:.2f} GB, {c['depth'] + 1} times)"}
 
-    # The step's public calls captured once into a CUDA graph per device
-    # input buffer (the calls never synchronise or allocate, and dependent
-    # launches are kept as graph edges): the timed loops replay them, one
-    # host launch per step.  The library's launches per step are counted on
-    # the eager step that precedes each capture.
+
+def graphs_of(wl, stream, dev):
+    """The step's public calls captured once into a CUDA graph per device
+    input buffer (the calls never synchronise or allocate, and dependent
+    launches are kept as graph edges).  The library's launches per step are
+    counted on the eager step that precedes each capture."""
     graphs, per_step = [], 0
     for b in range(2):
         wl.use(b)
@@ -595,6 +615,23 @@ def run_ours(args, rank, world):
         graphs.append(g)
     wl.use(0)
     torch.cuda.synchronize()
+    return graphs, per_step
+
+
+def measure_workload(name, args, rank, world, clk, peaks, peak_kind, detail=True):
+    """Every GPU measurement of one workload: the timed steps (device
+    resident), the LM-head launches, the end-to-end loop, the per-call rows
+    and (``detail``) the drafter calls."""
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    wl = Workload(name, dev, seed=args.seed + 1000 * rank)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    st = eb.read_status(wl.status)
+    if st != 0:
+        raise RuntimeError(f"device status {eb.STATUS.get(st, st)} after warm-up ({name})")
+    graphs, per_step = graphs_of(wl, stream, dev)
 
     # ---- device-resident timing (per-step events).  No L2 flush: every step
     # streams the LM-head weights (>= 1 GB, 8x the L2) once per draft depth and
@@ -603,22 +640,20 @@ def run_ours(args, rank, world):
     step_events = []
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        t_wall0 = time.perf_counter()
-        for _ in range(args.steps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            graphs[0].replay()
-            e1.record(stream)
-            step_events.append((e0, e1))
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graphs[0].replay()
+        e1.record(stream)
+        step_events.append((e0, e1))
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
     launches = per_step * args.steps
 
-    # ---- the dominant kernel's launch durations: a second pass of the same
-    # steps with CUDA events around every LM-head GEMM launch (events between
-    # kernels stop the next kernel's early launch, so this pass is not the one
-    # timed)
+    # ---- the LM-head GEMM launches: a second pass of the same steps with
+    # CUDA events around every LM-head GEMM launch (events between kernels
+    # stop the next kernel's early launch, so this pass is not the one timed)
     lm_events = []
     barrier(world)
     torch.cuda.synchronize()
@@ -626,18 +661,14 @@ def run_ours(args, rank, world):
         wl.step(lm_events)
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in step_events]
-    total_ms = sum(step_ms)
-    total_ms = max_over_ranks(total_ms, world)
+    total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     nodes = wl.B * wl.N * world
     value = nodes / (ms_per_step / 1e3)
-
-    # dominant kernel: the LM-head GEMM + top-k (reads the whole W_U per call)
     lm_ms = [a.elapsed_time(b) for a, b, _, _ in lm_events]
     lm_bytes = [wl.lm_bytes(M, k) for _, _, M, k in lm_events]
     lm_avg_ms = sum(lm_ms) / len(lm_ms)
     achieved = (sum(lm_bytes) / len(lm_bytes)) / (lm_avg_ms / 1e3) / 1e9
-    peaks, peak_kind = measured_peaks()
 
     # ---- end to end through the public API: every step uploads its inputs
     # from pinned host memory, runs, and the host reads its result (accepted
@@ -672,53 +703,76 @@ def run_ours(args, rank, world):
         done.synchronize()
     e2e_total = max_over_ranks(e_start.elapsed_time(done), world)
     e2e_value = nodes / (e2e_total / args.steps / 1e3)
-
     st = eb.read_status(wl.status)
     if st != 0:
-        raise RuntimeError(f"device status {eb.STATUS.get(st, st)}")
-    clocks = clk.summary()
+        raise RuntimeError(f"device status {eb.STATUS.get(st, st)} ({name})")
+
     rows = row_rooflines(wl, max(min(args.steps, 50), 3), peaks)
-    rows["lmhead_topk"] = {"avg_call_us": round(lm_avg_ms * 1e3, 2), "bound": "hbm", "achieved": round(achieved, 1),
-                           "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                           "timing": "the GEMM launch; see roofline"}
-    rows.update({"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"]),
-            "draft_layer": measure_draft_layer(wl, max(min(args.steps, 50), 10), peaks["hbm_gbs"]),
-            "draft_round": measure_draft_round(wl, max(min(args.steps // 10, 10), 3), peaks["hbm_gbs"])})
-    res = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "step_us": round(ms_per_step * 1e3, 1), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if wl.dt == torch.bfloat16 else "f32",
-        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
-        "config": {"workload": wl.name, "batch": wl.B, "hidden": wl.d, "heads": f"{wl.Hq}/{wl.Hkv}x{wl.D}",
-                   "vocab": wl.V, "ctx": list(wl.c["ctx"]), "tree": f"depth {wl.depth}, top-k {wl.k}, "
-                   f"width {wl.width}, budget {wl.N}", "temperature": wl.T,
-                   "parallelism": f"replicas x{world}",
-                   "launch": "each timed step replays a CUDA graph of the step's public calls",
-                   "l2": "not flushed: inputs larger than L2 (each step streams W_U, "
-                         f"{wl.V * wl.d * wl.w_lm.element_size() / 1e9:.2f} GB, "
-                         f"{len(lm_events) // args.steps} times)"},
-        "gpu_launches": launches,
-        "roofline": {"kernel": "lmhead_topk_kernel (tcgen05 LM head + top-k)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
-                     "traffic": profile_traffic(), "avg_launch_us": round(lm_avg_ms * 1e3, 2),
-                     "launches_per_step": len(lm_events) // args.steps,
-                     "timing": "CUDA events around each launch of the LM-head GEMM kernel "
-                               "(eagle_lmhead_topk_partial; its partial merge follows outside the "
-                               "events) in a second pass of the timed steps; the statistics-mode "
-                               "verification call of T > 0 workloads is not among them"},
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": hb,
-                "d2h_bytes_per_step": db,
-                "timing": "first upload to last read-back; each step's result is read on the host "
-                          "before the next step is issued, and step k+1's upload (copy stream, second "
-                          "device buffer) overlaps step k; the step's public calls are captured once "
-                          "into a CUDA graph per input buffer and replayed"},
-        "clocks": clocks,
-        "rows": rows,
-        "wall_s": round(t_wall, 3),
-    }
+    rows["lmhead_topk"] = {"avg_call_us": round(lm_avg_ms * 1e3, 2), "calls_per_step": len(lm_events) // args.steps,
+                           "bound": "hbm", "achieved": round(achieved, 1), "unit": "GB/s",
+                           "frac": round(achieved / peaks["hbm_gbs"], 4),
+                           "timing": "CUDA events around each launch of the LM-head GEMM kernel"}
+    if detail:
+        rows.update({"draft_input": measure_draft_input(wl, max(args.steps, 10), peaks["hbm_gbs"]),
+                     "draft_layer": measure_draft_layer(wl, max(min(args.steps, 50), 10), peaks["hbm_gbs"]),
+                     "draft_round": measure_draft_round(wl, max(min(args.steps // 10, 10), 3),
+                                                        peaks["hbm_gbs"])})
+    lm_roof = {"kernel": "lmhead_topk_kernel (tcgen05 LM head + top-k)", "bound": "hbm",
+               "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
+               "traffic": profile_traffic() if name == "llama8b" else None,
+               "avg_launch_us": round(lm_avg_ms * 1e3, 2),
+               "launches_per_step": len(lm_events) // args.steps,
+               "timing": "CUDA events around each launch of the LM-head GEMM kernel "
+                         "(eagle_lmhead_topk_partial; its partial merge follows outside the "
+                         "events) in a second pass of the timed steps; the statistics-mode "
+                         "verification call of T > 0 workloads is not among them"}
+    res = {"value": round(value, 1), "unit": UNIT, "ms_per_step": round(ms_per_step, 4),
+           "step_us": round(ms_per_step * 1e3, 1),
+           "median_step_us": round(statistics.median(step_ms) * 1e3, 1),
+           "dtype": "bf16" if wl.dt == torch.bfloat16 else "f32",
+           "config": workload_config(name, world), "gpu_launches": launches, "roofline": lm_roof,
+           "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": hb,
+                   "d2h_bytes_per_step": db,
+                   "timing": "first upload to last read-back; each step's result is read on the host "
+                             "before the next step is issued, and step k+1's upload (copy stream, second "
+                             "device buffer) overlaps step k; the step's public calls are captured once "
+                             "into a CUDA graph per input buffer and replayed"},
+           "clocks": clk.summary(t_wall0, t_wall1), "rows": rows,
+           "launch": "each timed step replays a CUDA graph of the step's public calls",
+           "wall_s": round(t_wall1 - t_wall0, 3)}
+    # the other calls that bound the step (per-call rows above)
+    others = {k: rows[k] for k in ("lmhead_verify_stats", "tree_attn", "fuse_proj") if k in rows}
+    res["rooflines"] = {k: {kk: v[kk] for kk in ("bound", "achieved", "peak", "unit", "frac", "avg_call_us")
+                            if kk in v} for k, v in others.items()}
+    del graphs
     return res, wl
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = measured_peaks()
+    names = [args.workload] + [n for n in args.also if n != args.workload]
+    out = {}
+    with ClockSampler(dev.index) as clk:
+        for i, name in enumerate(names):
+            r, wl = measure_workload(name, args, rank, world, clk, peaks, peak_kind)
+            out[name] = r
+            del wl
+            torch.cuda.empty_cache()
+    head = out[names[0]]
+    res = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+           "step_us": head["step_us"], "median_step_us": head["median_step_us"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+           "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+           "config": head["config"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
+           "rooflines": head["rooflines"], "e2e": head["e2e"], "clocks": head["clocks"],
+           "rows": head["rows"], "launch": head["launch"], "wall_s": head["wall_s"]}
+    if len(names) > 1:
+        res["workloads"] = {n: out[n] for n in names[1:]}
+    return res
 
 
 def barrier(world):
@@ -738,9 +792,12 @@ def max_over_ranks(x, world):
 # ------------------------------------------------------------ CPU oracle
 class OracleStep:
     """The CPU oracle running one full step of the workload (test
-    infrastructure, used only for the CPU baseline and the reference arm)."""
+    infrastructure, used only for the CPU baseline and the reference arm).
+    ``requests`` < B runs the step on the first ``requests`` requests of the
+    batch only (a bounded sample of a large workload: apart from the weight
+    reads, the oracle's work is per request)."""
 
-    def __init__(self, name, seed=0):
+    def __init__(self, name, seed=0, requests=None):
         import numpy as np
         import oracle
         self.np, self.oracle = np, oracle
@@ -748,28 +805,30 @@ class OracleStep:
         self.c = c
         B, d, V, width, depth, N = c["B"], c["d"], c["V"], c["width"], c["depth"], c["N"]
         R = N + 1
+        b = B if requests is None else max(1, min(int(requests), B))
+        self.B = b
         gen = synth.generator(seed)
         dt = synth.torch_dtype(c["dtype"])
         f64 = lambda t: t.double().numpy()
         self.w_lm = f64(synth.normal((V, d), synth.WEIGHT_STD, dt, gen))
         self.w_proj = f64(synth.normal((d, 3 * d), synth.WEIGHT_STD, dt, gen))
-        self.ctx = synth.ctx_lengths(c, gen)
+        self.ctx = synth.ctx_lengths(c, gen)[:b]
         kc, vc, table = synth.paged_kv(self.ctx.tolist(), c["Hkv"], c["D"], c["page"], dt, gen)
         self.kc, self.vc, self.table = f64(kc), f64(vc), table.numpy()
-        self.rows = [f64(synth.normal((B * (1 if s == 0 else width), d), 1.0, dt, gen))
+        self.rows = [f64(synth.normal((b * (1 if s == 0 else width), d), 1.0, dt, gen))
                      for s in range(depth)]
-        self.q = f64(synth.normal((B, R, c["Hq"], c["D"]), 1.0, dt, gen))
-        self.kt = f64(synth.normal((B, R, c["Hkv"], c["D"]), 1.0, dt, gen))
-        self.vt = f64(synth.normal((B, R, c["Hkv"], c["D"]), 1.0, dt, gen))
-        self.hs = [f64(synth.normal((B * R, d), 1.0, dt, gen)) for _ in range(3)]
-        self.xv = f64(synth.normal((B * R, d), 1.0, dt, gen))
+        self.q = f64(synth.normal((b, R, c["Hq"], c["D"]), 1.0, dt, gen))
+        self.kt = f64(synth.normal((b, R, c["Hkv"], c["D"]), 1.0, dt, gen))
+        self.vt = f64(synth.normal((b, R, c["Hkv"], c["D"]), 1.0, dt, gen))
+        self.hs = [f64(synth.normal((b * R, d), 1.0, dt, gen)) for _ in range(3)]
+        self.xv = f64(synth.normal((b * R, d), 1.0, dt, gen))
         self.T = c["temps"][0]
-        self.nodes = B * N
+        self.nodes = b * N
 
     def run(self):
         """One step; returns its wall seconds."""
         np, oracle, c = self.np, self.oracle, self.c
-        B, k, width, depth, N = c["B"], c["topk"], c["width"], c["depth"], c["N"]
+        B, k, width, depth, N = self.B, c["topk"], c["width"], c["depth"], c["N"]
         R = N + 1
         t0 = time.perf_counter()
         sts = [oracle.tree_expand_init(7) for _ in range(B)]
@@ -798,16 +857,74 @@ class OracleStep:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(name, budget_s=12.0):
-    """Oracle timed on a bounded sample: whole steps until ~budget_s of CPU work."""
-    o = OracleStep(name)
+# bounded samples of each workload for the CPU figures: (requests, seconds of
+# timed oracle work to aim for), on all cores and on one core
+CPU_SAMPLE = {"serve64": (8, 4), "chain3": (8, 4), "long4": (1, 1)}
+
+
+def sample_requests(name, one_core):
+    c = synth.CONFIGS[name]
+    req = CPU_SAMPLE.get(name, (c["B"], c["B"]))[1 if one_core else 0]
+    return min(req, c["B"])
+
+
+def time_oracle(name, requests, budget_s, max_steps=50):
+    """Whole oracle steps on ``requests`` requests until about ``budget_s``
+    seconds of CPU work (at least one step); returns (nodes per step, step
+    seconds)."""
+    o = OracleStep(name, requests=requests)
     secs = [o.run()]
-    while sum(secs) < budget_s and len(secs) < 50:
+    while sum(secs) < budget_s and len(secs) < max_steps:
         secs.append(o.run())
-    per = sum(secs) / len(secs)
-    return {"value": round(o.nodes / per, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{len(secs)} full {name} step(s), {sum(secs):.1f} s of CPU time, "
-                      f"{per * 1e3:.0f} ms per step"}
+    return o.nodes, secs
+
+
+def oracle_figure(name, nodes, secs, cores, requests, where):
+    mean = sum(secs) / len(secs)
+    B = synth.CONFIGS[name]["B"]
+    part = f" on {requests} of its {B} requests" if requests < B else ""
+    return {"value": round(nodes / mean, 3), "median_value": round(nodes / statistics.median(secs), 3),
+            "unit": UNIT, "cores": cores,
+            "sample": f"{len(secs)} {name} step(s){part} {where}, {sum(secs):.1f} s of CPU time, "
+                      f"{mean * 1e3:.0f} ms per step (mean; nodes/s = nodes of the sample / step time)"}
+
+
+def one_core_figure(name):
+    """The oracle on one core: a child process with one BLAS thread, pinned
+    to one CPU before its timed steps."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-core", name],
+                             env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError) as e:
+        return {"error": f"one-core oracle run failed: {type(e).__name__}"}
+
+
+def one_core_child(name):
+    """Body of the child process of one_core_figure."""
+    req = sample_requests(name, one_core=True)
+    o = OracleStep(name, requests=req)  # set-up on the process's threads
+    cpu = sorted(os.sched_getaffinity(0))[0]
+    os.sched_setaffinity(0, {cpu})
+    torch.set_num_threads(1)
+    secs = [o.run()]
+    while sum(secs) < 10.0 and len(secs) < 20:
+        secs.append(o.run())
+    print(json.dumps(oracle_figure(name, o.nodes, secs, 1, req, "on one core (one BLAS thread)")))
+
+
+def cpu_baseline(name):
+    """The oracle on the host cores: a bounded sample of the workload on all
+    cores (the headline ``value``), and the same on one core."""
+    req = sample_requests(name, one_core=False)
+    nodes, secs = time_oracle(name, req, 12.0)
+    res = oracle_figure(name, nodes, secs, cpu_cores(), req, "on all cores")
+    res["kind"] = "oracle"
+    res["one_core"] = one_core_figure(name)
+    return res
 
 
 def cpu_cores():
@@ -819,25 +936,36 @@ def cpu_cores():
 
 def run_reference(args, rank, world):
     """The CPU oracle timed as the reference arm (rank 0 only): each step is
-    one full oracle step of the workload on the host cores."""
+    one oracle step of the workload on the host cores (a bounded sample of
+    the requests where a whole step would take minutes)."""
     if rank != 0:
         return None
-    o = OracleStep(args.workload)
+    req = sample_requests(args.workload, one_core=False)
+    o = OracleStep(args.workload, requests=req)
     for _ in range(args.warmup):
         o.run()
     secs = [o.run() for _ in range(args.steps)]
+    fig = oracle_figure(args.workload, o.nodes, secs, cpu_cores(), req, "on all cores")
     ms = 1e3 * sum(secs) / len(secs)
-    value = o.nodes / (ms / 1e3)
-    cores = cpu_cores()
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"one full {args.workload} step per timed step"},
-            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+    value = fig["value"]
+    fig["kind"] = "oracle"
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 1), "median_step_us": round(statistics.median(secs) * 1e6, 1),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+           "config": workload_config(args.workload, world), "cpu_baseline": fig,
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    extra = [n for n in args.also if n != args.workload]
+    if extra:
+        res["workloads"] = {}
+        for n in extra:
+            req = sample_requests(n, one_core=False)
+            nodes, secs = time_oracle(n, req, 8.0, max_steps=args.steps)
+            f = oracle_figure(n, nodes, secs, cpu_cores(), req, "on all cores")
+            res["workloads"][n] = {"value": f["value"], "unit": UNIT, "config": workload_config(n, world),
+                                   "cpu_baseline": dict(f, kind="oracle")}
+    return res
 
 
 def main():
@@ -846,11 +974,24 @@ def main():
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default 1000; 20 for --impl reference, whose steps run the CPU oracle)")
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS),
+                    help="the headline workload (value, roofline, e2e of the line)")
+    ap.add_argument("--also", default="serve64",
+                    help="comma-separated further workloads measured in the same run and reported "
+                         "under 'workloads' ('none' for none); default: serve64, the batch-64 half "
+                         "of the metric")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-one-core", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_one_core:
+        one_core_child(args.oracle_one_core)
+        return
+    args.also = [] if args.also in ("", "none") else args.also.split(",")
+    for n in args.also:
+        if n not in synth.CONFIGS:
+            ap.error(f"unknown workload {n}")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.steps is None:
@@ -864,10 +1005,15 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
-        res, wl = run_ours(args, rank, world)
+        res = run_ours(args, rank, world)
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            del wl
+            torch.cuda.empty_cache()
             res["cpu_baseline"] = cpu_baseline(args.workload)
+            for n, w in res.get("workloads", {}).items():
+                req = sample_requests(n, one_core=False)
+                nodes, secs = time_oracle(n, req, 8.0)
+                w["cpu_baseline"] = dict(oracle_figure(n, nodes, secs, cpu_cores(), req, "on all cores"),
+                                         kind="oracle")
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -343,17 +343,17 @@ def eagle_tree_verify(parent_row, token, temperature, max_depth, accept_len, pat
 
 def eagle_tree_verify_noalloc(parent_row, token, temperature, max_depth, accept_len, path_rows,
                               out_tokens, n_rows=None, target_logits=None, target_argmax=None,
-                              proposal_mode=EAGLE_PROPOSAL_DETERMINISTIC, seed=0, offset=0,
-                              uniforms_override=None, V=None, status=None, stream=None):
+                              draft_logits=None, proposal_mode=EAGLE_PROPOSAL_DETERMINISTIC, seed=0,
+                              offset=0, uniforms_override=None, V=None, status=None, stream=None):
     """eagle_tree_verify for callers that cannot allocate: no workspace
     argument, statistics kept in the library's fixed device buffer
-    (B * R <= 65536)."""
+    (B * R <= 65536; at T > 0 also B * ceil(V / 4096) <= 65536)."""
     B, R = parent_row.shape
     if V is None:
         V = target_logits.shape[2]
     _check("eagle_tree_verify_noalloc", lib().eagle_tree_verify_noalloc(
         B, R, V, _ptr(parent_row), _ptr(token), _ptr(n_rows), _ptr(target_logits),
-        _ptr(target_argmax), None, float(temperature), proposal_mode, int(seed), int(offset),
+        _ptr(target_argmax), _ptr(draft_logits), float(temperature), proposal_mode, int(seed), int(offset),
         _ptr(uniforms_override), max_depth, _ptr(accept_len), _ptr(path_rows), _ptr(out_tokens),
         _ptr(status), _stream(stream)))
 

@@ -23,6 +23,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <cudaTypedefs.h>
 #include <mutex>
 
 #include "common.cuh"
@@ -777,29 +778,89 @@ constexpr size_t kNoAllocScratchBytes =
 // start at zero: every statistic is written before it is read.
 static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchBytes];
 
-constexpr int kNoAllocMaxDevices = 64;
-std::atomic<void*> g_scratch_ptr[kNoAllocMaxDevices];
+// The buffer's device address belongs to the module loaded in one CUDA
+// context, so it is cached per context, never per device ordinal: a caller
+// may make a non-primary context current, and cudaDeviceReset destroys the
+// primary context (a new one can even reuse the old handle).  A call made
+// outside stream capture therefore looks the address up again and refreshes
+// its context's entry; a call made during capture, when no lookup should be
+// issued, uses the entry that an earlier call in the same context left, and
+// fails cleanly if there is none.
+constexpr int kNoAllocMaxContexts = 64;
+struct ScratchEntry {
+  CUcontext ctx;
+  void* ptr;
+};
+ScratchEntry g_scratch_cache[kNoAllocMaxContexts];
+int g_scratch_used = 0;
 std::mutex g_scratch_mu;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
 
-// Device address of g_verify_scratch on the current device.  In host code the
-// symbol's name is only a host-side stand-in, so the address is looked up
-// with cudaGetSymbolAddress once per device, with that device current.
-void* noalloc_scratch(eagle_status* st) {
+bool current_context(CUcontext* ctx) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  *ctx = nullptr;
+  return g_ctx_current && g_ctx_current(ctx) == CUDA_SUCCESS && *ctx;
+}
+
+// Device address of g_verify_scratch in the current context, or nullptr with
+// *st set.  In host code the symbol's name is only a host-side stand-in, so
+// the address comes from cudaGetSymbolAddress, issued with the caller's
+// device current.  A failed runtime call's error is taken out of the
+// runtime's last-error slot, so that a later launch check does not report it.
+void* noalloc_scratch(cudaStream_t stream, eagle_status* st) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    (void)cudaGetLastError();
     *st = EAGLE_ERR_CUDA;
     return nullptr;
   }
-  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (p) return p;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-  if (!p) {
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || !p) {
-      *st = EAGLE_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    *st = EAGLE_ERR_CUDA;
+    return nullptr;
+  }
+  CUcontext ctx = nullptr;
+  if (!current_context(&ctx)) {
+    // the runtime has not made a context current yet: only a lookup (which
+    // initialises the primary context) can give the address
+    if (cap != cudaStreamCaptureStatusNone) {
+      *st = EAGLE_ERR_INVALID_ARG;
       return nullptr;
     }
-    g_scratch_ptr[dev].store(p, std::memory_order_release);
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (cap != cudaStreamCaptureStatusNone) {
+    for (int i = 0; i < g_scratch_used; ++i)
+      if (g_scratch_cache[i].ctx == ctx) return g_scratch_cache[i].ptr;
+    *st = EAGLE_ERR_INVALID_ARG;  // no call outside capture has run in this context
+    return nullptr;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || !p) {
+    (void)cudaGetLastError();
+    *st = EAGLE_ERR_CUDA;
+    return nullptr;
+  }
+  if (!ctx && !current_context(&ctx)) return p;  // nothing to key the cache by
+  for (int i = 0; i < g_scratch_used; ++i)
+    if (g_scratch_cache[i].ctx == ctx) {
+      g_scratch_cache[i].ptr = p;
+      return p;
+    }
+  if (g_scratch_used < kNoAllocMaxContexts) {
+    g_scratch_cache[g_scratch_used++] = ScratchEntry{ctx, p};
+  } else {  // a full table: recycle the oldest slot
+    for (int i = 1; i < kNoAllocMaxContexts; ++i) g_scratch_cache[i - 1] = g_scratch_cache[i];
+    g_scratch_cache[kNoAllocMaxContexts - 1] = ScratchEntry{ctx, p};
   }
   return p;
 }
@@ -827,7 +888,7 @@ extern "C" int eagle_tree_verify_noalloc(int B, int R, int V, const int32_t* par
   VerifyScratch w{};
   if (temperature != 0.f || !target_argmax) {
     eagle_status st = EAGLE_OK;
-    void* base = noalloc_scratch(&st);
+    void* base = noalloc_scratch(static_cast<cudaStream_t>(stream), &st);
     if (!base) return st;
     w = carve_scratch(base, B, R, V, temperature != 0.f);
   }

@@ -586,8 +586,14 @@ int eagle_tree_commit(int B, int R, int Hkv, int D, int max_depth, int dtype, co
  *   race partials) is a static device
  *   array: every GPU that loads the library holds one copy until the process
  *   exits, and no call allocates or frees memory.
- *   The first call on a device looks up the buffer's device address (with
- *   that device current); make that first call before any stream capture.
+ *   The buffer's device address is looked up in the current CUDA context
+ *   (with cudaGetSymbolAddress) on every call made outside stream capture,
+ *   and kept per context.  A call made while `stream` is capturing uses the
+ *   address an earlier call in the same context looked up, and returns
+ *   EAGLE_ERR_INVALID_ARG, launching nothing, if no such call has run: make
+ *   the first call in each context (and the first after cudaDeviceReset,
+ *   which replaces the context) outside capture.  A failed lookup returns
+ *   EAGLE_ERR_CUDA and clears the runtime's last error.
  *   All calls on a device share the buffer and it keeps the last call's
  *   contents (no field needs to start at zero); calls whose kernels overlap
  *   on the same device race on it, so serialise them (e.g. one stream).

@@ -1,7 +1,9 @@
 """One small pass of the whole hot path on cuda:0, checked against the CPU oracle.
 
-Used by ``__graft_entry__.smoke()``.  Workload: the toy shape (batch 1,
-d 256, 4/2 heads x 64, V 1024, ctx 128, depth 4, top-k 4, budget 16), fp32:
+Used by ``__graft_entry__.smoke()``; it lives with the tests because it
+calls the CPU oracle, which the library package never imports.  Workload:
+the toy shape (batch 1, d 256, 4/2 heads x 64, V 1024, ctx 128, depth 4,
+top-k 4, budget 16), fp32:
   draft round : LM-head top-k on synthetic drafter rows + tree expansion per
                 depth, then rerank/flatten
   drafter     : the input FC with the embedding lookup and the decoder layer
@@ -15,9 +17,9 @@ import torch
 
 
 def run(device="cuda:0"):
-    import oracle  # test infrastructure, allowed here
-    from . import binding as b
-    from . import synth
+    import oracle  # test infrastructure: the checker of the smoke pass
+    from eagle_speculative_decoding_gb300 import binding as b
+    from eagle_speculative_decoding_gb300 import synth
 
     torch.cuda.set_device(device)
     c = synth.CONFIGS["toy"]

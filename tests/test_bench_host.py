@@ -19,3 +19,40 @@ def test_profile_traffic_reads_bytes_only_for_the_current_source(tmp_path, monke
     assert bench.profile_traffic() == 1054075904.0
     monkeypatch.setattr(bench, "PROFILE", _profile(tmp_path, "0" * 16))
     assert bench.profile_traffic() is None
+
+
+def _sampler(lines):
+    s = bench.ClockSampler(0)
+    s.samples = lines
+    return s
+
+
+def test_clock_summary_uses_the_window_and_falls_back_to_loaded_samples():
+    busy = "2070, 2070, 100, Not Active, Not Active, Not Active, Active"
+    idle = "345, 2070, 0, Not Active, Not Active, Not Active, Not Active"
+    s = _sampler([(1.0, idle), (2.0, busy), (3.0, busy), (9.0, idle)])
+    w = s.summary(1.5, 3.5)
+    assert w["window"] == "timed region" and w["sm_mhz"] == 2070 and w["samples"] == 2
+    assert w["reasons"] == ["sw_power_cap"]
+    # a timed region shorter than the sampling period: the loaded samples of the run
+    f = s.summary(5.0, 5.01)
+    assert f["samples"] == 2 and f["sm_mhz"] == 2070 and f["window"].startswith("whole GPU run")
+    assert _sampler([]).summary(0, 1) is None
+    assert _sampler([(1.0, "garbage")]).summary(0, 2) is None
+
+
+def test_both_arms_print_the_same_config():
+    for name in ("llama8b", "serve64"):
+        a = bench.workload_config(name, 1)
+        assert a == bench.workload_config(name, 1)
+        assert a["workload"] == name and a["parallelism"] == "replicas x1"
+    assert "7 times" in bench.workload_config("llama8b", 1)["l2"]
+
+
+def test_cpu_samples_are_bounded_subsets_of_the_batch():
+    assert bench.sample_requests("llama8b", False) == 1
+    assert bench.sample_requests("serve64", False) == 8
+    assert bench.sample_requests("serve64", True) == 4
+    for name, c in bench.synth.CONFIGS.items():
+        for one in (False, True):
+            assert 1 <= bench.sample_requests(name, one) <= c["B"]
