@@ -35,6 +35,7 @@ from .eagle_oracle import (  # noqa: F401
     draft_rows,
     eagle2_tree,
     fuse_proj,
+    fuse_proj_accepted,
     linear,
     lmhead_topk,
     rms_norm,

@@ -44,6 +44,43 @@ def fuse_proj(h_low, h_mid, h_high, w_proj, bias=None):
     return g
 
 
+def fuse_proj_accepted(h_low, h_mid, h_high, w_proj, path_rows, accept_len, bias=None):
+    """Fused feature of the accepted rows only, fp64.
+
+    [M7.5] 0x05D "Feature And KV Commit": after verification only the
+    accepted path is published -- its target features are gathered for the
+    next draft round and every other tree row is discarded; [E3] "Stage 2:
+    Verification" and section 3.4 "Change 2: The fusion FC layer": the
+    drafter's next input is the fusion g = W_proj [l; m; h] of those target
+    features.  So the fusion is needed on the accepted rows only.
+
+    Reading (as for the commit): the accepted rows of request b are
+    path_rows[b, 0 .. accept_len[b]] in path order; the feature rows of
+    request b are rows b*R + row of h_* [B*R, d].  Output [B, Dmax+1, d]:
+    slot j <= accept_len[b] holds the fusion of row path_rows[b, j]; the
+    other slots are zero (the commit's layout of gathered features).
+    """
+    path = np.asarray(path_rows)
+    acc = np.asarray(accept_len)
+    B, slots = path.shape
+    hs = [np.asarray(h, np.float64) for h in (h_low, h_mid, h_high)]
+    if hs[0].shape[0] % B:
+        raise ValueError("h_* must hold B*R rows")
+    R = hs[0].shape[0] // B
+    d = np.asarray(w_proj).shape[0]
+    out = np.zeros((B, slots, d))
+    for b in range(B):
+        n = int(acc[b]) + 1
+        if not 1 <= n <= slots:
+            raise ValueError("accept_len out of range")
+        rows = [int(path[b, j]) for j in range(n)]
+        if any(not 0 <= r < R for r in rows):
+            raise ValueError("path row out of range")
+        idx = [b * R + r for r in rows]
+        out[b, :n] = fuse_proj(hs[0][idx], hs[1][idx], hs[2][idx], w_proj, bias)
+    return out
+
+
 def draft_input(r, token_ids, embed, w_in, bias=None):
     """Drafter input u = W_I [r; e(x)] (+ bias), fp64.
 

@@ -5,6 +5,11 @@ import torch
 
 REL_TOL = 2e-2     # attention / projection outputs, bf16 in, fp32 accumulate
 LOGPROB_TOL = 1e-3
+# Norm-wise regression bar under the stated 2e-2: a bf16 output vector
+# carries rounding of about 2^-9 relative per element (~1e-3 norm-wise), and
+# attention adds the bf16 rounding of P; 5e-3 leaves room for both while a
+# kernel 5x less accurate than it is now fails.
+NORM_TOL = 5e-3
 
 
 def need_gpu():
@@ -32,6 +37,17 @@ def rel_err(gpu, ref):
     rms = np.sqrt(np.mean(o * o, axis=1, keepdims=True))
     elem = np.abs(g - o) / (np.abs(o) + rms + 1e-30)
     return float(max(norm.max(), elem.max()))
+
+
+def norm_err(gpu, ref):
+    """max over output vectors (last axis) of ||g - o|| / ||o||."""
+    g = np.asarray(gpu, np.float64)
+    o = np.asarray(ref, np.float64)
+    if o.size == 0:
+        return 0.0
+    g = g.reshape(-1, o.shape[-1])
+    o = o.reshape(-1, o.shape[-1])
+    return float((np.linalg.norm(g - o, axis=1) / np.maximum(np.linalg.norm(o, axis=1), 1e-30)).max())
 
 
 def check_topk(gpu_ids, gpu_lp, z_ref, lp_ref_fn, k, tie_tol):

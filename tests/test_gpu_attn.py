@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from eagle_speculative_decoding_gb300 import synth
-from gpu_helpers import REL_TOL, need_gpu, rel_err
+from gpu_helpers import NORM_TOL, REL_TOL, need_gpu, norm_err, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,9 @@ def test_bf16_small_cases(B, R, Hq, Hkv, D, lo, hi, splits):
     out, lse, st = _gpu(b, *case, num_splits=splits)
     ref_o, ref_l = _ref(*case)
     assert st == 0
-    assert rel_err(out, ref_o) < REL_TOL
+    err, nerr = rel_err(out, ref_o), norm_err(out, ref_o)
+    print(f"B={B} R={R} Hq={Hq} D={D}: rel {err:.2e}, norm-wise {nerr:.2e}")
+    assert err < REL_TOL and nerr < NORM_TOL
     assert np.abs(lse - ref_l).max() < 2e-2
 
 
@@ -68,7 +70,8 @@ def test_chain_tree_bf16():
     b = need_gpu()
     case = _case(7, 1, 12, 8, 2, 128, 77, 77, "bf16", chain=True)
     out, lse, st = _gpu(b, *case)
-    assert rel_err(out, _ref(*case)[0]) < REL_TOL
+    ref_o = _ref(*case)[0]
+    assert rel_err(out, ref_o) < REL_TOL and norm_err(out, ref_o) < NORM_TOL
 
 
 def test_toy_fp32():
@@ -105,5 +108,7 @@ def test_full_size_sampled(cfg):
     ref = _ref(*case, sample=sample)
     got = np.stack([out[s] for s in sample])
     want = np.stack([ref[s][0] for s in sample])
-    assert rel_err(got, want) < REL_TOL
+    err, nerr = rel_err(got, want), norm_err(got, want)
+    print(f"{cfg}: rel {err:.2e}, norm-wise {nerr:.2e}")
+    assert err < REL_TOL and nerr < NORM_TOL
     assert max(abs(lse[s] - ref[s][1]) for s in sample) < 2e-2

@@ -103,7 +103,8 @@ def test_stochastic_matches_oracle_on_shared_philox(B, R, V, depth, T):
         assert acc[bb] == ref["accept_len"][bb], bb
         assert np.array_equal(path[bb], ref["path_rows"][bb]), bb
         assert np.array_equal(out[bb], ref["out_tokens"][bb]), bb
-    assert checked >= B - max(1, B // 10)
+    print(f"B={B} R={R} V={V}: {B - checked} of {B} requests within {MARGIN} of a threshold")
+    assert checked == B  # these seeds put no decision within MARGIN of its threshold
     assert ref["accept_len"].max() >= 1  # the case exercises accepted paths
 
 
@@ -249,7 +250,8 @@ def test_sampled_proposals_match_oracle(B, R, V, depth, T):
         assert acc[bb].item() == ref["accept_len"][bb], bb
         assert path[bb].tolist() == ref["path_rows"][bb].tolist(), bb
         assert out[bb].tolist() == ref["out_tokens"][bb].tolist(), bb
-    assert checked >= B - max(1, B // 4)
+    print(f"sampled B={B} R={R} V={V}: {B - checked} of {B} requests within 1e-4 of a threshold")
+    assert checked == B  # these seeds put no decision within 1e-4 of its threshold
 
 
 def test_sampled_proposals_chi_square():

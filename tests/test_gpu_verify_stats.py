@@ -120,7 +120,8 @@ def test_walk_from_statistics_matches_full_logit_walk(B, R, V, d, T):
         assert acc[bb].item() == ref["accept_len"][bb], bb
         assert path[bb].tolist() == ref["path_rows"][bb].tolist(), bb
         assert out[bb].tolist() == ref["out_tokens"][bb].tolist(), bb
-    assert checked >= B - max(1, B // 5)
+    print(f"B={B} R={R} V={V}: {B - checked} of {B} requests within {MARGIN} of a threshold")
+    assert checked == B  # these seeds put no decision within MARGIN of its threshold
     assert ref["accept_len"].max() >= 1
 
 
