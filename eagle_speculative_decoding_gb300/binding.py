@@ -29,6 +29,8 @@ _SIGS = {
     "eagle_selftest_wait_timeout": (_I, [ctypes.c_uint, _P, _P]),
     "eagle_fuse_proj_workspace_size": (_Z, [_I, _I, _I]),
     "eagle_fuse_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _Z, _P, _P]),
+    "eagle_fuse_proj_accepted_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "eagle_fuse_proj_accepted": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P, _P]),
     "eagle_draft_input_workspace_size": (_Z, [_I, _I, _I]),
     "eagle_linear_workspace_size": (_Z, [_I, _I, _I, _I]),
     "eagle_linear": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P, _P]),
@@ -146,6 +148,27 @@ def eagle_fuse_proj(h_low, h_mid, h_high, w_proj, g, bias=None, ws=None, status=
     _check("eagle_fuse_proj", lib().eagle_fuse_proj(
         _ptr(h_low), _ptr(h_mid), _ptr(h_high), _ptr(w_proj), _ptr(bias), _ptr(g), M, d, dt,
         _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
+    return g
+
+
+def eagle_fuse_proj_accepted_workspace_size(B, max_depth, d, dtype):
+    return int(lib().eagle_fuse_proj_accepted_workspace_size(B, max_depth, d, dtype))
+
+
+def eagle_fuse_proj_accepted(h_low, h_mid, h_high, w_proj, path_rows, accept_len, g, bias=None, ws=None,
+                             status=None, stream=None):
+    """g[b, j] = W_proj [h_low; h_mid; h_high] of row path_rows[b, j] (rows
+    b*R + row of the [B*R, d] features) for j <= accept_len[b], zero past it;
+    g is [B, max_depth+1, d]."""
+    B, slots = path_rows.shape
+    d = h_low.shape[1]
+    R = h_low.shape[0] // B
+    dt = _dtype(h_low)
+    if ws is None:
+        ws = workspace(eagle_fuse_proj_accepted_workspace_size(B, slots - 1, d, dt), h_low.device)
+    _check("eagle_fuse_proj_accepted", lib().eagle_fuse_proj_accepted(
+        _ptr(h_low), _ptr(h_mid), _ptr(h_high), _ptr(w_proj), _ptr(bias), _ptr(path_rows), _ptr(accept_len),
+        B, R, slots - 1, d, dt, _ptr(g), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
     return g
 
 

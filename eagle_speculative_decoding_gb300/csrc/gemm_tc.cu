@@ -802,7 +802,29 @@ struct FpParams {
   float* part;    // [n_tiles][max_contrib][bn][128]
   int32_t* status;
   const void* residual;  // [M, d] of the output dtype added to the result, or null
+  // Rows known only on the device (the accepted-rows fusion): with m_dev set,
+  // only the first *m_dev of the M activation rows are projected -- the
+  // stream-K split is re-planned on the device over the groups that hold
+  // them -- and activation row i lands in output row row_map[i].
+  const int32_t* m_dev;
+  const int32_t* row_map;
 };
+
+// The activation rows and stream-K chunk count of one launch: all M rows
+// (W chunks) unless the row count comes from the device.
+struct FpLive {
+  int m;
+  long long W;
+};
+__device__ __forceinline__ FpLive fp_live(const FpParams& p) {
+  FpLive l{p.M, p.W};
+  if (p.m_dev) {
+    const int m = __ldcg(p.m_dev);
+    l.m = m < 0 ? 0 : (m > p.M ? p.M : m);
+    l.W = (long long)p.n_otiles * ((l.m + p.bn - 1) / p.bn) * p.nk;
+  }
+  return l;
+}
 
 __host__ __device__ inline long long sk_lo(long long c, long long W, int n) { return c * W / n; }
 // CTA whose stream-K range holds chunk x
@@ -846,13 +868,15 @@ template <bool TF32>
 __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p) {
   pdl_wait();
   pdl_trigger();
+  const FpLive lv = fp_live(p);
   const int tile = blockIdx.y;
   const long long x0 = (long long)tile * p.nk;
-  const int c_first = sk_owner(x0, p.W, p.n_ctas);
-  const int c_last = sk_owner(x0 + p.nk - 1, p.W, p.n_ctas);
+  if (x0 >= lv.W) return;  // a group past the live rows
+  const int c_first = sk_owner(x0, lv.W, p.n_ctas);
+  const int c_last = sk_owner(x0 + p.nk - 1, lv.W, p.n_ctas);
   if (c_first == c_last) return;  // one CTA held the whole tile and wrote it
   const int ot = tile % p.n_otiles, gr = tile / p.n_otiles;
-  const int m0 = gr * p.bn, ncol = min(p.bn, p.M - m0);
+  const int m0 = gr * p.bn, ncol = min(p.bn, lv.m - m0);
   const int f = blockIdx.x * 256 + threadIdx.x;  // float4 index in the [ncol][128] tile
   if (f >= ncol * 32) return;
   const int ncontrib = c_last - c_first + 1;
@@ -880,7 +904,8 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
     acc.z += p.bias[oo + 2];
     acc.w += p.bias[oo + 3];
   }
-  const size_t idx = (size_t)(m0 + col) * p.d + oo;
+  const int orow = p.row_map ? p.row_map[m0 + col] : m0 + col;
+  const size_t idx = (size_t)orow * p.d + oo;
   if (p.residual) {
     if (TF32) {
       const float4 rv = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.residual) + idx);
@@ -952,8 +977,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cta_init(sh, stages);
   int pre = 0;
-  if (threadIdx.x == 0) pre = prefetch_weights<TF32>(sc, sh, rg);
+  // a device row count is only known once the previous grid is done, so the
+  // weights of such a launch are not fetched early
+  if (threadIdx.x == 0 && !p.m_dev) pre = prefetch_weights<TF32>(sc, sh, rg);
   cta_start(sh, tmem_cols);
+  const FpLive lv = fp_live(p);
+  if (p.m_dev) {
+    sc.lo = sk_lo(blockIdx.x, lv.W, p.n_ctas);
+    sc.hi = sk_lo(blockIdx.x + 1, lv.W, p.n_ctas);
+  }
 
   if (warp == 0) {
     if (lane == 0) run_producer<TF32>(sc, sh, rg, pre);
@@ -969,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!epi_wait(sh, smem_u32(&sh.acc_full[buf]), aph)) break;
       tc_fence_after();
       const int ot = sg.tile % p.n_otiles, gr = sg.tile / p.n_otiles;
-      const int o = ot * 128 + e, m0 = gr * bn, ncol = min(bn, p.M - m0);
+      const int o = ot * 128 + e, m0 = gr * bn, ncol = min(bn, lv.m - m0);
       const uint32_t taddr = sh.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * bn);
       const bool whole = sg.k0 == 0 && sg.k1 == p.nk;
       const float bias_o = p.bias ? p.bias[o] : 0.f;
@@ -981,7 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             const int col = c16 * 16 + j;
             if (col < ncol) {
-              const size_t idx = (size_t)(m0 + col) * p.d + o;
+              const int orow = p.row_map ? p.row_map[m0 + col] : m0 + col;
+              const size_t idx = (size_t)orow * p.d + o;
               float y = v[j] + bias_o;
               if (p.residual)
                 y += TF32 ? reinterpret_cast<const float*>(p.residual)[idx]
@@ -1000,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stream-K partial: write it; fuse_proj_reduce_kernel sums the
         // contributors of the tile afterwards
         const long long x0 = (long long)sg.tile * p.nk;
-        const int c_first = sk_owner(x0, p.W, p.n_ctas);
+        const int c_first = sk_owner(x0, lv.W, p.n_ctas);
         const int slot = blockIdx.x - c_first;
         float* part = p.part + (((size_t)sg.tile * p.max_contrib + slot) * bn) * 128;
         for (int c16 = 0; c16 * 16 < ncol; ++c16) {
@@ -1019,6 +1052,135 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   cta_teardown(sh, tmem_cols, p.status);
+}
+
+// Accepted-rows fusion, first half: the accepted rows of every request
+// (path_rows[b, 0 .. accept_len[b]], in path order) are packed, request after
+// request, into three compact [cap, d] buffers that the projection reads by
+// TMA; row_map[i] is the output slot b * slots + j of packed row i, *m_out the
+// number of packed rows.  Output slots past a request's accepted length are
+// zeroed here.  A request with accept_len outside [0, slots) or a path row
+// outside [0, R) records EAGLE_ERR_BAD_TREE and contributes no row (all its
+// slots are zeroed).  Every CTA scans the per-request counts itself (B <= 4096
+// entries, 16 per thread), then all CTAs copy 16-byte chunks.
+constexpr int kAccThreads = 256;
+constexpr int kAccMaxB = 4096;
+__global__ void __launch_bounds__(kAccThreads) accepted_gather_kernel(
+    int B, int R, int slots, int chunks /* 16-byte chunks per row */,
+    const int32_t* __restrict__ path_rows, const int32_t* __restrict__ accept_len,
+    const uint4* __restrict__ hl, const uint4* __restrict__ hm, const uint4* __restrict__ hh,
+    uint4* __restrict__ cl, uint4* __restrict__ cm, uint4* __restrict__ ch, int32_t* __restrict__ row_map,
+    int32_t* __restrict__ m_out, uint4* __restrict__ g_out, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_off[kAccMaxB + 1];
+  __shared__ int s_warp[kAccThreads / 32];
+  constexpr int kPer = kAccMaxB / kAccThreads;  // requests per thread
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  int n[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int b = t * kPer + i;
+    n[i] = 0;
+    if (b < B) {
+      const int a = accept_len[b];
+      bool ok = a >= 0 && a < slots;
+      for (int j = 0; ok && j <= a; ++j) {
+        const int r = path_rows[(size_t)b * slots + j];
+        ok = r >= 0 && r < R;
+      }
+      if (ok)
+        n[i] = a + 1;
+      else if (blockIdx.x == 0)
+        set_status(status, EAGLE_ERR_BAD_TREE);
+    }
+    sum += n[i];
+  }
+  // block exclusive scan of the per-thread sums
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_warp[w];
+  int run = wbase + x - sum;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int b = t * kPer + i;
+    if (b < B) s_off[b] = run;
+    run += n[i];
+  }
+  if (t == kAccThreads - 1) s_off[B] = run;  // the last thread's running total is the grand total
+  __syncthreads();
+  const int total = s_off[B];
+  if (blockIdx.x == 0 && t == 0) *m_out = total;
+  // packed rows [0, total) and the zeroed output slots, chunk by chunk
+  const long long cap = (long long)B * slots;
+  const long long work = cap * chunks;
+  for (long long w = (long long)blockIdx.x * kAccThreads + t; w < work; w += (long long)gridDim.x * kAccThreads) {
+    const int i = (int)(w / chunks), c = (int)(w % chunks);
+    if (i < total) {
+      int lo = 0, hi = B;  // request b with s_off[b] <= i < s_off[b + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= i) lo = mid; else hi = mid;
+      }
+      const int b = lo, j = i - s_off[b];
+      const size_t src = ((size_t)b * R + path_rows[(size_t)b * slots + j]) * chunks + c;
+      const size_t dst = (size_t)i * chunks + c;
+      cl[dst] = __ldg(hl + src);
+      cm[dst] = __ldg(hm + src);
+      ch[dst] = __ldg(hh + src);
+      if (c == 0) row_map[i] = b * slots + j;
+    }
+    // output slot i = (b, j): zero past the request's accepted rows
+    const int b = i / slots, j = i % slots;
+    if (j >= s_off[b + 1] - s_off[b]) g_out[(size_t)i * chunks + c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// fp32 accepted-rows fusion on the CUDA cores (exact fp32): one warp per
+// output element g[b, j, o]; slots past the accepted path (or of a request
+// whose path is invalid) are zero.
+__global__ void __launch_bounds__(256)
+    fuse_proj_accepted_f32_kernel(const float* __restrict__ hl, const float* __restrict__ hm,
+                                  const float* __restrict__ hh, const float* __restrict__ w,
+                                  const float* __restrict__ bias, const int32_t* __restrict__ path_rows,
+                                  const int32_t* __restrict__ accept_len, float* __restrict__ g, int B, int R,
+                                  int slots, int d, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)B * slots * d) return;
+  const int o = (int)(gw % d);
+  const int bj = (int)(gw / d), b = bj / slots, j = bj % slots;
+  const int a = accept_len[b];
+  bool ok = a >= 0 && a < slots;
+  for (int jj = 0; ok && jj <= a; ++jj) {
+    const int r = path_rows[(size_t)b * slots + jj];
+    ok = r >= 0 && r < R;
+  }
+  if (!ok && j == 0 && o == 0 && lane == 0) set_status(status, EAGLE_ERR_BAD_TREE);
+  if (!ok || j > a) {
+    if (lane == 0) g[gw] = 0.f;
+    return;
+  }
+  const size_t m = (size_t)b * R + path_rows[(size_t)b * slots + j];
+  const float* wr = w + (size_t)o * 3 * d;
+  float acc = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    acc = fmaf(wr[c], hl[m * d + c], acc);
+    acc = fmaf(wr[d + c], hm[m * d + c], acc);
+    acc = fmaf(wr[2 * d + c], hh[m * d + c], acc);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) g[gw] = acc + (bias ? bias[o] : 0.f);
 }
 
 // fp32 fused projection on the CUDA cores (exact fp32): one warp per output
@@ -1400,16 +1562,36 @@ FpPlan fp_plan(int M, int n_out, int kseg, int esz, int n_ctas_cap, int nseg) {
   return f;
 }
 
-// gathered: room for the [M, d] looked-up embedding rows (drafter input FC)
-size_t fp_workspace(int M, int n_out, int kseg, int dtype, int nseg, bool gathered) {
+// Contributor slots a tile needs when only the first g of the plan's groups
+// hold live rows (a row count known on the device): the same CTAs split the
+// smaller chunk range, so a tile may be shared by more of them.
+int fp_live_contrib(const FpPlan& f) {
+  int mc = f.max_contrib;
+  for (int g = 1; g < f.G; ++g) {
+    const long long W = (long long)f.n_otiles * g * f.nk;
+    const long long per = W / f.n_ctas;
+    long long c = per > 0 ? (f.nk + per - 1) / per + 1 : f.nk;
+    if (c > f.n_ctas) c = f.n_ctas;
+    if (c > mc) mc = (int)c;
+  }
+  return mc;
+}
+
+// gathered: room for the [M, d] looked-up embedding rows (drafter input FC);
+// live: a device row count (the accepted-rows fusion), whose partials need
+// fp_live_contrib slots and which packs nseg [M, kseg] segments, a row map
+// and the count into the workspace
+size_t fp_workspace(int M, int n_out, int kseg, int dtype, int nseg, bool gathered, bool live = false) {
   if (M <= 0 || n_out <= 0 || kseg <= 0 || n_out % 128 || kseg % 64) return 0;
   const int esz = dtype == EAGLE_BF16 ? 2 : 4;
   // sized for the largest grid the library launches (kMaxCtas CTAs)
   size_t best = 0;
   for (int cap = 1; cap <= kMaxCtas; ++cap) {
     const FpPlan f = fp_plan(M, n_out, kseg, esz, cap, nseg);
-    const size_t sz = round_up((size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4, 256) + 1024 +
-                      (gathered ? round_up((size_t)M * kseg * esz, 256) : 0);
+    const int mc = live ? fp_live_contrib(f) : f.max_contrib;
+    size_t sz = round_up((size_t)f.n_tiles * mc * f.bn * 128 * 4, 256) + 1024 +
+                (gathered ? round_up((size_t)M * kseg * esz, 256) : 0);
+    if (live) sz += nseg * round_up((size_t)M * kseg * esz, 256) + round_up((size_t)M * 4, 256) + 256;
     best = sz > best ? sz : best;
   }
   return best;
@@ -1418,9 +1600,18 @@ size_t fp_workspace(int M, int n_out, int kseg, int dtype, int nseg, bool gather
 // bf16 tensor-core launch shared by both projections: xs[0..nseg) are the
 // [M, d] activation segments, read by TMA; with `ids` set the last segment is
 // first looked up from `table` ([n_rows, d]) into the workspace.
+// Rows of an accepted-rows fusion: the packed activation segments, their
+// output rows and their count are written by a gather kernel on the device.
+struct FpLiveRows {
+  const int32_t* path_rows;
+  const int32_t* accept_len;
+  int B, R, slots;
+};
+
 int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const void* table, int n_rows,
                    const void* w, const float* bias, const void* residual, void* out, int M, int n_out,
-                   int kseg, void* ws, int32_t* dev_status, cudaStream_t s) {
+                   int kseg, void* ws, int32_t* dev_status, cudaStream_t s,
+                   const FpLiveRows* live = nullptr) {
   constexpr int esz = 2, bke = 64;
   int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
@@ -1428,10 +1619,28 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
   const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
+  const int max_contrib = live ? fp_live_contrib(f) : f.max_contrib;
 
   char* cur = static_cast<char*>(ws);
-  float* part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * f.max_contrib * f.bn * 128 * 4));
+  float* part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * max_contrib * f.bn * 128 * 4));
   const void* seg[3] = {xs[0], nseg > 1 ? xs[1] : xs[0], nseg > 2 ? xs[2] : xs[0]};
+  int32_t* row_map = nullptr;
+  int32_t* m_dev = nullptr;
+  if (live) {
+    void* packed[3];
+    for (int i = 0; i < 3; ++i) packed[i] = ws_carve(cur, (size_t)M * kseg * esz);
+    row_map = static_cast<int32_t*>(ws_carve(cur, (size_t)M * 4));
+    m_dev = static_cast<int32_t*>(ws_carve(cur, 4));
+    const long long work = (long long)M * (kseg / 8);
+    const long long blocks = (work + kAccThreads - 1) / kAccThreads;
+    launch(accepted_gather_kernel, (unsigned)(blocks < 2LL * sms ? blocks : 2LL * sms), kAccThreads, 0, s,
+           live->B, live->R, live->slots, kseg / 8, live->path_rows, live->accept_len,
+           static_cast<const uint4*>(seg[0]), static_cast<const uint4*>(seg[1]),
+           static_cast<const uint4*>(seg[2]), static_cast<uint4*>(packed[0]), static_cast<uint4*>(packed[1]),
+           static_cast<uint4*>(packed[2]), row_map, m_dev, static_cast<uint4*>(out), dev_status);
+    note_launch();
+    for (int i = 0; i < 3; ++i) seg[i] = packed[i];
+  }
   void* gathered = nullptr;
   if (ids) {
     gathered = ws_carve(cur, (size_t)M * kseg * esz);
@@ -1469,6 +1678,9 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.residual = residual;
   p.out = out;
   p.status = dev_status;
+  p.m_dev = m_dev;
+  p.row_map = row_map;
+  p.max_contrib = max_contrib;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
   launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
@@ -1503,6 +1715,42 @@ extern "C" int eagle_fuse_proj(const void* h_low, const void* h_mid, const void*
   const void* xs[3] = {h_low, h_mid, h_high};
   return fp_launch_bf16(xs, 3, nullptr, nullptr, 0, w_proj, bias, nullptr, g, M, d, d, ws, dev_status,
                         static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t eagle_fuse_proj_accepted_workspace_size(int B, int max_depth, int d, int dtype) {
+  if (B <= 0 || max_depth < 0 || (long long)B * (max_depth + 1) > 4096) return 0;
+  if (dtype == EAGLE_FP32) return 256;
+  return fp_workspace(B * (max_depth + 1), d, d, dtype, 3, false, true);
+}
+
+extern "C" int eagle_fuse_proj_accepted(const void* h_low, const void* h_mid, const void* h_high,
+                                        const void* w_proj, const float* bias, const int32_t* path_rows,
+                                        const int32_t* accept_len, int B, int R, int max_depth, int d,
+                                        int dtype, void* g, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                        void* stream) {
+  if (!h_low || !h_mid || !h_high || !w_proj || !g || !path_rows || !accept_len) return EAGLE_ERR_INVALID_ARG;
+  if (B <= 0 || R <= 0 || max_depth < 0 || d <= 0) return EAGLE_ERR_INVALID_ARG;
+  if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return EAGLE_ERR_INVALID_ARG;
+  const long long cap = (long long)B * (max_depth + 1);
+  if (cap > 4096 || B > kAccMaxB || d % 128 || d > 16384 || (long long)B * R > 2147483647LL / d)
+    return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned16(h_low) || !aligned16(h_mid) || !aligned16(h_high) || !aligned16(w_proj) || !aligned16(g))
+    return EAGLE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < eagle_fuse_proj_accepted_workspace_size(B, max_depth, d, dtype))
+    return EAGLE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == EAGLE_FP32) {
+    const long long outs = cap * d;
+    launch(fuse_proj_accepted_f32_kernel, (unsigned)((outs + 7) / 8), 256, 0, s, (const float*)h_low,
+           (const float*)h_mid, (const float*)h_high, (const float*)w_proj, bias, path_rows, accept_len,
+           (float*)g, B, R, max_depth + 1, d, dev_status);
+    note_launch();
+    return last_launch_status();
+  }
+  const void* xs[3] = {h_low, h_mid, h_high};
+  const FpLiveRows live{path_rows, accept_len, B, R, max_depth + 1};
+  return fp_launch_bf16(xs, 3, nullptr, nullptr, 0, w_proj, bias, nullptr, g, (int)cap, d, d, ws, dev_status, s,
+                        &live);
 }
 
 extern "C" size_t eagle_draft_input_workspace_size(int M, int d, int dtype) {

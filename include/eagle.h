@@ -126,6 +126,43 @@ int eagle_fuse_proj(const void* h_low, const void* h_mid, const void* h_high,
                     void* stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_fuse_proj_accepted -- the fusion of eagle_fuse_proj over the accepted
+ * rows only.
+ * [M7.5] section 0x05D "Feature And KV Commit" (only the verified path is
+ * published: its target features are gathered for the next draft round, every
+ * other tree row is discarded); [E3] "Stage 2: Verification" with section 3.4
+ * "Change 2: The fusion FC layer" (the next round's drafter input is the fused
+ * feature of those rows).  The accepted rows of request b are
+ * path_rows[b, 0 .. accept_len[b]] in path order -- the rows
+ * eagle_tree_commit publishes.
+ *   g[b, j, :] = W_proj [h_low[r]; h_mid[r]; h_high[r]] (+ bias),
+ *                r = b * R + path_rows[b, j], for j <= accept_len[b];
+ *   g[b, j, :] = 0 for accept_len[b] < j <= max_depth.
+ *
+ *   h_low, h_mid, h_high : [B*R, d] verify-row features, dtype `dtype`
+ *   w_proj, bias         : as eagle_fuse_proj
+ *   path_rows, accept_len: outputs of eagle_tree_verify ([B, max_depth+1], [B])
+ *   g                    : [B, max_depth+1, d] output, dtype `dtype`
+ * bf16: a gather kernel packs the accepted rows (and their output slots) into
+ * `ws`, and the tensor-core projection runs on the packed rows only: its
+ * stream-K split is planned on the device from the accepted-row count, so
+ * rejected tree rows cost neither weight traffic nor MMAs.  fp32: CUDA cores,
+ * exact fp32.  Unlike eagle_fuse_proj, w_proj is not read before the previous
+ * kernel on the stream has completed.
+ * Device-detected: accept_len[b] outside [0, max_depth] or a path row outside
+ * [0, R) -> EAGLE_ERR_BAD_TREE; that request projects no row (all its slots
+ * are zeroed).
+ * Limits: B * (max_depth + 1) <= 4096, d % 128 == 0, d <= 16384; 16-byte
+ * aligned arrays.
+ * ---------------------------------------------------------------------- */
+size_t eagle_fuse_proj_accepted_workspace_size(int B, int max_depth, int d, int dtype);
+int eagle_fuse_proj_accepted(const void* h_low, const void* h_mid, const void* h_high,
+                             const void* w_proj, const float* bias, const int32_t* path_rows,
+                             const int32_t* accept_len, int B, int R, int max_depth, int d,
+                             int dtype, void* g, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
  * eagle_draft_input -- drafter input FC with the token-embedding lookup fused.
  *   u[i, o] = sum_c W[o, c] r[i, c] + W[o, d+c] embed[token_ids[i], c]
  *             (+ bias[o])
