@@ -810,18 +810,24 @@ struct FpParams {
   const int32_t* row_map;
 };
 
-// The activation rows and stream-K chunk count of one launch: all M rows
-// (W chunks) unless the row count comes from the device.
+// The activation rows, stream-K chunk count and active CTAs of one launch:
+// all M rows (W chunks over every CTA) unless the row count comes from the
+// device.  The chunks are split over at most W CTAs, so that every active
+// CTA holds at least one chunk and a tile's contributors are consecutive CTAs
+// (the partial slot of a contributor is its distance from the tile's first
+// one); CTAs past the active count do nothing.
 struct FpLive {
   int m;
   long long W;
+  int n;
 };
 __device__ __forceinline__ FpLive fp_live(const FpParams& p) {
-  FpLive l{p.M, p.W};
+  FpLive l{p.M, p.W, p.n_ctas};
   if (p.m_dev) {
     const int m = __ldcg(p.m_dev);
     l.m = m < 0 ? 0 : (m > p.M ? p.M : m);
     l.W = (long long)p.n_otiles * ((l.m + p.bn - 1) / p.bn) * p.nk;
+    l.n = l.W < p.n_ctas ? (int)l.W : p.n_ctas;
   }
   return l;
 }
@@ -872,8 +878,8 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
   const int tile = blockIdx.y;
   const long long x0 = (long long)tile * p.nk;
   if (x0 >= lv.W) return;  // a group past the live rows
-  const int c_first = sk_owner(x0, lv.W, p.n_ctas);
-  const int c_last = sk_owner(x0 + p.nk - 1, lv.W, p.n_ctas);
+  const int c_first = sk_owner(x0, lv.W, lv.n);
+  const int c_last = sk_owner(x0 + p.nk - 1, lv.W, lv.n);
   if (c_first == c_last) return;  // one CTA held the whole tile and wrote it
   const int ot = tile % p.n_otiles, gr = tile / p.n_otiles;
   const int m0 = gr * p.bn, ncol = min(p.bn, lv.m - m0);
@@ -983,8 +989,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cta_start(sh, tmem_cols);
   const FpLive lv = fp_live(p);
   if (p.m_dev) {
-    sc.lo = sk_lo(blockIdx.x, lv.W, p.n_ctas);
-    sc.hi = sk_lo(blockIdx.x + 1, lv.W, p.n_ctas);
+    const bool active = (int)blockIdx.x < lv.n;
+    sc.lo = active ? sk_lo(blockIdx.x, lv.W, lv.n) : 0;
+    sc.hi = active ? sk_lo(blockIdx.x + 1, lv.W, lv.n) : 0;
   }
 
   if (warp == 0) {
@@ -1033,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stream-K partial: write it; fuse_proj_reduce_kernel sums the
         // contributors of the tile afterwards
         const long long x0 = (long long)sg.tile * p.nk;
-        const int c_first = sk_owner(x0, lv.W, p.n_ctas);
+        const int c_first = sk_owner(x0, lv.W, lv.n);
         const int slot = blockIdx.x - c_first;
         float* part = p.part + (((size_t)sg.tile * p.max_contrib + slot) * bn) * 128;
         for (int c16 = 0; c16 * 16 < ncol; ++c16) {
@@ -1569,9 +1576,10 @@ int fp_live_contrib(const FpPlan& f) {
   int mc = f.max_contrib;
   for (int g = 1; g < f.G; ++g) {
     const long long W = (long long)f.n_otiles * g * f.nk;
-    const long long per = W / f.n_ctas;
-    long long c = per > 0 ? (f.nk + per - 1) / per + 1 : f.nk;
-    if (c > f.n_ctas) c = f.n_ctas;
+    const int n = W < f.n_ctas ? (int)W : f.n_ctas;  // the active CTAs (fp_live)
+    const long long per = W / n;                       // >= 1
+    long long c = (f.nk + per - 1) / per + 1;
+    if (c > n) c = n;
     if (c > mc) mc = (int)c;
   }
   return mc;
