@@ -239,9 +239,21 @@ int eagle_linear(const void* x, const void* w, const float* bias, const void* re
  *   tree_mask    : [B, R] uint64, bit j = row j visible (self bit required)
  *   out          : [B, R, Hq, D] dtype `dtype`;  lse: [B, R, Hq] fp32 or NULL
  *   scale        : score scale (pass 1/sqrt(D) for the standard one)
- *   num_splits   : split-KV factor (0 = choose from the SM count)
+ *   num_splits   : schedule.  0 = automatic: with many 64-key blocks per SM
+ *                  (>= 16, counted with the block table's width) the stream
+ *                  schedule -- one persistent CTA per SM, the key blocks of
+ *                  every (request, kv head, query-tile group) split evenly
+ *                  over the SMs from the real ctx_lens, planned on the device,
+ *                  and the pieces of a split unit merged by a second kernel;
+ *                  otherwise the split schedule -- one CTA per (query-tile
+ *                  group, KV range, request x kv head) with the KV-range count
+ *                  chosen from the SM count, the ranges merged by a second
+ *                  kernel.  n > 0 = the split schedule with n KV ranges;
+ *                  -1 = the stream schedule.
+ * The workspace size depends on the schedule: query it with the same
+ * num_splits.
  * Limits: R <= 64, D in {64, 128}, page_size == 16, Hq % Hkv == 0,
- * Hq / Hkv <= 16.
+ * Hq / Hkv <= 16, num_splits >= -1.
  * ---------------------------------------------------------------------- */
 size_t eagle_tree_attn_workspace_size(int B, int R, int Hq, int Hkv, int D,
                                       int max_pages, int page_size, int num_splits,

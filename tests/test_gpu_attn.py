@@ -66,6 +66,32 @@ def test_bf16_small_cases(B, R, Hq, Hkv, D, lo, hi, splits):
     assert np.abs(lse - ref_l).max() < 2e-2
 
 
+@pytest.mark.parametrize("B,R,Hq,Hkv,D,lo,hi", [
+    (1, 17, 4, 2, 64, 128, 128),
+    (2, 13, 8, 2, 128, 1, 300),
+    (3, 61, 32, 8, 128, 0, 200),       # empty prefixes: units of the tree block only
+    (1, 64, 16, 1, 128, 100, 100),
+    (4, 5, 4, 4, 64, 33, 97),
+    (2, 20, 12, 4, 128, 50, 400),
+    (3, 33, 10, 2, 64, 0, 260),
+    (40, 9, 32, 8, 128, 0, 700),       # many requests: segments cross requests, some empty
+    (2, 61, 32, 8, 128, 4000, 5000),   # two query tiles per unit
+])
+def test_bf16_stream_schedule(B, R, Hq, Hkv, D, lo, hi):
+    """The persistent stream schedule (num_splits = -1) on shapes the
+    automatic choice gives to the split schedule: units split between CTAs,
+    merged pieces, segments crossing requests."""
+    b = need_gpu()
+    case = _case(B * 37 + R + 1, B, R, Hq, Hkv, D, lo, hi, "bf16")
+    out, lse, st = _gpu(b, *case, num_splits=-1)
+    ref_o, ref_l = _ref(*case)
+    assert st == 0
+    err, nerr = rel_err(out, ref_o), norm_err(out, ref_o)
+    print(f"stream B={B} R={R} Hq={Hq} D={D}: rel {err:.2e}, norm-wise {nerr:.2e}")
+    assert err < REL_TOL and nerr < NORM_TOL
+    assert np.abs(lse - ref_l).max() < 2e-2
+
+
 def test_chain_tree_bf16():
     b = need_gpu()
     case = _case(7, 1, 12, 8, 2, 128, 77, 77, "bf16", chain=True)
