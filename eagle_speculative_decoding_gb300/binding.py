@@ -48,6 +48,8 @@ _SIGS = {
     "eagle_lmhead_topk_partial": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P, _P]),
     "eagle_lmhead_topk_merge": (_I, [_I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _Z, _P, _P]),
     "eagle_tree_expand": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "eagle_tree_expand_lmhead": (_I, [_I, _I, _I, _I, _I, _P, _Z, _I, _I, _F, _I, _P, _P, _P, _P, _P, _P, _P,
+                                      _P, _P, _P]),
     "eagle_tree_expand_static": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       _P]),
     "eagle_tree_expand_finalize": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -318,6 +320,21 @@ def eagle_tree_expand(step, width, cand_ids, cand_logprobs, root_token, node_par
         B, step, width, k, max_nodes, _ptr(cand_ids), _ptr(cand_logprobs), _ptr(root_token),
         _ptr(node_parent), _ptr(node_token), _ptr(node_logv), _ptr(node_depth), _ptr(node_count),
         _ptr(frontier), _ptr(n_frontier), _ptr(status), _stream(stream)))
+
+
+def eagle_tree_expand_lmhead(step, width, k, lm_ws, d, V, root_token, node_parent, node_token, node_logv,
+                             node_depth, node_count, frontier, n_frontier, temperature=1.0, dtype=None,
+                             status=None, stream=None):
+    """One expansion step whose candidate lists are merged from the partials
+    that eagle_lmhead_topk_partial left in lm_ws (B * P rows, P = 1 at step 0,
+    else width)."""
+    B, max_nodes = node_parent.shape
+    if dtype is None:
+        dtype = EAGLE_BF16
+    _check("eagle_tree_expand_lmhead", lib().eagle_tree_expand_lmhead(
+        B, step, width, k, max_nodes, _ptr(lm_ws), lm_ws.numel(), d, V, float(temperature), dtype,
+        _ptr(root_token), _ptr(node_parent), _ptr(node_token), _ptr(node_logv), _ptr(node_depth),
+        _ptr(node_count), _ptr(frontier), _ptr(n_frontier), _ptr(status), _stream(stream)))
 
 
 def eagle_tree_expand_static(step, width, fanout, cand_ids, cand_logprobs, root_token, node_parent, node_token,

@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "lm_merge.cuh"
 
 namespace eagle {
 namespace {
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmPar
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(16) unsigned char msm[];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int m = blockIdx.x;
   const int K = p.K, nc = p.ctas_per_group, n = nc * K;
   float* sv = reinterpret_cast<float*>(msm);
@@ -536,7 +537,6 @@ __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmPar
   const float* gv = p.part_v + (size_t)m * n;
   const int* gi = p.part_i + (size_t)m * n;
   const int* gc = p.part_cnt + (size_t)m * nc;
-  const float2* gms = p.part_ms + (size_t)m * nc;
   constexpr int kU = 4;
   for (int f0 = tid; f0 < n; f0 += kMergeThreads * kU) {
     float v[kU];
@@ -557,81 +557,19 @@ __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmPar
     }
   }
   for (int c = tid; c < nc; c += kMergeThreads) sc[c] = __ldcg(gc + c);
-  constexpr int kPer = kMaxCtas / 32;  // lists owned per lane of warp 0
-  float2 ms[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = lane + 32 * i;
-    ms[i] = tid < 32 && c < nc ? __ldcg(gms + c) : make_float2(-INFINITY, 0.f);
-  }
   __syncthreads();
   if (tid >= 32) return;
-  float M = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) M = fmaxf(M, ms[i].x);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float S = 0.f;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i)
-    if (ms[i].x != -INFINITY) S += ms[i].y * exp2f((ms[i].x - M) * kLog2e);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-  float hv[kPer];
-  int hi[kPer], hp[kPer], hc[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = lane + 32 * i;
-    hp[i] = 0;
-    hc[i] = c < nc ? sc[c] : 0;
-    hv[i] = hc[i] > 0 ? sv[c * K] : -INFINITY;
-    hi[i] = hc[i] > 0 ? si[c * K] : 0x7fffffff;
-  }
-  const float lse = M + logf(S);
-  const size_t ob = (size_t)m * K;
-  for (int rnd = 0; rnd < K; ++rnd) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff, bs = -1;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (hp[i] < hc[i] && better(hv[i], hi[i], bv, bi)) {
-        bv = hv[i];
-        bi = hi[i];
-        bs = i;
-      }
-    int owner = bs >= 0 ? lane : 32;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ow = __shfl_xor_sync(0xffffffffu, owner, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-        owner = ow;
-      }
-    }
-    if (lane == 0) {
-      p.topk_ids[ob + rnd] = bi == 0x7fffffff ? -1 : bi;
-      p.topk_lp[ob + rnd] = bi == 0x7fffffff ? -INFINITY : (p.race ? bv : bv * p.inv_t - lse);
-    }
-    if (lane == owner && bs >= 0) {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (i == bs) {
-          const int c = lane + 32 * i;
-          ++hp[i];
-          if (hp[i] < hc[i]) {
-            hv[i] = sv[c * K + hp[i]];
-            hi[i] = si[c * K + hp[i]];
-          }
-        }
-    }
-  }
-  if (lane == 0) {
-    if (p.row_max) p.row_max[m] = M;
-    if (p.row_sumexp) p.row_sumexp[m] = S;
-  }
+  LmPartials lp;
+  lp.ms = p.part_ms;
+  lp.v = p.part_v;
+  lp.id = p.part_i;
+  lp.cnt = p.part_cnt;
+  lp.cpg = nc;
+  lp.K = K;
+  lp.inv_t = p.inv_t;
+  lp.race = p.race;
+  lm_merge_row(lp, m, sv, si, sc, p.topk_ids + (size_t)m * K, p.topk_lp + (size_t)m * K, p.row_max,
+               p.row_sumexp);
 }
 
 template <int KMAX>
@@ -1333,6 +1271,33 @@ struct RaceCfg {
 // only the merge of partials a kPartial call left in ws (kMerge).
 enum LmPhase { kBoth = 0, kPartial = 1, kMerge = 2 };
 
+// Activation groups (128 rows each), CTAs per group and vocabulary rows per
+// tile of one LM-head call.
+struct LmPlan {
+  int G, cpg, tn, n_vtiles;
+};
+LmPlan lm_plan(int M, int V, int dtype, int sms) {
+  LmPlan pl;
+  pl.G = (M + 127) / 128;
+  sms = sms > kMaxCtas ? kMaxCtas : sms;
+  int cpg = sms / pl.G;
+  if (cpg < 1) cpg = 1;
+  if (cpg > kMaxCtas / pl.G) cpg = kMaxCtas / pl.G;
+  // vocabulary rows per tile: 128 (fewer, larger K-chunks per byte of W_U
+  // measured faster than narrower tiles with better balance); narrower only
+  // when V is smaller than one tile per CTA
+  int tn = 128;
+  while (tn > 16 && (V + tn - 1) / tn < cpg) tn -= 16;
+  // several activation groups re-read every W_U tile from L2: 256-row tiles
+  // (two 256-column TMEM buffers) cut that traffic per flop by a third
+  if (pl.G >= 2 && dtype == EAGLE_BF16 && (V + 255) / 256 >= 4 * cpg) tn = 256;
+  pl.tn = tn;
+  pl.n_vtiles = (V + tn - 1) / tn;
+  if (cpg > pl.n_vtiles) cpg = pl.n_vtiles;
+  pl.cpg = cpg;
+  return pl;
+}
+
 int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d, int V, int k,
                float temperature, int32_t* topk_ids, float* topk_logprobs, float* row_max,
                float* row_sumexp, int dtype, void* ws, size_t ws_bytes, int32_t* dev_status,
@@ -1346,23 +1311,10 @@ int lmhead_run(const void* x, const void* w_lm, const float* bias, int M, int d,
   if (M > 2048 || k > 32 || d % 64 || V % 16) return EAGLE_ERR_UNSUPPORTED;
   if (phase != kMerge && (!aligned16(x) || !aligned16(w_lm))) return EAGLE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < eagle_lmhead_topk_workspace_size(M, d, V, k, dtype)) return EAGLE_ERR_WORKSPACE;
-  const int G = (M + 127) / 128;
-  int sms = sm_count();
+  const int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
-  sms = sms > kMaxCtas ? kMaxCtas : sms;
-  int cpg = sms / G;
-  if (cpg < 1) cpg = 1;
-  if (cpg > kMaxCtas / G) cpg = kMaxCtas / G;
-  // vocabulary rows per tile: 128 (fewer, larger K-chunks per byte of W_U
-  // measured faster than narrower tiles with better balance); narrower only
-  // when V is smaller than one tile per CTA
-  int tn = 128;
-  while (tn > 16 && (V + tn - 1) / tn < cpg) tn -= 16;
-  // several activation groups re-read every W_U tile from L2: 256-row tiles
-  // (two 256-column TMEM buffers) cut that traffic per flop by a third
-  if (G >= 2 && dtype == EAGLE_BF16 && (V + 255) / 256 >= 4 * cpg) tn = 256;
-  const int n_vtiles = (V + tn - 1) / tn;
-  if (cpg > n_vtiles) cpg = n_vtiles;
+  const LmPlan pl = lm_plan(M, V, dtype, sms);
+  const int G = pl.G, cpg = pl.cpg, tn = pl.tn, n_vtiles = pl.n_vtiles;
   const int n_ctas = cpg * G;
   const size_t lists = 0;
   const int rows_g = M < 128 ? M : 128;           // rows of the largest group
@@ -1492,6 +1444,32 @@ __global__ void __launch_bounds__(256) child_logit_kernel(
   if (lane == 0) out[gw] = ok ? acc + (bias ? bias[t] : 0.f) : 0.f;
 }
 }  // namespace
+}  // namespace eagle
+
+namespace eagle {
+// The partials an eagle_lmhead_topk_partial call left in ws (the carve of lmhead_run).
+bool lm_partials_view(void* ws, size_t ws_bytes, int M, int d, int V, int k, int dtype, float temperature,
+                      LmPartials* out) {
+  if (!ws || M <= 0 || d <= 0 || V <= 0 || k <= 0 || k > 32 || k > V || M > 2048 || d % 64 || V % 16)
+    return false;
+  if (dtype != EAGLE_BF16 && dtype != EAGLE_FP32) return false;
+  if (!(temperature > 0.f) || isinf(temperature)) return false;
+  if (ws_bytes < eagle_lmhead_topk_workspace_size(M, d, V, k, dtype)) return false;
+  const int sms = sm_count();
+  if (sms <= 0) return false;
+  const LmPlan pl = lm_plan(M, V, dtype, sms);
+  char* cur = static_cast<char*>(ws);
+  const size_t n = (size_t)pl.G * 128 * kMaxCtas;
+  out->ms = static_cast<const float2*>(ws_carve(cur, n * 8));
+  out->v = static_cast<const float*>(ws_carve(cur, n * k * 4));
+  out->id = static_cast<const int*>(ws_carve(cur, n * k * 4));
+  out->cnt = static_cast<const int*>(ws_carve(cur, n * 4));
+  out->cpg = pl.cpg;
+  out->K = k;
+  out->inv_t = 1.f / temperature;
+  out->race = 0;
+  return true;
+}
 }  // namespace eagle
 
 extern "C" int eagle_lmhead_topk(const void* x, const void* w_lm, const float* bias, int M, int d,

@@ -9,12 +9,13 @@
 // with ancestry-aware positions and a tree mask).
 //
 // One CTA per request.  A step ranks its (at most width*k) new nodes by
-// counting smaller keys (keys are unique: node ids differ); the final rerank
-// bitonic-sorts 64-bit order-preserving keys of all stored nodes.  log V is
+// counting smaller 64-bit order-preserving keys (unique: node ids differ);
+// the final rerank bitonic-sorts the keys of all stored nodes.  log V is
 // accumulated in fp32 with one correctly rounded addition per level.
 #include <math.h>
 
 #include "common.cuh"
+#include "lm_merge.cuh"
 
 namespace eagle {
 namespace {
@@ -25,13 +26,6 @@ constexpr int kMaxNodes = 2048;
 // log(1e-12) rounded to fp32: the ranking floor of a zero confidence.
 constexpr float kLogEps = -27.631021115928547f;
 constexpr float kMassTol = 1e-4f;
-
-// key(a) < key(b): larger log V first, then shallower, then smaller node id.
-__device__ __forceinline__ bool key_less(float va, int da, int ia, float vb, int db, int ib) {
-  if (va != vb) return va > vb;
-  if (da != db) return da < db;
-  return ia < ib;
-}
 
 // Order-preserving 64-bit sort key of a node: ascending key = descending
 // log V, then ascending depth, then ascending node id.
@@ -58,14 +52,17 @@ __device__ __forceinline__ int block_exclusive_scan(const int* flags, int* out, 
     if (lane == 0) s_warp[h * kW + warp] = __popc(bal);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int w = 0; w < 2 * kW; ++w) {
-      const int c = s_warp[w];
-      s_warp[w] = acc;
-      acc += c;
+  static_assert(2 * kW == 32, "one warp scans the warp totals");
+  if (warp == 0) {  // exclusive scan of the 32 warp totals by shuffles
+    const int c = s_warp[lane];
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
     }
-    s_total = acc;
+    s_warp[lane] = inc - c;
+    if (lane == 31) s_total = inc;
   }
   __syncthreads();
 #pragma unroll
@@ -77,15 +74,24 @@ __device__ __forceinline__ int block_exclusive_scan(const int* flags, int* out, 
   return s_total;
 }
 
+// One expansion step.  MERGE: the candidate lists are not read from
+// cand_ids / cand_lp but merged here from the per-CTA partials an LM-head call
+// left (lp; row b * P + j holds parent slot j of request b): stage_rows rows
+// at a time are staged in dynamic shared memory by all threads, then one warp
+// per row merges them straight into the candidate arrays.
+template <bool MERGE>
 __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     int step, int width, int k, int max_nodes, const int32_t* __restrict__ cand_ids,
-    const float* __restrict__ cand_lp, const int32_t* __restrict__ root_token,
+    const float* __restrict__ cand_lp, const LmPartials lp, int stage_rows,
+    const int32_t* __restrict__ root_token,
     int32_t* __restrict__ node_parent, int32_t* __restrict__ node_token,
     float* __restrict__ node_logv, int32_t* __restrict__ node_depth,
     int32_t* __restrict__ node_count, int32_t* __restrict__ frontier,
     int32_t* __restrict__ n_frontier, const int32_t* __restrict__ fanout, int32_t* dev_status) {
+  // the next kernel (an LM head that prefetches its weights) is let in only
+  // at the end: its prefetch would otherwise queue ahead of this kernel's
+  // few latency-bound loads
   pdl_wait();
-  pdl_trigger();
   const int b = blockIdx.x;
   const int P = step == 0 ? 1 : width;
   int32_t* np_ = node_parent + (size_t)b * max_nodes;
@@ -97,11 +103,15 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
   __shared__ float s_parv[64];
   __shared__ int s_pard[64];
   __shared__ float s_mass[64];
-  __shared__ int s_valid[kMaxCand];
+  // s_lp and s_valid share their bytes with the 64-bit ranking keys, which
+  // are written only after both are consumed
+  __shared__ __align__(16) unsigned char s_kbuf[kMaxCand * 8];
+  float* s_lp = reinterpret_cast<float*>(s_kbuf);
+  int* s_valid = reinterpret_cast<int*>(s_kbuf) + kMaxCand;
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(s_kbuf);
   __shared__ int s_scan[kMaxCand];
   __shared__ float s_v[kMaxCand];
   __shared__ int s_id[kMaxCand];
-  __shared__ float s_lp[kMaxCand];
   __shared__ int s_bad;
   __shared__ int s_fan[64];  // static tree: children kept per parent slot
 
@@ -144,11 +154,89 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
       s_pard[j] = nd_[p];
     }
   }
-  for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
-    const int j = t / k, i = t % k;
-    const size_t src = ((size_t)b * P + j) * k + i;
-    s_id[t] = cand_ids[src];
-    s_lp[t] = cand_lp[src];
+  if (MERGE) {
+    extern __shared__ __align__(16) unsigned char stage[];
+    const int nc = lp.cpg, n = nc * k, warp = threadIdx.x >> 5;
+    const size_t row_bytes = ((size_t)n * 8 + (size_t)nc * 4 + 15) / 16 * 16;
+    for (int j0 = 0; j0 < npar; j0 += stage_rows) {
+      const int nb = min(stage_rows, npar - j0);
+      // the batch's lists are contiguous ([row][cta][K] from row b * P + j0):
+      // 16-byte loads when the rows keep 16-byte alignment, four in flight
+      // per thread before any store
+      const size_t m0 = (size_t)b * P + j0;
+      if ((n & 3) == 0) {
+        const int n4 = n / 4, tot = nb * n4;
+        const float4* gv = reinterpret_cast<const float4*>(lp.v + m0 * n);
+        const int4* gi = reinterpret_cast<const int4*>(lp.id + m0 * n);
+        for (int f0 = threadIdx.x; f0 < tot; f0 += 4 * kExpandThreads) {
+          float4 v[4];
+          int4 id[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int f = f0 + u * kExpandThreads;
+            if (f < tot) {
+              v[u] = __ldcg(gv + f);
+              id[u] = __ldcg(gi + f);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int f = f0 + u * kExpandThreads;
+            if (f < tot) {
+              const int r = f / n4, e = f % n4;
+              float4* sv = reinterpret_cast<float4*>(stage + r * row_bytes);
+              sv[e] = v[u];
+              reinterpret_cast<int4*>(sv + n4)[e] = id[u];
+            }
+          }
+        }
+      } else {
+        const int tot = nb * n;
+        for (int f0 = threadIdx.x; f0 < tot; f0 += 4 * kExpandThreads) {
+          float v[4];
+          int id[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int f = f0 + u * kExpandThreads;
+            if (f < tot) {
+              v[u] = __ldcg(lp.v + m0 * n + f);
+              id[u] = __ldcg(lp.id + m0 * n + f);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int f = f0 + u * kExpandThreads;
+            if (f < tot) {
+              const int r = f / n, e = f % n;
+              float* sv = reinterpret_cast<float*>(stage + r * row_bytes);
+              sv[e] = v[u];
+              reinterpret_cast<int*>(sv + n)[e] = id[u];
+            }
+          }
+        }
+      }
+      for (int f = threadIdx.x; f < nb * nc; f += kExpandThreads) {
+        const int r = f / nc, c = f % nc;
+        const size_t m = (size_t)b * P + j0 + r;
+        int* sc = reinterpret_cast<int*>(stage + r * row_bytes) + 2 * n;
+        sc[c] = __ldcg(lp.cnt + m * nc + c);
+      }
+      __syncthreads();
+      if (warp < nb) {
+        const float* sv = reinterpret_cast<const float*>(stage + warp * row_bytes);
+        const int* si = reinterpret_cast<const int*>(sv + n);
+        lm_merge_row(lp, b * P + j0 + warp, sv, si, si + n, s_id + (j0 + warp) * k, s_lp + (j0 + warp) * k,
+                     nullptr, nullptr);
+      }
+      __syncthreads();
+    }
+  } else {
+    for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
+      const int j = t / k, i = t % k;
+      const size_t src = ((size_t)b * P + j) * k + i;
+      s_id[t] = cand_ids[src];
+      s_lp[t] = cand_lp[src];
+    }
   }
   __syncthreads();
   // validation (duplicates, non-finite values, sibling mass) and values
@@ -180,6 +268,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
       n_frontier[b] = 0;
       if (step == 0) node_count[b] = 1;
     }
+    pdl_trigger();
     return;
   }
   // creation-ordered node ids (slot, then rank) via a block prefix sum
@@ -189,26 +278,44 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
       set_status(dev_status, EAGLE_ERR_INVALID_ARG);
       n_frontier[b] = 0;
     }
+    pdl_trigger();
     return;
   }
-  for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
-    if (!s_valid[t]) continue;
+  // the ranking key of each new node (all of the same depth): larger log V
+  // first, then smaller node id; a discarded candidate sorts last
+  constexpr int kPerT = kMaxCand / kExpandThreads;
+  unsigned long long key[kPerT];
+#pragma unroll
+  for (int h = 0; h < kPerT; ++h) {
+    const int t = h * kExpandThreads + threadIdx.x;
+    key[h] = ~0ull;
+    if (t < ncand && s_valid[t]) key[h] = node_key(s_v[t] + 0.f, 0, count0 + s_scan[t]);
+  }
+  __syncthreads();  // s_valid and s_lp are read: their bytes become the keys
+#pragma unroll
+  for (int h = 0; h < kPerT; ++h) {
+    const int t = h * kExpandThreads + threadIdx.x;
+    if (t < ncand) s_key[t] = key[h];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < kPerT; ++h) {
+    const int t = h * kExpandThreads + threadIdx.x;
+    const unsigned long long mk = key[h];
+    if (t >= ncand || mk == ~0ull) continue;
     const int j = t / k;
     const int node = count0 + s_scan[t];
     np_[node] = s_par[j];
     nt_[node] = s_id[t];
     nv_[node] = s_v[t];
     nd_[node] = s_pard[j] + 1;
-    // next frontier: rank of this node among the new nodes (same depth) by
-    // key; a static tree keeps creation order
+    // next frontier: rank of this node among the new nodes by key (keys are
+    // unique: node ids differ); a static tree keeps creation order
     int rank = s_scan[t];
     if (!fanout) {
-      const float v = s_v[t];
       rank = 0;
-      for (int u = 0; u < ncand; ++u) {
-        if (!s_valid[u] || u == t) continue;
-        rank += key_less(s_v[u], 0, count0 + s_scan[u], v, 0, node) ? 1 : 0;
-      }
+#pragma unroll 8
+      for (int u = 0; u < ncand; ++u) rank += s_key[u] < mk ? 1 : 0;
     }
     if (rank < width) frontier[(size_t)b * width + rank] = node;
   }
@@ -217,6 +324,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
     n_frontier[b] = nnew < width ? nnew : width;
     node_count[b] = count0 + nnew;
   }
+  pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
@@ -324,22 +432,40 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
 using namespace eagle;
 
 namespace {
+// Dynamic shared memory the merging expansion stages partial lists in.
+constexpr size_t kStageBytes = 192 * 1024;
+
 int expand_launch(int B, int step, int width, int k, int max_nodes, const int32_t* fanout,
-                  const int32_t* cand_ids, const float* cand_logprobs, const int32_t* root_token,
-                  int32_t* node_parent, int32_t* node_token, float* node_logv, int32_t* node_depth,
-                  int32_t* node_count, int32_t* frontier, int32_t* n_frontier, int32_t* dev_status,
-                  void* stream) {
+                  const int32_t* cand_ids, const float* cand_logprobs, const LmPartials* lp,
+                  const int32_t* root_token, int32_t* node_parent, int32_t* node_token, float* node_logv,
+                  int32_t* node_depth, int32_t* node_count, int32_t* frontier, int32_t* n_frontier,
+                  int32_t* dev_status, void* stream) {
   if (B <= 0 || step < 0 || width < 1 || k < 1 || max_nodes < 1) return EAGLE_ERR_INVALID_ARG;
-  if (!cand_ids || !cand_logprobs || !node_parent || !node_token || !node_logv || !node_depth ||
+  if ((!lp && (!cand_ids || !cand_logprobs)) || !node_parent || !node_token || !node_logv || !node_depth ||
       !node_count || !frontier || !n_frontier)
     return EAGLE_ERR_INVALID_ARG;
   if (step == 0 && !root_token) return EAGLE_ERR_INVALID_ARG;
   if (width > 64 || k > 32 || width * k > kMaxCand || max_nodes > kMaxNodes || B > 65535)
     return EAGLE_ERR_UNSUPPORTED;
   if ((long long)max_nodes < 1LL + k + (long long)step * width * k) return EAGLE_ERR_INVALID_ARG;
-  launch(expand_step_kernel, B, kExpandThreads, 0, static_cast<cudaStream_t>(stream),
-      step, width, k, max_nodes, cand_ids, cand_logprobs, root_token, node_parent, node_token,
-      node_logv, node_depth, node_count, frontier, n_frontier, fanout, dev_status);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (lp) {
+    const size_t row_bytes = ((size_t)lp->cpg * k * 8 + (size_t)lp->cpg * 4 + 15) / 16 * 16;
+    const int P = step == 0 ? 1 : width;
+    int rows = (int)(kStageBytes / row_bytes);
+    rows = rows < kExpandThreads / 32 ? rows : kExpandThreads / 32;
+    rows = rows < P ? rows : P;
+    if (rows < 1) return EAGLE_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)rows * row_bytes;
+    cudaFuncSetAttribute(expand_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    launch(expand_step_kernel<true>, B, kExpandThreads, smem, s, step, width, k, max_nodes, cand_ids,
+           cand_logprobs, *lp, rows, root_token, node_parent, node_token, node_logv, node_depth, node_count,
+           frontier, n_frontier, fanout, dev_status);
+  } else {
+    launch(expand_step_kernel<false>, B, kExpandThreads, 0, s, step, width, k, max_nodes, cand_ids,
+           cand_logprobs, LmPartials{}, 0, root_token, node_parent, node_token, node_logv, node_depth,
+           node_count, frontier, n_frontier, fanout, dev_status);
+  }
   note_launch();
   return last_launch_status();
 }
@@ -351,9 +477,26 @@ extern "C" int eagle_tree_expand(int B, int step, int width, int k, int max_node
                                  int32_t* node_token, float* node_logv, int32_t* node_depth,
                                  int32_t* node_count, int32_t* frontier, int32_t* n_frontier,
                                  int32_t* dev_status, void* stream) {
-  return expand_launch(B, step, width, k, max_nodes, nullptr, cand_ids, cand_logprobs, root_token,
+  return expand_launch(B, step, width, k, max_nodes, nullptr, cand_ids, cand_logprobs, nullptr, root_token,
                        node_parent, node_token, node_logv, node_depth, node_count, frontier, n_frontier,
                        dev_status, stream);
+}
+
+extern "C" int eagle_tree_expand_lmhead(int B, int step, int width, int k, int max_nodes,
+                                        const void* lm_ws, size_t lm_ws_bytes, int d, int V,
+                                        float temperature, int dtype, const int32_t* root_token,
+                                        int32_t* node_parent, int32_t* node_token, float* node_logv,
+                                        int32_t* node_depth, int32_t* node_count, int32_t* frontier,
+                                        int32_t* n_frontier, int32_t* dev_status, void* stream) {
+  if (B <= 0 || width < 1 || step < 0) return EAGLE_ERR_INVALID_ARG;
+  const long long M = (long long)B * (step == 0 ? 1 : width);
+  if (M > 2048) return EAGLE_ERR_UNSUPPORTED;
+  LmPartials lp;
+  if (!lm_partials_view(const_cast<void*>(lm_ws), lm_ws_bytes, (int)M, d, V, k, dtype, temperature, &lp))
+    return lm_ws ? EAGLE_ERR_WORKSPACE : EAGLE_ERR_INVALID_ARG;
+  return expand_launch(B, step, width, k, max_nodes, nullptr, nullptr, nullptr, &lp, root_token, node_parent,
+                       node_token, node_logv, node_depth, node_count, frontier, n_frontier, dev_status,
+                       stream);
 }
 
 extern "C" int eagle_tree_expand_static(int B, int step, int width, int k, int max_nodes,
@@ -363,7 +506,7 @@ extern "C" int eagle_tree_expand_static(int B, int step, int width, int k, int m
                                         int32_t* node_depth, int32_t* node_count, int32_t* frontier,
                                         int32_t* n_frontier, int32_t* dev_status, void* stream) {
   if (!fanout) return EAGLE_ERR_INVALID_ARG;
-  return expand_launch(B, step, width, k, max_nodes, fanout, cand_ids, cand_logprobs, root_token,
+  return expand_launch(B, step, width, k, max_nodes, fanout, cand_ids, cand_logprobs, nullptr, root_token,
                        node_parent, node_token, node_logv, node_depth, node_count, frontier, n_frontier,
                        dev_status, stream);
 }

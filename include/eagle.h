@@ -431,6 +431,29 @@ int eagle_tree_expand(int B, int step, int width, int k, int max_nodes,
                       int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_tree_expand_lmhead -- eagle_tree_expand whose candidate lists come
+ * straight from an LM-head call's partial results.
+ * [M7.5] sections 0x06A, 0x06B (as eagle_tree_expand) with [E1]
+ * "Tree-Structured Draft Generation" (the children are the top-k tokens of
+ * the parent's drafter row).  The call follows an eagle_lmhead_topk_partial
+ * over M = B * P drafter rows (P = 1 at step 0, else width; row b * P + j =
+ * parent slot j of request b) with the same k, d, V, dtype and temperature,
+ * and takes its workspace `lm_ws`: each parent row's top-k ids and log-probs
+ * are merged from the LM head's per-CTA partial lists inside the expansion
+ * kernel, so no merge kernel and no [M, k] candidate arrays sit between the
+ * LM head and the expansion.  The merged lists equal those of
+ * eagle_lmhead_topk_merge bit for bit, and the tree state equals that of
+ * eagle_lmhead_topk_merge followed by eagle_tree_expand.
+ * Limits: those of eagle_tree_expand and eagle_lmhead_topk (M <= 2048).
+ * ---------------------------------------------------------------------- */
+int eagle_tree_expand_lmhead(int B, int step, int width, int k, int max_nodes,
+                             const void* lm_ws, size_t lm_ws_bytes, int d, int V,
+                             float temperature, int dtype, const int32_t* root_token,
+                             int32_t* node_parent, int32_t* node_token, float* node_logv,
+                             int32_t* node_depth, int32_t* node_count, int32_t* frontier,
+                             int32_t* n_frontier, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * eagle_tree_expand_static -- one depth of a static (EAGLE-1) draft tree.
  * [E1] "Tree-Structured Draft Generation" and its note on the tree used: a
  * fixed tree whose root branches into its top-4 tokens and whose deeper
