@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
   const float* nv_ = node_logv + (size_t)b * max_nodes;
   const int32_t* nd_ = node_depth + (size_t)b * max_nodes;
   __shared__ unsigned long long s_key[kMaxNodes];
+  __shared__ unsigned long long s_sel[64];  // the selected nodes' keys, rank order
   __shared__ int s_row_of[kMaxNodes];
   __shared__ int s_prow[64];
   __shared__ int s_bad;
@@ -358,24 +359,38 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
   for (int i = threadIdx.x; i < count; i += kExpandThreads) s_row_of[i] = -1;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  // bitonic sort of the keys (ascending)
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += kExpandThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long a = s_key[lo], c = s_key[hi];
-        if ((a > c) == up) {
-          s_key[lo] = c;
-          s_key[hi] = a;
-        }
-      }
-      __syncthreads();
+  if (n <= 1024) {
+    // the rank of each candidate = how many keys are smaller (keys are
+    // unique); branch-free, every thread reads the same key at a time
+    for (int i = threadIdx.x; i < n; i += kExpandThreads) {
+      const unsigned long long mk = s_key[i];
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < n; ++j) rank += s_key[j] < mk ? 1 : 0;
+      if (rank < nsel) s_sel[rank] = mk;
     }
+  } else {
+    // bitonic sort of the keys (ascending)
+    for (int size = 2; size <= P; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = threadIdx.x; i < P / 2; i += kExpandThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const unsigned long long a = s_key[lo], c = s_key[hi];
+          if ((a > c) == up) {
+            s_key[lo] = c;
+            s_key[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int r = threadIdx.x; r < nsel; r += kExpandThreads) s_sel[r] = s_key[r];
   }
+  __syncthreads();
   for (int r = 1 + threadIdx.x; r <= nsel; r += kExpandThreads)
-    s_row_of[(int)(s_key[r - 1] & 0xFFFFu)] = r;
+    s_row_of[(int)(s_sel[r - 1] & 0xFFFFu)] = r;
   if (threadIdx.x == 0) s_row_of[0] = 0;
   __syncthreads();
   // parent rows (a parent always precedes its child in key order)
@@ -384,7 +399,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
       s_prow[0] = -1;
       continue;
     }
-    const int nd = (int)(s_key[r - 1] & 0xFFFFu);
+    const int nd = (int)(s_sel[r - 1] & 0xFFFFu);
     const int p = np_[nd];
     int pr = (p >= 0 && p < count) ? s_row_of[p] : -1;
     if (pr < 0 || pr >= r) {
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
   const size_t o = (size_t)b * R;
   for (int r = threadIdx.x; r < R; r += kExpandThreads) {
     if (r <= nsel) {
-      const int nd = r == 0 ? 0 : (int)(s_key[r - 1] & 0xFFFFu);
+      const int nd = r == 0 ? 0 : (int)(s_sel[r - 1] & 0xFFFFu);
       uint64_t m = 1ull << r;
       int j = r, guard = 0;
       while (j != 0 && guard++ < 64) {  // ancestry bits by walking the parent rows
