@@ -95,6 +95,8 @@ struct Bars {
   long long tot;  // blocks of one head over all requests
   int n_groups;   // active head groups
   long long warp_sum[32];
+  int stop;          // a uniform leave decision of the softmax warps
+  float xlse[64];    // two-copy tiles: the second copy's row lse at a segment's end
 };
 struct Params {
   const int32_t* block_table;
@@ -111,6 +113,7 @@ struct Params {
   int qtiles;     // query tiles of a (request, kv head)
   int ncq;        // query-tile groups (units) per (request, kv head)
   int tr;         // tree keys loaded: R rounded up to 16
+  int q_box_rows; // tree rows per Q box: nr, or the rows of one copy of a two-copy tile
   int n_ctas;     // stream schedule: the grid, groups of Hkv CTAs, one per kv head
   int splits;     // split schedule: KV ranges per (query-tile group, request x kv head)
   float scale_log2;
@@ -253,7 +256,14 @@ struct SegWalk {
 };
 }  // namespace tc
 
-template <int D, int TPC>
+// COPIES = 2 (one query tile of at most 64 rows): the tile's rows are loaded
+// twice, at TMEM lanes 0.. and 64.., so one S MMA gives each row's scores
+// twice; the first copy takes keys 0-31 of every block and the second keys
+// 32-63 (each writes zeros into its P row for the other half), each with its
+// own m, l and O rows, and the copies are merged at the end of a segment.
+// Each softmax warp thus handles half the keys of a block, and the four warps
+// of the tile (four sub-partitions) all have rows.
+template <int D, int TPC, int COPIES>
 __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     tree_attn_stream_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
@@ -261,6 +271,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
                         const __grid_constant__ CUtensorMap map_kt,
                         const __grid_constant__ CUtensorMap map_vt, const tc::Params p) {
   using namespace tc;
+  static_assert(COPIES == 1 || (COPIES == 2 && TPC == 1), "two copies of a single query tile");
   constexpr int NH = D / 64;                         // 128-byte column halves of a row
   constexpr uint32_t kTileQ = 128u * 128u * NH;      // 128 rows x D
   constexpr uint32_t kTileKV = (uint32_t)kBlk * 128u * NH;
@@ -284,6 +295,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
+    sb.stop = 0;
     mbar_init(smem_u32(&sb.q_full), 1);
     mbar_init(smem_u32(&sb.q_empty), 1);
     for (int x = 0; x < kSt; ++x) {
@@ -371,12 +383,16 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         // the Q tile is free once S of the previous segment's last block is complete
         if (nq > 0) ok = mbar_wait(smem_u32(&sb.q_empty), (uint32_t)(nq - 1) & 1u, abort_flag);
         if (ok) {
-          mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)(nt * NH * rows_tile) * 128u);
+          const uint32_t box_rows = (uint32_t)(p.q_box_rows * p.G);
+          mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)(nt * NH * COPIES) * box_rows * 128u);
           for (int t = 0; t < nt; ++t)
 #pragma unroll
-            for (int h = 0; h < NH; ++h)
-              tma_load_3d(sQ + t * kTileQ + h * 16384u, &map_q, smem_u32(&sb.q_full), h * 64,
-                          sg.kvh * p.G, sg.b * p.R + (TPC * sg.cq + t) * p.nr, pol_q);
+            for (int c = 0; c < COPIES; ++c)
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+                tma_load_3d(sQ + t * kTileQ + h * 16384u + (uint32_t)c * (128u / COPIES) * 128u, &map_q,
+                            smem_u32(&sb.q_full), h * 64, sg.kvh * p.G, sg.b * p.R + (TPC * sg.cq + t) * p.nr,
+                            pol_q);
           ++nq;
         }
       }
@@ -577,9 +593,14 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
+    constexpr int KC = kBlk / COPIES;   // keys of a block this warp's copy takes
+    constexpr int LC = 128 / COPIES;    // TMEM lanes per copy
     const int tq = (warp - 4) / 4;      // query tile of this warp group
     const int q4 = warp & 3;            // TMEM lane quarter of this warp
-    const int i = q4 * 32 + lane;       // query row of the tile = TMEM lane
+    const int i = q4 * 32 + lane;       // TMEM lane
+    const int cpy = COPIES == 1 ? 0 : (q4 * 32) / LC;  // the copy this lane belongs to
+    const int il = i - cpy * LC;        // query row of the tile
+    const int kc0 = cpy * KC;           // first key of a block this copy takes
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     const uint32_t o_addr = tmem + lane_addr + kColO + (uint32_t)(tq * D);
     unsigned char* prow0 = gbase + (sP - base) + 2 * tq * kTileP + i * 128;
@@ -601,18 +622,18 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     SegWalk wk;
     wk.init(p, sb);
     Seg sg;
-    while (ok && wk.next(p, sg)) {
+    while (wk.next(p, sg)) {
       const int nt = min(TPC, p.qtiles - TPC * sg.cq);
-      const int gi = (TPC * sg.cq + tq) * rows_tile + i;
-      const bool row_ok = tq < nt && i < rows_tile && gi < rows_total;
+      const int gi = (TPC * sg.cq + tq) * rows_tile + il;
+      const bool row_ok = tq < nt && il < rows_tile && gi < rows_total;
       // a quarter with no query row keeps only the barrier protocol: its P rows
       // and O rows feed nothing that is written out
       const int tile_rows = tq < nt ? min(rows_tile, rows_total - (TPC * sg.cq + tq) * rows_tile) : 0;
-      const bool quad_live = q4 * 32 < tile_rows;
+      const bool quad_live = q4 * 32 - cpy * LC < tile_rows;
       const int r_i = row_ok ? gi / p.G : 0;
       const uint64_t mrow = row_ok ? p.tree_mask[(size_t)sg.b * p.R + r_i] : 0ull;
       float m = -INFINITY, l = 0.f;
-      for (int u = sg.u0; u < sg.u1; ++u, ++j) {
+      for (int u = sg.u0; ok && u < sg.u1; ++u, ++j) {
         const int x = (int)(j & 1);
         const uint32_t sph = (uint32_t)(j >> 1) & 1u;
         if (lane == 0) ok = mbar_wait(smem_u32(&sb.s_full[x]), sph, abort_flag);
@@ -631,23 +652,23 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
           continue;
         }
         const bool tree = u == sg.L - 1;
-        // visible keys of this block as a 64-bit mask (all set for a full
-        // prefix block); a masked score reads as -inf through a select
+        // visible keys of this block as a 64-bit mask, then this copy's KC
+        // of them; a masked score reads as -inf through a select
         uint64_t vis;
-        bool full = false;
         if (tree) {
           vis = p.R >= 64 ? mrow : (mrow & ((1ull << p.R) - 1ull));
         } else {
           const int lim = sg.ctx - u * kBlk;  // >= 1
-          full = lim >= kBlk;
           vis = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
         }
-        // the block's 64 scores of this row, loaded once; the S buffer is free
+        const uint64_t myvis = KC == 64 ? vis : ((vis >> kc0) & ((1ull << KC) - 1ull));
+        const bool full = KC == 64 ? vis == ~0ull : myvis == ((1ull << KC) - 1ull);
+        // this copy's KC scores of the row, loaded once; the S buffer is free
         // for S(j + 2) as soon as they are in registers
-        const uint32_t sa = tmem + lane_addr + (uint32_t)(tq * 2 * kBlk + x * kBlk);
-        uint32_t sr[kBlk];
-        tmem_ld32_issue(sa, sr);
-        tmem_ld32_issue(sa + 32u, sr + 32);
+        const uint32_t sa = tmem + lane_addr + (uint32_t)(tq * 2 * kBlk + x * kBlk + kc0);
+        uint32_t sr[KC];
+#pragma unroll
+        for (int c = 0; c < KC / 32; ++c) tmem_ld32_issue(sa + 32u * c, sr + 32 * c);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -658,11 +679,11 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int k = 0; k < kBlk; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]));
+          for (int k = 0; k < KC; ++k) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]));
         } else {
 #pragma unroll
-          for (int k = 0; k < kBlk; ++k)
-            mx[k & 7] = fmaxf(mx[k & 7], ((vis >> k) & 1ull) ? __uint_as_float(sr[k]) : -INFINITY);
+          for (int k = 0; k < KC; ++k)
+            mx[k & 7] = fmaxf(mx[k & 7], ((myvis >> k) & 1ull) ? __uint_as_float(sr[k]) : -INFINITY);
         }
         const float bm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
@@ -690,18 +711,18 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
           l *= alpha;
         }
         if (need) m = bm;
-        // pass 2: P = 2^(S * scale_log2 - m) as bf16 into the swizzled P tile,
-        // once P V(j - 2) has read this buffer (the P V thread commits it
-        // separately from the S MMAs, so S(j) being complete says nothing
-        // about it)
+        // pass 2: P = 2^(S * scale_log2 - m) as bf16 into the swizzled P tile
+        // (zeros in the other copy's key chunks), once P V(j - 2) has read
+        // this buffer (the P V thread commits it separately from the S MMAs,
+        // so S(j) being complete says nothing about it)
         if (j >= 2 && !(ok = wait_pv(j - 2))) break;
         const float neg_m = m == -INFINITY ? 0.f : -m;
         unsigned char* prow = prow0 + x * kTileP;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kBlk / 32; ++c) {
+        for (int c = 0; c < KC / 32; ++c) {
           const uint32_t* r = sr + c * 32;
-          const uint32_t w = (uint32_t)(vis >> (c * 32));
+          const uint32_t w = (uint32_t)(myvis >> (c * 32));
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -714,12 +735,19 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
             ls[k & 3] += e0 + e1;
             pk[k] = pack_bf16(e0, e1);
           }
-          // 32 keys = half of the row's 128 bytes: chunks 4 c .. 4 c + 3
+          // 32 keys = half of the row's 128 bytes: chunks kc0 / 8 + 4 c .. + 3
 #pragma unroll
           for (int uu = 0; uu < 4; ++uu) {
-            const int ch = c * 4 + uu;
+            const int ch = kc0 / 8 + c * 4 + uu;
             *reinterpret_cast<uint4*>(prow + ((ch ^ (i & 7)) << 4)) =
                 make_uint4(pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+          }
+        }
+        if (COPIES == 2) {  // the other copy's keys contribute nothing to these rows
+#pragma unroll
+          for (int uu = 0; uu < 4; ++uu) {
+            const int ch = (kc0 == 0 ? 4 : 0) + uu;
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (i & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -728,52 +756,127 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sb.p_full[x]));
       }
-      if (!ok) break;
       // O of the segment is final once its last P V completes
-      if (quad_live && !(ok = wait_pv(j - 1))) break;
+      if (ok && quad_live) ok = wait_pv(j - 1);
       const bool whole = sg.u0 == 0 && sg.u1 == sg.L;
-      if (quad_live) {
-        const int h = sg.kvh * p.G + gi % p.G;
-        const size_t row = ((size_t)sg.b * p.R + r_i) * p.Hq + h;
-        // a piece of a unit split between CTAs: slot 0 holds the CTA's first
-        // segment, slot 1 its last (any other segment is a whole unit)
-        const size_t slot = (size_t)blockIdx.x * 2 + (seg_i == 0 ? 0 : 1);
-        const size_t prow_i = (slot * TPC + tq) * 128 + i;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      // a piece of a unit split between CTAs: slot 0 holds the CTA's first
+      // segment, slot 1 its last (any other segment is a whole unit)
+      const size_t slot = (size_t)blockIdx.x * 2 + (seg_i == 0 ? 0 : 1);
+      const size_t prow_i = (slot * TPC + tq) * 128 + il;
+      const int h = sg.kvh * p.G + gi % p.G;
+      const size_t row = ((size_t)sg.b * p.R + r_i) * p.Hq + h;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (COPIES == 1) {
+        if (!ok) break;
+        if (quad_live) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32_issue(o_addr + (uint32_t)(c * 32), o);
-          tmem_wait_ld();
-          if (!row_ok) continue;
-          if (whole) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_issue(o_addr + (uint32_t)(c * 32), o);
+            tmem_wait_ld();
+            if (!row_ok) continue;
+            if (whole) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
 #pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-              const float* f = reinterpret_cast<const float*>(o + 8 * uu);
-              dst[uu] = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
-                                   pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
+              for (int uu = 0; uu < 4; ++uu) {
+                const float* f = reinterpret_cast<const float*>(o + 8 * uu);
+                dst[uu] = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
+                                     pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
+              }
+            } else {
+              float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D + c * 32);
+#pragma unroll
+              for (int uu = 0; uu < 8; ++uu) {
+                const float* f = reinterpret_cast<const float*>(o + 4 * uu);
+                po[uu] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+              }
             }
-          } else {
-            float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D + c * 32);
+          }
+          if (row_ok) {
+            if (whole) {
+              if (p.lse) p.lse[row] = lse;
+            } else {
+              p.part_lse[prow_i] = lse;
+            }
+          }
+          // O is read out before this warp's next arrival on p_full lets the
+          // next segment's first P V overwrite it
+          tc_fence_before();
+        }
+      } else {
+        // Two copies: the second copy's O / l and lse go through the P tiles
+        // (every P V of the segment is complete, and no P of the next segment
+        // is written before the last barrier below); the first copy merges
+        // them with its own and writes the rows.  All four softmax warps pass
+        // the three barriers of every segment, also after an abort, and leave
+        // together on one decision.
+        float* xo = reinterpret_cast<float*>(gbase + (sP - base));
+        if (ok && quad_live && cpy == 1) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_issue(o_addr + (uint32_t)(c * 32), o);
+            tmem_wait_ld();
+            if (!row_ok) continue;
+            float4* xr = reinterpret_cast<float4*>(xo + (size_t)il * D + c * 32);
 #pragma unroll
             for (int uu = 0; uu < 8; ++uu) {
               const float* f = reinterpret_cast<const float*>(o + 4 * uu);
-              po[uu] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+              xr[uu] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+            }
+          }
+          if (row_ok) sb.xlse[il] = lse;
+        }
+        tc_fence_before();
+        named_bar(1, 128);
+        if (threadIdx.x == 128) sb.stop = *abort_flag ? 1 : 0;
+        named_bar(2, 128);
+        const bool stop = *reinterpret_cast<volatile int*>(&sb.stop) != 0;
+        if (!stop && quad_live && cpy == 0) {
+          const float lse1 = row_ok ? sb.xlse[il] : -INFINITY;
+          const float Lm = fmaxf(lse, lse1);
+          const float w0 = Lm == -INFINITY || lse == -INFINITY ? 0.f : exp2f((lse - Lm) * kLog2e);
+          const float w1 = Lm == -INFINITY || lse1 == -INFINITY ? 0.f : exp2f((lse1 - Lm) * kLog2e);
+          const float ws = w0 + w1;
+          const float iw = ws > 0.f ? 1.f / ws : 0.f;
+          const float a0 = w0 * inv * iw, a1 = w1 * iw;
+          lse = ws > 0.f ? Lm + logf(ws) : -INFINITY;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_issue(o_addr + (uint32_t)(c * 32), o);
+            tmem_wait_ld();
+            if (!row_ok) continue;
+            const float* xr = xo + (size_t)il * D + c * 32;
+            float f[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) f[k] = a0 * __uint_as_float(o[k]) + (w1 > 0.f ? a1 * xr[k] : 0.f);
+            if (whole) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
+#pragma unroll
+              for (int uu = 0; uu < 4; ++uu)
+                dst[uu] = make_uint4(pack_bf16(f[8 * uu], f[8 * uu + 1]), pack_bf16(f[8 * uu + 2], f[8 * uu + 3]),
+                                     pack_bf16(f[8 * uu + 4], f[8 * uu + 5]), pack_bf16(f[8 * uu + 6], f[8 * uu + 7]));
+            } else {
+              float4* po = reinterpret_cast<float4*>(p.part_o + prow_i * D + c * 32);
+#pragma unroll
+              for (int uu = 0; uu < 8; ++uu)
+                po[uu] = make_float4(f[4 * uu], f[4 * uu + 1], f[4 * uu + 2], f[4 * uu + 3]);
+            }
+          }
+          if (row_ok) {
+            if (whole) {
+              if (p.lse) p.lse[row] = lse;
+            } else {
+              p.part_lse[prow_i] = lse;
             }
           }
         }
-        if (row_ok) {
-          if (whole) {
-            if (p.lse) p.lse[row] = lse;
-          } else {
-            p.part_lse[prow_i] = lse;
-          }
-        }
-        // O is read out before this warp's next arrival on p_full lets the
-        // next segment's first P V overwrite it
         tc_fence_before();
+        named_bar(3, 128);  // the exchange is read before any P of the next segment
+        if (stop) break;
+        ok = true;
       }
       ++seg_i;
     }
@@ -1466,6 +1569,7 @@ __global__ void __launch_bounds__(256) tree_attn_f32_kernel(
 
 struct Plan {
   int nr, qtiles, tpc, ncq;
+  int copies;   // stream schedule: 2 when one query tile of at most 64 rows is replicated
   bool stream;  // the persistent stream schedule (else the split schedule)
   int n_ctas;   // stream: the grid
   int splits;   // split: KV ranges per (query-tile group, request x kv head)
@@ -1502,6 +1606,9 @@ Plan make_plan(int B, int R, int Hq, int Hkv, int max_pages, int num_splits) {
   pl.stream = num_splits < 0 || (num_splits == 0 && work >= 16LL * sms);
   pl.n_ctas = 0;
   pl.splits = 1;
+  // a single query tile whose rows fit in 64 TMEM lanes is loaded twice so
+  // that each softmax warp takes half the keys of a block
+  pl.copies = (pl.stream && pl.qtiles == 1 && pl.tpc == 1 && R <= 64 / G) ? 2 : 1;
   if (pl.stream) {
     // groups of Hkv CTAs (one per kv head), as many as fit on the SMs
     const long long groups = min((long long)max(1, sms / Hkv), 65535LL / Hkv);
@@ -1604,6 +1711,7 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   p.num_pages = num_pages;
   p.nr = pl.nr;
   p.tr = (R + 15) / 16 * 16;
+  p.q_box_rows = pl.copies == 2 ? 64 / G : pl.nr;
   p.qtiles = pl.qtiles;
   p.ncq = pl.ncq;
   p.n_ctas = pl.n_ctas;
@@ -1624,7 +1732,7 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   // tree K/V as [B*R][Hkv][D]; boxes of 64 columns (128 bytes)
   CUtensorMap mq, mk, mv, mkt, mvt;
   const uint64_t hb = (uint64_t)D * 2;
-  if (!make_tmap_3d_bf16(&mq, q, D, Hq, (uint64_t)B * R, hb, hb * Hq, 64, G, pl.nr) ||
+  if (!make_tmap_3d_bf16(&mq, q, D, Hq, (uint64_t)B * R, hb, hb * Hq, 64, G, (uint32_t)p.q_box_rows) ||
       !make_tmap_3d_bf16(&mk, k_cache, D, Hkv, (uint64_t)num_pages * 16, hb, hb * Hkv, 64, 1, 16) ||
       !make_tmap_3d_bf16(&mv, v_cache, D, Hkv, (uint64_t)num_pages * 16, hb, hb * Hkv, 64, 1, 16) ||
       !make_tmap_3d_bf16(&mkt, k_tree, D, Hkv, (uint64_t)B * R, hb, hb * Hkv, 64, 1, p.tr) ||
@@ -1656,14 +1764,18 @@ extern "C" int eagle_tree_attn(const void* q, const void* k_tree, const void* v_
   if (pl.stream) {
     if (D == 128) {
       if (pl.tpc == 2)
-        run_stream(tree_attn_stream_kernel<128, 2>, tree_attn_stream_merge_kernel<128, 2>, tc_smem<128>(2), 384);
+        run_stream(tree_attn_stream_kernel<128, 2, 1>, tree_attn_stream_merge_kernel<128, 2>, tc_smem<128>(2), 384);
+      else if (pl.copies == 2)
+        run_stream(tree_attn_stream_kernel<128, 1, 2>, tree_attn_stream_merge_kernel<128, 1>, tc_smem<128>(1), 256);
       else
-        run_stream(tree_attn_stream_kernel<128, 1>, tree_attn_stream_merge_kernel<128, 1>, tc_smem<128>(1), 256);
+        run_stream(tree_attn_stream_kernel<128, 1, 1>, tree_attn_stream_merge_kernel<128, 1>, tc_smem<128>(1), 256);
     } else {
       if (pl.tpc == 2)
-        run_stream(tree_attn_stream_kernel<64, 2>, tree_attn_stream_merge_kernel<64, 2>, tc_smem<64>(2), 384);
+        run_stream(tree_attn_stream_kernel<64, 2, 1>, tree_attn_stream_merge_kernel<64, 2>, tc_smem<64>(2), 384);
+      else if (pl.copies == 2)
+        run_stream(tree_attn_stream_kernel<64, 1, 2>, tree_attn_stream_merge_kernel<64, 1>, tc_smem<64>(1), 256);
       else
-        run_stream(tree_attn_stream_kernel<64, 1>, tree_attn_stream_merge_kernel<64, 1>, tc_smem<64>(1), 256);
+        run_stream(tree_attn_stream_kernel<64, 1, 1>, tree_attn_stream_merge_kernel<64, 1>, tc_smem<64>(1), 256);
     }
   } else {
     if (D == 128) {
