@@ -7,7 +7,7 @@
 // Acceleration of Large Language Models via Training-Time Test", "Stage 2:
 // Verification".
 //
-// Three kernels:
+// Deterministic proposals and greedy verification take up to three kernels:
 //   rowstats : one CTA per (row, request): max and sum-exp of z/T (stochastic)
 //              or the argmax (greedy without a caller-provided argmax),
 //              streamed with 16-byte loads, four in flight per thread.
@@ -20,6 +20,8 @@
 //              the stop row, split over 4096-id chunks of the vocabulary; each
 //              CTA reduces its chunk and the last CTA of a request (atomic
 //              ticket, no waiting) merges the chunk winners.
+// Sampled proposals take one kernel, a cluster of CTAs per request that reads
+// only the target and draft rows its walk visits (verify_walk_sampled_kernel).
 #include <math.h>
 
 #include <atomic>
@@ -445,37 +447,176 @@ __global__ void __launch_bounds__(kRaceThreads) verify_race_kernel(
 // is accepted when u < p(t) / q(t), with p the current target distribution;
 // after a rejection p <- norm(max(0, p - q)) (p unchanged when that mass is
 // 0); if every child is rejected the bonus token is the exponential race
-// argmax_y log p(y) - log(-log u_y) over the final p.  The residual is never
-// stored: after r rejections at a row, p_r(y) is rebuilt from p_0(y) and
-// q(y) with the r normalising masses kept in shared memory, so each
-// rejection costs one vocabulary-wide pass for the next mass.  One CTA per
-// request; every thread runs the walk in step.
-__global__ void __launch_bounds__(kWalkThreads) verify_walk_sampled_kernel(
-    int R, int V, const int32_t* __restrict__ parent_row, const int32_t* __restrict__ token,
+// argmax_y p(y) / E_y, E_y = -log u_y, over the final p (the race in ratio
+// form: the same argmax as log p(y) - log(-log u_y)).
+//
+// The residual is never stored.  All siblings of a row share q, so after r
+// rejections p_r = max(0, p_0 - c_r q) / S_r exactly, with c_0 = 0, S_0 = 1,
+// c_{r+1} = c_r + S_r and S_{r+1} = sum_y max(0, p_0(y) - c_{r+1} q(y)) (the
+// step is skipped when that sum is 0): by induction, max(0, p_r - q) =
+// max(0, p_0 - (c_r + S_r) q) / S_r, since p_0 - c_r q <= 0 implies
+// p_0 - (c_r + S_r) q < 0.  The race drops the common 1 / S_r.
+//
+// One thread-block cluster of `cs` CTAs per request (cs = 1..8, chosen so
+// that the clusters fill the SMs); CTA k of the cluster owns the k-th slice
+// of the vocabulary (16-byte groups of 4 ids).  Every CTA runs the whole walk
+// in step; a vocabulary-wide quantity is reduced per CTA and the cs partials
+// are exchanged through distributed shared memory behind one cluster barrier
+// (two exchange slots used alternately, so one barrier per exchange
+// suffices), each CTA combining them in rank order, so all CTAs take the same
+// decisions.  Per visited row: one pass for the row statistics of p_0 and q
+// (max and sum of 2^(z T^-1 log2 e - max), both rows), then per rejection one
+// pass for S_{r+1}; the last rejection's pass is folded into the race pass,
+// which keeps the race winners for both c_r and c_{r+1}.  Rows the walk does
+// not visit are never read.
+constexpr int kSampThreads = 1024;
+constexpr int kSampWarps = kSampThreads / 32;
+constexpr int kSampMaxCluster = 8;
+constexpr int kSampUnroll = 4;         // 16-byte loads per logit row in flight per thread
+constexpr int kRaceUnroll = 2;         // the same in the race pass (Philox keeps more registers live)
+constexpr int kSampMinGroups = 256;    // vocabulary groups per CTA, at least (host choice of cs)
+constexpr int kNoWinner = 0x7fffffff;
+static_assert(kSampWarps == 32, "cluster_reduce folds one value per warp in warp 0");
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes made
+// before it are visible to the cluster's loads after it.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster_f4(const float4* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
+// Online (max, sum 2^(y - max)) of four base-2 values.
+__device__ __forceinline__ void lse2_add4(float& m, float& s, float y0, float y1, float y2, float y3) {
+  const float m4 = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+  if (m4 > m) {
+    s *= exp2f(m - m4);
+    m = m4;
+  }
+  if (m != -INFINITY) s += exp2f(y0 - m) + exp2f(y1 - m) + exp2f(y2 - m) + exp2f(y3 - m);
+}
+__device__ __forceinline__ void lse2_merge(float& m, float& s, float om, float os) {
+  const float nm = fmaxf(m, om);
+  s = (m == -INFINITY ? 0.f : s * exp2f(m - nm)) + (om == -INFINITY ? 0.f : os * exp2f(om - nm));
+  m = nm;
+}
+
+// Combination rules of the exchanged float4s (commutative, so a butterfly
+// leaves every lane with the same value).
+struct CombLse {  // (max, sum) of the target row in .xy, of the draft row in .zw
+  __device__ void operator()(float4& a, const float4& b) const {
+    lse2_merge(a.x, a.y, b.x, b.y);
+    lse2_merge(a.z, a.w, b.z, b.w);
+  }
+};
+struct CombSum {
+  __device__ void operator()(float4& a, const float4& b) const { a.x += b.x; }
+};
+struct CombRace {  // two (key, id) winners: .xy and .zw, ids as bit patterns
+  __device__ void operator()(float4& a, const float4& b) const {
+    int i0 = __float_as_int(a.y), i1 = __float_as_int(a.w);
+    argmax_merge(a.x, i0, b.x, __float_as_int(b.y));
+    argmax_merge(a.z, i1, b.z, __float_as_int(b.w));
+    a.y = __int_as_float(i0);
+    a.w = __int_as_float(i1);
+  }
+};
+
+__device__ __forceinline__ float4 shfl_xor4(float4 v, int o) {
+  return make_float4(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o),
+                     __shfl_xor_sync(0xffffffffu, v.z, o), __shfl_xor_sync(0xffffffffu, v.w, o));
+}
+
+// Reduces v over the CTA, exchanges the CTA results through slot `xb` of
+// every CTA of the cluster and returns their rank-order combination (the
+// same value in every thread of every CTA).  Every thread must call it.
+template <class Op>
+__device__ __forceinline__ float4 cluster_reduce(float4 v, Op op, float4* s_red, float4* s_x, int& xb,
+                                                 int cs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) op(v, shfl_xor4(v, o));
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = s_red[lane];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) op(v, shfl_xor4(v, o));
+    if (lane == 0) s_x[xb] = v;
+  }
+  cluster_barrier();
+  float4 r = ld_cluster_f4(&s_x[xb], 0);
+  for (int k = 1; k < cs; ++k) op(r, ld_cluster_f4(&s_x[xb], (uint32_t)k));
+  xb ^= 1;
+  return r;
+}
+
+// Streams groups [g0, g1) of two logit rows, U 16-byte loads per row in
+// flight per thread, and calls f(z4, zd4, g) per group; ids >= V read as -inf.
+template <int U, class F>
+__device__ __forceinline__ void stream_rows(const float* z, const float* zd, int g0, int g1, int V, bool vec,
+                                            F&& f) {
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  auto ld = [&](const float* row, int g) -> float4 {
+    if (vec) return __ldg(reinterpret_cast<const float4*>(row) + g);
+    const int y = 4 * g;
+    return make_float4(row[y], y + 1 < V ? row[y + 1] : -INFINITY, y + 2 < V ? row[y + 2] : -INFINITY,
+                       y + 3 < V ? row[y + 3] : -INFINITY);
+  };
+  for (int i0 = g0 + (int)threadIdx.x; i0 < g1; i0 += kSampThreads * U) {
+    float4 a[U], d[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = i0 + u * kSampThreads;
+      a[u] = g < g1 ? ld(z, g) : ninf;
+      d[u] = g < g1 ? ld(zd, g) : ninf;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = i0 + u * kSampThreads;
+      if (g < g1) f(a[u], d[u], g);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSampThreads, 1) verify_walk_sampled_kernel(
+    int R, int V, int cs, const int32_t* __restrict__ parent_row, const int32_t* __restrict__ token,
     const int32_t* __restrict__ n_rows, const float* __restrict__ logits,
-    const float* __restrict__ draft, const RowStat* __restrict__ st_t,
-    const RowStat* __restrict__ st_d, float inv_t, uint32_t key0, uint32_t key1,
-    uint32_t ctr2_accept, uint32_t ctr3, const float* __restrict__ uniforms_override,
-    int max_depth, int32_t* __restrict__ accept_len, int32_t* __restrict__ path_rows,
-    int32_t* __restrict__ out_tokens, int32_t* dev_status) {
+    const float* __restrict__ draft, float inv_t, uint32_t key0, uint32_t key1, uint32_t ctr2_accept,
+    uint32_t ctr3, const float* __restrict__ uniforms_override, int max_depth,
+    int32_t* __restrict__ accept_len, int32_t* __restrict__ path_rows, int32_t* __restrict__ out_tokens,
+    int32_t* dev_status) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / cs, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = (int)cluster_ctarank();
   __shared__ int s_parent[kMaxVerifyRows];
   __shared__ int s_token[kMaxVerifyRows];
   __shared__ float s_u[kMaxVerifyRows];
   __shared__ int s_ch[kMaxVerifyRows];
-  __shared__ float s_mass[kMaxVerifyRows];  // normalising masses of the rejections at this row
   __shared__ int s_path[65];
-  __shared__ float s_rv[kWalkThreads / 32];
-  __shared__ int s_ri[kWalkThreads / 32];
+  __shared__ float4 s_red[kSampWarps];
+  __shared__ float4 s_x[2];
   __shared__ int s_bad, s_nch, s_acc;
 
   const int n = n_rows ? n_rows[b] : R;
   if (tid == 0) s_bad = (n < 1 || n > R) ? 1 : 0;
   __syncthreads();
   const int nn = s_bad ? 1 : n;
-  for (int i = tid; i < nn; i += kWalkThreads) {
+  for (int i = tid; i < nn; i += kSampThreads) {
     const size_t gi = (size_t)b * R + i;
     const int p = parent_row[gi], t = token[gi];
     s_parent[i] = p;
@@ -489,65 +630,84 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_sampled_kernel(
     }
   }
   __syncthreads();
-  // p_r(y) from the stored masses: p_0 = softmax(z/T), q = softmax(zd/T)
-  auto p_of = [&](float zy, float zdy, const RowStat& pt, const RowStat& qd, int nrej, float& q) {
-    float pv = exp2f((zy * inv_t - pt.m) * kLog2e) / pt.s;
-    q = exp2f((zdy * inv_t - qd.m) * kLog2e) / qd.s;
-    for (int r = 0; r < nrej; ++r)
-      if (s_mass[r] > 0.f) pv = fmaxf(0.f, pv - q) / s_mass[r];
-    return pv;
-  };
-  int bad = s_bad, cur = 0, plen = 1, nrej = 0;
+  // this CTA's vocabulary slice, in groups of 4 ids
+  const int G = (V + 3) / 4;
+  const int g0 = (int)((long long)G * rank / cs), g1 = (int)((long long)G * (rank + 1) / cs);
+  const float at = inv_t * kLog2e;  // z T^-1 in base 2
+  const bool vec = (V & 3) == 0;
+  int xb = 0;  // exchange slot of the next cluster_reduce
+  int bad = s_bad, cur = 0, plen = 1;
+  bool nan_seen = false;
+  // row cur: p_0(y) = 2^(z at - pm) ips, q(y) = 2^(zd at - qm) iqs; the
+  // residual is max(0, p_0 - c q) / S; `pending`: the last child was rejected
+  // and S_{r+1} is not formed yet
+  float pm = 0.f, ips = 1.f, qm = 0.f, iqs = 1.f, c = 0.f, S = 1.f;
+  bool pending = false;
   if (tid == 0) s_path[0] = 0;
   while (!bad) {
     // the children of cur in row order (warp 0, by ballots)
     if (warp == 0) {
       int nch = 0;
       for (int c0 = cur + 1; c0 < nn; c0 += 32) {
-        const int c = c0 + lane;
-        const bool is_child = c < nn && s_parent[c] == cur;
+        const int ch = c0 + lane;
+        const bool is_child = ch < nn && s_parent[ch] == cur;
         const unsigned m = __ballot_sync(0xffffffffu, is_child);
-        if (is_child) s_ch[nch + __popc(m & ((1u << lane) - 1u))] = c;
+        if (is_child) s_ch[nch + __popc(m & ((1u << lane) - 1u))] = ch;
         nch += __popc(m);
       }
       if (lane == 0) s_nch = nch;
     }
-    __syncthreads();
-    const int nch = s_nch;
     const float* z = logits + ((size_t)b * R + cur) * V;
     const float* zd = draft + ((size_t)b * R + cur) * V;
-    const RowStat pt = st_t[(size_t)b * R + cur], qd = st_d[(size_t)b * R + cur];
+    {  // row statistics of p_0 and q
+      float4 v = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      stream_rows<kSampUnroll>(z, zd, g0, g1, V, vec, [&](const float4& a, const float4& d, int) {
+        nan_seen |= isnan(a.x) | isnan(a.y) | isnan(a.z) | isnan(a.w) | isnan(d.x) | isnan(d.y) |
+                    isnan(d.z) | isnan(d.w);
+        lse2_add4(v.x, v.y, a.x * at, a.y * at, a.z * at, a.w * at);
+        lse2_add4(v.z, v.w, d.x * at, d.y * at, d.z * at, d.w * at);
+      });
+      v = cluster_reduce(v, CombLse{}, s_red, s_x, xb, cs);  // also publishes s_nch, s_ch
+      pm = v.x;
+      ips = 1.f / v.y;
+      qm = v.z;
+      iqs = 1.f / v.w;
+    }
+    const int nch = s_nch;
+    c = 0.f;
+    S = 1.f;
+    pending = false;
     int accepted = -1;
-    nrej = 0;
     for (int j = 0; j < nch; ++j) {
+      if (pending) {  // S_{r+1} = sum_y max(0, p_0 - (c + S) q)
+        const float c2 = c + S;
+        float acc = 0.f;
+        stream_rows<kSampUnroll>(z, zd, g0, g1, V, vec, [&](const float4& a, const float4& d, int) {
+          acc += fmaxf(0.f, fmaf(-c2, exp2f(fmaf(d.x, at, -qm)) * iqs, exp2f(fmaf(a.x, at, -pm)) * ips));
+          acc += fmaxf(0.f, fmaf(-c2, exp2f(fmaf(d.y, at, -qm)) * iqs, exp2f(fmaf(a.y, at, -pm)) * ips));
+          acc += fmaxf(0.f, fmaf(-c2, exp2f(fmaf(d.z, at, -qm)) * iqs, exp2f(fmaf(a.z, at, -pm)) * ips));
+          acc += fmaxf(0.f, fmaf(-c2, exp2f(fmaf(d.w, at, -qm)) * iqs, exp2f(fmaf(a.w, at, -pm)) * ips));
+        });
+        const float tot = cluster_reduce(make_float4(acc, 0.f, 0.f, 0.f), CombSum{}, s_red, s_x, xb, cs).x;
+        if (tot > 0.f) {  // a zero mass keeps p (a probability-zero event in exact arithmetic)
+          c = c2;
+          S = tot;
+        }
+        pending = false;
+      }
       if (tid == 0) {
-        const int c = s_ch[j], t = s_token[c];
-        float q;
-        const float pv = p_of(z[t], zd[t], pt, qd, nrej, q);
+        const int ch = s_ch[j], t = s_token[ch];
+        const float p0 = exp2f(fmaf(z[t], at, -pm)) * ips;
+        const float q = exp2f(fmaf(zd[t], at, -qm)) * iqs;
+        const float pv = fmaxf(0.f, fmaf(-c, q, p0)) / S;
         const float ratio = q > 0.f ? pv / q : (pv > 0.f ? INFINITY : 0.f);
-        s_acc = s_u[c] < ratio ? c : -1;
+        s_acc = s_u[ch] < ratio ? ch : -1;
       }
       __syncthreads();
       accepted = s_acc;
+      __syncthreads();  // s_acc is rewritten by the next test
       if (accepted >= 0) break;
-      // rejected: mass of max(0, p - q) for the next residual
-      float acc = 0.f;
-      for (int y = tid; y < V; y += kWalkThreads) {
-        float q;
-        const float pv = p_of(z[y], zd[y], pt, qd, nrej, q);
-        acc += fmaxf(0.f, pv - q);
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) s_rv[warp] = acc;
-      __syncthreads();
-      if (tid == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < kWalkThreads / 32; ++w) tot += s_rv[w];
-        s_mass[nrej] = tot;
-      }
-      __syncthreads();
-      ++nrej;
+      pending = true;
     }
     if (accepted < 0) break;
     if (plen > max_depth) {
@@ -557,66 +717,63 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_sampled_kernel(
     if (tid == 0) s_path[plen] = accepted;
     ++plen;
     cur = accepted;
-    __syncthreads();
   }
-  if (bad) {
-    if (tid == 0) {
-      set_status(dev_status, EAGLE_ERR_BAD_TREE);
-      accept_len[b] = 0;
-    }
-    for (int i = tid; i <= max_depth; i += kWalkThreads) {
-      path_rows[(size_t)b * (max_depth + 1) + i] = (i == 0) ? 0 : -1;
-      out_tokens[(size_t)b * (max_depth + 1) + i] = -1;
-    }
-    return;
-  }
-  // bonus: exponential race over the final residual at the stop row
-  {
+  int bonus = -1;
+  if (!bad) {
+    // bonus: argmax_y max(0, p_0 - c q) / E_y at the stop row, and with
+    // c + S when a rejection is pending (used when its mass is positive)
     const float* z = logits + ((size_t)b * R + cur) * V;
     const float* zd = draft + ((size_t)b * R + cur) * V;
-    const RowStat pt = st_t[(size_t)b * R + cur], qd = st_d[(size_t)b * R + cur];
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    bool nan_seen = false;
-    for (int g = tid; g * 4 < V; g += kWalkThreads) {
+    const float c2 = c + S;
+    float4 v = make_float4(-INFINITY, __int_as_float(kNoWinner), -INFINITY, __int_as_float(kNoWinner));
+    int bi = kNoWinner, bi2 = kNoWinner;
+    stream_rows<kRaceUnroll>(z, zd, g0, g1, V, vec, [&](const float4& a, const float4& d, int g) {
       const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)b, ctr2_accept + 1u, ctr3), key0, key1);
       const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+      const float za[4] = {a.x, a.y, a.z, a.w}, zq[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int y = g * 4 + k;
-        if (y >= V) break;
-        const float zy = z[y];
-        nan_seen |= isnan(zy);
-        float q;
-        const float pv = p_of(zy, zd[y], pt, qd, nrej, q);
-        if (pv > 0.f) argmax_merge(bv, bi, logf(pv) - logf(-logf(bits_to_uniform(words[k]))), y);
+        const int y = 4 * g + k;
+        const float p0 = exp2f(fmaf(za[k], at, -pm)) * ips, q = exp2f(fmaf(zq[k], at, -qm)) * iqs;
+        const float r = 1.f / -logf(bits_to_uniform(words[k]));
+        const float a1 = fmaf(-c, q, p0);
+        if (a1 > 0.f && y < V) argmax_merge(v.x, bi, a1 * r, y);
+        if (pending) {
+          const float a2 = fmaf(-c2, q, p0);
+          if (a2 > 0.f && y < V) argmax_merge(v.z, bi2, a2 * r, y);
+        }
       }
-    }
-    if (nan_seen) set_status(dev_status, EAGLE_ERR_NONFINITE);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      argmax_merge(bv, bi, ov, oi);
-    }
-    if (lane == 0) {
-      s_rv[warp] = bv;
-      s_ri[warp] = bi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      for (int w = 1; w < kWalkThreads / 32; ++w) argmax_merge(bv, bi, s_rv[w], s_ri[w]);
-      s_acc = bi == 0x7fffffff ? -1 : bi;
-    }
-    __syncthreads();
+    });
+    v.y = __int_as_float(bi);
+    v.w = __int_as_float(bi2);
+    v = cluster_reduce(v, CombRace{}, s_red, s_x, xb, cs);
+    bi = __float_as_int(v.y);
+    bi2 = __float_as_int(v.w);
+    const int win = (pending && bi2 != kNoWinner) ? bi2 : bi;
+    bonus = win == kNoWinner ? -1 : win;
   }
-  const int bonus = s_acc;
-  for (int i = tid; i <= max_depth; i += kWalkThreads) {
-    const size_t o = (size_t)b * (max_depth + 1) + i;
-    path_rows[o] = i < plen ? s_path[i] : -1;
-    out_tokens[o] = i + 1 < plen ? s_token[s_path[i + 1]] : (i + 1 == plen ? bonus : -1);
+  if (nan_seen) set_status(dev_status, EAGLE_ERR_NONFINITE);
+  if (rank == 0) {
+    if (bad) {
+      if (tid == 0) {
+        set_status(dev_status, EAGLE_ERR_BAD_TREE);
+        accept_len[b] = 0;
+      }
+      for (int i = tid; i <= max_depth; i += kSampThreads) {
+        path_rows[(size_t)b * (max_depth + 1) + i] = (i == 0) ? 0 : -1;
+        out_tokens[(size_t)b * (max_depth + 1) + i] = -1;
+      }
+    } else {
+      __syncthreads();  // s_path
+      for (int i = tid; i <= max_depth; i += kSampThreads) {
+        const size_t o = (size_t)b * (max_depth + 1) + i;
+        path_rows[o] = i < plen ? s_path[i] : -1;
+        out_tokens[o] = i + 1 < plen ? s_token[s_path[i + 1]] : (i + 1 == plen ? bonus : -1);
+      }
+      if (tid == 0) accept_len[b] = plen - 1;
+    }
   }
-  if (tid == 0) accept_len[b] = plen - 1;
+  cluster_barrier();  // no CTA leaves while a peer may still read its exchange slots
 }
 
 int race_chunks(int V) { return (V + kRaceChunk - 1) / kRaceChunk; }
@@ -625,7 +782,6 @@ int race_chunks(int V) { return (V + kRaceChunk - 1) / kRaceChunk; }
 // allocation-free variant (library buffer).
 struct VerifyScratch {
   RowStat* stats;
-  RowStat* stats_d;  // draft-logit row statistics (sampled proposals)
   int32_t* amax;
   int32_t* excl;
   VerifyReq* req;
@@ -634,7 +790,7 @@ struct VerifyScratch {
 
 
 size_t scratch_bytes(int B, int R, int V) {
-  return round_up((size_t)B * R * sizeof(RowStat), 256) * 2 + round_up((size_t)B * R * 4, 256) * 2 +
+  return round_up((size_t)B * R * sizeof(RowStat), 256) + round_up((size_t)B * R * 4, 256) * 2 +
          round_up((size_t)B * sizeof(VerifyReq), 256) +
          round_up((size_t)B * race_chunks(V) * sizeof(RacePart), 256) + 256;
 }
@@ -643,7 +799,6 @@ VerifyScratch carve_scratch(void* base, int B, int R, int V, bool race) {
   char* cur = static_cast<char*>(base);
   VerifyScratch w;
   w.stats = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
-  w.stats_d = static_cast<RowStat*>(ws_carve(cur, (size_t)B * R * sizeof(RowStat)));
   w.amax = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
   w.excl = static_cast<int32_t*>(ws_carve(cur, (size_t)B * R * 4));
   w.req = static_cast<VerifyReq*>(ws_carve(cur, (size_t)B * sizeof(VerifyReq)));
@@ -688,15 +843,16 @@ int verify_enqueue(int B, int R, int V, const int32_t* parent_row, const int32_t
   const uint32_t off_hi = (uint32_t)(offset >> 32), off_lo = (uint32_t)offset;
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   if (proposal_mode == EAGLE_PROPOSAL_SAMPLED) {
-    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s, target_logits, n_rows, R,
-           V, inv_t, 0, w.stats, w.amax, dev_status);
-    launch(verify_rowstats_kernel, (unsigned)(B * R), kStatThreads, 0, s, draft_logits, n_rows, R,
-           V, inv_t, 0, w.stats_d, w.amax, dev_status);
-    launch(verify_walk_sampled_kernel, B, kWalkThreads, 0, s, R, V, parent_row, token, n_rows,
-           target_logits, draft_logits, (const RowStat*)w.stats, (const RowStat*)w.stats_d, inv_t,
-           key0, key1, 2u * off_hi, off_lo, uniforms_override, max_depth, accept_len, path_rows,
-           out_tokens, dev_status);
-    note_launch(3);
+    // a cluster of cs CTAs per request: clusters that fill the SMs, at least
+    // kSampMinGroups vocabulary groups per CTA
+    const int G = (V + 3) / 4, sms = sm_count();
+    int cs = 1;
+    while (cs < kSampMaxCluster && 2LL * B * cs <= sms && 2LL * cs * kSampMinGroups <= G) cs *= 2;
+    launch_cluster(verify_walk_sampled_kernel, (unsigned)(B * cs), kSampThreads, (unsigned)cs, 0, s, R, V,
+                   cs, parent_row, token, n_rows, target_logits, draft_logits, inv_t, key0, key1,
+                   2u * off_hi, off_lo, uniforms_override, max_depth, accept_len, path_rows, out_tokens,
+                   dev_status);
+    note_launch();
     return last_launch_status();
   }
   if (need_stats) {
@@ -768,9 +924,9 @@ namespace {
 constexpr int kNoAllocMaxRows = 65536;    // B * R rows of statistics
 constexpr int kNoAllocMaxChunks = 65536;  // B * ceil(V / 4096) race chunks
 constexpr size_t kNoAllocScratchBytes =
-    (size_t)kNoAllocMaxRows * sizeof(RowStat) * 2 + (size_t)kNoAllocMaxRows * 4 * 2 +
+    (size_t)kNoAllocMaxRows * sizeof(RowStat) + (size_t)kNoAllocMaxRows * 4 * 2 +
     (size_t)kNoAllocMaxRows * sizeof(VerifyReq) + (size_t)kNoAllocMaxChunks * sizeof(RacePart) +
-    6 * 256;
+    5 * 256;
 
 // One copy per GPU that loads the library, kept until the process exits.
 // Every call on a device shares it: two calls whose kernels overlap on that

@@ -222,8 +222,14 @@ def _sampled_case(B, R, V, depth, T, seed):
     return torch.from_numpy(parent), torch.from_numpy(tok), torch.from_numpy(z), torch.from_numpy(zd)
 
 
+# The kernel runs a cluster of 1, 2, 4 or 8 CTAs per request (fewer when B is
+# large or V small): (16, 64) and (8, 500) take one CTA, (64, 4096) two,
+# (20, 8192) four, and (4, 32000), (3, 20001) (V not a multiple of 4) and the
+# 8B-shaped (1, 128256) eight, on a 152-SM GPU.
 @pytest.mark.parametrize("B,R,V,depth,T", [(16, 13, 64, 4, 1.0), (8, 21, 500, 5, 0.7),
-                                           (4, 9, 32000, 3, 1.0)])
+                                           (4, 9, 32000, 3, 1.0), (64, 9, 4096, 4, 1.0),
+                                           (20, 13, 8192, 4, 0.8), (3, 9, 20001, 3, 1.0),
+                                           (1, 61, 128256, 6, 1.0)])
 def test_sampled_proposals_match_oracle(B, R, V, depth, T):
     b = need_gpu()
     T = float(np.float32(T))
