@@ -37,12 +37,20 @@ struct LmPartials {
 bool lm_partials_view(void* ws, size_t ws_bytes, int M, int d, int V, int k, int dtype,
                       float temperature, LmPartials* out);
 
+// Order-preserving key of a non-NaN float: a larger value gets a larger key;
+// -0 and +0 get the same key (they compare equal as floats).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // One warp merges row m, whose lists were staged in shared memory (sv, si:
 // [cpg][K]; sc: [cpg]).  Log-sum-exp by max / rescale over the CTAs, then the
 // top-K by K rounds of "best head among the CTAs' sorted lists".  Lane 0
 // writes ids (-1 past the available candidates) and log-probs (z/T - lse, or
 // the race key) to out_ids / out_lp (global or shared), and the row's max and
-// sum when the pointers are set.  Every lane of the warp must call it.
+// sum when the pointers are set.  Every lane of the warp must call it.  The
+// lists hold no NaN (the LM head never lists one).
 __device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const float* sv, const int* si,
                                              const int* sc, int32_t* out_ids, float* out_lp, float* row_max,
                                              float* row_sumexp) {
@@ -78,9 +86,14 @@ __device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const f
     hi[i] = hc[i] > 0 ? si[c * K] : 0x7fffffff;
   }
   const float lse = M + logf(S);
-  for (int rnd = 0; rnd < K; ++rnd) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff, bs = -1;
+  // each lane keeps its best head (bv, bi) of list bs (-1: none left); only
+  // the lane whose head wins a round advances that list and rescans its heads
+  float bv;
+  int bi, bs;
+  auto lane_best = [&]() {
+    bv = -INFINITY;
+    bi = 0x7fffffff;
+    bs = -1;
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
       if (hp[i] < hc[i] && better(hv[i], hi[i], bv, bi)) {
@@ -88,23 +101,30 @@ __device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const f
         bi = hi[i];
         bs = i;
       }
-    int owner = bs >= 0 ? lane : 32;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ow = __shfl_xor_sync(0xffffffffu, owner, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-        owner = ow;
+  };
+  lane_best();
+  for (int rnd = 0; rnd < K; ++rnd) {
+    // the round's winner: the largest value (order-preserving key, -0 = +0),
+    // then the smallest id among equal values
+    const uint32_t key = bs >= 0 ? order_key(bv) : 0u;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const unsigned tie = __ballot_sync(0xffffffffu, bs >= 0 && key == kmax);
+    if (tie == 0) {  // every list is exhausted
+      if (lane == 0) {
+        out_ids[rnd] = -1;
+        out_lp[rnd] = -INFINITY;
       }
+      continue;
     }
-    if (lane == 0) {
-      out_ids[rnd] = bi == 0x7fffffff ? -1 : bi;
-      out_lp[rnd] = bi == 0x7fffffff ? -INFINITY : (p.race ? bv : bv * p.inv_t - lse);
+    int owner = __ffs(tie) - 1;
+    if (tie & (tie - 1)) {
+      const bool in = (tie >> lane) & 1u;
+      const unsigned mid = __reduce_min_sync(0xffffffffu, in ? (unsigned)bi : 0xffffffffu);
+      owner = __ffs(__ballot_sync(0xffffffffu, in && (unsigned)bi == mid)) - 1;
     }
-    if (lane == owner && bs >= 0) {
+    if (lane == owner) {
+      out_ids[rnd] = bi;
+      out_lp[rnd] = p.race ? bv : bv * p.inv_t - lse;
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
         if (i == bs) {
@@ -115,6 +135,7 @@ __device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const f
             hi[i] = si[c * K + hp[i]];
           }
         }
+      lane_best();
     }
   }
   if (lane == 0) {

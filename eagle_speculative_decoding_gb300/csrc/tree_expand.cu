@@ -8,322 +8,35 @@
 // and keep the verification budget) and 0x05C "Target Verification" (flatten
 // with ancestry-aware positions and a tree mask).
 //
-// One CTA per request.  A step ranks its (at most width*k) new nodes by
-// counting smaller 64-bit order-preserving keys (unique: node ids differ);
-// the final rerank bitonic-sorts the keys of all stored nodes.  log V is
-// accumulated in fp32 with one correctly rounded addition per level.
+// One CTA per request (the step body is expand_step_block, expand_step.cuh).
+// A step ranks its (at most width*k) new nodes by counting smaller 64-bit
+// order-preserving keys (unique: node ids differ); the final rerank ranks or
+// bitonic-sorts the keys of all stored nodes.  log V is accumulated in fp32
+// with one correctly rounded addition per level.
 #include <math.h>
 
 #include "common.cuh"
+#include "expand_step.cuh"
 #include "lm_merge.cuh"
 
 namespace eagle {
 namespace {
 
 constexpr int kExpandThreads = 512;
-constexpr int kMaxCand = 1024;      // width * k
-constexpr int kMaxNodes = 2048;
-// log(1e-12) rounded to fp32: the ranking floor of a zero confidence.
-constexpr float kLogEps = -27.631021115928547f;
-constexpr float kMassTol = 1e-4f;
+constexpr int kMaxCand = 1024;  // width * k
+constexpr int kMaxNodes = kExpandMaxNodes;
 
-// Order-preserving 64-bit sort key of a node: ascending key = descending
-// log V, then ascending depth, then ascending node id.
-__device__ __forceinline__ unsigned long long node_key(float v, int d, int id) {
-  uint32_t f = __float_as_uint(v);
-  f = (f & 0x80000000u) ? ~f : (f | 0x80000000u);  // ascending as unsigned
-  return ((unsigned long long)(~f) << 32) | ((unsigned long long)(uint32_t)d << 16) |
-         (unsigned long long)(uint32_t)id;
-}
-
-// Exclusive prefix sum of 0/1 flags over n <= kMaxCand entries (block-wide).
-__device__ __forceinline__ int block_exclusive_scan(const int* flags, int* out, int n) {
-  __shared__ int s_warp[kExpandThreads / 32 * 2];
-  __shared__ int s_total;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kW = kExpandThreads / 32;
-  int pref[2], v[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = h * kExpandThreads + threadIdx.x;
-    v[h] = t < n ? flags[t] : 0;
-    const unsigned bal = __ballot_sync(0xffffffffu, v[h]);
-    pref[h] = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) s_warp[h * kW + warp] = __popc(bal);
-  }
-  __syncthreads();
-  static_assert(2 * kW == 32, "one warp scans the warp totals");
-  if (warp == 0) {  // exclusive scan of the 32 warp totals by shuffles
-    const int c = s_warp[lane];
-    int inc = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += y;
-    }
-    s_warp[lane] = inc - c;
-    if (lane == 31) s_total = inc;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = h * kExpandThreads + threadIdx.x;
-    if (t < n) out[t] = s_warp[h * kW + warp] + pref[h];
-  }
-  __syncthreads();
-  return s_total;
-}
-
-// One expansion step.  MERGE: the candidate lists are not read from
-// cand_ids / cand_lp but merged here from the per-CTA partials an LM-head call
-// left (lp; row b * P + j holds parent slot j of request b): stage_rows rows
-// at a time are staged in dynamic shared memory by all threads, then one warp
-// per row merges them straight into the candidate arrays.
+// One expansion step per CTA (request blockIdx.x); see expand_step_block.
+// The next kernel (an LM head that prefetches its weights) is let in only at
+// the end: its prefetch would otherwise queue ahead of this kernel's few
+// latency-bound loads.
 template <bool MERGE>
-__global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(
-    int step, int width, int k, int max_nodes, const int32_t* __restrict__ cand_ids,
-    const float* __restrict__ cand_lp, const LmPartials lp, int stage_rows,
-    const int32_t* __restrict__ root_token,
-    int32_t* __restrict__ node_parent, int32_t* __restrict__ node_token,
-    float* __restrict__ node_logv, int32_t* __restrict__ node_depth,
-    int32_t* __restrict__ node_count, int32_t* __restrict__ frontier,
-    int32_t* __restrict__ n_frontier, const int32_t* __restrict__ fanout, int32_t* dev_status) {
-  // the next kernel (an LM head that prefetches its weights) is let in only
-  // at the end: its prefetch would otherwise queue ahead of this kernel's
-  // few latency-bound loads
+__global__ void __launch_bounds__(kExpandThreads) expand_step_kernel(const ExpandArgs a, const LmPartials lp,
+                                                                     int stage_rows) {
+  __shared__ ExpandSmem<kMaxCand> sm;
+  extern __shared__ __align__(16) unsigned char stage[];
   pdl_wait();
-  const int b = blockIdx.x;
-  const int P = step == 0 ? 1 : width;
-  int32_t* np_ = node_parent + (size_t)b * max_nodes;
-  int32_t* nt_ = node_token + (size_t)b * max_nodes;
-  float* nv_ = node_logv + (size_t)b * max_nodes;
-  int32_t* nd_ = node_depth + (size_t)b * max_nodes;
-
-  __shared__ int s_par[64];  // expanded parent node ids (slot j)
-  __shared__ float s_parv[64];
-  __shared__ int s_pard[64];
-  __shared__ float s_mass[64];
-  // s_lp and s_valid share their bytes with the 64-bit ranking keys, which
-  // are written only after both are consumed
-  __shared__ __align__(16) unsigned char s_kbuf[kMaxCand * 8];
-  float* s_lp = reinterpret_cast<float*>(s_kbuf);
-  int* s_valid = reinterpret_cast<int*>(s_kbuf) + kMaxCand;
-  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(s_kbuf);
-  __shared__ int s_scan[kMaxCand];
-  __shared__ float s_v[kMaxCand];
-  __shared__ int s_id[kMaxCand];
-  __shared__ int s_bad;
-  __shared__ int s_fan[64];  // static tree: children kept per parent slot
-
-  const int npar = step == 0 ? 1 : max(0, min(width, n_frontier[b]));
-  const int count0 = step == 0 ? 1 : node_count[b];
-  const int ncand = npar * k;
-  if (threadIdx.x == 0) s_bad = 0;
-  if (threadIdx.x < 64) s_mass[threadIdx.x] = 0.f;
-  __syncthreads();  // the error word is reset before any thread can raise it
-  if (threadIdx.x < npar) {
-    int f = k;
-    if (fanout) {
-      f = fanout[threadIdx.x];
-      if (f < 0 || f > k) {
-        atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
-        f = 0;
-      }
-    }
-    s_fan[threadIdx.x] = f;
-  }
-  // the expanded parents, loaded in parallel
-  if (threadIdx.x < npar) {
-    const int j = threadIdx.x;
-    if (step == 0) {
-      s_par[0] = 0;
-      s_parv[0] = 0.f;
-      s_pard[0] = 0;
-      np_[0] = -1;
-      nt_[0] = root_token ? root_token[b] : -1;
-      nv_[0] = 0.f;
-      nd_[0] = 0;
-    } else {
-      int p = frontier[(size_t)b * width + j];
-      if (p < 0 || p >= count0) {
-        atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
-        p = 0;
-      }
-      s_par[j] = p;
-      s_parv[j] = nv_[p];
-      s_pard[j] = nd_[p];
-    }
-  }
-  if (MERGE) {
-    extern __shared__ __align__(16) unsigned char stage[];
-    const int nc = lp.cpg, n = nc * k, warp = threadIdx.x >> 5;
-    const size_t row_bytes = ((size_t)n * 8 + (size_t)nc * 4 + 15) / 16 * 16;
-    for (int j0 = 0; j0 < npar; j0 += stage_rows) {
-      const int nb = min(stage_rows, npar - j0);
-      // the batch's lists are contiguous ([row][cta][K] from row b * P + j0):
-      // 16-byte loads when the rows keep 16-byte alignment, four in flight
-      // per thread before any store
-      const size_t m0 = (size_t)b * P + j0;
-      if ((n & 3) == 0) {
-        const int n4 = n / 4, tot = nb * n4;
-        const float4* gv = reinterpret_cast<const float4*>(lp.v + m0 * n);
-        const int4* gi = reinterpret_cast<const int4*>(lp.id + m0 * n);
-        for (int f0 = threadIdx.x; f0 < tot; f0 += 4 * kExpandThreads) {
-          float4 v[4];
-          int4 id[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int f = f0 + u * kExpandThreads;
-            if (f < tot) {
-              v[u] = __ldcg(gv + f);
-              id[u] = __ldcg(gi + f);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int f = f0 + u * kExpandThreads;
-            if (f < tot) {
-              const int r = f / n4, e = f % n4;
-              float4* sv = reinterpret_cast<float4*>(stage + r * row_bytes);
-              sv[e] = v[u];
-              reinterpret_cast<int4*>(sv + n4)[e] = id[u];
-            }
-          }
-        }
-      } else {
-        const int tot = nb * n;
-        for (int f0 = threadIdx.x; f0 < tot; f0 += 4 * kExpandThreads) {
-          float v[4];
-          int id[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int f = f0 + u * kExpandThreads;
-            if (f < tot) {
-              v[u] = __ldcg(lp.v + m0 * n + f);
-              id[u] = __ldcg(lp.id + m0 * n + f);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int f = f0 + u * kExpandThreads;
-            if (f < tot) {
-              const int r = f / n, e = f % n;
-              float* sv = reinterpret_cast<float*>(stage + r * row_bytes);
-              sv[e] = v[u];
-              reinterpret_cast<int*>(sv + n)[e] = id[u];
-            }
-          }
-        }
-      }
-      for (int f = threadIdx.x; f < nb * nc; f += kExpandThreads) {
-        const int r = f / nc, c = f % nc;
-        const size_t m = (size_t)b * P + j0 + r;
-        int* sc = reinterpret_cast<int*>(stage + r * row_bytes) + 2 * n;
-        sc[c] = __ldcg(lp.cnt + m * nc + c);
-      }
-      __syncthreads();
-      if (warp < nb) {
-        const float* sv = reinterpret_cast<const float*>(stage + warp * row_bytes);
-        const int* si = reinterpret_cast<const int*>(sv + n);
-        lm_merge_row(lp, b * P + j0 + warp, sv, si, si + n, s_id + (j0 + warp) * k, s_lp + (j0 + warp) * k,
-                     nullptr, nullptr);
-      }
-      __syncthreads();
-    }
-  } else {
-    for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
-      const int j = t / k, i = t % k;
-      const size_t src = ((size_t)b * P + j) * k + i;
-      s_id[t] = cand_ids[src];
-      s_lp[t] = cand_lp[src];
-    }
-  }
-  __syncthreads();
-  // validation (duplicates, non-finite values, sibling mass) and values
-  for (int t = threadIdx.x; t < ncand; t += kExpandThreads) {
-    const int j = t / k, i = t % k;
-    const int id = s_id[t];
-    float lp = s_lp[t];
-    int valid = id >= 0 && i < s_fan[j];
-    if (valid) {
-      if (isnan(lp) || lp == INFINITY) {
-        atomicCAS(&s_bad, 0, EAGLE_ERR_NONFINITE);
-        valid = 0;
-      }
-      for (int i2 = 0; i2 < i; ++i2)
-        if (s_id[j * k + i2] == id) atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
-      lp = fminf(lp, 0.f);
-      atomicAdd(&s_mass[j], expf(lp));
-      // log V(child) = log V(parent) + log max(c, eps): one fp32 addition
-      s_v[t] = __fadd_rn(s_parv[j], fmaxf(lp, kLogEps));
-    }
-    s_valid[t] = valid;
-  }
-  __syncthreads();
-  if (threadIdx.x < npar && s_mass[threadIdx.x] > 1.f + kMassTol) atomicCAS(&s_bad, 0, EAGLE_ERR_BAD_TREE);
-  __syncthreads();
-  if (s_bad) {
-    if (threadIdx.x == 0) {
-      set_status(dev_status, s_bad);
-      n_frontier[b] = 0;
-      if (step == 0) node_count[b] = 1;
-    }
-    pdl_trigger();
-    return;
-  }
-  // creation-ordered node ids (slot, then rank) via a block prefix sum
-  const int nnew = block_exclusive_scan(s_valid, s_scan, ncand);
-  if (count0 + nnew > max_nodes) {
-    if (threadIdx.x == 0) {
-      set_status(dev_status, EAGLE_ERR_INVALID_ARG);
-      n_frontier[b] = 0;
-    }
-    pdl_trigger();
-    return;
-  }
-  // the ranking key of each new node (all of the same depth): larger log V
-  // first, then smaller node id; a discarded candidate sorts last
-  constexpr int kPerT = kMaxCand / kExpandThreads;
-  unsigned long long key[kPerT];
-#pragma unroll
-  for (int h = 0; h < kPerT; ++h) {
-    const int t = h * kExpandThreads + threadIdx.x;
-    key[h] = ~0ull;
-    if (t < ncand && s_valid[t]) key[h] = node_key(s_v[t] + 0.f, 0, count0 + s_scan[t]);
-  }
-  __syncthreads();  // s_valid and s_lp are read: their bytes become the keys
-#pragma unroll
-  for (int h = 0; h < kPerT; ++h) {
-    const int t = h * kExpandThreads + threadIdx.x;
-    if (t < ncand) s_key[t] = key[h];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < kPerT; ++h) {
-    const int t = h * kExpandThreads + threadIdx.x;
-    const unsigned long long mk = key[h];
-    if (t >= ncand || mk == ~0ull) continue;
-    const int j = t / k;
-    const int node = count0 + s_scan[t];
-    np_[node] = s_par[j];
-    nt_[node] = s_id[t];
-    nv_[node] = s_v[t];
-    nd_[node] = s_pard[j] + 1;
-    // next frontier: rank of this node among the new nodes by key (keys are
-    // unique: node ids differ); a static tree keeps creation order
-    int rank = s_scan[t];
-    if (!fanout) {
-      rank = 0;
-#pragma unroll 8
-      for (int u = 0; u < ncand; ++u) rank += s_key[u] < mk ? 1 : 0;
-    }
-    if (rank < width) frontier[(size_t)b * width + rank] = node;
-  }
-  if (threadIdx.x == 0) {
-    if (fanout && nnew > width) set_status(dev_status, EAGLE_ERR_BAD_TREE);  // a depth wider than the frontier
-    n_frontier[b] = nnew < width ? nnew : width;
-    node_count[b] = count0 + nnew;
-  }
+  expand_step_block<kExpandThreads, kMaxCand, MERGE>(a, blockIdx.x, sm, lp, stage, stage_rows);
   pdl_trigger();
 }
 
@@ -460,10 +173,12 @@ int expand_launch(int B, int step, int width, int k, int max_nodes, const int32_
       !node_count || !frontier || !n_frontier)
     return EAGLE_ERR_INVALID_ARG;
   if (step == 0 && !root_token) return EAGLE_ERR_INVALID_ARG;
-  if (width > 64 || k > 32 || width * k > kMaxCand || max_nodes > kMaxNodes || B > 65535)
-    return EAGLE_ERR_UNSUPPORTED;
-  if ((long long)max_nodes < 1LL + k + (long long)step * width * k) return EAGLE_ERR_INVALID_ARG;
+  const int chk = expand_check(B, step, width, k, max_nodes, kMaxCand);
+  if (chk != EAGLE_OK) return chk;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const ExpandArgs a{step,      width,       k,          max_nodes,  cand_ids,   cand_logprobs, root_token,
+                     node_parent, node_token, node_logv, node_depth, node_count, frontier,      n_frontier,
+                     fanout,    dev_status};
   if (lp) {
     const size_t row_bytes = ((size_t)lp->cpg * k * 8 + (size_t)lp->cpg * 4 + 15) / 16 * 16;
     const int P = step == 0 ? 1 : width;
@@ -473,13 +188,9 @@ int expand_launch(int B, int step, int width, int k, int max_nodes, const int32_
     if (rows < 1) return EAGLE_ERR_UNSUPPORTED;
     const size_t smem = (size_t)rows * row_bytes;
     cudaFuncSetAttribute(expand_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch(expand_step_kernel<true>, B, kExpandThreads, smem, s, step, width, k, max_nodes, cand_ids,
-           cand_logprobs, *lp, rows, root_token, node_parent, node_token, node_logv, node_depth, node_count,
-           frontier, n_frontier, fanout, dev_status);
+    launch(expand_step_kernel<true>, B, kExpandThreads, smem, s, a, *lp, rows);
   } else {
-    launch(expand_step_kernel<false>, B, kExpandThreads, 0, s, step, width, k, max_nodes, cand_ids,
-           cand_logprobs, LmPartials{}, 0, root_token, node_parent, node_token, node_logv, node_depth,
-           node_count, frontier, n_frontier, fanout, dev_status);
+    launch(expand_step_kernel<false>, B, kExpandThreads, 0, s, a, LmPartials{}, 0);
   }
   note_launch();
   return last_launch_status();
