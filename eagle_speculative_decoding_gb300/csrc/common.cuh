@@ -56,18 +56,18 @@ cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, c
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
-// The same launch with thread-block clusters of cluster_x CTAs along x (grid.x
-// a multiple of cluster_x).
+// The same launch with thread-block clusters of the given shape (each grid
+// dimension a multiple of the cluster's).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, unsigned cluster_x, size_t smem,
+cudaError_t launch_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, dim3 cluster, size_t smem,
                            cudaStream_t s, Args... args) {
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = cluster_x;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  attr[1].val.clusterDim.x = cluster.x;
+  attr[1].val.clusterDim.y = cluster.y;
+  attr[1].val.clusterDim.z = cluster.z;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -85,6 +85,8 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait
+
+
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) {
   if (st) atomicCAS(st, 0, code);
@@ -120,6 +122,28 @@ __device__ __forceinline__ float bits_to_uniform(uint32_t x) {
 // ------------------------------------------------ shared-memory address math
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes made
+// before it are visible to the cluster's loads after it.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster_f4(const float4* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
 }
 
 // ------------------------------------------------------------------ mbarrier

@@ -478,27 +478,6 @@ constexpr int kSampMinGroups = 256;    // vocabulary groups per CTA, at least (h
 constexpr int kNoWinner = 0x7fffffff;
 static_assert(kSampWarps == 32, "cluster_reduce folds one value per warp in warp 0");
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster arrives; shared-memory writes made
-// before it are visible to the cluster's loads after it.
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float4 ld_cluster_f4(const float4* local, uint32_t rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(ra)
-               : "memory");
-  return v;
-}
-
 // Online (max, sum 2^(y - max)) of four base-2 values.
 __device__ __forceinline__ void lse2_add4(float& m, float& s, float y0, float y1, float y2, float y3) {
   const float m4 = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
@@ -848,7 +827,7 @@ int verify_enqueue(int B, int R, int V, const int32_t* parent_row, const int32_t
     const int G = (V + 3) / 4, sms = sm_count();
     int cs = 1;
     while (cs < kSampMaxCluster && 2LL * B * cs <= sms && 2LL * cs * kSampMinGroups <= G) cs *= 2;
-    launch_cluster(verify_walk_sampled_kernel, (unsigned)(B * cs), kSampThreads, (unsigned)cs, 0, s, R, V,
+    launch_cluster(verify_walk_sampled_kernel, (unsigned)(B * cs), kSampThreads, dim3((unsigned)cs), 0, s, R, V,
                    cs, parent_row, token, n_rows, target_logits, draft_logits, inv_t, key0, key1,
                    2u * off_hi, off_lo, uniforms_override, max_depth, accept_len, path_rows, out_tokens,
                    dev_status);
