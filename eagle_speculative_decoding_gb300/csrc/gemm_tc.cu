@@ -27,6 +27,9 @@
 // truncate them to TF32): small SIMT kernels that share the top-k epilogue.
 #include <math.h>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "lm_merge.cuh"
 
@@ -746,6 +749,11 @@ struct FpParams {
   // them -- and activation row i lands in output row row_map[i].
   const int32_t* m_dev;
   const int32_t* row_map;
+  // cs >= 1 (one activation group, all rows known on the host): output tile
+  // t is computed by CTAs t * cs .. t * cs + cs - 1, each over an equal share
+  // of the K chunks; with cs >= 2 they are one thread-block cluster that sums
+  // the shares through distributed shared memory.  0: the stream-K split.
+  int cs;
 };
 
 // The activation rows, stream-K chunk count and active CTAs of one launch:
@@ -908,6 +916,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.mx[2] = &map_h;
   sc.lo = sk_lo(blockIdx.x, p.W, p.n_ctas);
   sc.hi = sk_lo(blockIdx.x + 1, p.W, p.n_ctas);
+  if (p.cs) {
+    const long long t = blockIdx.x / p.cs, r = blockIdx.x % p.cs;
+    sc.lo = t * p.nk + r * p.nk / p.cs;
+    sc.hi = t * p.nk + (r + 1) * p.nk / p.cs;
+  }
   sc.nk = p.nk;
   sc.nkd = p.nkd;
   sc.n_otiles = p.n_otiles;
@@ -974,6 +987,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
+      } else if (p.cs) {
+        // this CTA's K share of the tile: kept in shared memory (over the
+        // ring, whose stages are all consumed) for the cluster's sum below
+        float* xs = reinterpret_cast<float*>(dsmem + (base - smem_u32(dsmem)));
+        for (int c16 = 0; c16 * 16 < ncol; ++c16) {
+          float v[16];
+          tmem_ld16(taddr + c16 * 16, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c16 * 16 + j;
+            if (col < ncol) xs[col * 128 + e] = v[j];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
       } else {
         // stream-K partial: write it; fuse_proj_reduce_kernel sums the
         // contributors of the tile afterwards
@@ -997,6 +1026,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   cta_teardown(sh, tmem_cols, p.status);
+  if (!TF32 && p.cs > 1) {
+    // the cluster's sum: CTA r of the cluster takes an equal share of the
+    // tile's activation rows and adds the cs K shares in rank order (a fixed
+    // order, so the result does not depend on timing), then bias / residual
+    cluster_barrier();  // every share is in its CTA's shared memory
+    const int t = blockIdx.x / p.cs, r = blockIdx.x % p.cs;
+    const int ot = t % p.n_otiles, ncol = min(bn, p.M);
+    const int c0 = r * ncol / p.cs, c1 = (r + 1) * ncol / p.cs;
+    const float4* xs4 = reinterpret_cast<const float4*>(dsmem + (base - smem_u32(dsmem)));
+    for (int f = threadIdx.x; f < (c1 - c0) * 32; f += kThreads) {
+      const int col = c0 + f / 32, e4 = f % 32;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < p.cs; ++s2) {
+        const float4 v = ld_cluster_f4(xs4 + col * 32 + e4, (uint32_t)s2);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const int oo = ot * 128 + e4 * 4;
+      if (p.bias) {
+        acc.x += p.bias[oo];
+        acc.y += p.bias[oo + 1];
+        acc.z += p.bias[oo + 2];
+        acc.w += p.bias[oo + 3];
+      }
+      const size_t idx = (size_t)col * p.d + oo;
+      if (p.residual) {
+        const uint2 rv = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.residual) + idx);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rv.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rv.y));
+        acc.x += a.x;
+        acc.y += a.y;
+        acc.z += b.x;
+        acc.w += b.y;
+      }
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + idx) = pk;
+    }
+    cluster_barrier();  // no CTA leaves while another reads its share
+  }
 }
 
 // Accepted-rows fusion, first half: the accepted rows of every request
@@ -1594,6 +1668,62 @@ struct FpLiveRows {
   int B, R, slots;
 };
 
+// Clusters of cs CTAs of the projection kernel (with `smem` bytes of shared
+// memory) that the current device runs at once; cached per (device, cs, smem).
+int fp_max_clusters(int cs, size_t smem) {
+  struct Entry {
+    int dev, cs;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.cs == cs && e.smem == smem) return e.n;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fuse_proj_kernel<false>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache.push_back(Entry{dev, cs, smem, n});
+  return n;
+}
+
+// The tile split of a projection with one activation group and a host row
+// count: the largest cs in {1, 2, 4, 8} whose n_otiles * cs CTAs fit on the
+// SMs in one wave (as clusters of cs) with at least kFpMinChunks K chunks
+// each, provided they occupy at least 3/5 of the SMs; else 0 (stream-K over
+// every SM, partial tiles summed by a second kernel).
+constexpr int kFpMinChunks = 4;
+int fp_cluster_size(const FpPlan& f, int sms, size_t smem) {
+  if (f.G != 1) return 0;
+  int best = 0;
+  for (int cs = 1; cs <= 8; cs *= 2) {
+    if ((long long)f.n_otiles * cs > sms || f.nk / cs < kFpMinChunks) break;
+    if (cs > 1 && fp_max_clusters(cs, smem) < f.n_otiles) break;
+    best = cs;
+  }
+  if (best && 5LL * f.n_otiles * best < 3LL * sms) return 0;
+  return best;
+}
+
 int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const void* table, int n_rows,
                    const void* w, const float* bias, const void* residual, void* out, int M, int n_out,
                    int kseg, void* ws, int32_t* dev_status, cudaStream_t s,
@@ -1668,6 +1798,19 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.row_map = row_map;
   p.max_contrib = max_contrib;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  p.cs = live ? 0 : fp_cluster_size(f, sms, smem);
+  if (p.cs) {
+    // one wave of n_otiles * cs CTAs, no partials in the workspace
+    const unsigned grid = (unsigned)(f.n_otiles * p.cs);
+    p.n_ctas = (int)grid;
+    if (p.cs > 1)
+      launch_cluster(fuse_proj_kernel<false>, grid, kThreads, dim3((unsigned)p.cs), smem, s, mw, mx[0], mx[1],
+                     mx[2], p);
+    else
+      launch(fuse_proj_kernel<false>, grid, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
+    note_launch();
+    return last_launch_status();
+  }
   launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
   launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
          256, 0, s, p);
