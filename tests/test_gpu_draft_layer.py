@@ -14,10 +14,16 @@ def _bf16_store(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).double().numpy()
 
 
+# One activation group with a host row count runs one cluster of cs CTAs per
+# 128-row output tile (on a 152-SM GPU): cs = 2 for the QKV shape, 4 for the
+# down projection, 8 for 1536 outputs, 1 (whole tiles, no split) for 12288
+# outputs over 4 K chunks; the others take the stream-K split.
 @pytest.mark.parametrize("M,n_out,k_in,dtype,bias,res", [
     (1, 128, 64, "bf16", False, False),
     (10, 6144, 4096, "bf16", False, False),     # QKV projection, llama8b drafter
     (10, 4096, 14336, "bf16", False, True),     # down projection + residual
+    (10, 1536, 4096, "bf16", True, True),       # clusters of eight
+    (20, 12288, 256, "bf16", True, False),      # one CTA per tile
     (37, 384, 320, "bf16", True, True),
     (300, 256, 192, "bf16", False, True),       # two activation groups
     (17, 256, 128, "fp32", True, True),
