@@ -749,6 +749,13 @@ struct FpParams {
   // them -- and activation row i lands in output row row_map[i].
   const int32_t* m_dev;
   const int32_t* row_map;
+  // tile order: output-tile-major (tile t = output tile t / groups, group
+  // t % groups) when several groups share each weight tile and the rows are
+  // known on the host, so that the groups' passes over one weight tile are
+  // neighbouring work and re-read it from L2; group-major (output tile
+  // t % n_otiles, group t / n_otiles) otherwise, so that the live groups of a
+  // device row count form a prefix of the tiles
+  int tmajor;
   // cs >= 1 (one activation group, all rows known on the host): output tile
   // t is computed by CTAs t * cs .. t * cs + cs - 1, each over an equal share
   // of the K chunks; with cs >= 2 they are one thread-block cluster that sums
@@ -793,7 +800,7 @@ struct FpSched {
   const CUtensorMap* mw;
   const CUtensorMap* mx[3];
   long long lo, hi;
-  int nk, nkd, n_otiles, bn;
+  int nk, nkd, n_otiles, bn, groups, tmajor;
   __device__ bool seg(int i, Seg& s) const {
     if (lo >= hi) return false;
     const int t = (int)(lo / nk) + i;
@@ -802,14 +809,15 @@ struct FpSched {
     s.tile = t;
     s.k0 = (int)(max(lo, a) - a);
     s.k1 = (int)(min(hi, a + nk) - a);
-    s.a_row = (t % n_otiles) * 128;
-    s.b_row = (t / n_otiles) * bn;
+    s.a_row = (tmajor ? t / groups : t % n_otiles) * 128;
+    s.b_row = (tmajor ? t % groups : t / n_otiles) * bn;
     return true;
   }
   __device__ const CUtensorMap* map_a() const { return mw; }
   __device__ const CUtensorMap* map_b(int kc) const { return mx[kc / nkd]; }
   __device__ int b_x(int kc) const { return (kc % nkd) * (TF32 ? 32 : 64); }
-  __device__ uint64_t a_policy() const { return l2_policy_evict_first(); }
+  // a weight tile that several groups read stays in L2 for their passes
+  __device__ uint64_t a_policy() const { return groups > 1 ? l2_policy_evict_normal() : l2_policy_evict_first(); }
   __device__ uint64_t b_policy() const { return l2_policy_evict_last(); }
 };
 
@@ -827,7 +835,8 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
   const int c_first = sk_owner(x0, lv.W, lv.n);
   const int c_last = sk_owner(x0 + p.nk - 1, lv.W, lv.n);
   if (c_first == c_last) return;  // one CTA held the whole tile and wrote it
-  const int ot = tile % p.n_otiles, gr = tile / p.n_otiles;
+  const int ot = p.tmajor ? tile / p.groups : tile % p.n_otiles;
+  const int gr = p.tmajor ? tile % p.groups : tile / p.n_otiles;
   const int m0 = gr * p.bn, ncol = min(p.bn, lv.m - m0);
   const int f = blockIdx.x * 256 + threadIdx.x;  // float4 index in the [ncol][128] tile
   if (f >= ncol * 32) return;
@@ -925,6 +934,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.nkd = p.nkd;
   sc.n_otiles = p.n_otiles;
   sc.bn = bn;
+  sc.groups = p.groups;
+  sc.tmajor = p.tmajor;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&map_w);
@@ -958,7 +969,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aph = (uint32_t)(acc / rg.nbuf) & 1u;
       if (!epi_wait(sh, smem_u32(&sh.acc_full[buf]), aph)) break;
       tc_fence_after();
-      const int ot = sg.tile % p.n_otiles, gr = sg.tile / p.n_otiles;
+      const int ot = p.tmajor ? sg.tile / p.groups : sg.tile % p.n_otiles;
+      const int gr = p.tmajor ? sg.tile % p.groups : sg.tile / p.n_otiles;
       const int o = ot * 128 + e, m0 = gr * bn, ncol = min(bn, lv.m - m0);
       const uint32_t taddr = sh.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * bn);
       const bool whole = sg.k0 == 0 && sg.k1 == p.nk;
@@ -1797,6 +1809,7 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.m_dev = m_dev;
   p.row_map = row_map;
   p.max_contrib = max_contrib;
+  p.tmajor = (!live && f.G > 1) ? 1 : 0;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   p.cs = live ? 0 : fp_cluster_size(f, sms, smem);
   if (p.cs) {
