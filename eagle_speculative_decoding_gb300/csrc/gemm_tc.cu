@@ -751,11 +751,16 @@ struct FpParams {
   const int32_t* row_map;
   // tile order: output-tile-major (tile t = output tile t / groups, group
   // t % groups) when several groups share each weight tile and the rows are
-  // known on the host, so that the groups' passes over one weight tile are
-  // neighbouring work and re-read it from L2; group-major (output tile
-  // t % n_otiles, group t / n_otiles) otherwise, so that the live groups of a
-  // device row count form a prefix of the tiles
+  // known on the host; group-major (output tile t % n_otiles, group
+  // t / n_otiles) otherwise, so that the live groups of a device row count
+  // form a prefix of the tiles
   int tmajor;
+  // lanes > 0 (with tmajor): CTA c computes group c % groups over lane
+  // c / groups's share of the (output tile, K chunk) items of one group, so
+  // the groups' CTAs of a lane stream the same weight chunks at the same time
+  // (one HBM read, the others' from L2); a tile's contributors are
+  // consecutive lanes
+  int lanes;
   // cs >= 1 (one activation group, all rows known on the host): output tile
   // t is computed by CTAs t * cs .. t * cs + cs - 1, each over an equal share
   // of the K chunks; with cs >= 2 they are one thread-block cluster that sums
@@ -801,16 +806,23 @@ struct FpSched {
   const CUtensorMap* mx[3];
   long long lo, hi;
   int nk, nkd, n_otiles, bn, groups, tmajor;
+  int lane_gr;  // lanes: this CTA's group (the items [lo, hi) are output tiles x K chunks), else -1
   __device__ bool seg(int i, Seg& s) const {
     if (lo >= hi) return false;
     const int t = (int)(lo / nk) + i;
     const long long a = (long long)t * nk;
     if (a >= hi) return false;
-    s.tile = t;
     s.k0 = (int)(max(lo, a) - a);
     s.k1 = (int)(min(hi, a + nk) - a);
-    s.a_row = (tmajor ? t / groups : t % n_otiles) * 128;
-    s.b_row = (tmajor ? t % groups : t / n_otiles) * bn;
+    if (lane_gr >= 0) {
+      s.tile = t * groups + lane_gr;
+      s.a_row = t * 128;
+      s.b_row = lane_gr * bn;
+    } else {
+      s.tile = t;
+      s.a_row = (tmajor ? t / groups : t % n_otiles) * 128;
+      s.b_row = (tmajor ? t % groups : t / n_otiles) * bn;
+    }
     return true;
   }
   __device__ const CUtensorMap* map_a() const { return mw; }
@@ -830,10 +842,17 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
   pdl_trigger();
   const FpLive lv = fp_live(p);
   const int tile = blockIdx.y;
-  const long long x0 = (long long)tile * p.nk;
-  if (x0 >= lv.W) return;  // a group past the live rows
-  const int c_first = sk_owner(x0, lv.W, lv.n);
-  const int c_last = sk_owner(x0 + p.nk - 1, lv.W, lv.n);
+  int c_first, c_last;
+  if (p.lanes) {  // contributors: consecutive lanes over the tile's K chunks
+    const long long W1 = (long long)p.n_otiles * p.nk, x0 = (long long)(tile / p.groups) * p.nk;
+    c_first = sk_owner(x0, W1, p.lanes);
+    c_last = sk_owner(x0 + p.nk - 1, W1, p.lanes);
+  } else {
+    const long long x0 = (long long)tile * p.nk;
+    if (x0 >= lv.W) return;  // a group past the live rows
+    c_first = sk_owner(x0, lv.W, lv.n);
+    c_last = sk_owner(x0 + p.nk - 1, lv.W, lv.n);
+  }
   if (c_first == c_last) return;  // one CTA held the whole tile and wrote it
   const int ot = p.tmajor ? tile / p.groups : tile % p.n_otiles;
   const int gr = p.tmajor ? tile % p.groups : tile / p.n_otiles;
@@ -925,10 +944,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.mx[2] = &map_h;
   sc.lo = sk_lo(blockIdx.x, p.W, p.n_ctas);
   sc.hi = sk_lo(blockIdx.x + 1, p.W, p.n_ctas);
+  sc.lane_gr = -1;
   if (p.cs) {
     const long long t = blockIdx.x / p.cs, r = blockIdx.x % p.cs;
     sc.lo = t * p.nk + r * p.nk / p.cs;
     sc.hi = t * p.nk + (r + 1) * p.nk / p.cs;
+  } else if (p.lanes) {
+    const int j = blockIdx.x / p.groups;
+    const long long W1 = (long long)p.n_otiles * p.nk;
+    sc.lo = sk_lo(j, W1, p.lanes);
+    sc.hi = sk_lo(j + 1, W1, p.lanes);
+    sc.lane_gr = blockIdx.x % p.groups;
   }
   sc.nk = p.nk;
   sc.nkd = p.nkd;
@@ -1018,9 +1044,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // stream-K partial: write it; fuse_proj_reduce_kernel sums the
         // contributors of the tile afterwards
-        const long long x0 = (long long)sg.tile * p.nk;
-        const int c_first = sk_owner(x0, lv.W, lv.n);
-        const int slot = blockIdx.x - c_first;
+        int slot;
+        if (p.lanes) {  // consecutive lanes contribute to a tile
+          const long long x0 = (long long)(sg.tile / p.groups) * p.nk;
+          slot = (int)(blockIdx.x / p.groups) - sk_owner(x0, (long long)p.n_otiles * p.nk, p.lanes);
+        } else {
+          const long long x0 = (long long)sg.tile * p.nk;
+          slot = blockIdx.x - sk_owner(x0, lv.W, lv.n);
+        }
         float* part = p.part + (((size_t)sg.tile * p.max_contrib + slot) * bn) * 128;
         for (int c16 = 0; c16 * 16 < ncol; ++c16) {
           float v[16];
@@ -1810,6 +1841,7 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.row_map = row_map;
   p.max_contrib = max_contrib;
   p.tmajor = (!live && f.G > 1) ? 1 : 0;
+  p.lanes = 0;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   p.cs = live ? 0 : fp_cluster_size(f, sms, smem);
   if (p.cs) {
@@ -1824,7 +1856,13 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
     note_launch();
     return last_launch_status();
   }
-  launch(fuse_proj_kernel<false>, f.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
+  if (p.tmajor) {
+    // groups in lockstep: lanes of `groups` CTAs (n_ctas is at most W, so a
+    // lane holds at least one chunk of its group when W >= n_ctas)
+    p.lanes = f.n_ctas / f.G;
+    p.n_ctas = p.lanes * f.G;
+  }
+  launch(fuse_proj_kernel<false>, p.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
   launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
          256, 0, s, p);
   note_launch(2);
