@@ -33,6 +33,14 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t r
 bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
 
+// eagle_linear (bf16) whose M = B W activation rows are rows r0 .. r0 + W - 1
+// of each of B requests of a [B, Rmax, k_in] array x, read in place (gemm_tc.cu).
+// EAGLE_ERR_UNSUPPORTED, with nothing launched, when that view is not one
+// TMA box per stage (then the caller gathers the rows first).
+int linear_rows_bf16(const void* x, int B, int W, int Rmax, int r0, const void* w, const float* bias,
+                     const void* residual, void* y, int n_out, int k_in, void* ws, size_t ws_bytes,
+                     int32_t* dev_status, cudaStream_t s);
+
 // Every kernel of the library is launched with programmatic stream
 // serialization (programmatic dependent launch): its CTAs may be scheduled
 // while the previous kernel on the stream is still finishing.  Each kernel

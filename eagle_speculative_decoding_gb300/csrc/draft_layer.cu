@@ -342,14 +342,22 @@ extern "C" int eagle_draft_layer(const void* x, const void* w_norm1, const void*
   EAGLE_TRY(eagle_tree_attn(q_tree, k_tree, v_tree, k_cache, v_cache, num_pages, block_table, max_pages,
                             ctx_lens, tree_mask, attn, nullptr, B, Rmax, Hq, Hkv, D, 16,
                             1.f / sqrtf((float)D), 0, dtype, att_ws, L.att, dev_status, stream));
-  if (bf)
-    launch(rows_gather_kernel<__nv_bfloat16>, M, kRowThreads, 0, s, (const __nv_bfloat16*)attn, W, r0, Rmax,
-           Hq * D, (__nv_bfloat16*)a);
-  else
-    launch(rows_gather_kernel<float>, M, kRowThreads, 0, s, (const float*)attn, W, r0, Rmax, Hq * D, (float*)a);
-  note_launch();
-  // 5. x1 = x + a W_o^T
-  EAGLE_TRY(eagle_linear(a, w_o, nullptr, x, x1, M, d, Hq * D, dtype, lin_ws, L.lin, dev_status, stream));
+  // 5. x1 = x + a W_o^T, a = the new rows r0 .. r0 + W - 1 of each request's
+  // attention output, read in place by the projection (gathered first where
+  // that row view is not one TMA box per stage)
+  rc = bf ? linear_rows_bf16(attn, B, W, Rmax, r0, w_o, nullptr, x, x1, d, Hq * D, lin_ws, L.lin, dev_status, s)
+          : (int)EAGLE_ERR_UNSUPPORTED;
+  if (rc == EAGLE_ERR_UNSUPPORTED) {
+    if (bf)
+      launch(rows_gather_kernel<__nv_bfloat16>, M, kRowThreads, 0, s, (const __nv_bfloat16*)attn, W, r0, Rmax,
+             Hq * D, (__nv_bfloat16*)a);
+    else
+      launch(rows_gather_kernel<float>, M, kRowThreads, 0, s, (const float*)attn, W, r0, Rmax, Hq * D, (float*)a);
+    note_launch();
+    EAGLE_TRY(eagle_linear(a, w_o, nullptr, x, x1, M, d, Hq * D, dtype, lin_ws, L.lin, dev_status, stream));
+  } else if (rc != EAGLE_OK) {
+    return rc;
+  }
   // 6. h2 = RMSNorm(x1) * w_norm2
   if (bf)
     launch(rmsnorm_kernel<__nv_bfloat16>, M, kRowThreads, 0, s, (const __nv_bfloat16*)x1,

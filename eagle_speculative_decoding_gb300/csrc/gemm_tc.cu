@@ -105,7 +105,7 @@ __device__ __forceinline__ int prefetch_weights(const Sched& sc, CtaShared& sh, 
       if (Sched::kWeightIsA)
         tma_load_2d(rg.a0 + it * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, sc.a_policy());
       else
-        tma_load_2d(rg.b0 + it * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, sc.b_policy());
+        sc.load_b(rg.b0 + it * rg.b_stride, fb, kc, sg.b_row, sc.b_policy());
     }
   }
   return it;
@@ -140,14 +140,14 @@ __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, con
       const uint32_t fb = smem_u32(&sh.full[s]);
       if (it < pre) {  // weight half already in flight: the activation half only
         if (Sched::kWeightIsA)
-          tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
+          sc.load_b(rg.b0 + s * rg.b_stride, fb, kc, sg.b_row, pol_b);
         else
           tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
       } else {
         if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u, &sh.abort_flag)) goto drain;
         mbar_arrive_expect_tx(fb, tx);
         tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
-        tma_load_2d(rg.b0 + s * rg.b_stride, sc.map_b(kc), fb, sc.b_x(kc), sg.b_row, pol_b);
+        sc.load_b(rg.b0 + s * rg.b_stride, fb, kc, sg.b_row, pol_b);
       }
       if (++s == stages) {
         s = 0;
@@ -313,8 +313,10 @@ struct LmSched {
     return true;
   }
   __device__ const CUtensorMap* map_a() const { return mx; }
-  __device__ const CUtensorMap* map_b(int) const { return mw; }
   __device__ int b_x(int kc) const { return kc * 64; }
+  __device__ void load_b(uint32_t dst, uint32_t fb, int kc, int b_row, uint64_t pol) const {
+    tma_load_2d(dst, mw, fb, b_x(kc), b_row, pol);
+  }
   __device__ uint64_t a_policy() const { return l2_policy_evict_last(); }
   __device__ uint64_t b_policy() const {
     return w_reused ? l2_policy_evict_normal() : l2_policy_evict_first();
@@ -761,6 +763,10 @@ struct FpParams {
   // (one HBM read, the others' from L2); a tile's contributors are
   // consecutive lanes
   int lanes;
+  // view_w > 0: segment 0 is read through a row view, rows r0 .. r0 + view_w
+  // - 1 of each request of a [B, Rmax, K] array (activation row b view_w + j);
+  // a group then starts at a request boundary (bn a multiple of view_w)
+  int view_w;
   // cs >= 1 (one activation group, all rows known on the host): output tile
   // t is computed by CTAs t * cs .. t * cs + cs - 1, each over an equal share
   // of the K chunks; with cs >= 2 they are one thread-block cluster that sums
@@ -807,6 +813,7 @@ struct FpSched {
   long long lo, hi;
   int nk, nkd, n_otiles, bn, groups, tmajor;
   int lane_gr;  // lanes: this CTA's group (the items [lo, hi) are output tiles x K chunks), else -1
+  int view_w;   // rows per request of a row view of the activations (see FpParams::view_w), else 0
   __device__ bool seg(int i, Seg& s) const {
     if (lo >= hi) return false;
     const int t = (int)(lo / nk) + i;
@@ -828,6 +835,14 @@ struct FpSched {
   __device__ const CUtensorMap* map_a() const { return mw; }
   __device__ const CUtensorMap* map_b(int kc) const { return mx[kc / nkd]; }
   __device__ int b_x(int kc) const { return (kc % nkd) * (TF32 ? 32 : 64); }
+  // the activation rows b_row .. of one K chunk: a 2-D box, or with a row
+  // view (view_w > 0) a 3-D box of view_w rows of bn / view_w requests
+  __device__ void load_b(uint32_t dst, uint32_t fb, int kc, int b_row, uint64_t pol) const {
+    if (view_w > 0)
+      tma_load_3d(dst, map_b(kc), fb, b_x(kc), 0, b_row / view_w, pol);
+    else
+      tma_load_2d(dst, map_b(kc), fb, b_x(kc), b_row, pol);
+  }
   // a weight tile that several groups read stays in L2 for their passes
   __device__ uint64_t a_policy() const { return groups > 1 ? l2_policy_evict_normal() : l2_policy_evict_first(); }
   __device__ uint64_t b_policy() const { return l2_policy_evict_last(); }
@@ -962,6 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.bn = bn;
   sc.groups = p.groups;
   sc.tmajor = p.tmajor;
+  sc.view_w = p.view_w;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&map_w);
@@ -1710,6 +1726,11 @@ struct FpLiveRows {
   const int32_t* accept_len;
   int B, R, slots;
 };
+// Activations read as rows r0 .. r0 + W - 1 of each of B requests of a
+// [B, Rmax, K] array (one K segment), activation row b W + j.
+struct FpRowView {
+  int B, W, Rmax, r0;
+};
 
 // Clusters of cs CTAs of the projection kernel (with `smem` bytes of shared
 // memory) that the current device runs at once; cached per (device, cs, smem).
@@ -1770,11 +1791,14 @@ int fp_cluster_size(const FpPlan& f, int sms, size_t smem) {
 int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const void* table, int n_rows,
                    const void* w, const float* bias, const void* residual, void* out, int M, int n_out,
                    int kseg, void* ws, int32_t* dev_status, cudaStream_t s,
-                   const FpLiveRows* live = nullptr) {
+                   const FpLiveRows* live = nullptr, const FpRowView* view = nullptr) {
   constexpr int esz = 2, bke = 64;
   int sms = sm_count();
   if (sms <= 0) return EAGLE_ERR_CUDA;
   const FpPlan f = fp_plan(M, n_out, kseg, esz, sms > kMaxCtas ? kMaxCtas : sms, nseg);
+  if (view && (nseg != 1 || live || ids || view->W < 1 || view->W > 256 ||
+               (view->B > 1 && (f.bn % view->W || f.bn / view->W > 256))))
+    return EAGLE_ERR_UNSUPPORTED;  // nothing launched
   const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
   const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
@@ -1808,9 +1832,27 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   CUtensorMap mw, mx[3];
   if (!make_tmap_2d(&mw, w, esz, (uint64_t)n_out, (uint64_t)nseg * kseg, 128, (uint32_t)bke))
     return EAGLE_ERR_CUDA;
-  for (int i = 0; i < 3; ++i)
-    if (!make_tmap_2d(&mx[i], seg[i], esz, (uint64_t)M, (uint64_t)kseg, (uint32_t)f.bn, (uint32_t)bke))
-      return EAGLE_ERR_CUDA;
+  int view_w = 0;
+  if (view) {
+    // one request: its W rows are contiguous; several: a 3-D box of W rows
+    // of bn / W requests lands the bn rows as a 2-D box would
+    const char* vb = static_cast<const char*>(seg[0]) + (size_t)view->r0 * kseg * esz;
+    if (view->B == 1) {
+      if (!make_tmap_2d(&mx[0], vb, esz, (uint64_t)view->W, (uint64_t)kseg, (uint32_t)f.bn, (uint32_t)bke))
+        return EAGLE_ERR_CUDA;
+    } else {
+      if (!make_tmap_3d_bf16(&mx[0], vb, (uint64_t)kseg, (uint64_t)view->W, (uint64_t)view->B,
+                             (uint64_t)kseg * esz, (uint64_t)view->Rmax * kseg * esz, (uint32_t)bke,
+                             (uint32_t)view->W, (uint32_t)(f.bn / view->W)))
+        return EAGLE_ERR_CUDA;
+      view_w = view->W;
+    }
+    mx[1] = mx[2] = mx[0];
+  } else {
+    for (int i = 0; i < 3; ++i)
+      if (!make_tmap_2d(&mx[i], seg[i], esz, (uint64_t)M, (uint64_t)kseg, (uint32_t)f.bn, (uint32_t)bke))
+        return EAGLE_ERR_CUDA;
+  }
 
   if (ids) {
     const long long chunks = (long long)M * (kseg / 8);
@@ -1842,6 +1884,7 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.max_contrib = max_contrib;
   p.tmajor = (!live && f.G > 1) ? 1 : 0;
   p.lanes = 0;
+  p.view_w = view_w;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   p.cs = live ? 0 : fp_cluster_size(f, sms, smem);
   if (p.cs) {
@@ -1958,6 +2001,23 @@ extern "C" int eagle_draft_input(const void* r, const int32_t* token_ids, const 
   return fp_launch_bf16(xs, 2, token_ids, embed, vocab, w_in, bias, nullptr, u, M, d, d, ws, dev_status,
                         static_cast<cudaStream_t>(stream));
 }
+
+namespace eagle {
+int linear_rows_bf16(const void* x, int B, int W, int Rmax, int r0, const void* w, const float* bias,
+                     const void* residual, void* y, int n_out, int k_in, void* ws, size_t ws_bytes,
+                     int32_t* dev_status, cudaStream_t s) {
+  if (!x || !w || !y || B <= 0 || W <= 0 || r0 < 0 || r0 + W > Rmax) return EAGLE_ERR_INVALID_ARG;
+  const long long M = (long long)B * W;
+  if (M > 4096 || n_out % 128 || k_in % 64 || n_out > 65536 || k_in > 65536) return EAGLE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)))
+    return EAGLE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < eagle_linear_workspace_size((int)M, n_out, k_in, EAGLE_BF16)) return EAGLE_ERR_WORKSPACE;
+  const void* xs[1] = {x};
+  const FpRowView v{B, W, Rmax, r0};
+  return fp_launch_bf16(xs, 1, nullptr, nullptr, 0, w, bias, residual, y, (int)M, n_out, k_in, ws, dev_status, s,
+                        nullptr, &v);
+}
+}  // namespace eagle
 
 extern "C" size_t eagle_linear_workspace_size(int M, int n_out, int k_in, int dtype) {
   return fp_workspace(M, n_out, k_in, dtype, 1, false);
