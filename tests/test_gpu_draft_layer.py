@@ -25,7 +25,9 @@ def _bf16_store(a):
     (10, 1536, 4096, "bf16", True, True),       # clusters of eight
     (20, 12288, 256, "bf16", True, False),      # one CTA per tile
     (37, 384, 320, "bf16", True, True),
-    (300, 256, 192, "bf16", False, True),       # two activation groups
+    (300, 256, 192, "bf16", False, True),       # two activation groups (lockstep lanes)
+    (1000, 1024, 512, "bf16", True, False),     # four groups
+    (2048, 512, 256, "bf16", False, True),      # eight groups
     (17, 256, 128, "fp32", True, True),
 ])
 def test_linear(M, n_out, k_in, dtype, bias, res):
