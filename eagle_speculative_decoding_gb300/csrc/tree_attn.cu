@@ -45,8 +45,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // ----------------------------------------------------------------------------
 // tcgen05 path (bf16).  128 + 128 * TPC threads per CTA:
-//   warp 0     producer of Q (per segment, once the previous segment's S MMAs
-//              are complete) and of the K blocks (4 paged 16-key boxes per
+//   warp 0     producer of Q (split schedule; the stream schedule's S issuer
+//              loads each segment's Q itself once the previous segment's S
+//              MMAs are complete, so the K loads never stop at a segment's
+//              end) and of the K blocks (4 paged 16-key boxes per
 //              64-column half: a 3-D map over the pool viewed as
 //              [pages*16][Hkv][D], or the tree's own K rows), into a ring of
 //              kv_stages(TPC) stages; a K stage is free once S of its block is
@@ -347,24 +349,23 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     // nothing to run: fall through to the teardown
   } else if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
-    // warp 0: Q (per segment) and the K blocks, a K stage released as soon as
-    // S of its block is complete; warp 2: the V blocks, a V stage released
-    // after P V.  The K loads thus run ahead of the V loads by the softmax of
-    // a block.
+    // warp 0: the K blocks, a K stage released as soon as S of its block is
+    // complete; warp 2: the V blocks, a V stage released after P V.  The K
+    // loads thus run ahead of the V loads by the softmax of a block.  Q is
+    // loaded by the S issuer, so neither producer stops at a segment's end.
     const bool kload = warp == 0;
     const uint64_t pol_kv = l2_policy_evict_normal();  // other units of the request re-read it
-    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_tree = l2_policy_evict_first();
     const uint32_t oob_row = (uint32_t)p.num_pages * 16u;  // a row past the pool: reads zeros
     constexpr int kGrp = 32 / (kBlk / 16);  // blocks per group of 32 page ids
     SegWalk wk;
     wk.init(p, sb);
     Seg sg;
     bool ok = true;
-    int st = 0, nq = 0;
+    int st = 0;
     uint32_t ph = 0;
     long long issued = 0;
     while (ok && wk.next(p, sg)) {
-      const int nt = min(TPC, p.qtiles - TPC * sg.cq);
       const int nctx = sg.L - 1;  // prefix blocks of the unit
       // page ids, 32 at a time (8 blocks of 4 pages) from block u0: lane q
       // holds page slot q of the group; the next group is loaded one ahead
@@ -379,25 +380,6 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         }
         return pg;
       };
-      if (kload && lane == 0) {
-        // the Q tile is free once S of the previous segment's last block is complete
-        if (nq > 0) ok = mbar_wait(smem_u32(&sb.q_empty), (uint32_t)(nq - 1) & 1u, abort_flag);
-        if (ok) {
-          const uint32_t box_rows = (uint32_t)(p.q_box_rows * p.G);
-          mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)(nt * NH * COPIES) * box_rows * 128u);
-          for (int t = 0; t < nt; ++t)
-#pragma unroll
-            for (int c = 0; c < COPIES; ++c)
-#pragma unroll
-              for (int h = 0; h < NH; ++h)
-                tma_load_3d(sQ + t * kTileQ + h * 16384u + (uint32_t)c * (128u / COPIES) * 128u, &map_q,
-                            smem_u32(&sb.q_full), h * 64, sg.kvh * p.G, sg.b * p.R + (TPC * sg.cq + t) * p.nr,
-                            pol_q);
-          ++nq;
-        }
-      }
-      if (kload) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
       const int nblk = sg.u1 - sg.u0;
       int pg_cur = page_group(0), pg_next = kGrp < nblk ? page_group(1) : -1;
       for (int i = 0; i < nblk; ++i) {
@@ -434,7 +416,7 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
           mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
-            tma_load_3d(dst + h * kBlkBytesHalf, map, fb, h * 64, sg.kvh, sg.b * p.R, pol_q);
+            tma_load_3d(dst + h * kBlkBytesHalf, map, fb, h * 64, sg.kvh, sg.b * p.R, pol_tree);
         }
         if (++st == kSt) {
           st = 0;
@@ -452,12 +434,6 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
         while (!mbar_try_wait(bar, ph2) && globaltimer_ns() - t0 < 100000000ull) {
         }
       }
-      if (kload && nq > 0) {
-        const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(&sb.q_full), (uint32_t)(nq - 1) & 1u) &&
-               globaltimer_ns() - t0 < 100000000ull) {
-        }
-      }
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ S issuer
@@ -466,11 +442,30 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
     Seg sg;
     bool ok = true;
     long long j = 0;
-    int nq = 0;
+    int nq = 0, q_issued = 0;
     const uint64_t dq0 = smem_desc_sw128(sQ);
+    const uint64_t pol_q = l2_policy_evict_first();
     while (ok && wk.next(p, sg)) {
       const int nt = min(TPC, p.qtiles - TPC * sg.cq);
-      if (lane == 0) ok = mbar_wait(smem_u32(&sb.q_full), (uint32_t)nq & 1u, abort_flag);
+      if (lane == 0) {
+        // the Q tile is free once S of the previous segment's last block is
+        // complete (this thread's own commit)
+        if (nq > 0) ok = mbar_wait(smem_u32(&sb.q_empty), (uint32_t)(nq - 1) & 1u, abort_flag);
+        if (ok) {
+          const uint32_t box_rows = (uint32_t)(p.q_box_rows * p.G);
+          mbar_arrive_expect_tx(smem_u32(&sb.q_full), (uint32_t)(nt * NH * COPIES) * box_rows * 128u);
+          for (int t = 0; t < nt; ++t)
+#pragma unroll
+            for (int c = 0; c < COPIES; ++c)
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+                tma_load_3d(sQ + t * kTileQ + h * 16384u + (uint32_t)c * (128u / COPIES) * 128u, &map_q,
+                            smem_u32(&sb.q_full), h * 64, sg.kvh * p.G, sg.b * p.R + (TPC * sg.cq + t) * p.nr,
+                            pol_q);
+          q_issued = nq + 1;
+          ok = mbar_wait(smem_u32(&sb.q_full), (uint32_t)nq & 1u, abort_flag);
+        }
+      }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       ++nq;
@@ -511,6 +506,13 @@ __global__ void __launch_bounds__(128 + 128 * TPC, 1)
       }
     }
     if (lane == 0) {
+      // a Q load issued but not seen complete (abort): wait for it, bounded
+      if (q_issued > nq) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&sb.q_full), (uint32_t)(q_issued - 1) & 1u) &&
+               globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
       // drain (always: after an abort elsewhere no consumer may have waited
       // for the last S): every S MMA completes before tensor memory is freed
       mma_commit(smem_u32(&sb.drain));
