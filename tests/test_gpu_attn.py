@@ -75,6 +75,7 @@ def test_bf16_small_cases(B, R, Hq, Hkv, D, lo, hi, splits):
     (2, 20, 12, 4, 128, 50, 400),
     (3, 33, 10, 2, 64, 0, 260),
     (40, 9, 32, 8, 128, 0, 700),       # many requests: segments cross requests, some empty
+    (3, 32, 8, 4, 128, 10, 500),       # two-copy tile of 64 rows per copy, 32-row tree block
     (2, 61, 32, 8, 128, 4000, 5000),   # two query tiles per unit
 ])
 def test_bf16_stream_schedule(B, R, Hq, Hkv, D, lo, hi):
