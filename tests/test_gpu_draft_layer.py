@@ -23,6 +23,8 @@ def _bf16_store(a):
     (10, 6144, 4096, "bf16", False, False),     # QKV projection, llama8b drafter
     (10, 4096, 14336, "bf16", False, True),     # down projection + residual
     (10, 1536, 4096, "bf16", True, True),       # clusters of eight
+    (10, 6144, 4096, "bf16", False, True),      # 48 tiles (the drafter's QKV): clusters of two
+    (7, 3072, 2048, "bf16", True, False),       # 24 tiles: clusters of four
     (20, 12288, 256, "bf16", True, False),      # one CTA per tile
     (37, 384, 320, "bf16", True, True),
     (300, 256, 192, "bf16", False, True),       # two activation groups (lockstep lanes)
