@@ -53,8 +53,11 @@ struct Ring {
   uint32_t b0, b_stride, b_bytes;
   int stages;
   int n;     // MMA N (rows of the B tile)
-  int nbuf;  // TMEM accumulator buffers of n columns each
+  int nbuf;  // TMEM accumulator buffers of n columns each (2 n with DUAL)
 };
+// DUAL (a template flag of the pipeline below): each stage holds two 128-row
+// A tiles (rows a_row .. a_row + 255, the second at a0 + kTileA) that share
+// the B tile; two MMAs per K step into accumulators n columns apart.
 
 struct Seg {
   int a_row;  // first weight row of the tile
@@ -93,7 +96,7 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
 // the model; only the activations depend on that grid).  Each stage's full
 // barrier expects both halves; the activation half follows after the wait.
 // Returns the number of stages pre-issued.
-template <bool TF32, class Sched>
+template <bool TF32, bool DUAL, class Sched>
 __device__ __forceinline__ int prefetch_weights(const Sched& sc, CtaShared& sh, const Ring& rg) {
   constexpr int kBke = TF32 ? 32 : 64;
   int it = 0;
@@ -102,10 +105,14 @@ __device__ __forceinline__ int prefetch_weights(const Sched& sc, CtaShared& sh, 
     for (int kc = sg.k0; kc < sg.k1 && it < rg.stages; ++kc, ++it) {
       const uint32_t fb = smem_u32(&sh.full[it]);
       mbar_arrive_expect_tx(fb, rg.a_bytes + rg.b_bytes);
-      if (Sched::kWeightIsA)
+      if (Sched::kWeightIsA) {
         tma_load_2d(rg.a0 + it * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, sc.a_policy());
-      else
+        if (DUAL)
+          tma_load_2d(rg.a0 + it * rg.a_stride + kTileA, sc.map_a(), fb, kc * kBke, sg.a_row + 128,
+                      sc.a_policy());
+      } else {
         sc.load_b(rg.b0 + it * rg.b_stride, fb, kc, sg.b_row, sc.b_policy());
+      }
     }
   }
   return it;
@@ -124,7 +131,7 @@ __device__ __forceinline__ void drain_full(CtaShared& sh, int stages, int it) {
   }
 }
 
-template <bool TF32, class Sched>
+template <bool TF32, bool DUAL, class Sched>
 __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, const Ring& rg,
                                              int pre) {
   constexpr int kBke = TF32 ? 32 : 64;  // elements per 128-byte chunk
@@ -147,6 +154,8 @@ __device__ __forceinline__ void run_producer(const Sched& sc, CtaShared& sh, con
         if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u, &sh.abort_flag)) goto drain;
         mbar_arrive_expect_tx(fb, tx);
         tma_load_2d(rg.a0 + s * rg.a_stride, sc.map_a(), fb, kc * kBke, sg.a_row, pol_a);
+        if (DUAL)
+          tma_load_2d(rg.a0 + s * rg.a_stride + kTileA, sc.map_a(), fb, kc * kBke, sg.a_row + 128, pol_a);
         sc.load_b(rg.b0 + s * rg.b_stride, fb, kc, sg.b_row, pol_b);
       }
       if (++s == stages) {
@@ -160,7 +169,7 @@ drain:
   drain_full(sh, stages, it);
 }
 
-template <bool TF32, class Sched>
+template <bool TF32, bool DUAL, class Sched>
 __device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, const Ring& rg) {
   const uint32_t idesc = mma_idesc(TF32 ? 2 : 1, 128, rg.n);
   const int stages = rg.stages;
@@ -174,7 +183,7 @@ __device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, const Ri
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = sh.tmem_base + (uint32_t)(buf * rg.n);
+    const uint32_t d_tmem = sh.tmem_base + (uint32_t)(buf * rg.n * (DUAL ? 2 : 1));
     for (int kc = sg.k0; kc < sg.k1; ++kc) {
       if (!mbar_wait(smem_u32(&sh.full[s]), ph, &sh.abort_flag)) {
         ok = false;
@@ -192,6 +201,9 @@ __device__ __forceinline__ void run_mma(const Sched& sc, CtaShared& sh, const Ri
           mma_tf32(d_tmem, da + 2u * kk, db + 2u * kk, idesc, accum);
         else
           mma_bf16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, accum);
+        // the second A tile: +kTileA bytes = +kTileA / 16 in the address field
+        if (DUAL)
+          mma_bf16(d_tmem + (uint32_t)rg.n, da + (uint64_t)(kTileA >> 4) + 2u * kk, db + 2u * kk, idesc, accum);
       }
       mma_commit(smem_u32(&sh.empty[s]));
       if (++s == stages) {
@@ -622,13 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cta_init(sh, stages);
   int pre = 0;
-  if (threadIdx.x == 0) pre = prefetch_weights<false>(sc, sh, rg);
+  if (threadIdx.x == 0) pre = prefetch_weights<false, false>(sc, sh, rg);
   cta_start(sh, tmem_cols);
 
   if (warp == 0) {
-    if (lane == 0) run_producer<false>(sc, sh, rg, pre);
+    if (lane == 0) run_producer<false, false>(sc, sh, rg, pre);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<false>(sc, sh, rg);
+    if (lane == 0) run_mma<false, false>(sc, sh, rg);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;       // TMEM lane quarter of this warp
@@ -763,6 +775,10 @@ struct FpParams {
   // (one HBM read, the others' from L2); a tile's contributors are
   // consecutive lanes
   int lanes;
+  // dual (with lanes): the items are (pair of output tiles 2 t, 2 t + 1, K
+  // chunk); each stage's activation tile feeds both tiles' MMAs, so the
+  // activations are read from L2 once per pair instead of once per tile
+  int dual;
   // view_w > 0: segment 0 is read through a row view, rows r0 .. r0 + view_w
   // - 1 of each request of a [B, Rmax, K] array (activation row b view_w + j);
   // a group then starts at a request boundary (bn a multiple of view_w)
@@ -805,7 +821,7 @@ __device__ inline int sk_owner(long long x, long long W, int n) {
   return c;
 }
 
-template <bool TF32>
+template <bool TF32, bool DUAL = false>
 struct FpSched {
   static constexpr bool kWeightIsA = true;  // W_proj is the A operand
   const CUtensorMap* mw;
@@ -814,6 +830,7 @@ struct FpSched {
   int nk, nkd, n_otiles, bn, groups, tmajor;
   int lane_gr;  // lanes: this CTA's group (the items [lo, hi) are output tiles x K chunks), else -1
   int view_w;   // rows per request of a row view of the activations (see FpParams::view_w), else 0
+  // DUAL (lanes): the items are pairs of output tiles (s.tile = pair * groups + group)
   __device__ bool seg(int i, Seg& s) const {
     if (lo >= hi) return false;
     const int t = (int)(lo / nk) + i;
@@ -823,7 +840,7 @@ struct FpSched {
     s.k1 = (int)(min(hi, a + nk) - a);
     if (lane_gr >= 0) {
       s.tile = t * groups + lane_gr;
-      s.a_row = t * 128;
+      s.a_row = t * (DUAL ? 256 : 128);
       s.b_row = lane_gr * bn;
     } else {
       s.tile = t;
@@ -858,8 +875,9 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
   const FpLive lv = fp_live(p);
   const int tile = blockIdx.y;
   int c_first, c_last;
-  if (p.lanes) {  // contributors: consecutive lanes over the tile's K chunks
-    const long long W1 = (long long)p.n_otiles * p.nk, x0 = (long long)(tile / p.groups) * p.nk;
+  if (p.lanes) {  // contributors: consecutive lanes over the tile's (or its pair's) K chunks
+    const int sh = p.dual ? 1 : 0;
+    const long long W1 = (long long)(p.n_otiles >> sh) * p.nk, x0 = (long long)((tile / p.groups) >> sh) * p.nk;
     c_first = sk_owner(x0, W1, p.lanes);
     c_last = sk_owner(x0 + p.nk - 1, W1, p.lanes);
   } else {
@@ -931,8 +949,9 @@ __global__ void __launch_bounds__(256) fuse_proj_reduce_kernel(const FpParams p)
 }
 
 // K = nk chunks over nk / nkd segments of width d, segment i read through
-// map_l, map_m, map_h in that order (two segments: map_h is unused).
-template <bool TF32>
+// map_l, map_m, map_h in that order (two segments: map_h is unused).  DUAL:
+// the lanes schedule over pairs of output tiles (FpParams::dual).
+template <bool TF32, bool DUAL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fuse_proj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_l,
                      const __grid_constant__ CUtensorMap map_m, const __grid_constant__ CUtensorMap map_h,
@@ -941,18 +960,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char dsmem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bn = p.bn, stages = p.stages;
-  const uint32_t tmem_cols = tmem_cols_for(bn);
   const uint32_t base = align1024(smem_u32(dsmem));
+  static_assert(!(TF32 && DUAL), "pairs of output tiles are a bf16 schedule");
+  constexpr bool dual = DUAL;
+  const int acc_cols = dual ? 2 * bn : bn;  // TMEM columns of one accumulator buffer
+  const uint32_t tmem_cols = tmem_cols_for(acc_cols);
   Ring rg;
   rg.stages = stages;
   rg.n = bn;
-  rg.nbuf = acc_buffers_for(bn);
+  rg.nbuf = acc_buffers_for(acc_cols);
   rg.a0 = base;
-  rg.a_stride = rg.a_bytes = kTileA;
-  rg.b0 = base + stages * kTileA;
+  rg.a_stride = rg.a_bytes = (dual ? 2u : 1u) * kTileA;
+  rg.b0 = base + stages * rg.a_stride;
   rg.b_stride = rg.b_bytes = (uint32_t)bn * 128u;
 
-  FpSched<TF32> sc;
+  FpSched<TF32, DUAL> sc;
   sc.mw = &map_w;
   sc.mx[0] = &map_l;
   sc.mx[1] = &map_m;
@@ -966,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sc.hi = t * p.nk + (r + 1) * p.nk / p.cs;
   } else if (p.lanes) {
     const int j = blockIdx.x / p.groups;
-    const long long W1 = (long long)p.n_otiles * p.nk;
+    const long long W1 = (long long)(dual ? p.n_otiles / 2 : p.n_otiles) * p.nk;
     sc.lo = sk_lo(j, W1, p.lanes);
     sc.hi = sk_lo(j + 1, W1, p.lanes);
     sc.lane_gr = blockIdx.x % p.groups;
@@ -989,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int pre = 0;
   // a device row count is only known once the previous grid is done, so the
   // weights of such a launch are not fetched early
-  if (threadIdx.x == 0 && !p.m_dev) pre = prefetch_weights<TF32>(sc, sh, rg);
+  if (threadIdx.x == 0 && !p.m_dev) pre = prefetch_weights<TF32, DUAL>(sc, sh, rg);
   cta_start(sh, tmem_cols);
   const FpLive lv = fp_live(p);
   if (p.m_dev) {
@@ -999,9 +1021,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == 0) {
-    if (lane == 0) run_producer<TF32>(sc, sh, rg, pre);
+    if (lane == 0) run_producer<TF32, DUAL>(sc, sh, rg, pre);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<TF32>(sc, sh, rg);
+    if (lane == 0) run_mma<TF32, DUAL>(sc, sh, rg);
   } else {
     const int q = warp & 3, e = q * 32 + lane;
     int acc = 0;
@@ -1011,77 +1033,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aph = (uint32_t)(acc / rg.nbuf) & 1u;
       if (!epi_wait(sh, smem_u32(&sh.acc_full[buf]), aph)) break;
       tc_fence_after();
-      const int ot = p.tmajor ? sg.tile / p.groups : sg.tile % p.n_otiles;
-      const int gr = p.tmajor ? sg.tile % p.groups : sg.tile / p.n_otiles;
-      const int o = ot * 128 + e, m0 = gr * bn, ncol = min(bn, lv.m - m0);
-      const uint32_t taddr = sh.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * bn);
-      const bool whole = sg.k0 == 0 && sg.k1 == p.nk;
-      const float bias_o = p.bias ? p.bias[o] : 0.f;
-      if (whole) {
-        for (int c16 = 0; c16 * 16 < ncol; ++c16) {
-          float v[16];
-          tmem_ld16(taddr + c16 * 16, v);
+      // dual: the segment's pair of output tiles, one after the other
+      for (int h = 0; h < (dual ? 2 : 1); ++h) {
+        const int ot = dual ? 2 * (sg.tile / p.groups) + h : p.tmajor ? sg.tile / p.groups : sg.tile % p.n_otiles;
+        const int gr = p.tmajor ? sg.tile % p.groups : sg.tile / p.n_otiles;
+        const int tile = dual ? ot * p.groups + gr : sg.tile;  // output tile (partials, reduction)
+        const int o = ot * 128 + e, m0 = gr * bn, ncol = min(bn, lv.m - m0);
+        const uint32_t taddr =
+            sh.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * acc_cols + h * bn);
+        const bool whole = sg.k0 == 0 && sg.k1 == p.nk;
+        const float bias_o = p.bias ? p.bias[o] : 0.f;
+        if (whole) {
+          for (int c16 = 0; c16 * 16 < ncol; ++c16) {
+            float v[16];
+            tmem_ld16(taddr + c16 * 16, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c16 * 16 + j;
-            if (col < ncol) {
-              const int orow = p.row_map ? p.row_map[m0 + col] : m0 + col;
-              const size_t idx = (size_t)orow * p.d + o;
-              float y = v[j] + bias_o;
-              if (p.residual)
-                y += TF32 ? reinterpret_cast<const float*>(p.residual)[idx]
-                          : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.residual)[idx]);
-              if (TF32)
-                reinterpret_cast<float*>(p.out)[idx] = y;
-              else
-                reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16(y);
+            for (int j = 0; j < 16; ++j) {
+              const int col = c16 * 16 + j;
+              if (col < ncol) {
+                const int orow = p.row_map ? p.row_map[m0 + col] : m0 + col;
+                const size_t idx = (size_t)orow * p.d + o;
+                float y = v[j] + bias_o;
+                if (p.residual)
+                  y += TF32 ? reinterpret_cast<const float*>(p.residual)[idx]
+                            : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.residual)[idx]);
+                if (TF32)
+                  reinterpret_cast<float*>(p.out)[idx] = y;
+                else
+                  reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16(y);
+              }
+            }
+          }
+        } else if (p.cs) {
+          // this CTA's K share of the tile: kept in shared memory (over the
+          // ring, whose stages are all consumed) for the cluster's sum below
+          float* xs = reinterpret_cast<float*>(dsmem + (base - smem_u32(dsmem)));
+          for (int c16 = 0; c16 * 16 < ncol; ++c16) {
+            float v[16];
+            tmem_ld16(taddr + c16 * 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c16 * 16 + j;
+              if (col < ncol) xs[col * 128 + e] = v[j];
+            }
+          }
+        } else {
+          // stream-K partial: write it; fuse_proj_reduce_kernel sums the
+          // contributors of the tile afterwards
+          int slot;
+          if (p.lanes) {  // consecutive lanes contribute to a tile (or a pair)
+            const long long x0 = (long long)(sg.tile / p.groups) * p.nk;
+            const long long W1 = (long long)(dual ? p.n_otiles / 2 : p.n_otiles) * p.nk;
+            slot = (int)(blockIdx.x / p.groups) - sk_owner(x0, W1, p.lanes);
+          } else {
+            const long long x0 = (long long)sg.tile * p.nk;
+            slot = blockIdx.x - sk_owner(x0, lv.W, lv.n);
+          }
+          float* part = p.part + (((size_t)tile * p.max_contrib + slot) * bn) * 128;
+          for (int c16 = 0; c16 * 16 < ncol; ++c16) {
+            float v[16];
+            tmem_ld16(taddr + c16 * 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c16 * 16 + j;
+              if (col < ncol) part[(size_t)col * 128 + e] = v[j];
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
-      } else if (p.cs) {
-        // this CTA's K share of the tile: kept in shared memory (over the
-        // ring, whose stages are all consumed) for the cluster's sum below
-        float* xs = reinterpret_cast<float*>(dsmem + (base - smem_u32(dsmem)));
-        for (int c16 = 0; c16 * 16 < ncol; ++c16) {
-          float v[16];
-          tmem_ld16(taddr + c16 * 16, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c16 * 16 + j;
-            if (col < ncol) xs[col * 128 + e] = v[j];
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
-      } else {
-        // stream-K partial: write it; fuse_proj_reduce_kernel sums the
-        // contributors of the tile afterwards
-        int slot;
-        if (p.lanes) {  // consecutive lanes contribute to a tile
-          const long long x0 = (long long)(sg.tile / p.groups) * p.nk;
-          slot = (int)(blockIdx.x / p.groups) - sk_owner(x0, (long long)p.n_otiles * p.nk, p.lanes);
-        } else {
-          const long long x0 = (long long)sg.tile * p.nk;
-          slot = blockIdx.x - sk_owner(x0, lv.W, lv.n);
-        }
-        float* part = p.part + (((size_t)sg.tile * p.max_contrib + slot) * bn) * 128;
-        for (int c16 = 0; c16 * 16 < ncol; ++c16) {
-          float v[16];
-          tmem_ld16(taddr + c16 * 16, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c16 * 16 + j;
-            if (col < ncol) part[(size_t)col * 128 + e] = v[j];
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[buf]));
     }
   }
   cta_teardown(sh, tmem_cols, p.status);
@@ -1696,6 +1718,22 @@ int fp_live_contrib(const FpPlan& f) {
   return mc;
 }
 
+// The lanes schedule (several groups, rows known on the host) over pairs of
+// output tiles: taken when the tiles pair up and every lane still holds at
+// least 4 (pair, K chunk) items.  Contributor slots a tile then needs.
+bool fp_use_dual(const FpPlan& f) {
+  if (f.G < 2 || f.n_otiles % 2) return false;
+  const int lanes = f.n_ctas / f.G;
+  return lanes >= 1 && (long long)(f.n_otiles / 2) * f.nk >= 4LL * lanes;
+}
+int fp_dual_contrib(const FpPlan& f) {
+  const int lanes = f.n_ctas / f.G;
+  const long long per = (long long)(f.n_otiles / 2) * f.nk / lanes;  // >= 4
+  long long c = (f.nk + per - 1) / per + 1;
+  if (c > lanes) c = lanes;
+  return (int)c;
+}
+
 // gathered: room for the [M, d] looked-up embedding rows (drafter input FC);
 // live: a device row count (the accepted-rows fusion), whose partials need
 // fp_live_contrib slots and which packs nseg [M, kseg] segments, a row map
@@ -1707,7 +1745,8 @@ size_t fp_workspace(int M, int n_out, int kseg, int dtype, int nseg, bool gather
   size_t best = 0;
   for (int cap = 1; cap <= kMaxCtas; ++cap) {
     const FpPlan f = fp_plan(M, n_out, kseg, esz, cap, nseg);
-    const int mc = live ? fp_live_contrib(f) : f.max_contrib;
+    int mc = live ? fp_live_contrib(f) : f.max_contrib;
+    if (!live && fp_use_dual(f) && fp_dual_contrib(f) > mc) mc = fp_dual_contrib(f);
     size_t sz = round_up((size_t)f.n_tiles * mc * f.bn * 128 * 4, 256) + 1024 +
                 (gathered ? round_up((size_t)M * kseg * esz, 256) : 0);
     if (live) sz += nseg * round_up((size_t)M * kseg * esz, 256) + round_up((size_t)M * 4, 256) + 256;
@@ -1799,10 +1838,14 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   if (view && (nseg != 1 || live || ids || view->W < 1 || view->W > 256 ||
                (view->B > 1 && (f.bn % view->W || f.bn / view->W > 256))))
     return EAGLE_ERR_UNSUPPORTED;  // nothing launched
-  const int stages = pick_stages((size_t)kTileA + (size_t)f.bn * 128, 0);
+  // several groups with a host row count: lockstep lanes, over pairs of
+  // output tiles when they pair up (two A tiles per stage)
+  const bool dual = !live && fp_use_dual(f);
+  const size_t stage_bytes = (dual ? 2 : 1) * (size_t)kTileA + (size_t)f.bn * 128;
+  const int stages = pick_stages(stage_bytes, 0);
   if (stages < 2) return EAGLE_ERR_UNSUPPORTED;
-  const size_t smem = 1024 + (size_t)stages * (kTileA + (size_t)f.bn * 128);
-  const int max_contrib = live ? fp_live_contrib(f) : f.max_contrib;
+  const size_t smem = 1024 + (size_t)stages * stage_bytes;
+  const int max_contrib = dual ? fp_dual_contrib(f) : live ? fp_live_contrib(f) : f.max_contrib;
 
   char* cur = static_cast<char*>(ws);
   float* part = static_cast<float*>(ws_carve(cur, (size_t)f.n_tiles * max_contrib * f.bn * 128 * 4));
@@ -1884,8 +1927,11 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
   p.max_contrib = max_contrib;
   p.tmajor = (!live && f.G > 1) ? 1 : 0;
   p.lanes = 0;
+  p.dual = 0;
   p.view_w = view_w;
   cudaFuncSetAttribute(fuse_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (dual)
+    cudaFuncSetAttribute(fuse_proj_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   p.cs = live ? 0 : fp_cluster_size(f, sms, smem);
   if (p.cs) {
     // one wave of n_otiles * cs CTAs, no partials in the workspace
@@ -1904,8 +1950,12 @@ int fp_launch_bf16(const void* const* xs, int nseg, const int32_t* ids, const vo
     // lane holds at least one chunk of its group when W >= n_ctas)
     p.lanes = f.n_ctas / f.G;
     p.n_ctas = p.lanes * f.G;
+    p.dual = dual ? 1 : 0;
   }
-  launch(fuse_proj_kernel<false>, p.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
+  if (p.dual)
+    launch(fuse_proj_kernel<false, true>, p.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
+  else
+    launch(fuse_proj_kernel<false>, p.n_ctas, kThreads, smem, s, mw, mx[0], mx[1], mx[2], p);
   launch(fuse_proj_reduce_kernel<false>, dim3((unsigned)((f.bn * 32 + 255) / 256), (unsigned)f.n_tiles),
          256, 0, s, p);
   note_launch(2);

@@ -30,6 +30,8 @@ def _bf16_store(a):
     (300, 256, 192, "bf16", False, True),       # two activation groups (lockstep lanes)
     (1000, 1024, 512, "bf16", True, False),     # four groups
     (2048, 512, 256, "bf16", False, True),      # eight groups
+    (512, 4096, 2048, "bf16", True, True),      # two groups of 256 rows over pairs of output tiles
+    (700, 4096, 2048, "bf16", False, True),     # three groups of 240 rows, pairs of output tiles
     (17, 256, 128, "fp32", True, True),
 ])
 def test_linear(M, n_out, k_in, dtype, bias, res):
