@@ -15,17 +15,19 @@ def _bf16_store(a):
 
 
 # One activation group with a host row count runs one cluster of cs CTAs per
-# 128-row output tile (on a 152-SM GPU): cs = 2 for the QKV shape, 4 for the
-# down projection, 8 for 1536 outputs, 1 (whole tiles, no split) for 12288
-# outputs over 4 K chunks; the others take the stream-K split.
+# 128-row output tile when the clusters fill at least 4/5 of the SMs (on a
+# 152-SM GPU): cs = 4 for the 32 tiles of the down projection, 2 for 64
+# tiles, 1 (whole tiles, no split) for 128 tiles over 4 K chunks; the others
+# (the drafter's 48-tile QKV among them) take the stream-K split.
 @pytest.mark.parametrize("M,n_out,k_in,dtype,bias,res", [
     (1, 128, 64, "bf16", False, False),
-    (10, 6144, 4096, "bf16", False, False),     # QKV projection, llama8b drafter
-    (10, 4096, 14336, "bf16", False, True),     # down projection + residual
-    (10, 1536, 4096, "bf16", True, True),       # clusters of eight
-    (10, 6144, 4096, "bf16", False, True),      # 48 tiles (the drafter's QKV): clusters of two
-    (7, 3072, 2048, "bf16", True, False),       # 24 tiles: clusters of four
-    (20, 12288, 256, "bf16", True, False),      # one CTA per tile
+    (10, 6144, 4096, "bf16", False, False),     # QKV projection, llama8b drafter: stream-K
+    (10, 4096, 14336, "bf16", False, True),     # down projection + residual: clusters of four
+    (10, 1536, 4096, "bf16", True, True),       # 12 tiles: stream-K
+    (10, 8192, 1024, "bf16", False, True),      # 64 tiles: clusters of two
+    (7, 3072, 2048, "bf16", True, False),       # 24 tiles: stream-K
+    (20, 16384, 256, "bf16", True, False),      # 128 tiles: one CTA per tile
+    (20, 12288, 256, "bf16", True, False),      # 96 tiles, 4 K chunks: stream-K
     (37, 384, 320, "bf16", True, True),
     (300, 256, 192, "bf16", False, True),       # two activation groups (lockstep lanes)
     (1000, 1024, 512, "bf16", True, False),     # four groups
