@@ -364,6 +364,85 @@ def profile_traffic():
         return None
 
 
+def call_work(wl, name):
+    """Algorithmic (bytes, flops) of one call of the step, or None for the
+    latency-bound calls."""
+    es = wl.w_lm.element_size()
+    M = wl.B * wl.R
+    if name == "fuse_proj":
+        return 3 * wl.d * wl.d * es + 4 * M * wl.d * es, 2 * M * 3 * wl.d * wl.d
+    if name == "tree_attn":
+        # prefix K/V, tree K/V, Q and O; Q K^T and P V over every key of each row
+        ctx_sum = int(wl.ctx_lens.sum().item())
+        return ((ctx_sum + M) * wl.Hkv * wl.D * 2 * es + 2 * M * wl.Hq * wl.D * es,
+                4 * wl.R * wl.Hq * wl.D * (ctx_sum + wl.B * wl.R))
+    if name == "lmhead_verify_stats":
+        # W_U once plus the activation rows; 2 M d V flops
+        return wl.V * wl.d * es + M * wl.d * es, 2 * M * wl.d * wl.V
+    return None
+
+
+def graph_call_us(call, dev, reps=10):
+    """GPU time of one call replayed from a CUDA graph of `reps` x (256 MB
+    write, call), less a graph of the writes alone: no host launch in the
+    time and every call starts with a cold L2, as a call inside the step
+    graph does (the step streams W_U, 8x the L2, between two such calls)."""
+    flush = torch.zeros(64 * 1024 * 1024, device=dev)
+    def gtime(fn):
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            fn()
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / reps)
+        del g
+        return statistics.median(ts)
+    base = gtime(lambda: flush.add_(1.0))
+    t = gtime(lambda: (flush.add_(1.0), call()))
+    del flush
+    return max(t - base, 1e-3)
+
+
+def graph_rows(wl, rows, peaks, dev):
+    """Add to the rows of the calls that stream or contract their time from
+    CUDA-graph replays (graph_us) and its roofline fraction (graph_frac)."""
+    t, f, x = wl.tree, wl.flat, wl.dev_in
+    calls = {
+        "tree_attn": lambda: eb.eagle_tree_attn(
+            x["q"], x["k_tree"], x["v_tree"], wl.k_cache, wl.v_cache, wl.block_table, wl.ctx_lens, f["mask"],
+            wl.attn_out, ws=wl.ws_attn, status=wl.status),
+        "fuse_proj": lambda: eb.eagle_fuse_proj(x["h"][0], x["h"][1], x["h"][2], wl.w_proj, wl.g, ws=wl.ws_fp,
+                                                status=wl.status),
+    }
+    if wl.T != 0:
+        calls["lmhead_verify_stats"] = lambda: eb.eagle_lmhead_verify_stats(
+            x["x_v"], wl.w_lm, f["parent_row"], f["token"], wl.T, wl.race_k, wl.race_ids, wl.race_keys,
+            wl.row_max, wl.row_sumexp, wl.child_logit, n_rows=f["n_rows"], seed=1234, ws=wl.ws_lm,
+            status=wl.status)
+    for name, call in calls.items():
+        if name not in rows:
+            continue
+        us = graph_call_us(call, dev)
+        byts, flops = call_work(wl, name)
+        b = bound_row(byts, flops, us, peaks)
+        rows[name].update({"graph_us": round(us, 2), "graph_frac": b["frac"],
+                           "graph_timing": "CUDA-graph replays of 10 x (256 MB write, call), the writes' "
+                                           "own graph subtracted: no host launch, cold L2"})
+
+
 def row_rooflines(wl, steps, peaks):
     """Per-call timing of every other call of the step (CUDA events around
     each call in a separate pass; events between kernels stop the next
@@ -378,22 +457,13 @@ def row_rooflines(wl, steps, peaks):
     for _ in range(steps):
         wl.step(row_events=ev)
     torch.cuda.synchronize()
-    es = wl.w_lm.element_size()
-    M = wl.B * wl.R
-    ctx_sum = int(wl.ctx_lens.sum().item())
     out = {}
     for name, lst in ev.items():
         us = sum(a.elapsed_time(b) for a, b in lst) / len(lst) * 1e3
         row = {"avg_call_us": round(us, 2), "calls_per_step": len(lst) // steps}
-        if name == "fuse_proj":
-            row.update(bound_row(3 * wl.d * wl.d * es + 4 * M * wl.d * es, 2 * M * 3 * wl.d * wl.d, us, peaks))
-        elif name == "tree_attn":
-            # prefix K/V, tree K/V, Q and O; Q K^T and P V over every key of each row
-            row.update(bound_row((ctx_sum + M) * wl.Hkv * wl.D * 2 * es + 2 * M * wl.Hq * wl.D * es,
-                                 4 * wl.R * wl.Hq * wl.D * (ctx_sum + wl.B * wl.R), us, peaks))
-        elif name == "lmhead_verify_stats":
-            # W_U once plus the activation rows; 2 M d V flops
-            row.update(bound_row(wl.V * wl.d * es + M * wl.d * es, 2 * M * wl.d * wl.V, us, peaks))
+        work = call_work(wl, name)
+        if work is not None:
+            row.update(bound_row(work[0], work[1], us, peaks))
         else:
             row.update(bound="latency")
         out[name] = row
@@ -708,6 +778,7 @@ def measure_workload(name, args, rank, world, clk, peaks, peak_kind, detail=True
         raise RuntimeError(f"device status {eb.STATUS.get(st, st)} ({name})")
 
     rows = row_rooflines(wl, max(min(args.steps, 50), 3), peaks)
+    graph_rows(wl, rows, peaks, dev)
     rows["lmhead_topk"] = {"avg_call_us": round(lm_avg_ms * 1e3, 2), "calls_per_step": len(lm_events) // args.steps,
                            "bound": "hbm", "achieved": round(achieved, 1), "unit": "GB/s",
                            "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -743,7 +814,8 @@ def measure_workload(name, args, rank, world, clk, peaks, peak_kind, detail=True
            "wall_s": round(t_wall1 - t_wall0, 3)}
     # the other calls that bound the step (per-call rows above)
     others = {k: rows[k] for k in ("lmhead_verify_stats", "tree_attn", "fuse_proj") if k in rows}
-    res["rooflines"] = {k: {kk: v[kk] for kk in ("bound", "achieved", "peak", "unit", "frac", "avg_call_us")
+    res["rooflines"] = {k: {kk: v[kk] for kk in ("bound", "achieved", "peak", "unit", "frac", "avg_call_us",
+                                                 "graph_us", "graph_frac")
                             if kk in v} for k, v in others.items()}
     del graphs
     return res, wl
