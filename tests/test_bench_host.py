@@ -1,6 +1,9 @@
 """Host-side pieces of bench.py that need no GPU."""
 import hashlib
 import os
+import types
+
+import torch
 
 import bench
 
@@ -56,3 +59,21 @@ def test_cpu_samples_are_bounded_subsets_of_the_batch():
     for name, c in bench.synth.CONFIGS.items():
         for one in (False, True):
             assert 1 <= bench.sample_requests(name, one) <= c["B"]
+
+
+def test_call_work_is_the_algorithmic_bytes_and_flops():
+    """Per-call work the rows divide by: llama8b's fused projection moves
+    W_proj (3 d x d) plus h_low/mid/high and g (4 M d), 102.7 MB; its tree
+    attention the prefix and tree K/V of 8 kv heads plus Q and O, 9.6 MB,
+    with 4 R Hq D (ctx + R) flops; the statistics LM head W_U plus the rows."""
+    wl = types.SimpleNamespace(B=1, R=61, d=4096, Hq=32, Hkv=8, D=128, V=128256,
+                               w_lm=torch.empty(1, dtype=torch.bfloat16), ctx_lens=torch.tensor([2048]))
+    byts, flops = bench.call_work(wl, "fuse_proj")
+    assert byts == 3 * 4096 * 4096 * 2 + 4 * 61 * 4096 * 2 == 102_662_144
+    assert flops == 2 * 61 * 12288 * 4096
+    byts, flops = bench.call_work(wl, "tree_attn")
+    assert byts == (2048 + 61) * 8 * 128 * 2 * 2 + 2 * 61 * 32 * 128 * 2 == 9_637_888
+    assert flops == 4 * 61 * 32 * 128 * (2048 + 61)
+    byts, flops = bench.call_work(wl, "lmhead_verify_stats")
+    assert byts == 128256 * 4096 * 2 + 61 * 4096 * 2 and flops == 2 * 61 * 4096 * 128256
+    assert bench.call_work(wl, "tree_verify") is None
