@@ -140,6 +140,26 @@ __device__ void expand_step_block(const ExpandArgs& a, int b, ExpandSmem<MAXC>& 
   float* s_lp = reinterpret_cast<float*>(s.kbuf);
   int* s_valid = reinterpret_cast<int*>(s.kbuf) + MAXC;
 
+  // Loads whose addresses need only the arguments go out first, beside the
+  // frontier count they would otherwise wait for: the frontier's node ids
+  // ([B, width]) and the candidate lists ([B, P, k]); entries past the count
+  // are read but not used.
+  constexpr int kCandPerThread = (MAXC + NT - 1) / NT;
+  int fr = 0;
+  if (step > 0 && threadIdx.x < width) fr = a.frontier[(size_t)b * width + threadIdx.x];
+  int cid[kCandPerThread];
+  float clp[kCandPerThread];
+  if (!MERGE) {
+#pragma unroll
+    for (int h = 0; h < kCandPerThread; ++h) {
+      const int t = h * NT + threadIdx.x;
+      if (t < P * k) {
+        cid[h] = a.cand_ids[(size_t)b * P * k + t];
+        clp[h] = a.cand_lp[(size_t)b * P * k + t];
+      }
+    }
+  }
+
   const int npar = step == 0 ? 1 : max(0, min(width, a.n_frontier[b]));
   const int count0 = step == 0 ? 1 : a.node_count[b];
   const int ncand = npar * k;
@@ -169,7 +189,7 @@ __device__ void expand_step_block(const ExpandArgs& a, int b, ExpandSmem<MAXC>& 
       nv_[0] = 0.f;
       nd_[0] = 0;
     } else {
-      int p = a.frontier[(size_t)b * width + j];
+      int p = fr;
       if (p < 0 || p >= count0) {
         atomicCAS(&s.bad, 0, EAGLE_ERR_BAD_TREE);
         p = 0;
@@ -255,11 +275,13 @@ __device__ void expand_step_block(const ExpandArgs& a, int b, ExpandSmem<MAXC>& 
       __syncthreads();
     }
   } else {
-    for (int t = threadIdx.x; t < ncand; t += NT) {
-      const int j = t / k, i = t % k;
-      const size_t src = ((size_t)b * P + j) * k + i;
-      s.id[t] = a.cand_ids[src];
-      s_lp[t] = a.cand_lp[src];
+#pragma unroll
+    for (int h = 0; h < kCandPerThread; ++h) {
+      const int t = h * NT + threadIdx.x;
+      if (t < ncand) {
+        s.id[t] = cid[h];
+        s_lp[t] = clp[h];
+      }
     }
   }
   __syncthreads();

@@ -60,6 +60,19 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
   __shared__ int s_row_of[kMaxNodes];
   __shared__ int s_prow[64];
   __shared__ int s_bad;
+  // the stored nodes' log V and depth are read beside the node count instead
+  // of after it (every slot of the store; those past the count go unused)
+  constexpr int kPer = kMaxNodes / kExpandThreads;
+  float lv[kPer];
+  int dp[kPer];
+#pragma unroll
+  for (int h = 0; h < kPer; ++h) {
+    const int i = h * kExpandThreads + threadIdx.x;
+    if (i + 1 < max_nodes) {
+      lv[h] = nv_[i + 1];
+      dp[h] = nd_[i + 1];
+    }
+  }
   int count = node_count[b];
   count = count < 1 ? 1 : (count > max_nodes ? max_nodes : count);
   const int n = count - 1;  // candidates (the seed excluded)
@@ -67,12 +80,54 @@ __global__ void __launch_bounds__(kExpandThreads) expand_finalize_kernel(
   const int ctx = ctx_lens ? ctx_lens[b] : 0;
   int P = 1;
   while (P < n) P <<= 1;
-  for (int i = threadIdx.x; i < P; i += kExpandThreads)
-    s_key[i] = i < n ? node_key(nv_[i + 1], nd_[i + 1], i + 1) : ~0ull;
+#pragma unroll
+  for (int h = 0; h < kPer; ++h) {
+    const int i = h * kExpandThreads + threadIdx.x;
+    if (i < P) s_key[i] = i < n ? node_key(lv[h], dp[h], i + 1) : ~0ull;
+  }
   for (int i = threadIdx.x; i < count; i += kExpandThreads) s_row_of[i] = -1;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  if (n <= 1024) {
+  if (n > 64 && P <= kExpandThreads) {
+    // one key per thread: each warp sorts its 32 keys (shuffle bitonic),
+    // and a key's rank is its place in its warp plus, for every other warp,
+    // how many of that warp's sorted keys are smaller (binary search); keys
+    // of nodes are unique, and the padding (~0) sorts after all of them.
+    // (Measured: 8.65 -> 7.73 µs per call with 510 candidates; with a few
+    // dozen, counting is cheaper than the sort's barriers.)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool mine = (int)threadIdx.x < P;
+    unsigned long long key = mine ? s_key[threadIdx.x] : ~0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
+        const bool keep_min = ((lane & stride) == 0) == ((lane & size) == 0 || size == 32);
+        key = keep_min ? (other < key ? other : key) : (other > key ? other : key);
+      }
+    }
+    __syncthreads();  // every key is in registers before the sorted runs overwrite them
+    if (mine) s_key[threadIdx.x] = key;
+    __syncthreads();
+    if (mine && key != ~0ull) {
+      int rank = lane;
+      for (int w = 0; w * 32 < P; ++w) {
+        if (w == warp) continue;
+        const unsigned long long* run = s_key + w * 32;
+        int lo = 0, hi = 32;  // keys of run w below `key`: the first index whose key is >= it
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (run[mid] < key)
+            lo = mid + 1;
+          else
+            hi = mid;
+        }
+        rank += lo;
+      }
+      if (rank < nsel) s_sel[rank] = key;
+    }
+  } else if (n <= 1024) {
     // the rank of each candidate = how many keys are smaller (keys are
     // unique); branch-free, every thread reads the same key at a time
     for (int i = threadIdx.x; i < n; i += kExpandThreads) {
