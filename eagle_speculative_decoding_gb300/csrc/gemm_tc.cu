@@ -554,7 +554,20 @@ __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmPar
   const float* gv = p.part_v + (size_t)m * n;
   const int* gi = p.part_i + (size_t)m * n;
   const int* gc = p.part_cnt + (size_t)m * nc;
-  constexpr int kU = 4;
+  LmPartials lp;
+  lp.ms = p.part_ms;
+  lp.v = p.part_v;
+  lp.id = p.part_i;
+  lp.cnt = p.part_cnt;
+  lp.cpg = nc;
+  lp.K = K;
+  lp.inv_t = p.inv_t;
+  lp.race = p.race;
+  // the merging warp's (max, sum) pairs go out with the staging loads, and
+  // eight loads of each kind per thread stage 152 lists of 12 in one pass
+  float2 ms[kLmMergePer];
+  if (tid < 32) lm_load_ms(lp, m, ms);
+  constexpr int kU = 8;
   for (int f0 = tid; f0 < n; f0 += kMergeThreads * kU) {
     float v[kU];
     int id[kU];
@@ -576,17 +589,8 @@ __global__ void __launch_bounds__(kMergeThreads) lmhead_merge_kernel(const LmPar
   for (int c = tid; c < nc; c += kMergeThreads) sc[c] = __ldcg(gc + c);
   __syncthreads();
   if (tid >= 32) return;
-  LmPartials lp;
-  lp.ms = p.part_ms;
-  lp.v = p.part_v;
-  lp.id = p.part_i;
-  lp.cnt = p.part_cnt;
-  lp.cpg = nc;
-  lp.K = K;
-  lp.inv_t = p.inv_t;
-  lp.race = p.race;
-  lm_merge_row(lp, m, sv, si, sc, p.topk_ids + (size_t)m * K, p.topk_lp + (size_t)m * K, p.row_max,
-               p.row_sumexp);
+  lm_merge_row_ms(lp, m, ms, sv, si, sc, p.topk_ids + (size_t)m * K, p.topk_lp + (size_t)m * K, p.row_max,
+                  p.row_sumexp);
 }
 
 template <int KMAX>

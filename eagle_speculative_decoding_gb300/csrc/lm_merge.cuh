@@ -45,25 +45,35 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 }
 
 // One warp merges row m, whose lists were staged in shared memory (sv, si:
-// [cpg][K]; sc: [cpg]).  Log-sum-exp by max / rescale over the CTAs, then the
+// [cpg][K]; sc: [cpg]) (lm_merge_row_ms below, with lm_merge_row loading
+// the row's (max, sum) pairs first).  Log-sum-exp by max / rescale over the CTAs, then the
 // top-K by K rounds of "best head among the CTAs' sorted lists".  Lane 0
 // writes ids (-1 past the available candidates) and log-probs (z/T - lse, or
 // the race key) to out_ids / out_lp (global or shared), and the row's max and
 // sum when the pointers are set.  Every lane of the warp must call it.  The
 // lists hold no NaN (the LM head never lists one).
-__device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const float* sv, const int* si,
-                                             const int* sc, int32_t* out_ids, float* out_lp, float* row_max,
-                                             float* row_sumexp) {
+constexpr int kLmMergePer = kLmMaxCtas / 32;  // lists owned per lane of the merging warp
+
+// The (max, sum) pairs of row m's CTAs, lane-strided: lane l holds CTA
+// l + 32 i in ms[i].  Issued by the merging warp; the loads may go out before
+// the lists are staged.
+__device__ __forceinline__ void lm_load_ms(const LmPartials& p, int m, float2 (&ms)[kLmMergePer]) {
+  const int lane = threadIdx.x & 31;
+  const float2* gms = p.ms + (size_t)m * p.cpg;
+#pragma unroll
+  for (int i = 0; i < kLmMergePer; ++i) {
+    const int c = lane + 32 * i;
+    ms[i] = c < p.cpg ? __ldcg(gms + c) : make_float2(-INFINITY, 0.f);
+  }
+}
+
+// lm_merge_row with the row's (max, sum) pairs already loaded (lm_load_ms).
+__device__ __forceinline__ void lm_merge_row_ms(const LmPartials& p, int m, const float2 (&ms)[kLmMergePer],
+                                                const float* sv, const int* si, const int* sc, int32_t* out_ids,
+                                                float* out_lp, float* row_max, float* row_sumexp) {
   const int lane = threadIdx.x & 31;
   const int K = p.K, nc = p.cpg;
-  constexpr int kPer = kLmMaxCtas / 32;  // lists owned per lane
-  const float2* gms = p.ms + (size_t)m * nc;
-  float2 ms[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = lane + 32 * i;
-    ms[i] = c < nc ? __ldcg(gms + c) : make_float2(-INFINITY, 0.f);
-  }
+  constexpr int kPer = kLmMergePer;
   float M = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) M = fmaxf(M, ms[i].x);
@@ -142,6 +152,14 @@ __device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const f
     if (row_max) row_max[m] = M;
     if (row_sumexp) row_sumexp[m] = S;
   }
+}
+
+__device__ __forceinline__ void lm_merge_row(const LmPartials& p, int m, const float* sv, const int* si,
+                                             const int* sc, int32_t* out_ids, float* out_lp, float* row_max,
+                                             float* row_sumexp) {
+  float2 ms[kLmMergePer];
+  lm_load_ms(p, m, ms);
+  lm_merge_row_ms(p, m, ms, sv, si, sc, out_ids, out_lp, row_max, row_sumexp);
 }
 
 }  // namespace eagle
