@@ -1484,20 +1484,36 @@ __global__ void __launch_bounds__(256) tree_attn_split_combine_kernel(const floa
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= nrows) return;
   const float* pl = part_lse + (size_t)row * splits;
+  // the splits' lse across the lanes (one load each, a warp max), then the O
+  // rows four splits at a time with every load issued before the first is
+  // used; the sums run in split order
   float L = -INFINITY;
-  for (int s = 0; s < splits; ++s) L = fmaxf(L, pl[s]);
+  for (int s0 = 0; s0 < splits; s0 += 32) L = fmaxf(L, s0 + lane < splits ? pl[s0 + lane] : -INFINITY);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
   float acc[D / 32];
 #pragma unroll
   for (int j = 0; j < D / 32; ++j) acc[j] = 0.f;
   float wsum = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float ls = pl[s];
-    if (ls == -INFINITY) continue;
-    const float w = exp2f((ls - L) * kLog2e);
-    wsum += w;
-    const float* po = part_o + ((size_t)row * splits + s) * D;
+  constexpr int kS = 4;
+  for (int s0 = 0; s0 < splits; s0 += kS) {
+    float ls[kS], ov[kS][D / 32];
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) acc[j] += w * po[lane + 32 * j];
+    for (int u = 0; u < kS; ++u) {
+      const int s = s0 + u;
+      ls[u] = s < splits ? pl[s] : -INFINITY;
+      const float* po = part_o + ((size_t)row * splits + (s < splits ? s : 0)) * D;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) ov[u][j] = s < splits ? po[lane + 32 * j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kS; ++u) {
+      if (ls[u] == -INFINITY) continue;
+      const float w = exp2f((ls[u] - L) * kLog2e);
+      wsum += w;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) acc[j] += w * ov[u][j];
+    }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
