@@ -206,24 +206,48 @@ __global__ void __launch_bounds__(kWalkThreads) verify_walk_kernel(
   __shared__ int s_path[65];
   __shared__ int s_nexcl, s_stop, s_plen, s_bad;
 
+  // the [B, R] row arrays are read for all R rows beside the row count, not
+  // after it (rows past the count go unused)
+  constexpr int kRowsPerThread = kMaxVerifyRows / kWalkThreads;
+  const int32_t* am_src = target_argmax ? target_argmax : ws_argmax;
+  int pre_p[kRowsPerThread], pre_t[kRowsPerThread], pre_a[kRowsPerThread];
+  float pre_m[kRowsPerThread], pre_s[kRowsPerThread], pre_z[kRowsPerThread];
+#pragma unroll
+  for (int h = 0; h < kRowsPerThread; ++h) {
+    const int i = h * kWalkThreads + threadIdx.x;
+    if (i < R) {
+      const size_t gi = (size_t)b * R + i;
+      pre_p[h] = parent_row[gi];
+      pre_t[h] = token[gi];
+      if (greedy) {
+        pre_a[h] = am_src[gi];
+      } else if (race_ids) {
+        pre_m[h] = st_max[gi];
+        pre_s[h] = st_sumexp[gi];
+        pre_z[h] = child_logit[gi];
+      }
+    }
+  }
   const int n = n_rows ? n_rows[b] : R;
   if (threadIdx.x == 0) s_bad = (n < 1 || n > R) ? 1 : 0;
   __syncthreads();
   const int nn = s_bad ? 1 : n;
-  const int32_t* am_src = target_argmax ? target_argmax : ws_argmax;
-  for (int i = threadIdx.x; i < nn; i += kWalkThreads) {
+#pragma unroll
+  for (int h = 0; h < kRowsPerThread; ++h) {
+    const int i = h * kWalkThreads + threadIdx.x;
+    if (i >= nn) continue;
     const size_t gi = (size_t)b * R + i;
-    const int p = parent_row[gi];
-    const int t = token[gi];
+    const int p = pre_p[h];
+    const int t = pre_t[h];
     s_parent[i] = p;
     s_token[i] = t;
     const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i && t >= 0 && t < V);
     if (!ok) atomicExch(&s_bad, 1);
     if (greedy) {
-      s_amax[i] = am_src[gi];
+      s_amax[i] = pre_a[h];
     } else if (race_ids) {
-      s_stat[i] = RowStat{st_max[gi], st_sumexp[gi]};
-      s_zt[i] = child_logit[gi];
+      s_stat[i] = RowStat{pre_m[h], pre_s[h]};
+      s_zt[i] = pre_z[h];
     } else {
       s_stat[i] = stats[gi];
       s_zt[i] = (i > 0 && ok) ? logits[((size_t)b * R + p) * V + t] : 0.f;
